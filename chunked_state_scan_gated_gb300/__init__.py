@@ -1,0 +1,395 @@
+"""GB300 Gated DeltaNet core: Python binding of the C ABI in include/gdn.h.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+library ``libgdn.so`` (hand-written sm_103a kernels); PyTorch provides device
+memory and the stream.  If the library is missing the calls raise: there is no
+CPU fallback.
+
+The functions keep the C names (``gdn_fwd``, ``gdn_bwd``, ``gdn_summary``,
+``gdn_summary_bwd``, ``gdn_compose``, ``gdn_prefix_compose``,
+``gdn_prefix_compose_bwd``, ``gdn_apply_state``, ``gdn_apply_state_bwd``,
+``gdn_query_support``, ``gdn_workspace_size``, ``gdn_check_device_status``) and
+take torch tensors in the token-major layouts of the header: q, k
+[B,T,Hqk,dk]; v [B,T,H,dv]; a, b [B,T,H]; A_log, dt_bias [H] fp32; states
+[B,H,dk,dv] fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA, \
+    GDN_ERR_DEVICE_TIMEOUT = range(6)
+GDN_FP32, GDN_BF16 = 0, 1
+GDN_OP_FWD, GDN_OP_BWD, GDN_OP_SUMMARY, GDN_OP_SUMMARY_BWD = range(4)
+
+# Every symbol include/gdn.h declares (checked by the CPU test suite).
+EXPORTS = (
+    "gdn_status_string", "gdn_abi_version", "gdn_problem_init", "gdn_query_support",
+    "gdn_workspace_size", "gdn_fwd", "gdn_bwd", "gdn_summary", "gdn_summary_bwd",
+    "gdn_compose", "gdn_prefix_compose", "gdn_prefix_compose_bwd", "gdn_apply_state",
+    "gdn_apply_state_bwd", "gdn_check_device_status", "gdn_kernel_info", "gdn_fwd_kernel",
+    "gdn_bwd_kernel",
+)
+
+
+class GDNError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)}")
+
+
+class Problem(ctypes.Structure):
+    """Mirror of ``gdn_problem`` (include/gdn.h)."""
+
+    _fields_ = [("dtype", ctypes.c_int32), ("chunk", ctypes.c_int32),
+                ("B", ctypes.c_int64), ("T", ctypes.c_int64), ("T_stride", ctypes.c_int64),
+                ("Hqk", ctypes.c_int64), ("H", ctypes.c_int64), ("dk", ctypes.c_int64),
+                ("dv", ctypes.c_int64), ("l2norm_qk", ctypes.c_int32), ("l2_eps", ctypes.c_float),
+                ("scale", ctypes.c_float), ("segments", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+_VP = ctypes.c_void_p
+_PP = ctypes.POINTER(Problem)
+_I64 = ctypes.c_int64
+
+
+def load_library(path: str | None = None):
+    """Load libgdn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"GDN CUDA library not found at {p}; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(p)
+        sig = {
+            "gdn_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "gdn_abi_version": ([], ctypes.c_int32),
+            "gdn_problem_init": ([_PP], None),
+            "gdn_query_support": ([_PP], ctypes.c_int),
+            "gdn_workspace_size": ([_PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
+                                   ctypes.c_int),
+            "gdn_fwd": ([_PP] + [_VP] * 12 + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_apply_state": ([_PP] + [_VP] * 12 + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_bwd": ([_PP] + [_VP] * 18 + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_apply_state_bwd": ([_PP] + [_VP] * 18 + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_summary": ([_PP] + [_VP] * 10 + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_summary_bwd": ([_PP] + [_VP] * 10 + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_compose": ([_I64] * 3 + [_VP] * 7, ctypes.c_int),
+            "gdn_prefix_compose": ([_I64] * 4 + [_VP] * 6, ctypes.c_int),
+            "gdn_prefix_compose_bwd": ([_I64] * 4 + [_VP] * 6, ctypes.c_int),
+            "gdn_check_device_status": ([_VP, _VP], ctypes.c_int),
+            "gdn_kernel_info": ([_PP, ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.POINTER(ctypes.c_int32),
+                                 ctypes.POINTER(ctypes.c_char_p)], ctypes.c_int),
+            "gdn_fwd_kernel": ([_PP, ctypes.c_int32] + [_VP] * 12 + [ctypes.c_size_t, _VP],
+                               ctypes.c_int),
+            "gdn_bwd_kernel": ([_PP, ctypes.c_int32] + [_VP] * 18 + [ctypes.c_size_t, _VP],
+                               ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().gdn_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != GDN_OK:
+        raise GDNError(fn, status)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("GDN tensors must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("GDN tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return GDN_BF16
+    if dt == torch.float32:
+        return GDN_FP32
+    raise ValueError(f"unsupported I/O dtype {dt}")
+
+
+def make_problem(q_or_k: torch.Tensor, v_or_dO: torch.Tensor, *, T: int | None = None,
+                 T_stride: int = 0, segments: int = 0, l2norm: bool = True, eps: float = 1e-6,
+                 scale: float = 0.0) -> Problem:
+    B, Tq, Hqk, dk = q_or_k.shape
+    H, dv = v_or_dO.shape[2], v_or_dO.shape[3]
+    p = Problem()
+    load_library().gdn_problem_init(ctypes.byref(p))
+    p.dtype = _dtype_code(q_or_k.dtype)
+    p.B, p.T, p.T_stride = B, (Tq if T is None else T), T_stride
+    p.Hqk, p.H, p.dk, p.dv = Hqk, H, dk, dv
+    p.l2norm_qk = 1 if l2norm else 0
+    p.l2_eps = eps
+    p.scale = scale
+    p.segments = segments
+    return p
+
+
+def gdn_query_support(problem: Problem) -> int:
+    return load_library().gdn_query_support(ctypes.byref(problem))
+
+
+def gdn_workspace_size(problem: Problem, op: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("gdn_workspace_size",
+           load_library().gdn_workspace_size(ctypes.byref(problem), op, ctypes.byref(n)))
+    return n.value
+
+
+def workspace(problem: Problem, op: int, device=None) -> torch.Tensor:
+    """A caller-owned workspace buffer for `op` (uint8, 256-byte aligned by torch)."""
+    n = gdn_workspace_size(problem, op)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(problem, op, ws, device):
+    if ws is None:
+        ws = workspace(problem, op, device)
+    return ws
+
+
+def gdn_fwd(q, k, v, a, b, A_log, dt_bias, h0=None, valid_len=None, *, segments=0,
+            l2norm=True, eps=1e-6, scale=0.0, o=None, hT=None, want_hT=True, ws=None,
+            stream=None, problem=None):
+    """Forward: returns (o [B,T,H,dv] in q.dtype, hT [B,H,dk,dv] fp32 or None)."""
+    p = problem or make_problem(q, v, segments=segments, l2norm=l2norm, eps=eps, scale=scale)
+    B, T, H, dv = v.shape
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, q.shape[3], dv), dtype=torch.float32, device=q.device)
+    ws = _ws(p, GDN_OP_FWD, ws, q.device)
+    _check("gdn_fwd", load_library().gdn_fwd(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+        _ptr(dt_bias), _ptr(h0), _ptr(valid_len), _ptr(o), _ptr(hT), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return o, hT
+
+
+def gdn_apply_state(q, k, v, a, b, A_log, dt_bias, Hin, valid_len=None, **kw):
+    """Forward of a segment from its incoming state Hin (required)."""
+    if Hin is None:
+        raise ValueError("gdn_apply_state needs Hin")
+    p = kw.pop("problem", None) or make_problem(q, v, segments=kw.pop("segments", 0),
+                                                 l2norm=kw.pop("l2norm", True),
+                                                 eps=kw.pop("eps", 1e-6),
+                                                 scale=kw.pop("scale", 0.0))
+    B, T, H, dv = v.shape
+    o = kw.pop("o", None)
+    hT = kw.pop("hT", None)
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and kw.pop("want_hT", True):
+        hT = torch.empty((B, H, q.shape[3], dv), dtype=torch.float32, device=q.device)
+    ws = _ws(p, GDN_OP_FWD, kw.pop("ws", None), q.device)
+    _check("gdn_apply_state", load_library().gdn_apply_state(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+        _ptr(dt_bias), _ptr(Hin), _ptr(valid_len), _ptr(o), _ptr(hT), _ptr(ws), ws.numel(),
+        _stream(kw.pop("stream", None))))
+    return o, hT
+
+
+def _bwd_common(name, q, k, v, a, b, A_log, dt_bias, h0, valid_len, dO, dHT, want_dH0, kw):
+    p = kw.pop("problem", None) or make_problem(q, v, segments=kw.pop("segments", 0),
+                                                 l2norm=kw.pop("l2norm", True),
+                                                 eps=kw.pop("eps", 1e-6),
+                                                 scale=kw.pop("scale", 0.0))
+    B, T, H, dv = v.shape
+    def out(name, make):
+        t = kw.pop(name, None)
+        return make() if t is None else t
+
+    dq = out("dq", lambda: torch.empty_like(q))
+    dk = out("dk", lambda: torch.empty_like(k))
+    dv_ = out("dv", lambda: torch.empty_like(v))
+    dg = out("dg", lambda: torch.empty((B, T, H), dtype=torch.float32, device=q.device))
+    dbeta = out("dbeta", lambda: torch.empty((B, T, H), dtype=torch.float32, device=q.device))
+    dH0 = kw.pop("dH0", None)
+    if dH0 is None and want_dH0:
+        dH0 = torch.empty((B, H, q.shape[3], dv), dtype=torch.float32, device=q.device)
+    ws = _ws(p, GDN_OP_BWD, kw.pop("ws", None), q.device)
+    fn = getattr(load_library(), name)
+    _check(name, fn(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+                    _ptr(dt_bias), _ptr(h0), _ptr(valid_len), _ptr(dO), _ptr(dHT), _ptr(dq),
+                    _ptr(dk), _ptr(dv_), _ptr(dg), _ptr(dbeta), _ptr(dH0), _ptr(ws), ws.numel(),
+                    _stream(kw.pop("stream", None))))
+    return dq, dk, dv_, dg, dbeta, dH0
+
+
+def gdn_bwd(q, k, v, a, b, A_log, dt_bias, dO, dHT=None, h0=None, valid_len=None, *,
+            want_dH0=True, **kw):
+    """Backward: returns (dq, dk, dv, dg, dbeta, dH0)."""
+    return _bwd_common("gdn_bwd", q, k, v, a, b, A_log, dt_bias, h0, valid_len, dO, dHT,
+                       want_dH0, kw)
+
+
+def gdn_apply_state_bwd(q, k, v, a, b, A_log, dt_bias, Hin, dO, dHout=None, valid_len=None,
+                        **kw):
+    """Backward of a segment run from Hin: (dq, dk, dv, dg, dbeta, dHin)."""
+    if Hin is None:
+        raise ValueError("gdn_apply_state_bwd needs Hin")
+    return _bwd_common("gdn_apply_state_bwd", q, k, v, a, b, A_log, dt_bias, Hin, valid_len, dO,
+                       dHout, True, kw)
+
+
+def gdn_summary(k, v, a, b, A_log, dt_bias, valid_len=None, *, l2norm=True, eps=1e-6, M=None,
+                S=None, ws=None, stream=None, problem=None):
+    """Segment summary (M [B,H,dk,dk], S [B,H,dk,dv]) fp32."""
+    p = problem or make_problem(k, v, l2norm=l2norm, eps=eps)
+    B, T, H, dv = v.shape
+    dk = k.shape[3]
+    M = M if M is not None else torch.empty((B, H, dk, dk), dtype=torch.float32, device=k.device)
+    S = S if S is not None else torch.empty((B, H, dk, dv), dtype=torch.float32, device=k.device)
+    ws = _ws(p, GDN_OP_SUMMARY, ws, k.device)
+    _check("gdn_summary", load_library().gdn_summary(
+        ctypes.byref(p), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+        _ptr(valid_len), _ptr(M), _ptr(S), _ptr(ws), ws.numel(), _stream(stream)))
+    return M, S
+
+
+def gdn_summary_bwd(q, k, a, b, A_log, dt_bias, dO, valid_len=None, *, l2norm=True, eps=1e-6,
+                    scale=0.0, D=None, ws=None, stream=None, problem=None):
+    """Gradient summary D = d<dO, o>/dH_in [B,H,dk,dv] fp32."""
+    p = problem or make_problem(q, dO, l2norm=l2norm, eps=eps, scale=scale)
+    B, T, H, dv = dO.shape
+    D = D if D is not None else torch.empty((B, H, q.shape[3], dv), dtype=torch.float32,
+                                            device=q.device)
+    ws = _ws(p, GDN_OP_SUMMARY_BWD, ws, q.device)
+    _check("gdn_summary_bwd", load_library().gdn_summary_bwd(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+        _ptr(valid_len), _ptr(dO), _ptr(D), _ptr(ws), ws.numel(), _stream(stream)))
+    return D
+
+
+def gdn_compose(M2, S2, M1, S1, *, M=None, S=None, stream=None):
+    """(M2 M1, M2 S1 + S2), batched over the leading dims."""
+    dk, dv = S1.shape[-2], S1.shape[-1]
+    n = S1.numel() // (dk * dv)
+    M = M if M is not None else torch.empty_like(M1)
+    S = S if S is not None else torch.empty_like(S1)
+    _check("gdn_compose", load_library().gdn_compose(n, dk, dv, _ptr(M2), _ptr(S2), _ptr(M1),
+                                                     _ptr(S1), _ptr(M), _ptr(S),
+                                                     _stream(stream)))
+    return M, S
+
+
+def gdn_prefix_compose(M, S, h0=None, *, want_Hout=True, Hin=None, Hout=None, stream=None):
+    """Exclusive prefix over the leading (segment) dim -> (Hin [P,...], Hout [...])."""
+    P = S.shape[0]
+    dk, dv = S.shape[-2], S.shape[-1]
+    n = S.numel() // (P * dk * dv) if P else 0
+    Hin = Hin if Hin is not None else torch.empty_like(S)
+    if Hout is None and want_Hout:
+        Hout = torch.empty(S.shape[1:], dtype=torch.float32, device=S.device)
+    _check("gdn_prefix_compose", load_library().gdn_prefix_compose(
+        n, P, dk, dv, _ptr(M), _ptr(S), _ptr(h0), _ptr(Hin), _ptr(Hout), _stream(stream)))
+    return Hin, Hout
+
+
+def gdn_prefix_compose_bwd(M, D, dHT=None, *, want_dH0=True, dHout=None, dH0=None, stream=None):
+    """Reverse exclusive prefix of state gradients -> (dHout [P,...], dH0 [...])."""
+    P = D.shape[0]
+    dk, dv = D.shape[-2], D.shape[-1]
+    n = D.numel() // (P * dk * dv) if P else 0
+    dHout = dHout if dHout is not None else torch.empty_like(D)
+    if dH0 is None and want_dH0:
+        dH0 = torch.empty(D.shape[1:], dtype=torch.float32, device=D.device)
+    _check("gdn_prefix_compose_bwd", load_library().gdn_prefix_compose_bwd(
+        n, P, dk, dv, _ptr(M), _ptr(D), _ptr(dHT), _ptr(dHout), _ptr(dH0), _stream(stream)))
+    return dHout, dH0
+
+
+def gdn_kernel_info(problem: Problem, op: int):
+    """Names of the kernels `op` (GDN_OP_FWD / GDN_OP_BWD) launches, in order."""
+    lib = load_library()
+    count = ctypes.c_int32(0)
+    _check("gdn_kernel_info", lib.gdn_kernel_info(ctypes.byref(problem), op, -1,
+                                                  ctypes.byref(count), None))
+    names = []
+    for i in range(count.value):
+        nm = ctypes.c_char_p()
+        _check("gdn_kernel_info", lib.gdn_kernel_info(ctypes.byref(problem), op, i, None,
+                                                      ctypes.byref(nm)))
+        names.append(nm.value.decode())
+    return names
+
+
+def gdn_fwd_kernel(index, q, k, v, a, b, A_log, dt_bias, h0, valid_len, o, hT, ws, *,
+                   problem, stream=None):
+    """Launch only kernel `index` of gdn_fwd (after a full gdn_fwd on the same workspace)."""
+    _check("gdn_fwd_kernel", load_library().gdn_fwd_kernel(
+        ctypes.byref(problem), index, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+        _ptr(dt_bias), _ptr(h0), _ptr(valid_len), _ptr(o), _ptr(hT), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def gdn_bwd_kernel(index, q, k, v, a, b, A_log, dt_bias, h0, valid_len, dO, dHT, dq, dk, dv,
+                   dg, dbeta, dH0, ws, *, problem, stream=None):
+    """Launch only kernel `index` of gdn_bwd (after a full gdn_bwd on the same workspace)."""
+    _check("gdn_bwd_kernel", load_library().gdn_bwd_kernel(
+        ctypes.byref(problem), index, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+        _ptr(dt_bias), _ptr(h0), _ptr(valid_len), _ptr(dO), _ptr(dHT), _ptr(dq), _ptr(dk),
+        _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dH0), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def gdn_check_device_status(ws, stream=None) -> int:
+    """Synchronous: status recorded on the device by the last call that used `ws`."""
+    return load_library().gdn_check_device_status(_ptr(ws), _stream(stream))
+
+
+class GDNCore(torch.autograd.Function):
+    """Autograd wrapper: forward = gdn_fwd, backward = gdn_bwd (recomputes, saves inputs only)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, a, b, A_log, dt_bias, h0, valid_len, segments):
+        o, hT = gdn_fwd(q, k, v, a, b, A_log, dt_bias, h0, valid_len, segments=segments)
+        ctx.save_for_backward(q, k, v, a, b, A_log, dt_bias, h0, valid_len)
+        ctx.segments = segments
+        return o, hT
+
+    @staticmethod
+    def backward(ctx, dO, dHT):
+        if any(ctx.needs_input_grad[3:7]):
+            raise NotImplementedError(
+                "GDNCore returns dg and dbeta through gdn_bwd; gradients w.r.t. a, b, A_log "
+                "and dt_bias are not computed by this operator")
+        q, k, v, a, b, A_log, dt_bias, h0, valid_len = ctx.saved_tensors
+        dq, dk, dv, dg, dbeta, dH0 = gdn_bwd(
+            q, k, v, a, b, A_log, dt_bias, dO.contiguous(),
+            None if dHT is None else dHT.contiguous(), h0, valid_len,
+            want_dH0=h0 is not None, segments=ctx.segments)
+        # dg and dbeta are w.r.t. g and beta; the parameter chain to a, b,
+        # A_log, dt_bias is not part of this operator.
+        return dq, dk, dv, None, None, None, None, dH0, None, None

@@ -1,0 +1,517 @@
+// gdn_api.cu -- the extern "C" entry points declared in include/gdn.h:
+// validation, workspace layout and the order of kernel launches.
+//
+// Forward with P segments (the pages' p2p / all_gather algebra of "linear
+// attention cp #1035", run on one GPU): chunk prologue -> summaries [M|S] of
+// segments 0..P-2 -> exclusive prefix H_in -> state pass of every segment from
+// its H_in (chunk-start states, V') -> chunk-parallel output.
+// Backward: prologue -> summaries + prefix (forward states recomputed, nothing
+// saved by the forward) -> state pass -> gradient summaries D of segments
+// 1..P-1 -> reverse prefix dH_out -> state-gradient pass of every segment ->
+// chunk-parallel local gradients -> Q/K head sum and norm chain.
+#include <math.h>
+#include <string.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int64_t kTargetBlocks = 304;  // scan blocks to aim for (two per SM of a 152-SM part)
+constexpr int kScanCols = 32;           // state columns per scan block
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Pointer must be non-null and 16-byte aligned unless the tensor is empty.
+bool ok_ptr(const void* p, int64_t numel) {
+  if (numel == 0) return p == nullptr || aligned16(p);
+  return p != nullptr && aligned16(p);
+}
+bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
+
+int auto_segments(int64_t B, int64_t H, int64_t dv, int64_t NC) {
+  if (NC <= 1) return 1;
+  const int64_t per_seg = B * H * ((dv + kScanCols - 1) / kScanCols);
+  int64_t want = (kTargetBlocks + per_seg - 1) / (per_seg > 0 ? per_seg : 1);
+  int64_t P = 1;
+  while (P < want) P <<= 1;
+  if (P > NC) P = NC;
+  if (P > 64) P = 64;
+  return (int)P;
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+gdn_status resolve_op(const gdn_problem* p, int op, Prob* out) {
+  if (!p || !out) return GDN_ERR_INVALID_ARG;
+  if (p->dtype != GDN_FP32 && p->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (p->B < 0 || p->T < 0 || p->Hqk < 1 || p->H < 1 || p->dk < 1 || p->dv < 1)
+    return GDN_ERR_INVALID_ARG;
+  if (p->H % p->Hqk != 0) return GDN_ERR_INVALID_ARG;
+  if (p->T_stride != 0 && p->T_stride < p->T) return GDN_ERR_INVALID_ARG;
+  if (!(p->l2_eps >= 0.f)) return GDN_ERR_INVALID_ARG;
+  if (p->segments < 0) return GDN_ERR_INVALID_ARG;
+  if (p->B > (int64_t)1 << 30 || p->T > (int64_t)1 << 34 || p->H > 4096)
+    return GDN_ERR_INVALID_ARG;
+  if (p->chunk != kChunk) return GDN_ERR_UNSUPPORTED;
+  if (p->dk % 16 != 0 || p->dv % 16 != 0 || p->dk > kMaxHeadDim || p->dv > kMaxHeadDim)
+    return GDN_ERR_UNSUPPORTED;
+  if (p->dtype == GDN_BF16 && (p->dk != 128 || p->dv != 128)) return GDN_ERR_UNSUPPORTED;
+  Prob r;
+  r.dtype = p->dtype;
+  r.B = p->B;
+  r.T = p->T;
+  r.Ts = p->T_stride == 0 ? p->T : p->T_stride;
+  r.Hqk = p->Hqk;
+  r.H = p->H;
+  r.dk = p->dk;
+  r.dv = p->dv;
+  r.r = p->H / p->Hqk;
+  r.l2norm = p->l2norm_qk ? 1 : 0;
+  r.eps = p->l2_eps;
+  r.scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->dk);
+  r.NC = (p->T + kChunk - 1) / kChunk;
+  r.Tp = r.NC * kChunk;
+  const int64_t maxP = r.NC > 1 ? r.NC : 1;
+  if (p->segments > maxP) return GDN_ERR_INVALID_ARG;
+  int P = p->segments > 0 ? p->segments : auto_segments(r.B, r.H, r.dv, r.NC);
+  if (op == GDN_OP_SUMMARY || op == GDN_OP_SUMMARY_BWD) P = 1;
+  r.CPS = r.NC > 0 ? (r.NC + P - 1) / P : 0;
+  r.P = r.CPS > 0 ? (int)((r.NC + r.CPS - 1) / r.CPS) : 1;
+  *out = r;
+  return GDN_OK;
+}
+
+gdn_status resolve(const gdn_problem* p, Prob* out) { return resolve_op(p, GDN_OP_FWD, out); }
+
+size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws) {
+  WS w;
+  memset(&w, 0, sizeof(w));
+  size_t off = 0;
+  char* b = (char*)base;
+  auto take = [&](size_t nfloat) -> float* {
+    float* ptr = base ? (float*)(b + off) : nullptr;
+    off = align_up(off + nfloat * sizeof(float));
+    return ptr;
+  };
+  const size_t B = pr.B, H = pr.H, Hqk = pr.Hqk, dk = pr.dk, dv = pr.dv, Tp = pr.Tp,
+               NC = pr.NC, P = pr.P;
+  const bool bwd = op == GDN_OP_BWD;
+  const bool fwd = op == GDN_OP_FWD;
+  w.status = (int*)take(64);
+  w.Qh = take(B * Hqk * Tp * dk);
+  w.Kh = take(B * Hqk * Tp * dk);
+  w.G = take(B * H * Tp);
+  w.Bt = take(B * H * Tp);
+  w.W = take(B * H * Tp * dk);
+  w.U = take(B * H * Tp * dv);
+  if (bwd) w.Tm = take(B * H * NC * 64 * 64);
+  if (fwd || bwd) {
+    w.Hc = take(B * H * NC * dk * dv);
+    w.Vn = take(B * H * Tp * dv);
+    if (P > 1) {
+      w.Mseg = take(P * B * H * dk * dk);
+      w.Sseg = take(P * B * H * dk * dv);
+      w.Hin = take(P * B * H * dk * dv);
+    }
+  }
+  if (bwd) {
+    w.dHc = take(B * H * NC * dk * dv);
+    w.dVn = take(B * H * Tp * dv);
+    if (P > 1) {
+      w.Dseg = take(P * B * H * dk * dv);
+      w.dHout = take(P * B * H * dk * dv);
+    }
+    w.dqp = take(B * Tp * H * dk);
+    w.dkp = take(B * Tp * H * dk);
+  }
+  if (ws) *ws = w;
+  return off;
+}
+
+namespace {
+
+gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+// Launch filter of one call: run every kernel (only < 0), only the kernel with
+// launch index `only`, or none (dry run that counts launches and names one).
+struct Sched {
+  int only = -1;
+  bool dry = false;
+  int want = -1;
+  int idx = 0;
+  const char* name = nullptr;
+  bool go(const char* nm) {
+    const int i = idx++;
+    if (dry) {
+      if (i == want) name = nm;
+      return false;
+    }
+    return only < 0 || only == i;
+  }
+};
+
+#define GDN_TRY(expr)                              \
+  do {                                             \
+    cudaError_t e_ = (expr);                       \
+    if (e_ != cudaSuccess) return GDN_ERR_CUDA;    \
+  } while (0)
+
+#define GDN_RUN(sched, name, expr)                 \
+  do {                                             \
+    if ((sched).go(name)) GDN_TRY(expr);           \
+  } while (0)
+
+gdn_status prepare(const gdn_problem* p, int op, void* workspace, size_t workspace_bytes,
+                   cudaStream_t st, Prob* pr, WS* ws) {
+  gdn_status s = resolve_op(p, op, pr);
+  if (s != GDN_OK) return s;
+  const size_t need = workspace_layout(*pr, op, nullptr, nullptr);
+  if (workspace == nullptr || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return GDN_ERR_INVALID_ARG;
+  workspace_layout(*pr, op, workspace, ws);
+  if (cudaMemsetAsync(ws->status, 0, sizeof(int), st) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+bool inputs_ok(const Prob& pr, const Inputs& in, bool need_q, bool need_v) {
+  const int64_t nqk = pr.B * pr.T * pr.Hqk * pr.dk;
+  const int64_t nv = pr.B * pr.T * pr.H * pr.dv;
+  const int64_t ng = pr.B * pr.T * pr.H;
+  if (need_q && !ok_ptr(in.q, nqk)) return false;
+  if (!ok_ptr(in.k, nqk)) return false;
+  if (need_v && !ok_ptr(in.v, nv)) return false;
+  if (!ok_ptr(in.a, ng) || !ok_ptr(in.b, ng)) return false;
+  if (!ok_ptr(in.A_log, pr.H) || !ok_ptr(in.dt_bias, pr.H)) return false;
+  if (!ok_opt(in.valid_len)) return false;
+  return true;
+}
+
+gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* o, float* hT,
+                       const WS& ws, cudaStream_t st, Sched& sc) {
+  GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, false, st));
+  const float* init = h0;
+  int64_t init_stride = 0;
+  const int64_t sstride = pr.B * pr.H * pr.dk * pr.dv;
+  if (pr.P > 1) {
+    GDN_RUN(sc, "summary_scan",
+            launch_state_scan(pr, ws, 1, 0, pr.P - 1, nullptr, 0, nullptr, nullptr, nullptr,
+                              ws.Mseg, ws.Sseg, sstride, st));
+    GDN_RUN(sc, "prefix",
+            launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Sseg, h0, ws.Hin, nullptr,
+                          st));
+    init = ws.Hin;
+    init_stride = sstride;
+  }
+  GDN_RUN(sc, "state_scan",
+          launch_state_scan(pr, ws, 0, 0, pr.P, init, init_stride, ws.Hc, ws.Vn, hT, nullptr,
+                            nullptr, 0, st));
+  GDN_RUN(sc, "output", launch_output(pr, in, ws, o, st));
+  return GDN_OK;
+}
+
+gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const float* dHT,
+                        void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dH0,
+                        const WS& ws, cudaStream_t st, Sched& sc) {
+  GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, true, st));
+  const int64_t sstride = pr.B * pr.H * pr.dk * pr.dv;
+  const float* init = h0;
+  int64_t init_stride = 0;
+  if (pr.P > 1) {
+    GDN_RUN(sc, "summary_scan",
+            launch_state_scan(pr, ws, 1, 0, pr.P, nullptr, 0, nullptr, nullptr, nullptr, ws.Mseg,
+                              ws.Sseg, sstride, st));
+    GDN_RUN(sc, "prefix",
+            launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Sseg, h0, ws.Hin, nullptr,
+                          st));
+    init = ws.Hin;
+    init_stride = sstride;
+  }
+  GDN_RUN(sc, "state_scan",
+          launch_state_scan(pr, ws, 0, 0, pr.P, init, init_stride, ws.Hc, ws.Vn, nullptr, nullptr,
+                            nullptr, 0, st));
+  const float* dinit = dHT;
+  int64_t dinit_stride = 0;
+  if (pr.P > 1) {
+    GDN_RUN(sc, "grad_summary_scan",
+            launch_dstate_scan(pr, in, ws, 1, 1, pr.P - 1, nullptr, 0, nullptr, ws.Dseg, sstride,
+                               st));
+    GDN_RUN(sc, "prefix_bwd",
+            launch_prefix_bwd(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Dseg, dHT, ws.dHout,
+                              nullptr, st));
+    dinit = ws.dHout;
+    dinit_stride = sstride;
+  }
+  GDN_RUN(sc, "dstate_scan",
+          launch_dstate_scan(pr, in, ws, 0, 0, pr.P, dinit, dinit_stride, dH0, nullptr, 0, st));
+  GDN_RUN(sc, "grad", launch_grad(pr, in, ws, dv, dg, dbeta, st));
+  GDN_RUN(sc, "qk_grad", launch_qk_grad(pr, in, ws, dq, dk, st));
+  return GDN_OK;
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT";
+  }
+  return "GDN_ERR_UNKNOWN";
+}
+
+int32_t gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+void gdn_problem_init(gdn_problem* p) {
+  if (!p) return;
+  memset(p, 0, sizeof(*p));
+  p->dtype = GDN_BF16;
+  p->chunk = kChunk;
+  p->l2norm_qk = 1;
+  p->l2_eps = 1e-6f;
+  p->scale = 0.f;
+  p->segments = 0;
+}
+
+gdn_status gdn_query_support(const gdn_problem* p) {
+  Prob pr;
+  return resolve_op(p, GDN_OP_FWD, &pr);
+}
+
+gdn_status gdn_workspace_size(const gdn_problem* p, int32_t op, size_t* bytes) {
+  if (!bytes || op < GDN_OP_FWD || op > GDN_OP_SUMMARY_BWD) return GDN_ERR_INVALID_ARG;
+  Prob pr;
+  gdn_status s = resolve_op(p, op, &pr);
+  if (s != GDN_OK) return s;
+  *bytes = workspace_layout(pr, op, nullptr, nullptr);
+  return GDN_OK;
+}
+
+static gdn_status fwd_impl(const gdn_problem* p, const void* q, const void* k, const void* v,
+                           const void* a, const void* b, const float* A_log,
+                           const float* dt_bias, const float* h0, const int32_t* valid_len,
+                           void* o, float* hT, void* workspace, size_t workspace_bytes,
+                           void* stream, Sched& sc) {
+  Prob pr;
+  gdn_status s = resolve_op(p, GDN_OP_FWD, &pr);
+  if (s != GDN_OK) return s;
+  Inputs in{q, k, v, a, b, A_log, dt_bias, valid_len, nullptr};
+  if (!inputs_ok(pr, in, true, true)) return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr(o, pr.B * pr.T * pr.H * pr.dv) || !ok_opt(h0) || !ok_opt(hT))
+    return GDN_ERR_INVALID_ARG;
+  WS ws;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((s = prepare(p, GDN_OP_FWD, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK) return s;
+  return run_forward(pr, in, h0, o, hT, ws, st, sc);
+}
+
+static gdn_status bwd_impl(const gdn_problem* p, const void* q, const void* k, const void* v,
+                           const void* a, const void* b, const float* A_log,
+                           const float* dt_bias, const float* h0, const int32_t* valid_len,
+                           const void* dO, const float* dHT, void* dq, void* dk, void* dv,
+                           float* dg, float* dbeta, float* dH0, void* workspace,
+                           size_t workspace_bytes, void* stream, Sched& sc) {
+  Prob pr;
+  gdn_status s = resolve_op(p, GDN_OP_BWD, &pr);
+  if (s != GDN_OK) return s;
+  Inputs in{q, k, v, a, b, A_log, dt_bias, valid_len, dO};
+  if (!inputs_ok(pr, in, true, true)) return GDN_ERR_INVALID_ARG;
+  const int64_t nqk = pr.B * pr.T * pr.Hqk * pr.dk, nv = pr.B * pr.T * pr.H * pr.dv,
+                ng = pr.B * pr.T * pr.H;
+  if (!ok_ptr(dO, nv) || !ok_opt(dHT) || !ok_opt(h0) || !ok_opt(dH0)) return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr(dq, nqk) || !ok_ptr(dk, nqk) || !ok_ptr(dv, nv) || !ok_ptr(dg, ng) ||
+      !ok_ptr(dbeta, ng))
+    return GDN_ERR_INVALID_ARG;
+  WS ws;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((s = prepare(p, GDN_OP_BWD, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK) return s;
+  return run_backward(pr, in, h0, dHT, dq, dk, dv, dg, dbeta, dH0, ws, st, sc);
+}
+
+gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                   const void* a, const void* b, const float* A_log, const float* dt_bias,
+                   const float* h0, const int32_t* valid_len, void* o, float* hT,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  Sched sc;
+  return fwd_impl(p, q, k, v, a, b, A_log, dt_bias, h0, valid_len, o, hT, workspace,
+                  workspace_bytes, stream, sc);
+}
+
+gdn_status gdn_fwd_kernel(const gdn_problem* p, int32_t index, const void* q, const void* k,
+                          const void* v, const void* a, const void* b, const float* A_log,
+                          const float* dt_bias, const float* h0, const int32_t* valid_len,
+                          void* o, float* hT, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (index < 0) return GDN_ERR_INVALID_ARG;
+  Sched sc;
+  sc.only = index;
+  return fwd_impl(p, q, k, v, a, b, A_log, dt_bias, h0, valid_len, o, hT, workspace,
+                  workspace_bytes, stream, sc);
+}
+
+gdn_status gdn_bwd_kernel(const gdn_problem* p, int32_t index, const void* q, const void* k,
+                          const void* v, const void* a, const void* b, const float* A_log,
+                          const float* dt_bias, const float* h0, const int32_t* valid_len,
+                          const void* dO, const float* dHT, void* dq, void* dk, void* dv,
+                          float* dg, float* dbeta, float* dH0, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (index < 0) return GDN_ERR_INVALID_ARG;
+  Sched sc;
+  sc.only = index;
+  return bwd_impl(p, q, k, v, a, b, A_log, dt_bias, h0, valid_len, dO, dHT, dq, dk, dv, dg,
+                  dbeta, dH0, workspace, workspace_bytes, stream, sc);
+}
+
+gdn_status gdn_kernel_info(const gdn_problem* p, int32_t op, int32_t index, int32_t* count,
+                           const char** name) {
+  if (op != GDN_OP_FWD && op != GDN_OP_BWD) return GDN_ERR_INVALID_ARG;
+  Prob pr;
+  gdn_status s = resolve_op(p, op, &pr);
+  if (s != GDN_OK) return s;
+  Sched sc;
+  sc.dry = true;
+  sc.want = index;
+  WS ws;
+  memset(&ws, 0, sizeof(ws));
+  Inputs in{};
+  if (op == GDN_OP_FWD)
+    run_forward(pr, in, nullptr, nullptr, nullptr, ws, nullptr, sc);
+  else
+    run_backward(pr, in, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                 ws, nullptr, sc);
+  if (count) *count = sc.idx;
+  if (name) *name = sc.name;
+  return (index >= 0 && index >= sc.idx) ? GDN_ERR_INVALID_ARG : GDN_OK;
+}
+
+gdn_status gdn_apply_state(const gdn_problem* p, const void* q, const void* k, const void* v,
+                           const void* a, const void* b, const float* A_log,
+                           const float* dt_bias, const float* Hin, const int32_t* valid_len,
+                           void* o, float* hT, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (Hin == nullptr) return GDN_ERR_INVALID_ARG;
+  return gdn_fwd(p, q, k, v, a, b, A_log, dt_bias, Hin, valid_len, o, hT, workspace,
+                 workspace_bytes, stream);
+}
+
+gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                   const void* a, const void* b, const float* A_log, const float* dt_bias,
+                   const float* h0, const int32_t* valid_len, const void* dO, const float* dHT,
+                   void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dH0,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  Sched sc;
+  return bwd_impl(p, q, k, v, a, b, A_log, dt_bias, h0, valid_len, dO, dHT, dq, dk, dv, dg,
+                  dbeta, dH0, workspace, workspace_bytes, stream, sc);
+}
+
+gdn_status gdn_apply_state_bwd(const gdn_problem* p, const void* q, const void* k,
+                               const void* v, const void* a, const void* b, const float* A_log,
+                               const float* dt_bias, const float* Hin,
+                               const int32_t* valid_len, const void* dO, const float* dHout,
+                               void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                               float* dHin, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (Hin == nullptr) return GDN_ERR_INVALID_ARG;
+  return gdn_bwd(p, q, k, v, a, b, A_log, dt_bias, Hin, valid_len, dO, dHout, dq, dk, dv, dg,
+                 dbeta, dHin, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_summary(const gdn_problem* p, const void* k, const void* v, const void* a,
+                       const void* b, const float* A_log, const float* dt_bias,
+                       const int32_t* valid_len, float* M, float* S, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  Prob pr;
+  gdn_status s = resolve_op(p, GDN_OP_SUMMARY, &pr);
+  if (s != GDN_OK) return s;
+  Inputs in{nullptr, k, v, a, b, A_log, dt_bias, valid_len, nullptr};
+  if (!inputs_ok(pr, in, false, true)) return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr(M, pr.B * pr.H * pr.dk * pr.dk) || !ok_ptr(S, pr.B * pr.H * pr.dk * pr.dv))
+    return GDN_ERR_INVALID_ARG;
+  WS ws;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((s = prepare(p, GDN_OP_SUMMARY, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK)
+    return s;
+  GDN_TRY(launch_prep(pr, in, ws, false, false, st));
+  GDN_TRY(launch_state_scan(pr, ws, 1, 0, 1, nullptr, 0, nullptr, nullptr, nullptr, M, S, 0, st));
+  return GDN_OK;
+}
+
+gdn_status gdn_summary_bwd(const gdn_problem* p, const void* q, const void* k, const void* a,
+                           const void* b, const float* A_log, const float* dt_bias,
+                           const int32_t* valid_len, const void* dO, float* D,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  Prob pr;
+  gdn_status s = resolve_op(p, GDN_OP_SUMMARY_BWD, &pr);
+  if (s != GDN_OK) return s;
+  // The gradient summary does not depend on v: the prologue skips U when v is null.
+  Inputs in{q, k, nullptr, a, b, A_log, dt_bias, valid_len, dO};
+  if (!inputs_ok(pr, in, true, false)) return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr(dO, pr.B * pr.T * pr.H * pr.dv) || !ok_ptr(D, pr.B * pr.H * pr.dk * pr.dv))
+    return GDN_ERR_INVALID_ARG;
+  WS ws;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((s = prepare(p, GDN_OP_SUMMARY_BWD, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK)
+    return s;
+  GDN_TRY(launch_prep(pr, in, ws, true, false, st));
+  GDN_TRY(launch_dstate_scan(pr, in, ws, 1, 0, 1, nullptr, 0, nullptr, D, 0, st));
+  return GDN_OK;
+}
+
+gdn_status gdn_compose(int64_t n, int64_t dk, int64_t dv, const float* M2, const float* S2,
+                       const float* M1, const float* S1, float* M, float* S, void* stream) {
+  if (n < 0 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
+  if (dk > kMaxHeadDim || dv > kMaxHeadDim) return GDN_ERR_UNSUPPORTED;
+  const int64_t nm = n * dk * dk, ns = n * dv * dk;
+  if (!ok_ptr(M2, nm) || !ok_ptr(M1, nm) || !ok_ptr(M, nm) || !ok_ptr(S2, ns) ||
+      !ok_ptr(S1, ns) || !ok_ptr(S, ns))
+    return GDN_ERR_INVALID_ARG;
+  return cuda_status(launch_compose(n, dk, dv, M2, S2, M1, S1, M, S, (cudaStream_t)stream));
+}
+
+gdn_status gdn_prefix_compose(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
+                              const float* S, const float* h0, float* Hin, float* Hout,
+                              void* stream) {
+  if (n < 0 || P < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
+  if (dk > kMaxHeadDim || dv > kMaxHeadDim) return GDN_ERR_UNSUPPORTED;
+  const int64_t nm = P * n * dk * dk, ns = P * n * dk * dv;
+  if (!ok_ptr(M, nm) || !ok_ptr(S, ns) || !ok_ptr(Hin, ns) || !ok_opt(h0) || !ok_opt(Hout))
+    return GDN_ERR_INVALID_ARG;
+  return cuda_status(launch_prefix(n, P, dk, dv, M, S, h0, Hin, Hout, (cudaStream_t)stream));
+}
+
+gdn_status gdn_prefix_compose_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
+                                  const float* D, const float* dHT, float* dHout, float* dH0,
+                                  void* stream) {
+  if (n < 0 || P < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
+  if (dk > kMaxHeadDim || dv > kMaxHeadDim) return GDN_ERR_UNSUPPORTED;
+  const int64_t nm = P * n * dk * dk, ns = P * n * dk * dv;
+  if (!ok_ptr(M, nm) || !ok_ptr(D, ns) || !ok_ptr(dHout, ns) || !ok_opt(dHT) || !ok_opt(dH0))
+    return GDN_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_prefix_bwd(n, P, dk, dv, M, D, dHT, dHout, dH0, (cudaStream_t)stream));
+}
+
+gdn_status gdn_check_device_status(void* workspace, void* stream) {
+  if (workspace == nullptr || ((uintptr_t)workspace & 255u) != 0) return GDN_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return GDN_ERR_CUDA;
+  if (word & kStatusTimeout) return GDN_ERR_DEVICE_TIMEOUT;
+  if (word & kStatusClamped) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// gdn_internal.h -- shared declarations of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;          // tokens per chunk
+constexpr int kMaxHeadDim = 128;    // largest dk / dv
+constexpr int kStatusClamped = 1;   // device status bit: a valid_len was outside [0, T]
+constexpr int kStatusTimeout = 2;   // device status bit: a bounded wait ran out
+
+// A validated problem with every derived size.
+struct Prob {
+  int dtype;
+  int64_t B, T, Ts, Hqk, H, dk, dv, r;
+  int l2norm;
+  float eps, scale;
+  int64_t NC;   // chunks per row, ceil(T / 64)
+  int64_t Tp;   // NC * 64
+  int P;        // segments
+  int64_t CPS;  // chunks per segment (last one may be shorter)
+};
+
+// Workspace regions (device pointers into the caller's buffer); null when unused.
+struct WS {
+  int* status;  // device status word
+  float* Qh;    // [B][Hqk][Tp][dk]  normalised, scaled q
+  float* Kh;    // [B][Hqk][Tp][dk]  normalised k
+  float* G;     // [B][H][Tp]        cumulative gate inside each chunk
+  float* Bt;    // [B][H][Tp]        beta
+  float* W;     // [B][H][Tp][dk]    T diag(beta*gamma) K
+  float* U;     // [B][H][Tp][dv]    T diag(beta) V
+  float* Tm;    // [B][H][NC][64][64] (I + A)^-1
+  float* Hc;    // [B][H][NC][dk][dv] state at each chunk start
+  float* Vn;    // [B][H][Tp][dv]    V' = U - W S
+  float* Mseg;  // [P][B][H][dk][dk]
+  float* Sseg;  // [P][B][H][dk][dv]
+  float* Hin;   // [P][B][H][dk][dv]
+  float* dHc;   // [B][H][NC][dk][dv] gradient of each chunk's end state
+  float* dVn;   // [B][H][Tp][dv]    gradient of V'
+  float* Dseg;  // [P][B][H][dk][dv]
+  float* dHout; // [P][B][H][dk][dv]
+  float* dqp;   // [B][Tp][H][dk]    per-V-head gradient of q_hat
+  float* dkp;   // [B][Tp][H][dk]    per-V-head gradient of k_hat
+};
+
+// Raw inputs of a call (device pointers; type of q..dO is Prob::dtype).
+struct Inputs {
+  const void *q, *k, *v, *a, *b;
+  const float *A_log, *dt_bias;
+  const int32_t* valid_len;
+  const void* dO;
+};
+
+gdn_status resolve(const gdn_problem* p, Prob* out);
+size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws);
+
+// ---- SIMT (fp32 CUDA-core) kernels; each returns the launch's cudaError_t ----
+cudaError_t launch_prep(const Prob& pr, const Inputs& in, const WS& ws, bool need_q,
+                        bool need_T, cudaStream_t st);
+// mode 0: forward states (writes Hc/Vn when non-null, final state of the last
+// segment to `final_out`); mode 1: summary of [M|S] (writes M/S per segment).
+cudaError_t launch_state_scan(const Prob& pr, const WS& ws, int mode, int seg_first, int nseg,
+                              const float* init, int64_t init_seg_stride, float* Hc, float* Vn,
+                              float* final_out, float* M_out, float* S_out,
+                              int64_t out_seg_stride, cudaStream_t st);
+cudaError_t launch_output(const Prob& pr, const Inputs& in, const WS& ws, void* o,
+                          cudaStream_t st);
+// mode 0: store dHc/dVn, start gradient of segment 0 to `start_out`;
+// mode 1: gradient summary from zero, start gradient of every segment to D_out[seg].
+cudaError_t launch_dstate_scan(const Prob& pr, const Inputs& in, const WS& ws, int mode,
+                               int seg_first, int nseg, const float* init,
+                               int64_t init_seg_stride, float* start_out, float* D_out,
+                               int64_t out_seg_stride, cudaStream_t st);
+cudaError_t launch_grad(const Prob& pr, const Inputs& in, const WS& ws, void* dv, float* dg,
+                        float* dbeta, cudaStream_t st);
+cudaError_t launch_qk_grad(const Prob& pr, const Inputs& in, const WS& ws, void* dq, void* dk,
+                           cudaStream_t st);
+cudaError_t launch_compose(int64_t n, int64_t dk, int64_t dv, const float* M2, const float* S2,
+                           const float* M1, const float* S1, float* M, float* S,
+                           cudaStream_t st);
+// Hin[s] for s < P; applies map s only when s < P-1 or Hout != null.
+cudaError_t launch_prefix(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
+                          const float* S, const float* h0, float* Hin, float* Hout,
+                          cudaStream_t st);
+// dHout[s] for s >= 0 in reverse; applies M[s]^T . + D[s] only when s > 0 or dH0 != null.
+cudaError_t launch_prefix_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
+                              const float* D, const float* dHT, float* dHout, float* dH0,
+                              cudaStream_t st);
+
+}  // namespace gdn

@@ -1,0 +1,259 @@
+/*
+ * gdn.h -- C ABI of the GB300 Gated DeltaNet (GDN) core library.
+ *
+ * The operator is the gated delta rule of Qwen3.5's linear-attention layers,
+ * per batch row b and value head h, with state S in R^{dk x dv}:
+ *
+ *   q_hat = scale * q / sqrt(|q|^2 + eps),  k_hat = k / sqrt(|k|^2 + eps)
+ *   g_t   = -exp(A_log[h]) * softplus(a_t + dt_bias[h]),  alpha_t = exp(g_t)
+ *   beta_t = sigmoid(b_t)
+ *   S_t   = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *   o_t   = S_t^T q_t
+ *
+ * evaluated in chunks of 64 tokens.  Interface and conventions follow the pages:
+ *  - "Linear Attention CP 融合算子 PR #1114 测试报告", section 4.1: the core takes
+ *    q, k, v, g, beta and an initial state, returns the token output and the
+ *    final state, and its backward returns dq, dk, dv, dg, dbeta, dH0; the 16
+ *    Q/K heads are copied by grouping onto the 32 V heads (V head h reads Q/K
+ *    head h / (H/Hqk)).
+ *  - same report, section 3.1: fail fast, with no silent fallback, when the
+ *    fast path cannot take a shape (head_dim != 128 or chunk_size != 64).
+ *  - same report, section 5.2: trailing padding (B=2, valid_length=7777) gives
+ *    zero output for padded tokens and leaves the state unchanged.
+ *  - "linear attention cp #1035", section "What does this PR do": each rank
+ *    summarises its segment as the affine map H_out = M @ H_in + S ("p2p"),
+ *    the summaries of earlier ranks are merged into the initial state
+ *    ("all_gather"), and the state gradient travels back the reverse way.
+ *    Here the segments live on one GPU.
+ *
+ * Conventions for every call
+ *  - Layout is token-major and contiguous: q, k [B, T_stride, Hqk, dk];
+ *    v, o, dO, dv [B, T_stride, H, dv]; a, b, dg, dbeta [B, T_stride, H];
+ *    only tokens [0, T) of each row are read or written.  States h0, hT, dHT,
+ *    dH0, S, D, H_in [B, H, dk, dv] and M [B, H, dk, dk] are fp32 row-major.
+ *    A_log and dt_bias are fp32 [H].  valid_len is int32 [B] or NULL.
+ *  - Every pointer except the host `gdn_problem*` and `bytes*` arguments is a
+ *    DEVICE pointer, 16-byte aligned, on the current device.  The caller owns all
+ *    memory, including the workspace.  The library never allocates, frees or
+ *    synchronises (gdn_check_device_status is the one synchronous call); every
+ *    launch is ordered on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream).  Outputs must not alias inputs.  The library keeps no global state.
+ *  - Host-side validation runs before any launch and returns a status; nothing
+ *    is launched unless it returns GDN_OK.  Errors raised by CUDA while
+ *    launching come back as GDN_ERR_CUDA.  Faults found by a kernel (a
+ *    valid_len outside [0, T], an exhausted bounded wait) are recorded in the
+ *    workspace's status word, read by gdn_check_device_status.
+ *  - Results are deterministic run to run for a fixed problem and segment count.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad shape, H % Hqk != 0, ... */
+  GDN_ERR_UNSUPPORTED = 2,    /* valid problem the library does not take (chunk != 64, ...) */
+  GDN_ERR_WORKSPACE = 3,      /* workspace missing or smaller than gdn_workspace_size */
+  GDN_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+  GDN_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up a bounded wait (device status word) */
+} gdn_status;
+
+typedef enum gdn_dtype {
+  GDN_FP32 = 0,  /* fp32 I/O, fp32 arithmetic on CUDA cores; any dk, dv in {16..128}/16 */
+  GDN_BF16 = 1   /* bf16 I/O, fp32 accumulation; dk = dv = 128 */
+} gdn_dtype;
+
+typedef enum gdn_op {
+  GDN_OP_FWD = 0,         /* gdn_fwd, gdn_apply_state */
+  GDN_OP_BWD = 1,         /* gdn_bwd, gdn_apply_state_bwd */
+  GDN_OP_SUMMARY = 2,     /* gdn_summary */
+  GDN_OP_SUMMARY_BWD = 3  /* gdn_summary_bwd */
+} gdn_op;
+
+/* Problem description.  Fill with gdn_problem_init, then set the sizes. */
+typedef struct gdn_problem {
+  int32_t dtype;     /* gdn_dtype of q, k, v, a, b, o, dO, dq, dk, dv */
+  int32_t chunk;     /* chunk length; must be 64 */
+  int64_t B;         /* batch rows, >= 0 */
+  int64_t T;         /* tokens per row handled by this call, >= 0 */
+  int64_t T_stride;  /* tokens between consecutive rows in memory; 0 means T (must be >= T) */
+  int64_t Hqk;       /* query/key heads, >= 1 */
+  int64_t H;         /* value heads, a multiple of Hqk */
+  int64_t dk;        /* key/query head dim */
+  int64_t dv;        /* value head dim */
+  int32_t l2norm_qk; /* 1: L2-normalise q and k inside (default); 0: use them as given */
+  float l2_eps;      /* eps inside the norm, x / sqrt(|x|^2 + eps); default 1e-6 */
+  float scale;       /* scale applied to q after the norm; <= 0 means 1/sqrt(dk) */
+  int32_t segments;  /* sequence segments the call splits T into (time parallelism);
+                        0 = automatic, else 1..ceil(T/64).  Results agree across
+                        segment counts to rounding. */
+} gdn_problem;
+
+/* Human-readable name of a status. Never NULL. */
+const char* gdn_status_string(gdn_status status);
+
+/* GDN_ABI_VERSION of the loaded library. */
+int32_t gdn_abi_version(void);
+
+/* Defaults: dtype BF16, chunk 64, l2norm on, eps 1e-6, scale 1/sqrt(dk), segments auto,
+   all sizes 0.  Does nothing if p is NULL. */
+void gdn_problem_init(gdn_problem* p);
+
+/*
+ * Capability check ("is the problem supported?") without side effects:
+ * GDN_OK, GDN_ERR_INVALID_ARG (malformed: negative sizes, H % Hqk != 0,
+ * T_stride < T, eps < 0, segments out of range) or GDN_ERR_UNSUPPORTED
+ * (well formed but not taken: chunk != 64, dk or dv not a multiple of 16 in
+ * [16, 128], bf16 with dk or dv != 128).  Mirrors the fail-fast capability check
+ * of the test report, section 3.1.
+ */
+gdn_status gdn_query_support(const gdn_problem* p);
+
+/* Workspace bytes needed by `op` for problem p on the current device (writes *bytes).
+   Always at least 256 (the device status word lives there). */
+gdn_status gdn_workspace_size(const gdn_problem* p, int32_t op, size_t* bytes);
+
+/*
+ * Forward.  o = token outputs [B,T,H,dv] in p->dtype (zero for t >= valid_len[b]);
+ * hT (nullable) = state after the last valid token [B,H,dk,dv] fp32.
+ * h0 (nullable: zero initial state) [B,H,dk,dv] fp32.
+ * Internally the sequence may be split into segments whose summaries are
+ * composed on the device (the pages' p2p/all_gather algebra on one GPU).
+ */
+gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                   const void* a, const void* b, const float* A_log, const float* dt_bias,
+                   const float* h0, const int32_t* valid_len, void* o, float* hT,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward of L = sum_t <dO_t, o_t> + <dHT, hT> w.r.t. the forward inputs.
+ * Takes the forward inputs again and recomputes the chunk intermediates (no
+ * saved context).  dO [B,T,H,dv] p->dtype (values at padded tokens are ignored);
+ * dHT nullable (zero).  Writes dq, dk [B,T,Hqk,dk] and dv [B,T,H,dv] in
+ * p->dtype (w.r.t. the raw q, k before the norm and scale, summed over the V
+ * heads sharing a Q/K head); dg, dbeta [B,T,H] fp32 (w.r.t. g_t and beta_t);
+ * dH0 [B,H,dk,dv] fp32 (nullable).  Padded tokens get zero gradients.
+ */
+gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                   const void* a, const void* b, const float* A_log, const float* dt_bias,
+                   const float* h0, const int32_t* valid_len, const void* dO, const float* dHT,
+                   void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dH0,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Segment summary (PR #1035, "p2p": H_out = M @ H_in + S for the local
+ * segment).  The segment is tokens [0, T) of the given rows (pass pointers to
+ * the segment's first token and T_stride = the full row length).
+ * M [B,H,dk,dk] = A_T ... A_1 with A_t = alpha_t (I - beta_t k_t k_t^T);
+ * S [B,H,dk,dv] = state reached from zero.
+ */
+gdn_status gdn_summary(const gdn_problem* p, const void* k, const void* v, const void* a,
+                       const void* b, const float* A_log, const float* dt_bias,
+                       const int32_t* valid_len, float* M, float* S, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * Gradient summary of a segment: D = d(sum_t <dO_t, o_t>)/dH_in [B,H,dk,dv].
+ * Together with M it is the segment's backward affine map dH_in = M^T dH_out + D
+ * (the reverse-direction state-gradient pass of PR #1035).  Independent of v and
+ * of H_in.
+ */
+gdn_status gdn_summary_bwd(const gdn_problem* p, const void* q, const void* k, const void* a,
+                           const void* b, const float* A_log, const float* dt_bias,
+                           const int32_t* valid_len, const void* dO, float* D,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* (M, S) = (M2 M1, M2 S1 + S2) for n independent maps: M* [n,dk,dk], S* [n,dk,dv]. */
+gdn_status gdn_compose(int64_t n, int64_t dk, int64_t dv, const float* M2, const float* S2,
+                       const float* M1, const float* S1, float* M, float* S, void* stream);
+
+/*
+ * Exclusive prefix over P segments (PR #1035, "all_gather": merge the summaries
+ * of earlier ranks into the initial state): M [P,n,dk,dk], S [P,n,dk,dv],
+ * h0 [n,dk,dv] nullable (zero).  H_in[0] = h0, H_in[i] = M[i-1] H_in[i-1] + S[i-1]
+ * into Hin [P,n,dk,dv]; Hout (nullable) [n,dk,dv] = M[P-1] H_in[P-1] + S[P-1].
+ */
+gdn_status gdn_prefix_compose(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
+                              const float* S, const float* h0, float* Hin, float* Hout,
+                              void* stream);
+
+/*
+ * Reverse exclusive prefix of state gradients: dHT [n,dk,dv] nullable (zero).
+ * dH_out[P-1] = dHT, dH_out[i] = M[i+1]^T dH_out[i+1] + D[i+1] into dHout
+ * [P,n,dk,dv]; dH0 (nullable) [n,dk,dv] = M[0]^T dH_out[0] + D[0].
+ */
+gdn_status gdn_prefix_compose_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
+                                  const float* D, const float* dHT, float* dHout, float* dH0,
+                                  void* stream);
+
+/*
+ * State apply (PR #1035, "p2p": once the initial state arrives, compute the
+ * segment's token output): the forward of a segment from Hin [B,H,dk,dv]
+ * (required).  Same as gdn_fwd with h0 = Hin; hT nullable.
+ */
+gdn_status gdn_apply_state(const gdn_problem* p, const void* q, const void* k, const void* v,
+                           const void* a, const void* b, const float* A_log,
+                           const float* dt_bias, const float* Hin, const int32_t* valid_len,
+                           void* o, float* hT, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * Backward of a segment started from Hin, given the gradient dHout of its end
+ * state (nullable: zero): gdn_bwd with h0 = Hin, dHT = dHout; dHin (nullable)
+ * receives the gradient of its initial state.
+ */
+gdn_status gdn_apply_state_bwd(const gdn_problem* p, const void* q, const void* k,
+                               const void* v, const void* a, const void* b, const float* A_log,
+                               const float* dt_bias, const float* Hin,
+                               const int32_t* valid_len, const void* dO, const float* dHout,
+                               void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                               float* dHin, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
+ * Profiling aid (no counterpart on the pages): gdn_fwd and gdn_bwd are a short
+ * sequence of kernel launches.  gdn_kernel_info gives, for `op` (GDN_OP_FWD or
+ * GDN_OP_BWD) and problem p, the number of launches (*count, nullable) and the
+ * name of launch `index` (*name, nullable; a static string).  gdn_fwd_kernel /
+ * gdn_bwd_kernel take the arguments of gdn_fwd / gdn_bwd plus `index` and
+ * launch only that kernel, so that a caller can time it alone with CUDA events.
+ * They read the intermediates that the earlier kernels of the full call left in
+ * the workspace: call the full gdn_fwd / gdn_bwd with the same arguments and
+ * workspace first.  Results of the full call are unchanged by re-running a
+ * kernel (every launch rewrites what it writes).
+ */
+gdn_status gdn_kernel_info(const gdn_problem* p, int32_t op, int32_t index, int32_t* count,
+                           const char** name);
+gdn_status gdn_fwd_kernel(const gdn_problem* p, int32_t index, const void* q, const void* k,
+                          const void* v, const void* a, const void* b, const float* A_log,
+                          const float* dt_bias, const float* h0, const int32_t* valid_len,
+                          void* o, float* hT, void* workspace, size_t workspace_bytes,
+                          void* stream);
+gdn_status gdn_bwd_kernel(const gdn_problem* p, int32_t index, const void* q, const void* k,
+                          const void* v, const void* a, const void* b, const float* A_log,
+                          const float* dt_bias, const float* h0, const int32_t* valid_len,
+                          const void* dO, const float* dHT, void* dq, void* dk, void* dv,
+                          float* dg, float* dbeta, float* dH0, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, reads the device status word of `workspace` (written by
+ * earlier calls that used it), clears it and returns GDN_OK,
+ * GDN_ERR_INVALID_ARG (a kernel clamped a valid_len outside [0, T]),
+ * GDN_ERR_DEVICE_TIMEOUT (a bounded wait ran out) or GDN_ERR_CUDA.
+ */
+gdn_status gdn_check_device_status(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,155 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every symbol
+include/gdn.h declares, and host-side validation returns the documented status
+before any launch (no GPU needed: these calls never reach CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_state_scan_gated_gb300 as gdn
+from chunked_state_scan_gated_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdn.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|gdn_status|int32_t|void|size_t)\s+"
+                                 r"(gdn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("gdn_fwd", "gdn_bwd", "gdn_summary", "gdn_summary_bwd", "gdn_compose",
+                 "gdn_prefix_compose", "gdn_prefix_compose_bwd", "gdn_apply_state",
+                 "gdn_apply_state_bwd", "gdn_query_support", "gdn_workspace_size"):
+        assert must in names
+    assert set(names) == set(gdn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.gdn_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["GDN_OK", "GDN_ERR_INVALID_ARG", "GDN_ERR_UNSUPPORTED",
+                                 "GDN_ERR_WORKSPACE", "GDN_ERR_CUDA", "GDN_ERR_DEVICE_TIMEOUT"]):
+        assert gdn.status_string(code) == name
+
+
+def problem(**kw):
+    p = gdn.Problem()
+    gdn.load_library().gdn_problem_init(ctypes.byref(p))
+    p.B, p.T, p.Hqk, p.H, p.dk, p.dv = 1, 8192, 16, 32, 128, 128
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_problem_defaults(lib):
+    p = problem()
+    assert p.dtype == gdn.GDN_BF16 and p.chunk == 64 and p.l2norm_qk == 1
+    assert abs(p.l2_eps - 1e-6) < 1e-12 and p.scale == 0 and p.segments == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, gdn.GDN_OK),
+    ({"chunk": 32}, gdn.GDN_ERR_UNSUPPORTED),                    # fail fast: chunk != 64
+    ({"dk": 64}, gdn.GDN_ERR_UNSUPPORTED),                       # bf16 needs head dim 128
+    ({"dtype": gdn.GDN_FP32, "dk": 64, "dv": 32}, gdn.GDN_OK),   # fp32 path takes it
+    ({"dtype": gdn.GDN_FP32, "dk": 24}, gdn.GDN_ERR_UNSUPPORTED),
+    ({"dtype": gdn.GDN_FP32, "dk": 256}, gdn.GDN_ERR_UNSUPPORTED),
+    ({"H": 24}, gdn.GDN_ERR_INVALID_ARG),                        # H % Hqk != 0
+    ({"Hqk": 0}, gdn.GDN_ERR_INVALID_ARG),
+    ({"T": -1}, gdn.GDN_ERR_INVALID_ARG),
+    ({"T_stride": 100}, gdn.GDN_ERR_INVALID_ARG),                # stride < T
+    ({"T_stride": 9000}, gdn.GDN_OK),
+    ({"segments": 129}, gdn.GDN_ERR_INVALID_ARG),                # more segments than chunks
+    ({"segments": 128}, gdn.GDN_OK),
+    ({"l2_eps": -1.0}, gdn.GDN_ERR_INVALID_ARG),
+    ({"dtype": 7}, gdn.GDN_ERR_INVALID_ARG),
+    ({"T": 0}, gdn.GDN_OK),
+    ({"B": 0}, gdn.GDN_OK),
+])
+def test_query_support(lib, kw, status):
+    assert gdn.gdn_query_support(problem(**kw)) == status
+
+
+def test_workspace_size(lib):
+    p = problem()
+    sizes = [gdn.gdn_workspace_size(p, op) for op in range(4)]
+    assert all(s >= 256 for s in sizes)
+    assert sizes[gdn.GDN_OP_BWD] > sizes[gdn.GDN_OP_FWD]
+    n = ctypes.c_size_t(0)
+    assert lib.gdn_workspace_size(ctypes.byref(p), 9, ctypes.byref(n)) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_workspace_size(ctypes.byref(p), 0, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+A = 1 << 20      # a 16-byte aligned stand-in address; validation fails before any use
+
+
+def fwd_args(**over):
+    args = dict(q=A, k=A, v=A, a=A, b=A, A_log=A, dt_bias=A, h0=None, valid_len=None, o=A,
+                hT=None, ws=A, ws_bytes=1 << 40)
+    args.update(over)
+    return args
+
+
+def call_fwd(lib, p, args):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return lib.gdn_fwd(ctypes.byref(p), vp(args["q"]), vp(args["k"]), vp(args["v"]),
+                       vp(args["a"]), vp(args["b"]), vp(args["A_log"]), vp(args["dt_bias"]),
+                       vp(args["h0"]), vp(args["valid_len"]), vp(args["o"]), vp(args["hT"]),
+                       vp(args["ws"]), args["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    ({"q": None}, gdn.GDN_ERR_INVALID_ARG),
+    ({"o": None}, gdn.GDN_ERR_INVALID_ARG),
+    ({"k": A + 2}, gdn.GDN_ERR_INVALID_ARG),          # misaligned
+    ({"h0": A + 8}, gdn.GDN_ERR_INVALID_ARG),
+    ({"ws": None}, gdn.GDN_ERR_WORKSPACE),
+    ({"ws_bytes": 1024}, gdn.GDN_ERR_WORKSPACE),
+    ({"ws": A + 16}, gdn.GDN_ERR_INVALID_ARG),        # workspace must be 256-byte aligned
+])
+def test_fwd_validation_fails_before_launch(lib, over, status):
+    assert call_fwd(lib, problem(), fwd_args(**over)) == status
+
+
+def test_unsupported_shape_is_refused_before_pointers(lib):
+    assert call_fwd(lib, problem(chunk=128), fwd_args()) == gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_bwd_and_summary_validation(lib):
+    p = problem()
+    vp = ctypes.c_void_p
+    base = [vp(A)] * 7 + [None, None, vp(A), None]       # ..., h0, valid_len, dO, dHT
+    outs_bad = [None] + [vp(A)] * 4 + [None]
+    assert lib.gdn_bwd(ctypes.byref(p), *base, *outs_bad, vp(A), 1 << 40,
+                       None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_summary(ctypes.byref(p), vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), None,
+                           None, vp(A), vp(A), 1 << 40, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_apply_state(ctypes.byref(p), *[vp(A)] * 7, None, None, vp(A), None, vp(A),
+                               1 << 40, None) == gdn.GDN_ERR_INVALID_ARG     # Hin required
+
+
+def test_compose_prefix_validation(lib):
+    vp = ctypes.c_void_p
+    assert lib.gdn_compose(-1, 4, 4, *[vp(A)] * 6, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_compose(2, 256, 4, *[vp(A)] * 6, None) == gdn.GDN_ERR_UNSUPPORTED
+    assert lib.gdn_compose(2, 4, 4, None, *[vp(A)] * 5, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_prefix_compose(2, 0, 4, 4, vp(A), vp(A), None, vp(A), None,
+                                  None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_prefix_compose_bwd(2, 3, 4, 4, vp(A), vp(A + 4), None, vp(A), None,
+                                      None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_check_device_status(None, None) == gdn.GDN_ERR_INVALID_ARG
