@@ -103,7 +103,7 @@ size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws) {
   w.status = (int*)take(64);
   w.Qh = take(B * Hqk * Tp * dk);
   w.Kh = take(B * Hqk * Tp * dk);
-  w.G = take(B * H * Tp);
+  w.G = (double*)take(2 * B * H * Tp);
   w.Bt = take(B * H * Tp);
   w.W = take(B * H * Tp * dk);
   w.U = take(B * H * Tp * dv);

@@ -31,7 +31,7 @@ struct WS {
   int* status;  // device status word
   float* Qh;    // [B][Hqk][Tp][dk]  normalised, scaled q
   float* Kh;    // [B][Hqk][Tp][dk]  normalised k
-  float* G;     // [B][H][Tp]        cumulative gate inside each chunk
+  double* G;    // [B][H][Tp]        cumulative gate inside each chunk (fp64, see gdn_simt.cu)
   float* Bt;    // [B][H][Tp]        beta
   float* W;     // [B][H][Tp][dk]    T diag(beta*gamma) K
   float* U;     // [B][H][Tp][dv]    T diag(beta) V

@@ -17,6 +17,10 @@
 // segment summary [M | S] and its composition come from "linear attention cp
 // #1035", section "What does this PR do" (p2p / all_gather modes).
 //
+// The cumulative gate G is kept in fp64: with the default gate distribution it
+// reaches about -500 inside a chunk, and fp32 differences G_i - G_j would carry
+// ~3e-5 absolute error into every decay factor exp(G_i - G_j).
+//
 // Work is split into: a chunk-parallel prologue (norms, gates, T, W, U), a
 // sequential state pass per (V head, column slice, segment), a chunk-parallel
 // output pass, a reverse state-gradient pass and a chunk-parallel gradient pass.
@@ -104,14 +108,14 @@ __device__ void blk_gemm(int m, int n, int kk, float alpha, const float* __restr
 }
 
 // Inclusive prefix sum of x[0..63] in place, by warp 0.
-__device__ void cumsum64(float* x) {
+__device__ void cumsum64(double* x) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    float v0 = x[lane], v1 = x[lane + 32];
+    double v0 = x[lane], v1 = x[lane + 32];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      float y0 = __shfl_up_sync(0xffffffffu, v0, o);
-      float y1 = __shfl_up_sync(0xffffffffu, v1, o);
+      double y0 = __shfl_up_sync(0xffffffffu, v0, o);
+      double y1 = __shfl_up_sync(0xffffffffu, v1, o);
       if (lane >= o) {
         v0 += y0;
         v1 += y1;
@@ -144,6 +148,9 @@ __device__ void revsum64(float* x) {
   }
 }
 
+// exp(Ga - Gb) from fp64 cumulative gates (the difference is taken in fp64).
+__device__ __forceinline__ float dexp(double ga, double gb) { return expf((float)(ga - gb)); }
+
 struct KArgs {
   int64_t B, T, Ts, Hqk, H, dk, dv, r, NC, Tp, CPS;
   int P, l2norm;
@@ -169,16 +176,17 @@ __global__ void __launch_bounds__(NT) k_prep(KArgs ka, const TIn* __restrict__ q
                                             const float* __restrict__ dt_bias,
                                             const int32_t* __restrict__ valid_len, WS ws,
                                             int need_q, int need_T) {
-  extern __shared__ float sm[];
+  extern __shared__ double smd[];
   const int dk = (int)ka.dk, dv = (int)ka.dv;
   const int LK = dk + 1, LV = dv + 1;
+  double* gG = smd;                     // [64] cumulative gate (fp64)
+  float* sm = (float*)(smd + 64);
   float* Ks = sm;               // [64][LK]
   float* Vs = Ks + 64 * LK;     // [64][LV]
   float* As = Vs + 64 * LV;     // [64][LS]
   float* Tms = As + 64 * LS;    // [64][LS]
   float* T2 = Tms + 64 * LS;    // [64][LS]
-  float* gG = T2 + 64 * LS;     // [64]
-  float* gB = gG + 64;          // [64]
+  float* gB = T2 + 64 * LS;     // [64]
   const int64_t c = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
   const int64_t t0 = c * kChunk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(NT) k_prep(KArgs ka, const TIn* __restrict__ q
         g = -expf(A_log[h]) * sp;
         be = 1.f / (1.f + expf(-ldf(bb, gi)));
       }
-      gG[tid] = g;
+      gG[tid] = (double)g;
       gB[tid] = be;
     }
     __syncthreads();
@@ -244,7 +252,7 @@ __global__ void __launch_bounds__(NT) k_prep(KArgs ka, const TIn* __restrict__ q
     __syncthreads();
     for (int e = tid; e < kChunk * kChunk; e += NT) {
       const int i = e >> 6, j = e & 63;
-      As[i * LS + j] = (i > j) ? gB[i] * As[i * LS + j] * expf(gG[i] - gG[j]) : 0.f;
+      As[i * LS + j] = (i > j) ? gB[i] * As[i * LS + j] * dexp(gG[i], gG[j]) : 0.f;
     }
     __syncthreads();
     // T = (I + A)^-1 by forward substitution, one column per thread
@@ -268,7 +276,7 @@ __global__ void __launch_bounds__(NT) k_prep(KArgs ka, const TIn* __restrict__ q
     // W = T diag(beta gamma) K
     for (int e = tid; e < kChunk * kChunk; e += NT) {
       const int i = e >> 6, j = e & 63;
-      T2[i * LS + j] = Tms[i * LS + j] * gB[j] * expf(gG[j]);
+      T2[i * LS + j] = Tms[i * LS + j] * gB[j] * dexp(gG[j], 0.0);
     }
     __syncthreads();
     blk_gemm(kChunk, dk, kChunk, 1.f, T2, LS, 1, Ks, LK, 1, false, ws.W + (bh * ka.Tp + t0) * dk,
@@ -300,17 +308,18 @@ __global__ void __launch_bounds__(NT) k_state_scan(KArgs ka, WS ws, int mode, in
                                                   int64_t init_seg_stride, float* Hc, float* Vn,
                                                   float* final_out, float* M_out, float* S_out,
                                                   int64_t out_seg_stride) {
-  extern __shared__ float sm[];
+  extern __shared__ double smd[];
   const int dk = (int)ka.dk, dv = (int)ka.dv;
   const int LK = dk + 1;
   const int width = mode == 1 ? dk + dv : dv;
+  double* gG = smd;               // [64]
+  float* sm = (float*)(smd + 64);
   float* Xs = sm;                 // [dk][CS]
   float* Ws = Xs + dk * CS;       // [64][LK]
   float* Ks = Ws + 64 * LK;       // [64][LK]
   float* Vp = Ks + 64 * LK;       // [64][CS]
   float* V2 = Vp + 64 * CS;       // [64][CS]
-  float* gG = V2 + 64 * CS;       // [64]
-  float* kt = gG + 64;            // [64]
+  float* kt = V2 + 64 * CS;       // [64]
   const int tid = threadIdx.x;
   const int c0 = blockIdx.x * CS;
   const int64_t h = blockIdx.y;
@@ -362,7 +371,7 @@ __global__ void __launch_bounds__(NT) k_state_scan(KArgs ka, WS ws, int mode, in
     __syncthreads();
     // V' = U - W X
     blk_gemm(kChunk, CS, dk, -1.f, Ws, LK, 1, Xs, CS, 1, true, Vp, CS, 1);
-    if (tid < 64) kt[tid] = expf(gG[63] - gG[tid]);
+    if (tid < 64) kt[tid] = dexp(gG[63], gG[tid]);
     __syncthreads();
     if (mode == 0 && Vn) {
       for (int e = tid; e < 64 * CS; e += NT) {
@@ -370,7 +379,7 @@ __global__ void __launch_bounds__(NT) k_state_scan(KArgs ka, WS ws, int mode, in
         if (col < dv) Vn[(bh * ka.Tp + t0 + i) * dv + col] = Vp[e];
       }
     }
-    const float gC = expf(gG[63]);
+    const float gC = dexp(gG[63], 0.0);
     for (int e = tid; e < 64 * CS; e += NT) V2[e] = kt[e / CS] * Vp[e];
     for (int e = tid; e < dk * CS; e += NT) Xs[e] *= gC;
     __syncthreads();
@@ -399,17 +408,18 @@ __global__ void __launch_bounds__(NT) k_state_scan(KArgs ka, WS ws, int mode, in
 template <typename TIn>
 __global__ void __launch_bounds__(NT) k_output(KArgs ka, WS ws, const int32_t* __restrict__ valid_len,
                                               TIn* __restrict__ o) {
-  extern __shared__ float sm[];
+  extern __shared__ double smd[];
   const int dk = (int)ka.dk, dv = (int)ka.dv;
   const int LK = dk + 1;
   const int nsl = (dv + CSO - 1) / CSO;
+  double* gG = smd;             // [64]
+  float* sm = (float*)(smd + 64);
   float* Qs = sm;               // [64][LK]
   float* Ks = Qs + 64 * LK;     // [64][LK]
   float* Ps = Ks + 64 * LK;     // [64][LS]
   float* Hs = Ps + 64 * LS;     // [dk][CSO]
   float* Vp = Hs + dk * CSO;    // [64][CSO]
   float* Os = Vp + 64 * CSO;    // [64][CSO]
-  float* gG = Os + 64 * CSO;    // [64]
   const int tid = threadIdx.x;
   const int64_t c = blockIdx.x, b = blockIdx.z;
   const int64_t h = blockIdx.y / nsl;
@@ -441,9 +451,9 @@ __global__ void __launch_bounds__(NT) k_output(KArgs ka, WS ws, const int32_t* _
   __syncthreads();
   for (int e = tid; e < 64 * 64; e += NT) {
     const int i = e >> 6, j = e & 63;
-    Ps[i * LS + j] = i >= j ? Ps[i * LS + j] * expf(gG[i] - gG[j]) : 0.f;
+    Ps[i * LS + j] = i >= j ? Ps[i * LS + j] * dexp(gG[i], gG[j]) : 0.f;
   }
-  for (int e = tid; e < 64 * CSO; e += NT) Os[e] *= expf(gG[e / CSO]);
+  for (int e = tid; e < 64 * CSO; e += NT) Os[e] *= dexp(gG[e / CSO], 0.0);
   __syncthreads();
   blk_gemm(kChunk, CSO, kChunk, 1.f, Ps, LS, 1, Vp, CSO, 1, true, Os, CSO, 1);
   __syncthreads();
@@ -465,9 +475,11 @@ __global__ void __launch_bounds__(NT) k_dstate_scan(KArgs ka, WS ws, const int32
                                                    const float* __restrict__ init,
                                                    int64_t init_seg_stride, float* start_out,
                                                    float* D_out, int64_t out_seg_stride) {
-  extern __shared__ float sm[];
+  extern __shared__ double smd[];
   const int dk = (int)ka.dk, dv = (int)ka.dv;
   const int LK = dk + 1;
+  double* gG = smd;              // [64]
+  float* sm = (float*)(smd + 64);
   float* dXs = sm;               // [dk][CS]
   float* Qs = dXs + dk * CS;     // [64][LK]
   float* Ks = Qs + 64 * LK;      // [64][LK]
@@ -475,8 +487,7 @@ __global__ void __launch_bounds__(NT) k_dstate_scan(KArgs ka, WS ws, const int32
   float* Ps = Ws + 64 * LK;      // [64][LS]
   float* dOs = Ps + 64 * LS;     // [64][CS]
   float* dVp = dOs + 64 * CS;    // [64][CS]
-  float* gG = dVp + 64 * CS;     // [64]
-  float* kt = gG + 64;           // [64]
+  float* kt = dVp + 64 * CS;     // [64]
   const int tid = threadIdx.x;
   const int c0 = blockIdx.x * CS;
   const int64_t h = blockIdx.y;
@@ -522,11 +533,11 @@ __global__ void __launch_bounds__(NT) k_dstate_scan(KArgs ka, WS ws, const int32
     blk_gemm(kChunk, kChunk, dk, 1.f, Qs, LK, 1, Ks, 1, LK, false, Ps, LS, 1);
     // K dX (scaled by kt below)
     blk_gemm(kChunk, CS, dk, 1.f, Ks, LK, 1, dXs, CS, 1, false, dVp, CS, 1);
-    if (tid < 64) kt[tid] = expf(gG[63] - gG[tid]);
+    if (tid < 64) kt[tid] = dexp(gG[63], gG[tid]);
     __syncthreads();
     for (int e = tid; e < 64 * 64; e += NT) {
       const int i = e >> 6, j = e & 63;
-      Ps[i * LS + j] = i >= j ? Ps[i * LS + j] * expf(gG[i] - gG[j]) : 0.f;
+      Ps[i * LS + j] = i >= j ? Ps[i * LS + j] * dexp(gG[i], gG[j]) : 0.f;
     }
     for (int e = tid; e < 64 * CS; e += NT) dVp[e] *= kt[e / CS];
     __syncthreads();
@@ -539,9 +550,9 @@ __global__ void __launch_bounds__(NT) k_dstate_scan(KArgs ka, WS ws, const int32
         if (col < dv) ws.dVn[(bh * ka.Tp + t0 + i) * dv + col] = dVp[e];
       }
     }
-    const float gC = expf(gG[63]);
+    const float gC = dexp(gG[63], 0.0);
     for (int e = tid; e < dk * CS; e += NT) dXs[e] *= gC;
-    for (int e = tid; e < 64 * CS; e += NT) dOs[e] *= expf(gG[e / CS]);
+    for (int e = tid; e < 64 * CS; e += NT) dOs[e] *= dexp(gG[e / CS], 0.0);
     __syncthreads();
     blk_gemm(dk, CS, kChunk, 1.f, Qs, 1, LK, dOs, CS, 1, true, dXs, CS, 1);
     __syncthreads();
@@ -569,10 +580,12 @@ __global__ void __launch_bounds__(NT) k_grad(KArgs ka, WS ws, const TIn* __restr
                                             const int32_t* __restrict__ valid_len,
                                             TIn* __restrict__ dv_out, float* __restrict__ dg_out,
                                             float* __restrict__ dbeta_out) {
-  extern __shared__ float sm[];
+  extern __shared__ double smd[];
   const int dk = (int)ka.dk, dv = (int)ka.dv;
   const int LK = dk + 1;
   const int LX = (dk > dv ? dk : dv) + 1;
+  double* gG = smd;            // [64] cumulative gate (fp64)
+  float* sm = (float*)(smd + 64);
   float* Qs = sm;              // [64][LX]  q_hat, later dKt, later dW
   float* Ks = Qs + 64 * LX;    // [64][LX]  k_hat
   float* X1 = Ks + 64 * LX;    // [64][LX]  dO, later dV'
@@ -581,8 +594,7 @@ __global__ void __launch_bounds__(NT) k_grad(KArgs ka, WS ws, const TIn* __restr
   float* Y1 = X3 + 64 * LX;    // [64][LS]  P, later dT, dA, E
   float* Y2 = Y1 + 64 * LS;    // [64][LS]  dP o Gamma, later Tt dT, K K^T
   float* Y3 = Y2 + 64 * LS;    // [64][LS]  T
-  float* gG = Y3 + 64 * LS;    // [64]
-  float* gB = gG + 64;         // [64]
+  float* gB = Y3 + 64 * LS;    // [64]
   float* gam = gB + 64;        // [64]
   float* kt = gam + 64;        // [64]
   float* dG = kt + 64;         // [64]
@@ -609,10 +621,10 @@ __global__ void __launch_bounds__(NT) k_grad(KArgs ka, WS ws, const TIn* __restr
     const float* Tg = ws.Tm + (bh * ka.NC + c) * (kChunk * kChunk);
     for (int e = tid; e < 64 * 64; e += NT) Y3[(e >> 6) * LS + (e & 63)] = Tg[e];
     if (tid < 64) {
-      const float g = ws.G[bh * ka.Tp + t0 + tid];
+      const double g = ws.G[bh * ka.Tp + t0 + tid];
       gG[tid] = g;
       gB[tid] = ws.Bt[bh * ka.Tp + t0 + tid];
-      gam[tid] = expf(g);
+      gam[tid] = dexp(g, 0.0);
       dG[tid] = 0.f;
       dbe[tid] = 0.f;
     }
@@ -625,14 +637,14 @@ __global__ void __launch_bounds__(NT) k_grad(KArgs ka, WS ws, const TIn* __restr
     }
   }
   __syncthreads();
-  if (tid < 64) kt[tid] = expf(gG[63] - gG[tid]);
+  if (tid < 64) kt[tid] = dexp(gG[63], gG[tid]);
   // 2. P = Q K^T (masked below); 4. dP = dO V'^T
   blk_gemm(kChunk, kChunk, dk, 1.f, Qs, LX, 1, Ks, 1, LX, false, Y1, LS, 1);
   blk_gemm(kChunk, kChunk, dv, 1.f, X1, LX, 1, X2, 1, LX, false, Y2, LS, 1);
   __syncthreads();
   for (int e = tid; e < 64 * 64; e += NT) {
     const int i = e >> 6, j = e & 63;
-    const float gm = i >= j ? expf(gG[i] - gG[j]) : 0.f;
+    const float gm = i >= j ? dexp(gG[i], gG[j]) : 0.f;
     Y1[i * LS + j] *= gm;   // P
     if (i < j) Y2[i * LS + j] = 0.f;
   }
@@ -647,7 +659,7 @@ __global__ void __launch_bounds__(NT) k_grad(KArgs ka, WS ws, const TIn* __restr
   __syncthreads();
   for (int e = tid; e < 64 * 64; e += NT) {
     const int i = e >> 6, j = e & 63;
-    if (i >= j) Y2[i * LS + j] *= expf(gG[i] - gG[j]);  // dP o Gamma
+    if (i >= j) Y2[i * LS + j] *= dexp(gG[i], gG[j]);  // dP o Gamma
   }
   // 6. dq_hat = diag(gamma) dO Hc^T + (dP o Gamma) K
   blk_gemm(kChunk, dk, dv, 1.f, X1, LX, 1, Hg, 1, dv, false, X3, LX, 1);
@@ -770,12 +782,12 @@ __global__ void __launch_bounds__(NT) k_grad(KArgs ka, WS ws, const TIn* __restr
     const int i = tid;
     float db = 0.f, row = 0.f, col = 0.f;
     for (int j = 0; j < i; ++j) {
-      const float kk = Y2[i * LS + j] * expf(gG[i] - gG[j]);   // (k_i.k_j) Gamma_ij
+      const float kk = Y2[i * LS + j] * dexp(gG[i], gG[j]);   // (k_i.k_j) Gamma_ij
       db += Y1[i * LS + j] * kk;
       row += Y1[i * LS + j] * gB[i] * kk;                        // dA_ij A_ij
     }
     for (int j = i + 1; j < 64; ++j) {
-      const float kk = Y2[j * LS + i] * expf(gG[j] - gG[i]);
+      const float kk = Y2[j * LS + i] * dexp(gG[j], gG[i]);
       col += Y1[j * LS + i] * gB[j] * kk;                        // dA_ji A_ji
     }
     dbe[i] += db;
@@ -784,7 +796,7 @@ __global__ void __launch_bounds__(NT) k_grad(KArgs ka, WS ws, const TIn* __restr
   __syncthreads();
   for (int e = tid; e < 64 * 64; e += NT) {
     const int i = e >> 6, j = e & 63;
-    Y1[i * LS + j] = i > j ? Y1[i * LS + j] * gB[i] * expf(gG[i] - gG[j]) : 0.f;  // E
+    Y1[i * LS + j] = i > j ? Y1[i * LS + j] * gB[i] * dexp(gG[i], gG[j]) : 0.f;  // E
   }
   __syncthreads();
   // 17. dk_hat += E K + E^T K
@@ -947,7 +959,7 @@ cudaError_t launch_prep(const Prob& pr, const Inputs& in, const WS& ws, bool nee
                         cudaStream_t st) {
   if (pr.B == 0 || pr.NC == 0) return cudaSuccess;
   const int LK = (int)pr.dk + 1, LV = (int)pr.dv + 1;
-  const size_t smem = sizeof(float) * (size_t)(64 * LK + 64 * LV + 3 * 64 * LS + 128);
+  const size_t smem = 64 * sizeof(double) + sizeof(float) * (size_t)(64 * LK + 64 * LV + 3 * 64 * LS + 64);
   dim3 grid((unsigned)pr.NC, (unsigned)pr.Hqk, (unsigned)pr.B);
   const KArgs ka = kargs(pr);
   cudaError_t e;
@@ -975,7 +987,7 @@ cudaError_t launch_state_scan(const Prob& pr, const WS& ws, int mode, int seg_fi
   if (pr.B == 0 || nseg <= 0) return cudaSuccess;
   const int width = mode == 1 ? (int)(pr.dk + pr.dv) : (int)pr.dv;
   const int LK = (int)pr.dk + 1;
-  const size_t smem = sizeof(float) * (size_t)(pr.dk * CS + 2 * 64 * LK + 2 * 64 * CS + 128);
+  const size_t smem = 64 * sizeof(double) + sizeof(float) * (size_t)(pr.dk * CS + 2 * 64 * LK + 2 * 64 * CS + 64);
   dim3 grid((unsigned)((width + CS - 1) / CS), (unsigned)pr.H, (unsigned)(pr.B * nseg));
   cudaError_t e;
   if ((e = set_smem(k_state_scan, smem)) != cudaSuccess) return e;
@@ -991,7 +1003,7 @@ cudaError_t launch_output(const Prob& pr, const Inputs& in, const WS& ws, void* 
   const int LK = (int)pr.dk + 1;
   const int nsl = (int)((pr.dv + CSO - 1) / CSO);
   const size_t smem =
-      sizeof(float) * (size_t)(2 * 64 * LK + 64 * LS + pr.dk * CSO + 2 * 64 * CSO + 64);
+      64 * sizeof(double) + sizeof(float) * (size_t)(2 * 64 * LK + 64 * LS + pr.dk * CSO + 2 * 64 * CSO);
   dim3 grid((unsigned)pr.NC, (unsigned)(pr.H * nsl), (unsigned)pr.B);
   cudaError_t e;
   if (pr.dtype == GDN_BF16) {
@@ -1013,7 +1025,7 @@ cudaError_t launch_dstate_scan(const Prob& pr, const Inputs& in, const WS& ws, i
   if (pr.B == 0 || nseg <= 0) return cudaSuccess;
   const int LK = (int)pr.dk + 1;
   const size_t smem =
-      sizeof(float) * (size_t)(pr.dk * CS + 3 * 64 * LK + 64 * LS + 2 * 64 * CS + 128);
+      64 * sizeof(double) + sizeof(float) * (size_t)(pr.dk * CS + 3 * 64 * LK + 64 * LS + 2 * 64 * CS + 64);
   dim3 grid((unsigned)((pr.dv + CS - 1) / CS), (unsigned)pr.H, (unsigned)(pr.B * nseg));
   cudaError_t e;
   if (pr.dtype == GDN_BF16) {
@@ -1036,7 +1048,8 @@ cudaError_t launch_grad(const Prob& pr, const Inputs& in, const WS& ws, void* dv
                         float* dbeta, cudaStream_t st) {
   if (pr.B == 0 || pr.NC == 0) return cudaSuccess;
   const int LX = (int)(pr.dk > pr.dv ? pr.dk : pr.dv) + 1;
-  const size_t smem = sizeof(float) * (size_t)(5 * 64 * LX + 3 * 64 * LS + 6 * 64 + NT / 32 + 8);
+  const size_t smem = 64 * sizeof(double) +
+                      sizeof(float) * (size_t)(5 * 64 * LX + 3 * 64 * LS + 5 * 64 + NT / 32 + 8);
   dim3 grid((unsigned)pr.NC, (unsigned)pr.H, (unsigned)pr.B);
   cudaError_t e;
   if (pr.dtype == GDN_BF16) {
