@@ -35,7 +35,7 @@ EXPORTS = (
     "gdn_workspace_size", "gdn_fwd", "gdn_bwd", "gdn_summary", "gdn_summary_bwd",
     "gdn_compose", "gdn_prefix_compose", "gdn_prefix_compose_bwd", "gdn_apply_state",
     "gdn_apply_state_bwd", "gdn_check_device_status", "gdn_kernel_info", "gdn_fwd_kernel",
-    "gdn_bwd_kernel",
+    "gdn_bwd_kernel", "gdn_fwd_noalloc",
 )
 
 
@@ -98,6 +98,7 @@ def load_library(path: str | None = None):
                                ctypes.c_int),
             "gdn_bwd_kernel": ([_PP, ctypes.c_int32] + [_VP] * 18 + [ctypes.c_size_t, _VP],
                                ctypes.c_int),
+            "gdn_fwd_noalloc": ([_PP] + [_VP] * 12, ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -195,6 +196,21 @@ def gdn_fwd(q, k, v, a, b, A_log, dt_bias, h0=None, valid_len=None, *, segments=
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
         _ptr(dt_bias), _ptr(h0), _ptr(valid_len), _ptr(o), _ptr(hT), _ptr(ws), ws.numel(),
         _stream(stream)))
+    return o, hT
+
+
+GDN_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def gdn_fwd_noalloc(q, k, v, a, b, A_log, dt_bias, h0=None, valid_len=None, *, o, hT=None,
+                    segments=0, l2norm=True, eps=1e-6, scale=0.0, stream=None, problem=None):
+    """Forward into caller-given outputs with no workspace: the library's static
+    device scratch (GDN_NOALLOC_SCRATCH_BYTES) is used instead.  For callers that
+    cannot allocate device memory; o (and hT if wanted) must be preallocated."""
+    p = problem or make_problem(q, v, segments=segments, l2norm=l2norm, eps=eps, scale=scale)
+    _check("gdn_fwd_noalloc", load_library().gdn_fwd_noalloc(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+        _ptr(dt_bias), _ptr(h0), _ptr(valid_len), _ptr(o), _ptr(hT), _stream(stream)))
     return o, hT
 
 

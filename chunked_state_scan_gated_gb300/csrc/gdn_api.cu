@@ -12,7 +12,15 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "gdn_internal.h"
+
+// Scratch of gdn_fwd_noalloc: one fixed array per device, reserved when the
+// library's device code is loaded and held until the process exits.  Host code
+// must never use this name as an address (on the host it is only a stand-in);
+// the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_gdn_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
 
 namespace gdn {
 namespace {
@@ -499,6 +507,42 @@ gdn_status gdn_prefix_compose_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, 
     return GDN_ERR_INVALID_ARG;
   return cuda_status(
       launch_prefix_bwd(n, P, dk, dv, M, D, dHT, dHout, dH0, (cudaStream_t)stream));
+}
+
+// Device address of g_gdn_noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+static gdn_status noalloc_scratch(void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_gdn_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return GDN_ERR_CUDA;
+    addr[dev] = ptr;
+  }
+  *out = addr[dev];
+  return GDN_OK;
+}
+
+gdn_status gdn_fwd_noalloc(const gdn_problem* p, const void* q, const void* k, const void* v,
+                           const void* a, const void* b, const float* A_log,
+                           const float* dt_bias, const float* h0, const int32_t* valid_len,
+                           void* o, float* hT, void* stream) {
+  Prob pr;
+  gdn_status s = resolve_op(p, GDN_OP_FWD, &pr);
+  if (s != GDN_OK) return s;
+  if (workspace_layout(pr, GDN_OP_FWD, nullptr, nullptr) > (size_t)GDN_NOALLOC_SCRATCH_BYTES)
+    return GDN_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != GDN_OK) return s;
+  Sched sc;
+  return fwd_impl(p, q, k, v, a, b, A_log, dt_bias, h0, valid_len, o, hT, scratch,
+                  (size_t)GDN_NOALLOC_SCRATCH_BYTES, stream, sc);
 }
 
 gdn_status gdn_check_device_status(void* workspace, void* stream) {

@@ -245,6 +245,33 @@ gdn_status gdn_bwd_kernel(const gdn_problem* p, int32_t index, const void* q, co
                           size_t workspace_bytes, void* stream);
 
 /*
+ * Forward without a caller-provided workspace (no counterpart on the pages).
+ * For callers that cannot allocate device memory or hand the library a buffer:
+ * code running while a stream is being captured into a CUDA graph (where a
+ * cudaMalloc would break the capture), operator plugins of inference runtimes
+ * that give an operator no workspace hook, or hosts whose allocator must not be
+ * entered from this call.  Same arguments and results as gdn_fwd, minus the
+ * workspace.  Scratch is one static device array of GDN_NOALLOC_SCRATCH_BYTES
+ * (64 MiB) that every GPU which loads the library reserves until the process
+ * exits; problems whose gdn_workspace_size(p, GDN_OP_FWD) exceeds it are
+ * rejected with GDN_ERR_UNSUPPORTED before any launch.  Nothing is allocated:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls on a device share the array, which
+ * keeps the last call's contents; each call clears the part that must start at
+ * zero (its status word) and overwrites the rest before reading it.  Calls that
+ * can run at the same time on one GPU (on different streams, or issued from
+ * host threads without an order between them) race on the array: the caller
+ * must order them.  gdn_check_device_status does not apply to this call.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+gdn_status gdn_fwd_noalloc(const gdn_problem* p, const void* q, const void* k, const void* v,
+                           const void* a, const void* b, const float* A_log,
+                           const float* dt_bias, const float* h0, const int32_t* valid_len,
+                           void* o, float* hT, void* stream);
+
+/*
  * Synchronises `stream`, reads the device status word of `workspace` (written by
  * earlier calls that used it), clears it and returns GDN_OK,
  * GDN_ERR_INVALID_ARG (a kernel clamped a valid_len outside [0, T]),
