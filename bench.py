@@ -120,6 +120,14 @@ def kernel_work(name, w, P):
         f = (2 * C * C * dk * 6 + 2 * C * C * dv * 2 + 2 * C * dk * dv * 3 + C * C * (dv + dk)
              + 4 * C ** 3)
         return "alu", f * ch, "flop"
+    if name == "apply_scan_tc":
+        # the whole forward of every chunk: F_fwd per token and V head
+        f_tok = 2 * C * (3 * dk + 2 * dv) + 6 * dk * dv + C * C / 3
+        return "tensor", f_tok * C * ch, "flop"
+    if name == "summary_scan_tc":
+        # per chunk of segments 0..P-2: K K^T, the solve, W, U, and the [M|S] state products
+        f = 2 * C * C * (2 * dk + dv) + C ** 3 / 3 + 4 * C * dk * (dk + dv)
+        return "tensor", f * ch * frac, "flop"
     if name == "qk_grad":
         r = H // Hqk
         byt = B * w.T * Hqk * dk * (2 * r * 4 + 2 * 2 + 2 * 2)

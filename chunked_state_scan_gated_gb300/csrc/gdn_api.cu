@@ -37,9 +37,10 @@ bool ok_ptr(const void* p, int64_t numel) {
 }
 bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
 
-int auto_segments(int64_t B, int64_t H, int64_t dv, int64_t NC) {
+int auto_segments(int64_t B, int64_t H, int64_t dv, int64_t NC, bool tensor_core) {
   if (NC <= 1) return 1;
-  const int64_t per_seg = B * H * ((dv + kScanCols - 1) / kScanCols);
+  // The tensor-core scan runs one CTA per (row, head, segment) and holds a whole SM.
+  const int64_t per_seg = tensor_core ? B * H : B * H * ((dv + kScanCols - 1) / kScanCols);
   int64_t want = (kTargetBlocks + per_seg - 1) / (per_seg > 0 ? per_seg : 1);
   int64_t P = 1;
   while (P < want) P <<= 1;
@@ -84,7 +85,8 @@ gdn_status resolve_op(const gdn_problem* p, int op, Prob* out) {
   r.Tp = r.NC * kChunk;
   const int64_t maxP = r.NC > 1 ? r.NC : 1;
   if (p->segments > maxP) return GDN_ERR_INVALID_ARG;
-  int P = p->segments > 0 ? p->segments : auto_segments(r.B, r.H, r.dv, r.NC);
+  const bool tcp = r.dtype == GDN_BF16 && r.dk == 128 && r.dv == 128 && r.B > 0 && r.NC > 0;
+  int P = p->segments > 0 ? p->segments : auto_segments(r.B, r.H, r.dv, r.NC, tcp);
   if (op == GDN_OP_SUMMARY || op == GDN_OP_SUMMARY_BWD) P = 1;
   r.CPS = r.NC > 0 ? (r.NC + P - 1) / P : 0;
   r.P = r.CPS > 0 ? (int)((r.NC + r.CPS - 1) / r.CPS) : 1;
@@ -109,6 +111,31 @@ size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws) {
   const bool bwd = op == GDN_OP_BWD;
   const bool fwd = op == GDN_OP_FWD;
   w.status = (int*)take(64);
+  if (tc_path(pr) && bwd) {
+    if (P > 1) {
+      w.Mseg = take(P * B * H * dk * dk);
+      w.Sseg = take(P * B * H * dk * dv);
+      w.Hin = take(P * B * H * dk * dv);
+      w.Dseg = take(P * B * H * dk * dv);
+      w.dHout = take(P * B * H * dk * dv);
+    }
+    w.hc16 = take(B * H * NC * dk * dv / 2);
+    w.dhc16 = take(B * H * NC * dk * dv / 2);
+    w.dqp = take(B * Tp * H * dk);
+    w.dkp = take(B * Tp * H * dk);
+    if (ws) *ws = w;
+    return off;
+  }
+  if (tc_path(pr) && (fwd || op == GDN_OP_SUMMARY)) {
+    // the tensor-core scan keeps every chunk intermediate on chip
+    if (fwd && P > 1) {
+      w.Mseg = take(P * B * H * dk * dk);
+      w.Sseg = take(P * B * H * dk * dv);
+      w.Hin = take(P * B * H * dk * dv);
+    }
+    if (ws) *ws = w;
+    return off;
+  }
   w.Qh = take(B * Hqk * Tp * dk);
   w.Kh = take(B * Hqk * Tp * dk);
   w.G = (double*)take(2 * B * H * Tp);
@@ -199,10 +226,26 @@ bool inputs_ok(const Prob& pr, const Inputs& in, bool need_q, bool need_v) {
 
 gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* o, float* hT,
                        const WS& ws, cudaStream_t st, Sched& sc) {
-  GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, false, st));
   const float* init = h0;
   int64_t init_stride = 0;
   const int64_t sstride = pr.B * pr.H * pr.dk * pr.dv;
+  if (tc_path(pr)) {
+    if (pr.P > 1) {
+      GDN_RUN(sc, "summary_scan_tc",
+              launch_chunk_scan_tc(pr, in, ws, 1, 0, pr.P - 1, nullptr, 0, nullptr, nullptr,
+                                   ws.Mseg, ws.Sseg, sstride, nullptr, st));
+      GDN_RUN(sc, "prefix",
+              launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Sseg, h0, ws.Hin,
+                            nullptr, st));
+      init = ws.Hin;
+      init_stride = sstride;
+    }
+    GDN_RUN(sc, "apply_scan_tc",
+            launch_chunk_scan_tc(pr, in, ws, 0, 0, pr.P, init, init_stride, o, hT, nullptr,
+                                 nullptr, 0, nullptr, st));
+    return GDN_OK;
+  }
+  GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, false, st));
   if (pr.P > 1) {
     GDN_RUN(sc, "summary_scan",
             launch_state_scan(pr, ws, 1, 0, pr.P - 1, nullptr, 0, nullptr, nullptr, nullptr,
@@ -223,8 +266,43 @@ gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* 
 gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const float* dHT,
                         void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dH0,
                         const WS& ws, cudaStream_t st, Sched& sc) {
-  GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, true, st));
   const int64_t sstride = pr.B * pr.H * pr.dk * pr.dv;
+  if (tc_path(pr)) {
+    const float* init = h0;
+    int64_t init_stride = 0;
+    if (pr.P > 1) {
+      GDN_RUN(sc, "summary_scan_tc",
+              launch_chunk_scan_tc(pr, in, ws, 1, 0, pr.P, nullptr, 0, nullptr, nullptr, ws.Mseg,
+                                   ws.Sseg, sstride, nullptr, st));
+      GDN_RUN(sc, "prefix",
+              launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Sseg, h0, ws.Hin,
+                            nullptr, st));
+      init = ws.Hin;
+      init_stride = sstride;
+    }
+    GDN_RUN(sc, "states_scan_tc",
+            launch_chunk_scan_tc(pr, in, ws, 2, 0, pr.P, init, init_stride, nullptr, nullptr,
+                                 nullptr, nullptr, 0, ws.hc16, st));
+    const float* dinit = dHT;
+    int64_t dinit_stride = 0;
+    if (pr.P > 1) {
+      GDN_RUN(sc, "grad_summary_scan_tc",
+              launch_dscan_tc(pr, in, ws, 1, 1, pr.P - 1, nullptr, 0, nullptr, nullptr, ws.Dseg,
+                              sstride, st));
+      GDN_RUN(sc, "prefix_bwd",
+              launch_prefix_bwd(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Dseg, dHT,
+                                ws.dHout, nullptr, st));
+      dinit = ws.dHout;
+      dinit_stride = sstride;
+    }
+    GDN_RUN(sc, "dstate_scan_tc",
+            launch_dscan_tc(pr, in, ws, 0, 0, pr.P, dinit, dinit_stride, ws.dhc16, dH0, nullptr,
+                            0, st));
+    GDN_RUN(sc, "grad_tc", launch_grad_tc(pr, in, ws, ws.hc16, ws.dhc16, dv, dg, dbeta, st));
+    GDN_RUN(sc, "qk_grad", launch_qk_grad(pr, in, ws, dq, dk, st));
+    return GDN_OK;
+  }
+  GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, true, st));
   const float* init = h0;
   int64_t init_stride = 0;
   if (pr.P > 1) {
@@ -449,6 +527,11 @@ gdn_status gdn_summary(const gdn_problem* p, const void* k, const void* v, const
   cudaStream_t st = (cudaStream_t)stream;
   if ((s = prepare(p, GDN_OP_SUMMARY, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK)
     return s;
+  if (tc_path(pr)) {
+    GDN_TRY(launch_chunk_scan_tc(pr, in, ws, 1, 0, 1, nullptr, 0, nullptr, nullptr, M, S, 0,
+                                 nullptr, st));
+    return GDN_OK;
+  }
   GDN_TRY(launch_prep(pr, in, ws, false, false, st));
   GDN_TRY(launch_state_scan(pr, ws, 1, 0, 1, nullptr, 0, nullptr, nullptr, nullptr, M, S, 0, st));
   return GDN_OK;

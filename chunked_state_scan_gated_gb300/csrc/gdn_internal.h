@@ -47,6 +47,8 @@ struct WS {
   float* dHout; // [P][B][H][dk][dv]
   float* dqp;   // [B][Tp][H][dk]    per-V-head gradient of q_hat
   float* dkp;   // [B][Tp][H][dk]    per-V-head gradient of k_hat
+  void* hc16;   // [B][H][NC][dk][dv] bf16 chunk-start states (tensor-core backward)
+  void* dhc16;  // [B][H][NC][dk][dv] bf16 chunk-end state gradients (tensor-core backward)
 };
 
 // Raw inputs of a call (device pointers; type of q..dO is Prob::dtype).
@@ -92,5 +94,26 @@ cudaError_t launch_prefix(int64_t n, int64_t P, int64_t dk, int64_t dv, const fl
 cudaError_t launch_prefix_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
                               const float* D, const float* dHT, float* dHout, float* dH0,
                               cudaStream_t st);
+
+// ---- tensor-core (tcgen05) kernels, bf16 with dk = dv = 128 ----
+bool tc_path(const Prob& pr);
+// mode 0: forward over `nseg` segments from `init` (o, final state of the last
+// segment); mode 1: summaries of segments seg_first.. (M_out, S_out); mode 2:
+// forward states only, every chunk-start state to `hc` (bf16 [B][H][NC][dk][dv]).
+cudaError_t launch_chunk_scan_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode,
+                                 int seg_first, int nseg, const float* init,
+                                 int64_t init_seg_stride, void* o, float* final_out,
+                                 float* M_out, float* S_out, int64_t out_seg_stride,
+                                 void* hc, cudaStream_t st);
+
+// mode 0: reverse state-gradient scan storing every chunk-end gradient (bf16)
+// and the start gradient of segment 0; mode 1: gradient summaries from zero.
+cudaError_t launch_dscan_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode, int seg_first,
+                            int nseg, const float* init, int64_t init_seg_stride, void* dhc,
+                            float* start_out, float* D_out, int64_t out_seg_stride,
+                            cudaStream_t st);
+// chunk-parallel gradients from chunk-start states and chunk-end state gradients
+cudaError_t launch_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, const void* hc,
+                           const void* dhc, void* dv, float* dg, float* dbeta, cudaStream_t st);
 
 }  // namespace gdn

@@ -1,0 +1,1068 @@
+// gdn_tc_bwd.cu -- tensor-core (tcgen05) kernels of the bf16 backward.
+//
+// The backward of the chunked gated delta rule (notation of gdn_simt.cu), with
+// dS the gradient of the state at the end of a chunk:
+//
+//   dV'   = P^T dO + diag(exp(G_C - G)) K dS
+//   dS   <- gamma_C dS + (diag(gamma) Q)^T dO - W^T dV'          (state chain)
+//   local gradients of the chunk from S (chunk start), dS, V', dV'  (chunk-parallel)
+//
+// k_dscan_tc runs the state chain in reverse over the chunks of one segment of
+// one (batch row, V head), storing every dS (bf16) or, from dS = 0, returning
+// the segment's gradient summary D (the reverse-direction state-gradient pass
+// of "linear attention cp #1035", p2p mode).  Layout and phases mirror the
+// forward chunk scan of gdn_tc_fwd.cu.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "gdn_internal.h"
+#include "gdn_tc_common.cuh"
+
+namespace gdn {
+
+// Shared with gdn_tc_fwd.cu: tensor-map encoder for [B, Ts, heads, 128] bf16.
+bool tc_make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t Ts, int64_t heads);
+bool tc_make_state_map(CUtensorMap* m, const void* ptr, int64_t n);
+
+namespace {
+
+using namespace tc;
+
+constexpr int FT = 256;
+constexpr uint32_t ATOM = 24576;                     // [W | Q | K] per 64-column atom
+constexpr uint32_t OFF_W = 0, OFF_Q = 8192, OFF_K = 16384;
+constexpr uint32_t OFF_DO = 49152, LBO_DO = 8192;    // dO tile
+constexpr uint32_t OFF_TA = 65536;                   // [T_u; T_w] (only T_w is used)
+constexpr uint32_t OFF_PZ = 81920;                   // [0; P]
+constexpr uint32_t OFF_DS = 98304, LBO_DS = 16384;   // dS bf16 (MN-major, 128 x 128)
+constexpr uint32_t OFF_NDV = 131072, LBO_NDV = 8192; // -dV' (64 x 128)
+constexpr uint32_t OFF_A = 131072;                   // fp32 A, T, Y of the solve (earlier)
+constexpr uint32_t OFF_T = OFF_A + 64 * LDA * 4;
+constexpr uint32_t OFF_Y = OFF_T + 64 * LDA * 4;
+constexpr uint32_t OFF_QKW1 = 172032;
+constexpr uint32_t OFF_SC = OFF_QKW1 + 2 * ATOM;
+constexpr uint32_t SMEM_BYTES = OFF_SC + 2048 + 1024;
+
+struct DscanArgs {
+  int64_t T, Ts, H, r, NC, CPS;
+  int l2norm;
+  float eps, scale;
+  const __nv_bfloat16* a;
+  const __nv_bfloat16* b;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* valid_len;
+  const float* init;          // mode 0: dH_out per segment (or dHT); mode 1 unused
+  int64_t init_seg_stride;
+  __nv_bfloat16* dhc;         // mode 0: chunk-end state gradients [B][H][NC][128][128]
+  float* start_out;           // mode 0: gradient of segment 0's initial state
+  float* D_out;               // mode 1: gradient summaries [P][B][H][128][128]
+  int64_t out_seg_stride;
+  int* status;
+  int mode, seg_first, nseg;
+};
+
+#define PHASE_SYNC()            \
+  do {                          \
+    fence_proxy_async();        \
+    tc_fence_before();          \
+    __syncthreads();            \
+    tc_fence_after();           \
+    if (*s_abort) goto done;    \
+  } while (0)
+
+__global__ void __launch_bounds__(FT, 1)
+    k_dscan_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mdo, DscanArgs ar) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const uint32_t base = smem_u32(sm);
+  float* sG = (float*)(sm + OFF_SC);
+  float* sGam = sG + 64;
+  float* sBeta = sGam + 64;
+  float* sKt = sBeta + 64;
+  uint64_t* bar_qk = (uint64_t*)(sm + OFF_SC + 1536);
+  uint64_t* bar_do = bar_qk + 2;
+  uint64_t* bar_mma = bar_qk + 3;
+  uint32_t* s_tmem = (uint32_t*)(bar_qk + 4);
+  int* s_abort = (int*)(s_tmem + 1);
+  float* sA = (float*)(sm + OFF_A);
+  float* sT = (float*)(sm + OFF_T);
+  float* sY = (float*)(sm + OFF_Y);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int row = quad * 32 + lane;
+  const bool store = ar.mode == 0;
+  const int64_t h = blockIdx.y;
+  const int64_t b = blockIdx.z / ar.nseg;
+  const int seg = ar.seg_first + (int)(blockIdx.z % ar.nseg);
+  const int64_t hq = h / ar.r, bh = b * ar.H + h;
+  const int64_t cs = (int64_t)seg * ar.CPS;
+  const int64_t ce = cs + ar.CPS < ar.NC ? cs + ar.CPS : ar.NC;
+  int64_t L = ar.T;
+  if (ar.valid_len) {
+    L = ar.valid_len[b];
+    if (L < 0 || L > ar.T) L = L < 0 ? 0 : ar.T;
+  }
+
+  if (tid == 0) {
+    mbar_init(bar_qk, 1);
+    mbar_init(bar_qk + 1, 1);
+    mbar_init(bar_do, 1);
+    mbar_init(bar_mma, 1);
+    fence_barrier_init();
+    *s_abort = 0;
+  }
+  if (warp == 0) tmem_alloc(s_tmem, 512);
+  for (int e = tid; e < 512; e += FT) reinterpret_cast<uint4*>(sm + OFF_PZ)[e] = make_uint4(0, 0, 0, 0);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tX = tmem, tD3 = tmem + 256;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+
+  float dS[64];  // gradient of the state at the end of the current chunk: row `row`, cols half*64..
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    const int col = half * 64 + j;
+    dS[j] = (store && ar.init) ? ar.init[seg * ar.init_seg_stride + (bh * 128 + row) * 128 + col] : 0.f;
+  }
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) st_chunk(sm + OFF_DS, mnmaj_chunk(row, half * 8 + cc, LBO_DS), &dS[cc * 8]);
+
+  {
+    uint32_t ph_mma = 0;
+    const uint32_t id_qk = idesc_bf16(128, 64, 0, 0);
+    const uint32_t id_kn = idesc_bf16(128, 128, 0, 1);
+    const uint32_t id_mn = idesc_bf16(128, 128, 1, 1);
+    auto issue_qk = [&](int64_t c) {  // chunk c into buffer (ce-1-c) & 1
+      const int64_t kl = ce - 1 - c;
+      const uint32_t qb = (kl & 1) ? OFF_QKW1 : 0u;
+      uint64_t* bar = bar_qk + (kl & 1);
+      mbar_arrive_expect_tx(bar, 32768u);
+      for (int at = 0; at < 2; ++at) {
+        tma_load_4d(sm + qb + at * ATOM + OFF_Q, &mq, at * 64, (int)hq, (int)(c * 64), (int)b, bar);
+        tma_load_4d(sm + qb + at * ATOM + OFF_K, &mk, at * 64, (int)hq, (int)(c * 64), (int)b, bar);
+      }
+    };
+    auto issue_do = [&](int64_t c) {
+      mbar_arrive_expect_tx(bar_do, 16384u);
+      for (int at = 0; at < 2; ++at)
+        tma_load_4d(sm + OFF_DO + at * LBO_DO, &mdo, at * 64, (int)h, (int)(c * 64), (int)b, bar_do);
+    };
+    float a_next = 0.f, b_next = 0.f;
+    auto load_gates = [&](int64_t c) {
+      const int64_t t = c * 64 + tid;
+      if (tid < 64 && t < L) {
+        const int64_t gi = (b * ar.Ts + t) * ar.H + h;
+        a_next = __bfloat162float(ar.a[gi]);
+        b_next = __bfloat162float(ar.b[gi]);
+      }
+    };
+    if (cs < ce) {
+      if (tid == 0) {
+        issue_qk(ce - 1);
+        issue_do(ce - 1);
+      }
+      load_gates(ce - 1);
+    }
+    for (int64_t c = ce - 1; c >= cs; --c) {
+      const int64_t t0 = c * 64;
+      const int64_t kl = ce - 1 - c;
+      const uint32_t qkw = (kl & 1) ? OFF_QKW1 : 0u;
+      fence_proxy_async();
+      __syncthreads();
+      if (tid == 0 && c - 1 >= cs) issue_qk(c - 1);
+      if (tid < 64) {
+        const int64_t t = t0 + tid;
+        float g = 0.f, be = 0.f;
+        if (t < L) {
+          const float x = a_next + ar.dt_bias[h];
+          const float sp = x > 20.f ? x : log1pf(expf(x));
+          g = -expf(ar.A_log[h]) * sp;
+          be = 1.f / (1.f + expf(-b_next));
+        }
+        sG[tid] = g * kLog2e;
+        sBeta[tid] = be;
+      }
+      if (c - 1 >= cs) load_gates(c - 1);
+      if (store) {  // gradient of chunk c's end state, bf16 row-major [dk][dv]
+        uint4* dst = reinterpret_cast<uint4*>(ar.dhc + ((bh * ar.NC + c) * 128 + row) * 128 + half * 64);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint4 pk;
+          pk.x = pack_bf16(dS[cc * 8 + 0], dS[cc * 8 + 1]);
+          pk.y = pack_bf16(dS[cc * 8 + 2], dS[cc * 8 + 3]);
+          pk.z = pack_bf16(dS[cc * 8 + 4], dS[cc * 8 + 5]);
+          pk.w = pack_bf16(dS[cc * 8 + 6], dS[cc * 8 + 7]);
+          dst[cc] = pk;
+        }
+      }
+      __syncthreads();
+      cumsum64f(sG);
+      __syncthreads();
+      if (tid < 64) {
+        sGam[tid] = exp2f(sG[tid]);
+        sKt[tid] = dexp_(sG[63], sG[tid]);
+      }
+      if (!mbar_wait(bar_qk + (kl & 1), (uint32_t)((kl >> 1) & 1), ar.status, kStatusTimeout)) *s_abort = 1;
+      if (!mbar_wait(bar_do, (uint32_t)(kl & 1), ar.status, kStatusTimeout)) *s_abort = 1;
+      // ---- row norms of q, k (in place); padded tokens get dO = 0
+      for (int it = 0; it < 8; ++it) {
+        const int rr = (tid >> 4) + 16 * it;
+        const bool isk = rr >= 64;
+        const int sub = tid & 15, at = sub >> 3, ch = sub & 7, r6 = rr & 63;
+        const uint32_t off = qkw + at * ATOM + (isk ? OFF_K : OFF_Q) + kmaj_chunk(r6, ch);
+        float x[8];
+        ld_chunk(sm, off, x);
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        float s = ar.l2norm ? rsqrtf(ss + ar.eps) : 1.f;
+        if (!isk) s *= ar.scale;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= s;
+        st_chunk(sm, off, x);
+      }
+      if (t0 + 64 > L) {
+        for (int idx = tid; idx < 1024; idx += FT) {
+          const int i = idx >> 4, cc = idx & 15;
+          if (t0 + i >= L) *reinterpret_cast<uint4*>(sm + OFF_DO + mnmaj_chunk(i, cc, LBO_DO)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      PHASE_SYNC();
+      // ---- MMA1: [Q;K] K^T -> P (rows 0..63), K K^T (rows 64..127)
+      if (tid == 0) {
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t at = ks >> 2, kk = ks & 3;
+          mma_bf16(tX, sdesc(base + qkw + at * ATOM + OFF_Q + kk * 32, 16, 1024),
+                   sdesc(base + qkw + at * ATOM + OFF_K + kk * 32, 16, 1024), id_qk, ks > 0);
+        }
+        mma_commit(bar_mma);
+      }
+      if (!mbar_wait(bar_mma, ph_mma, ar.status, kStatusTimeout)) *s_abort = 1;
+      ph_mma ^= 1;
+      tc_fence_after();
+      {
+        float v[32];
+        tmem_ld32(tX + lane_off + half * 32, v);
+        if (row < 64) {
+          const int i = row;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            float p[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int j = half * 32 + cc * 8 + e;
+              p[e] = (j <= i) ? v[cc * 8 + e] * dexp_(sG[i], sG[j]) : 0.f;
+            }
+            st_chunk(sm + OFF_PZ, kmaj_chunk(64 + i, half * 4 + cc), p);
+          }
+        } else {
+          const int i = row - 64;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = half * 32 + e;
+            sA[i * LDA + j] = (j < i) ? sBeta[i] * v[e] * dexp_(sG[i], sG[j]) : 0.f;
+          }
+        }
+      }
+      PHASE_SYNC();
+      solve_unit_lower64(sA, sT, sY);
+      for (int q = 0; q < 2; ++q) {  // T_w = T diag(beta gamma) into rows 64..127
+        const int idx = tid + FT * q;
+        const int i = idx >> 3, cc = idx & 7;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = cc * 8 + e;
+          x[e] = (j <= i) ? sT[i * LDA + j] * sBeta[j] * sGam[j] : 0.f;
+        }
+        st_chunk(sm + OFF_TA, kmaj_chunk(64 + i, cc), x);
+      }
+      PHASE_SYNC();
+      // ---- W = T_w K (rows 64..127 of X[0,128)); K dS (rows 64..127 of X[128,256));
+      //      P^T dO (rows 64..127 of D3)
+      if (tid == 0) {
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tX, sdesc(base + OFF_TA + ks * 32, 16, 1024),
+                   sdesc(base + qkw + OFF_K + ks * 2048, ATOM, 1024), id_kn, ks > 0);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t at = ks >> 2, kk = ks & 3;
+          mma_bf16(tX + 128, sdesc(base + qkw + at * ATOM + OFF_Q + kk * 32, 16, 1024),
+                   sdesc(base + OFF_DS + ks * 2048, LBO_DS, 1024), id_kn, ks > 0);
+        }
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tD3, sdesc(base + OFF_PZ + ks * 2048, 8192, 1024),
+                   sdesc(base + OFF_DO + ks * 2048, LBO_DO, 1024), id_mn, ks > 0);
+        mma_commit(bar_mma);
+      }
+      if (!mbar_wait(bar_mma, ph_mma, ar.status, kStatusTimeout)) *s_abort = 1;
+      ph_mma ^= 1;
+      tc_fence_after();
+      if (quad >= 2) {
+        const int i = row - 64;
+        const float kt = sKt[i];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float w[32], kd[32], pd[32];
+          tmem_ld32(tX + lane_off + half * 64 + hh * 32, w);
+          tmem_ld32(tX + lane_off + 128 + half * 64 + hh * 32, kd);
+          tmem_ld32(tD3 + lane_off + half * 64 + hh * 32, pd);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            st_chunk(sm + qkw + half * ATOM + OFF_W, kmaj_chunk(i, hh * 4 + cc), &w[cc * 8]);
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = -(kt * kd[cc * 8 + e] + pd[cc * 8 + e]);
+            st_chunk(sm + OFF_NDV, mnmaj_chunk(i, half * 8 + hh * 4 + cc, LBO_NDV), x);
+          }
+        }
+      }
+      // Q rows scaled by gamma (for (diag(gamma) Q)^T dO)
+      for (int q = 0; q < 4; ++q) {
+        const int idx = tid + FT * q;  // 64 rows x 16 chunks
+        const int i = idx >> 4, at = (idx >> 3) & 1, ch = idx & 7;
+        const uint32_t off = qkw + at * ATOM + OFF_Q + kmaj_chunk(i, ch);
+        float x[8];
+        ld_chunk(sm, off, x);
+        const float gm = sGam[i];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= gm;
+        st_chunk(sm, off, x);
+      }
+      PHASE_SYNC();
+      // ---- (diag(gamma) Q)^T dO + W^T (-dV') -> X[0,128)
+      if (tid == 0) {
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tX, sdesc(base + qkw + OFF_Q + ks * 2048, ATOM, 1024),
+                   sdesc(base + OFF_DO + ks * 2048, LBO_DO, 1024), id_mn, ks > 0);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tX, sdesc(base + qkw + OFF_W + ks * 2048, ATOM, 1024),
+                   sdesc(base + OFF_NDV + ks * 2048, LBO_NDV, 1024), id_mn, 1);
+        mma_commit(bar_mma);
+      }
+      if (!mbar_wait(bar_mma, ph_mma, ar.status, kStatusTimeout)) *s_abort = 1;
+      ph_mma ^= 1;
+      tc_fence_after();
+      if (tid == 0 && c - 1 >= cs) issue_do(c - 1);  // dO(c) consumed
+      {
+        const float gC = sGam[63];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[32];
+          tmem_ld32(tX + lane_off + half * 64 + hh * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dS[hh * 32 + e] = fmaf(gC, dS[hh * 32 + e], v[e]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          st_chunk(sm + OFF_DS, mnmaj_chunk(row, half * 8 + cc, LBO_DS), &dS[cc * 8]);
+      }
+      PHASE_SYNC();
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    const int col = half * 64 + j;
+    const int64_t off = (bh * 128 + row) * 128 + col;
+    if (store) {
+      if (ar.start_out && seg == 0) ar.start_out[off] = dS[j];
+    } else if (ar.D_out) {
+      ar.D_out[seg * ar.out_seg_stride + off] = dS[j];
+    }
+  }
+done:
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_dscan_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode, int seg_first,
+                            int nseg, const float* init, int64_t init_seg_stride, void* dhc,
+                            float* start_out, float* D_out, int64_t out_seg_stride,
+                            cudaStream_t st) {
+  if (nseg <= 0 || pr.B == 0 || pr.NC == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mdo;
+  memset(&mq, 0, sizeof(mq));
+  memset(&mk, 0, sizeof(mk));
+  memset(&mdo, 0, sizeof(mdo));
+  if (!tc_make_map(&mq, in.q, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mdo, in.dO, pr.B, pr.T, pr.Ts, pr.H))
+    return cudaErrorInvalidValue;
+  DscanArgs ar;
+  ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.r = pr.r; ar.NC = pr.NC; ar.CPS = pr.CPS;
+  ar.l2norm = pr.l2norm; ar.eps = pr.eps; ar.scale = pr.scale;
+  ar.a = (const __nv_bfloat16*)in.a; ar.b = (const __nv_bfloat16*)in.b;
+  ar.A_log = in.A_log; ar.dt_bias = in.dt_bias; ar.valid_len = in.valid_len;
+  ar.init = init; ar.init_seg_stride = init_seg_stride;
+  ar.dhc = (__nv_bfloat16*)dhc; ar.start_out = start_out; ar.D_out = D_out;
+  ar.out_seg_stride = out_seg_stride; ar.status = ws.status;
+  ar.mode = mode; ar.seg_first = seg_first; ar.nseg = nseg;
+  cudaError_t e = cudaFuncSetAttribute(k_dscan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(1, (unsigned)pr.H, (unsigned)(pr.B * nseg));
+  k_dscan_tc<<<grid, FT, SMEM_BYTES, st>>>(mq, mk, mdo, ar);
+  return cudaGetLastError();
+}
+
+// ============================================================================
+// k_grad_tc: every local gradient of one chunk and one V head, given S (the
+// state at the chunk start), dS (the gradient of the state at its end), q, k,
+// v, dO and the gates; one CTA per (chunk, V head, batch row), chunk-parallel.
+// With X_v = T^T dV', X_w = T^T dW (Lambda of the triangular system):
+//   dq  = diag(gamma) dO S^T + (dP o Gamma) K,      dP = dO V'^T (lower)
+//   dk  = (dP o Gamma)^T Q + diag(kt) V' dS^T + diag(beta gamma) X_w + E K + E^T K
+//   dv  = diag(beta) X_v,  dW = -dV' S^T,
+//   dA  = -(X_v U^T + X_w W^T) (strictly lower),  E = dA o beta_i Gamma
+//   dbeta, dG: row dots of the same pieces; dg = reverse cumsum of dG.
+// All MMAs are M = 64: row r of an accumulator lives in TMEM lane
+// (r % 16) + 32 (r / 16), so threads with lane < 16 of each warp own one row.
+namespace {
+
+constexpr uint32_t G_Q = 0, G_K = 16384, G_W = 32768, G_V = 49152, G_DO = 65536;  // [64][128]
+constexpr uint32_t G_S = 81920, G_DS = 114688;      // [128][128], atoms of 16 KB
+constexpr uint32_t G_TU = 147456, G_TW = 155648;    // [64][64]; later U [64][128]
+constexpr uint32_t G_P = 163840, G_TP = 172032;     // [64][64]; P later E; Y of the solve in TP
+constexpr uint32_t G_VP = 180224;                   // V' [64][128]; later dP o Gamma [64][64]
+constexpr uint32_t G_DV = 196608, G_DW = 212992;    // dV', dW [64][128]; earlier fp32 A, T
+constexpr uint32_t G_SC = 229376;                   // scalars
+constexpr uint32_t G_SMEM = G_SC + 1792 + 1024;
+constexpr int GLDA = 64;
+
+struct GradArgs {
+  int64_t T, Ts, H, r, NC, Tp;
+  int l2norm;
+  float eps, scale;
+  const __nv_bfloat16* a;
+  const __nv_bfloat16* b;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* valid_len;
+  __nv_bfloat16* dv;   // [B, Ts, H, 128]
+  float* dg;           // [B, Ts, H]
+  float* dbeta;
+  float* dqp;          // [B][Tp][H][128] per-V-head gradient of q_hat
+  float* dkp;
+  int* status;
+};
+
+// 64 consecutive fp32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  float a[32], c[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, c);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    v[j] = a[j];
+    v[32 + j] = c[j];
+  }
+}
+
+__global__ void __launch_bounds__(FT, 1)
+    k_grad_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+              const __grid_constant__ CUtensorMap ms, const __grid_constant__ CUtensorMap mds,
+              GradArgs ar) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const uint32_t base = smem_u32(sm);
+  float* sG = (float*)(sm + G_SC);     // cumulative gate (log2 units)
+  float* sGam = sG + 64;
+  float* sBeta = sGam + 64;
+  float* sKt = sBeta + 64;
+  float* sDG = sKt + 64;               // dG terms computed row-wise by threads 0..63
+  float* sMisc = sDG + 64;             // [8] block partials of <S, dS>
+  // half-row partial sums, [2][64] each, in the T tile's slot (free after RT5)
+  float* sRed = (float*)(sm + G_TP);   // dG
+  float* sRedB = sRed + 128;           // dbeta
+  float* sRedS = sRedB + 128;          // Kt terms
+  uint64_t* bar_ld = (uint64_t*)(sm + G_SC + 1536);
+  uint64_t* bar_mma = bar_ld + 1;
+  uint32_t* s_tmem = (uint32_t*)(bar_ld + 2);
+  int* s_abort = (int*)(s_tmem + 1);
+  float* sA = (float*)(sm + G_DV);
+  float* sT = (float*)(sm + G_DW);
+  float* sY = (float*)(sm + G_TP);
+  float* sZ = (float*)(sm + G_S);      // fp32 64 x 64 after S is consumed
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const bool own = lane < 16;          // owns accumulator row `ri` of M = 64 results
+  const int ri = quad * 16 + (lane & 15);
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t hq = h / ar.r, bh = b * ar.H + h;
+  const int64_t t0 = c * 64;
+  int64_t L = ar.T;
+  if (ar.valid_len) {
+    L = ar.valid_len[b];
+    if (L < 0 || L > ar.T) L = L < 0 ? 0 : ar.T;
+  }
+
+  if (tid == 0) {
+    mbar_init(bar_ld, 1);
+    mbar_init(bar_mma, 1);
+    fence_barrier_init();
+    *s_abort = 0;
+  }
+  if (warp == 0) tmem_alloc(s_tmem, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_ld, 131072u);
+    for (int at = 0; at < 2; ++at) {
+      tma_load_4d(sm + G_Q + at * 8192, &mq, at * 64, (int)hq, (int)t0, (int)b, bar_ld);
+      tma_load_4d(sm + G_K + at * 8192, &mk, at * 64, (int)hq, (int)t0, (int)b, bar_ld);
+      tma_load_4d(sm + G_V + at * 8192, &mv, at * 64, (int)h, (int)t0, (int)b, bar_ld);
+      tma_load_4d(sm + G_DO + at * 8192, &mdo, at * 64, (int)h, (int)t0, (int)b, bar_ld);
+      tma_load_4d(sm + G_S + at * 16384, &ms, at * 64, 0, (int)(bh * ar.NC + c), 0, bar_ld);
+      tma_load_4d(sm + G_DS + at * 16384, &mds, at * 64, 0, (int)(bh * ar.NC + c), 0, bar_ld);
+    }
+  }
+  if (tid < 64) {
+    const int64_t t = t0 + tid;
+    float g = 0.f, be = 0.f;
+    if (t < L) {
+      const int64_t gi = (b * ar.Ts + t) * ar.H + h;
+      const float x = __bfloat162float(ar.a[gi]) + ar.dt_bias[h];
+      const float sp = x > 20.f ? x : log1pf(expf(x));
+      g = -expf(ar.A_log[h]) * sp;
+      be = 1.f / (1.f + expf(-__bfloat162float(ar.b[gi])));
+    }
+    sG[tid] = g * kLog2e;
+    sBeta[tid] = be;
+    sDG[tid] = 0.f;
+  }
+  __syncthreads();
+  cumsum64f(sG);
+  __syncthreads();
+  if (tid < 64) {
+    sGam[tid] = exp2f(sG[tid]);
+    sKt[tid] = dexp_(sG[63], sG[tid]);
+  }
+  if (!mbar_wait(bar_ld, 0, ar.status, kStatusTimeout)) *s_abort = 1;
+  // norms (in place) and padded dO rows
+  for (int it = 0; it < 8; ++it) {
+    const int rr = (tid >> 4) + 16 * it;
+    const bool isk = rr >= 64;
+    const int sub = tid & 15, at = sub >> 3, ch = sub & 7, r6 = rr & 63;
+    const uint32_t off = (isk ? G_K : G_Q) + at * 8192 + kmaj_chunk(r6, ch);
+    float x[8];
+    ld_chunk(sm, off, x);
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    float s = ar.l2norm ? rsqrtf(ss + ar.eps) : 1.f;
+    if (!isk) s *= ar.scale;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] *= s;
+    st_chunk(sm, off, x);
+  }
+  if (t0 + 64 > L) {
+    for (int idx = tid; idx < 1024; idx += FT) {
+      const int i = idx >> 4, cc = idx & 15;
+      if (t0 + i >= L)
+        *reinterpret_cast<uint4*>(sm + G_DO + (cc >> 3) * 8192 + kmaj_chunk(i, cc & 7)) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  {
+  uint32_t ph = 0;
+  float dGacc = 0.f, dbacc = 0.f, sKacc = 0.f;  // this thread's half-row partial sums
+  float dq[64], dk[64], U[64];
+  const uint32_t id64 = idesc_bf16(64, 64, 0, 0);
+  const uint32_t id128kn = idesc_bf16(64, 128, 0, 1);
+  const uint32_t id128kk = idesc_bf16(64, 128, 0, 0);
+  const uint32_t id128mn = idesc_bf16(64, 128, 1, 1);
+  PHASE_SYNC();
+  // ---- RT1: Q K^T -> [0,64), K K^T -> [64,128)
+  if (tid == 0) {
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t at = ks >> 2, kk = ks & 3;
+      const uint64_t bk = sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024);
+      mma_bf16(tmem, sdesc(base + G_Q + at * 8192 + kk * 32, 16, 1024), bk, id64, ks > 0);
+      mma_bf16(tmem + 64, sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024), bk, id64, ks > 0);
+    }
+    mma_commit(bar_mma);
+  }
+  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
+  ph ^= 1;
+  tc_fence_after();
+  {
+    float qk[32], kk[32];
+    tmem_ld32(tmem + lane_off + half * 32, qk);
+    tmem_ld32(tmem + lane_off + 64 + half * 32, kk);
+    if (own) {
+      const int i = ri;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = half * 32 + cc * 8 + e;
+          p[e] = (j <= i) ? qk[cc * 8 + e] * dexp_(sG[i], sG[j]) : 0.f;
+        }
+        st_chunk(sm + G_P, kmaj_chunk(i, half * 4 + cc), p);
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = half * 32 + e;
+        sA[i * GLDA + j] = (j < i) ? sBeta[i] * kk[e] * dexp_(sG[i], sG[j]) : 0.f;
+      }
+    }
+  }
+  PHASE_SYNC();
+  solve_unit_lower64(sA, sT, sY, GLDA);
+  for (int q = 0; q < 2; ++q) {  // T_u, T_w and T into bf16 tiles
+    const int idx = tid + FT * q;
+    const int i = idx >> 3, cc = idx & 7;
+    float xu[8], xw[8], xp[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int j = cc * 8 + e;
+      const float t = (j <= i) ? sT[i * GLDA + j] : 0.f;
+      xp[e] = t;
+      xu[e] = t * sBeta[j];
+      xw[e] = xu[e] * sGam[j];
+    }
+    st_chunk(sm + G_TU, kmaj_chunk(i, cc), xu);
+    st_chunk(sm + G_TW, kmaj_chunk(i, cc), xw);
+    st_chunk(sm + G_TP, kmaj_chunk(i, cc), xp);
+  }
+  PHASE_SYNC();
+  // ---- RT2: W = T_w K -> [128,256), U = T_u V -> [256,384)
+  if (tid == 0) {
+    for (int ks = 0; ks < 4; ++ks) {
+      mma_bf16(tmem + 128, sdesc(base + G_TW + ks * 32, 16, 1024),
+               sdesc(base + G_K + ks * 2048, 8192, 1024), id128kn, ks > 0);
+      mma_bf16(tmem + 256, sdesc(base + G_TU + ks * 32, 16, 1024),
+               sdesc(base + G_V + ks * 2048, 8192, 1024), id128kn, ks > 0);
+    }
+    mma_commit(bar_mma);
+  }
+  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
+  ph ^= 1;
+  tc_fence_after();
+  {
+    float w[64];
+    tmem_ld64(tmem + lane_off + 128 + half * 64, w);
+    tmem_ld64(tmem + lane_off + 256 + half * 64, U);
+    if (own) {
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        st_chunk(sm + G_W + half * 8192, kmaj_chunk(ri, cc), &w[cc * 8]);
+        st_chunk(sm + G_TU + half * 8192, kmaj_chunk(ri, cc), &U[cc * 8]);  // U over T_u, T_w
+      }
+    }
+  }
+  PHASE_SYNC();
+  // ---- RT3: W S -> [384,512), K dS -> [0,128), P^T dO -> [128,256), dO S^T -> [256,384)
+  if (tid == 0) {
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t at = ks >> 2, kk = ks & 3;
+      mma_bf16(tmem + 384, sdesc(base + G_W + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_S + ks * 2048, 16384, 1024), id128kn, ks > 0);
+      mma_bf16(tmem, sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_DS + ks * 2048, 16384, 1024), id128kn, ks > 0);
+      mma_bf16(tmem + 256, sdesc(base + G_DO + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_S + at * 16384 + kk * 32, 16, 1024), id128kk, ks > 0);
+    }
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem + 128, sdesc(base + G_P + ks * 2048, 8192, 1024),
+               sdesc(base + G_DO + ks * 2048, 8192, 1024), id128mn, ks > 0);
+    mma_commit(bar_mma);
+  }
+  // <S, dS> (both tiles share the TMA layout): block reduction into sMisc[0]
+  {
+    float acc = 0.f;
+    for (int q = tid; q < 2048; q += FT) {
+      float x[8], y[8];
+      ld_chunk(sm + G_S, q * 16, x);
+      ld_chunk(sm + G_DS, q * 16, y);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(x[e], y[e], acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) sMisc[warp] = acc;
+  }
+  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
+  ph ^= 1;
+  tc_fence_after();
+  {
+    float ws[64], kd[64], pd[64];
+    tmem_ld64(tmem + lane_off + 384 + half * 64, ws);
+    tmem_ld64(tmem + lane_off + half * 64, kd);
+    tmem_ld64(tmem + lane_off + 128 + half * 64, pd);
+    tmem_ld64(tmem + lane_off + 256 + half * 64, dq);
+    if (own) {
+      const int i = ri;
+      const float kt = sKt[i], gm = sGam[i];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        ws[j] = U[j] - ws[j];                 // V'
+        kd[j] = fmaf(kt, kd[j], pd[j]);       // dV'
+        dq[j] *= gm;                          // diag(gamma) dO S^T
+      }
+      float part = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        st_chunk(sm + G_VP + half * 8192, kmaj_chunk(i, cc), &ws[cc * 8]);
+        st_chunk(sm + G_DV + half * 8192, kmaj_chunk(i, cc), &kd[cc * 8]);
+        float qx[8];
+        ld_chunk(sm + G_Q + half * 8192, kmaj_chunk(i, cc), qx);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part = fmaf(qx[e], dq[cc * 8 + e], part);
+      }
+      dGacc += part;                          // q_i . (gamma_i S dO_i)
+    }
+  }
+  PHASE_SYNC();
+  // ---- RT4: dV' S^T -> [0,128), V' dS^T -> [128,256), dP = dO V'^T -> [384,448)
+  if (tid == 0) {
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t at = ks >> 2, kk = ks & 3;
+      mma_bf16(tmem, sdesc(base + G_DV + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_S + at * 16384 + kk * 32, 16, 1024), id128kk, ks > 0);
+      mma_bf16(tmem + 128, sdesc(base + G_VP + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_DS + at * 16384 + kk * 32, 16, 1024), id128kk, ks > 0);
+      mma_bf16(tmem + 384, sdesc(base + G_DO + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_VP + at * 8192 + kk * 32, 16, 1024), id64, ks > 0);
+    }
+    mma_commit(bar_mma);
+  }
+  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
+  ph ^= 1;
+  tc_fence_after();
+  {
+    float x[64];
+    tmem_ld64(tmem + lane_off + half * 64, x);   // dV' S^T = -dW
+    if (own) {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) x[j] = -x[j];
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) st_chunk(sm + G_DW + half * 8192, kmaj_chunk(ri, cc), &x[cc * 8]);
+    }
+    tmem_ld64(tmem + lane_off + 128 + half * 64, x);  // dKt = V' dS^T
+    if (own) {
+      const int i = ri;
+      const float kt = sKt[i];
+      float part = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        float kx[8];
+        ld_chunk(sm + G_K + half * 8192, kmaj_chunk(i, cc), kx);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part = fmaf(kx[e], x[cc * 8 + e], part);
+      }
+      sKacc = kt * part;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) dk[j] = kt * x[j];
+    }
+    float dp[32];
+    tmem_ld32(tmem + lane_off + 384 + half * 32, dp);
+    if (own) {
+      const int i = ri;
+      float pv[32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) ld_chunk(sm + G_P, kmaj_chunk(i, half * 4 + cc), &pv[cc * 8]);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = half * 32 + cc * 8 + e;
+          const float dpv = (j <= i) ? dp[cc * 8 + e] : 0.f;
+          sZ[i * 64 + j] = dpv * pv[cc * 8 + e];                   // dP o P
+          y[e] = (j <= i) ? dpv * dexp_(sG[i], sG[j]) : 0.f;       // dP o Gamma
+        }
+        st_chunk(sm + G_VP, kmaj_chunk(i, half * 4 + cc), y);     // over V' (consumed)
+      }
+    }
+  }
+  PHASE_SYNC();
+  if (tid < 64) {  // gate terms of P: sum_j Z_ij - sum_j Z_ji
+    float acc = 0.f;
+    for (int j = 0; j < 64; ++j) acc += sZ[tid * 64 + j] - sZ[j * 64 + tid];
+    sDG[tid] += acc;
+  }
+  // ---- RT5: T^T dV' -> [0,128), T^T dW -> [128,256), (dP o Gamma) K -> [256,384)
+  if (tid == 0) {
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t at = sdesc(base + G_TP + ks * 2048, 8192, 1024);
+      mma_bf16(tmem, at, sdesc(base + G_DV + ks * 2048, 8192, 1024), id128mn, ks > 0);
+      mma_bf16(tmem + 128, at, sdesc(base + G_DW + ks * 2048, 8192, 1024), id128mn, ks > 0);
+      mma_bf16(tmem + 256, sdesc(base + G_VP + ks * 32, 16, 1024),
+               sdesc(base + G_K + ks * 2048, 8192, 1024), id128kn, ks > 0);
+    }
+    mma_commit(bar_mma);
+  }
+  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
+  ph ^= 1;
+  tc_fence_after();
+  {
+    const int i = ri;
+    const int64_t t = t0 + i;
+    const bool valid = t < L;
+    float x[64];
+    tmem_ld64(tmem + lane_off + half * 64, x);    // X_v
+    if (own) {
+      const float be = sBeta[i];
+      float part = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        float vx[8];
+        ld_chunk(sm + G_V + half * 8192, kmaj_chunk(i, cc), vx);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part = fmaf(x[cc * 8 + e], vx[e], part);
+        st_chunk(sm + G_DS + half * 8192, kmaj_chunk(i, cc), &x[cc * 8]);   // X_v over dS
+      }
+      dbacc += part;
+      if (t < ar.T) {
+        uint4* dst = reinterpret_cast<uint4*>(ar.dv + ((b * ar.Ts + t) * ar.H + h) * 128 + half * 64);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          float y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = valid ? be * x[cc * 8 + e] : 0.f;
+          uint4 pk;
+          pk.x = pack_bf16(y[0], y[1]);
+          pk.y = pack_bf16(y[2], y[3]);
+          pk.z = pack_bf16(y[4], y[5]);
+          pk.w = pack_bf16(y[6], y[7]);
+          dst[cc] = pk;
+        }
+      }
+    }
+    tmem_ld64(tmem + lane_off + 128 + half * 64, x);  // X_w
+    if (own) {
+      const float be = sBeta[i], gm = sGam[i];
+      float part = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        float kx[8];
+        ld_chunk(sm + G_K + half * 8192, kmaj_chunk(i, cc), kx);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part = fmaf(x[cc * 8 + e], kx[e], part);
+        st_chunk(sm + G_DS + 16384 + half * 8192, kmaj_chunk(i, cc), &x[cc * 8]);  // X_w
+      }
+      dbacc += gm * part;
+      dGacc += be * gm * part;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) dk[j] = fmaf(be * gm, x[j], dk[j]);
+    }
+    tmem_ld64(tmem + lane_off + 256 + half * 64, x);  // (dP o Gamma) K
+    if (own && t < ar.Tp) {
+      float* dst = ar.dqp + ((b * ar.Tp + t) * ar.H + h) * 128 + half * 64;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        float4 v4;
+        v4.x = valid ? dq[j] + x[j] : 0.f;
+        v4.y = valid ? dq[j + 1] + x[j + 1] : 0.f;
+        v4.z = valid ? dq[j + 2] + x[j + 2] : 0.f;
+        v4.w = valid ? dq[j + 3] + x[j + 3] : 0.f;
+        *reinterpret_cast<float4*>(dst + j) = v4;
+      }
+    }
+  }
+  PHASE_SYNC();
+  // ---- RT6: dA' = X_v U^T + X_w W^T -> [0,64), K K^T -> [64,128)
+  if (tid == 0) {
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t at = ks >> 2, kk = ks & 3;
+      mma_bf16(tmem, sdesc(base + G_DS + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_TU + at * 8192 + kk * 32, 16, 1024), id64, ks > 0);
+    }
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t at = ks >> 2, kk = ks & 3;
+      mma_bf16(tmem, sdesc(base + G_DS + 16384 + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_W + at * 8192 + kk * 32, 16, 1024), id64, 1);
+      mma_bf16(tmem + 64, sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024), id64, ks > 0);
+    }
+    mma_commit(bar_mma);
+  }
+  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
+  ph ^= 1;
+  tc_fence_after();
+  {
+    float da[32], kk[32];
+    tmem_ld32(tmem + lane_off + half * 32, da);
+    tmem_ld32(tmem + lane_off + 64 + half * 32, kk);
+    if (own) {
+      const int i = ri;
+      const float be = sBeta[i];
+      float part = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float ex[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = half * 32 + cc * 8 + e;
+          const float gmm = (j < i) ? dexp_(sG[i], sG[j]) : 0.f;
+          const float dA = (j < i) ? -da[cc * 8 + e] : 0.f;
+          const float kg = kk[cc * 8 + e] * gmm;
+          part = fmaf(dA, kg, part);                 // dbeta: dA (k_i . k_j) Gamma
+          sZ[i * 64 + j] = dA * be * kg;             // dA o A
+          ex[e] = dA * be * gmm;                     // E
+        }
+        st_chunk(sm + G_P, kmaj_chunk(i, half * 4 + cc), ex);   // E over P
+      }
+      dbacc += part;
+    }
+  }
+  PHASE_SYNC();
+  if (tid < 64) {
+    float acc = 0.f;
+    for (int j = 0; j < 64; ++j) acc += sZ[tid * 64 + j] - sZ[j * 64 + tid];
+    sDG[tid] += acc;
+  }
+  // ---- RT7: dk += (dP o Gamma)^T Q + E K + E^T K -> [0,128)
+  if (tid == 0) {
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem, sdesc(base + G_VP + ks * 2048, 8192, 1024),
+               sdesc(base + G_Q + ks * 2048, 8192, 1024), id128mn, ks > 0);
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem, sdesc(base + G_P + ks * 32, 16, 1024),
+               sdesc(base + G_K + ks * 2048, 8192, 1024), id128kn, 1);
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem, sdesc(base + G_P + ks * 2048, 8192, 1024),
+               sdesc(base + G_K + ks * 2048, 8192, 1024), id128mn, 1);
+    mma_commit(bar_mma);
+  }
+  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
+  ph ^= 1;
+  tc_fence_after();
+  {
+    float x[64];
+    tmem_ld64(tmem + lane_off + half * 64, x);
+    const int i = ri;
+    const int64_t t = t0 + i;
+    if (own && t < ar.Tp) {
+      const bool valid = t < L;
+      float* dst = ar.dkp + ((b * ar.Tp + t) * ar.H + h) * 128 + half * 64;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        float4 v4;
+        v4.x = valid ? dk[j] + x[j] : 0.f;
+        v4.y = valid ? dk[j + 1] + x[j + 1] : 0.f;
+        v4.z = valid ? dk[j + 2] + x[j + 2] : 0.f;
+        v4.w = valid ? dk[j + 3] + x[j + 3] : 0.f;
+        *reinterpret_cast<float4*>(dst + j) = v4;
+      }
+    }
+    if (own) {
+      sRed[half * 64 + i] = dGacc;
+      sRedB[half * 64 + i] = dbacc;
+      sRedS[half * 64 + i] = sKacc;
+    }
+  }
+  __syncthreads();
+  // ---- gate gradients: Kt terms, state term, reverse cumsum
+  if (tid < 64) {
+    const int i = tid;
+    const float s_i = sRedS[i] + sRedS[64 + i];
+    float d = sDG[i] + sRed[i] + sRed[64 + i];
+    if (i < 63) d -= s_i;
+    sDG[i] = d;
+    sRed[i] = (i < 63) ? s_i : 0.f;   // reuse: Kt terms to sum into dG_C
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float tot = 0.f;
+    for (int i = 0; i < 63; ++i) tot += sRed[i];
+    float sd = 0.f;
+    for (int w = 0; w < FT / 32; ++w) sd += sMisc[w];
+    sDG[63] += tot + sGam[63] * sd;
+  }
+  __syncthreads();
+  if (tid < 32) {  // dg_j = sum_{i >= j} dG_i (reverse cumsum, warp 0)
+    float v0 = sDG[63 - tid], v1 = sDG[31 - tid];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y0 = __shfl_up_sync(0xffffffffu, v0, o);
+      const float y1 = __shfl_up_sync(0xffffffffu, v1, o);
+      if (tid >= o) {
+        v0 += y0;
+        v1 += y1;
+      }
+    }
+    v1 += __shfl_sync(0xffffffffu, v0, 31);
+    __syncwarp();
+    sDG[63 - tid] = v0;
+    sDG[31 - tid] = v1;
+  }
+  __syncthreads();
+  if (tid < 64) {
+    const int64_t t = t0 + tid;
+    if (t < ar.T) {
+      const int64_t gi = (b * ar.Ts + t) * ar.H + h;
+      const bool valid = t < L;
+      // dG was accumulated in natural-log units (the log2 scaling only enters exponents)
+      ar.dg[gi] = valid ? sDG[tid] : 0.f;
+      ar.dbeta[gi] = valid ? sRedB[tid] + sRedB[64 + tid] : 0.f;
+    }
+  }
+  }
+done:
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, const void* hc,
+                           const void* dhc, void* dv, float* dg, float* dbeta, cudaStream_t st) {
+  if (pr.B == 0 || pr.NC == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv, mdo, ms, mds;
+  memset(&mq, 0, sizeof(mq));
+  memset(&mk, 0, sizeof(mk));
+  memset(&mv, 0, sizeof(mv));
+  memset(&mdo, 0, sizeof(mdo));
+  memset(&ms, 0, sizeof(ms));
+  memset(&mds, 0, sizeof(mds));
+  const int64_t n = pr.B * pr.H * pr.NC;
+  if (!tc_make_map(&mq, in.q, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mv, in.v, pr.B, pr.T, pr.Ts, pr.H) ||
+      !tc_make_map(&mdo, in.dO, pr.B, pr.T, pr.Ts, pr.H) || !tc_make_state_map(&ms, hc, n) ||
+      !tc_make_state_map(&mds, dhc, n))
+    return cudaErrorInvalidValue;
+  GradArgs ar;
+  ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.r = pr.r; ar.NC = pr.NC; ar.Tp = pr.Tp;
+  ar.l2norm = pr.l2norm; ar.eps = pr.eps; ar.scale = pr.scale;
+  ar.a = (const __nv_bfloat16*)in.a; ar.b = (const __nv_bfloat16*)in.b;
+  ar.A_log = in.A_log; ar.dt_bias = in.dt_bias; ar.valid_len = in.valid_len;
+  ar.dv = (__nv_bfloat16*)dv; ar.dg = dg; ar.dbeta = dbeta;
+  ar.dqp = ws.dqp; ar.dkp = ws.dkp; ar.status = ws.status;
+  cudaError_t e = cudaFuncSetAttribute(k_grad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)G_SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)pr.NC, (unsigned)pr.H, (unsigned)pr.B);
+  k_grad_tc<<<grid, FT, G_SMEM, st>>>(mq, mk, mv, mdo, ms, mds, ar);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,263 @@
+// gdn_tc_common.cuh -- sm_103a building blocks for the tensor-core kernels:
+// mbarriers with bounded waits, TMA tile loads, shared-memory matrix
+// descriptors (128-byte swizzle), tcgen05.mma (bf16 -> fp32 in TMEM), TMEM
+// allocation and loads, and the swizzled addressing used to stage operands
+// from registers.
+//
+// Operand layouts (bf16, 128-byte swizzle, tile base 1024-byte aligned):
+//  K-major tile (rows x 64 elements along K): element (r, k) at
+//    r*128 + (((k>>3) ^ (r&7)) << 4) + (k&7)*2; 8-row groups 1024 B apart (SBO);
+//    a K step of 16 elements advances the descriptor start by 32 B.
+//  MN-major tile (K rows, N contiguous): element (k, n) at
+//    (n>>6)*LBO + (k>>3)*1024 + (k&7)*128 + ((((n&63)>>3) ^ (k&7)) << 4) + (n&7)*2;
+//    a K step of 16 rows advances the start by 2048 B.
+//  M = 128 accumulators: row m lives in TMEM lane m, column n in column n.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+namespace tc {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits give up after 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Wait for the phase with parity `parity` of `bar` to complete, for at most
+// kWaitLimitNs; returns false (and sets `timeout_bit` in *status) on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          int timeout_bit) {
+  const uint32_t addr = smem_u32(bar);
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (it == 0) t0 = global_timer();
+    else if (global_timer() - t0 > kWaitLimitNs) {
+      if (status) atomicOr(status, timeout_bit);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 4-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: bf16 x bf16 -> fp32, M x N, A/B K-major (0) or MN-major (1).
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Whole-warp TMEM allocation; the base address is written to *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols));
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp-wide).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Byte offsets inside 128-byte-swizzled tiles (see the header comment).
+__device__ __forceinline__ uint32_t kmaj_chunk(int r, int c) {  // 16-byte chunk c of row r
+  return (uint32_t)(r * 128 + (((c ^ r) & 7) << 4));
+}
+__device__ __forceinline__ uint32_t mnmaj_chunk(int k, int c, uint32_t lbo) {  // n = 8c .. 8c+7
+  return (uint32_t)((c >> 3) * lbo + (k >> 3) * 1024 + (k & 7) * 128 + ((((c & 7) ^ k) & 7) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store 8 floats as bf16 into a 16-byte chunk.
+__device__ __forceinline__ void st_chunk(uint8_t* base, uint32_t off, const float* x) {
+  uint4 v;
+  v.x = pack_bf16(x[0], x[1]);
+  v.y = pack_bf16(x[2], x[3]);
+  v.z = pack_bf16(x[4], x[5]);
+  v.w = pack_bf16(x[6], x[7]);
+  *reinterpret_cast<uint4*>(base + off) = v;
+}
+
+// Load a 16-byte chunk of 8 bf16 as floats.
+__device__ __forceinline__ void ld_chunk(const uint8_t* base, uint32_t off, float* x) {
+  const uint4 v = *reinterpret_cast<const uint4*>(base + off);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    const float2 f = __bfloat1622float2(b);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+constexpr int LDA = 65;  // default leading dim of the fp32 64 x 64 tiles of the solve
+
+// Cumulative gates are kept in fp32 and in log2 units (G * log2 e), so every
+// decay factor is one exp2f of a difference; fp32 is ample at bf16 tolerance
+// (the fp64 pipe of this part is far too slow for 8K differences per chunk).
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float dexp_(float ga, float gb) { return exp2f(ga - gb); }
+
+// Inclusive prefix sum of x[0..63] in place, by warp 0.
+__device__ __forceinline__ void cumsum64f(float* x) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float v0 = x[lane], v1 = x[lane + 32];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y0 = __shfl_up_sync(0xffffffffu, v0, o);
+      const float y1 = __shfl_up_sync(0xffffffffu, v1, o);
+      if (lane >= o) {
+        v0 += y0;
+        v1 += y1;
+      }
+    }
+    v1 += __shfl_sync(0xffffffffu, v0, 31);
+    x[lane] = v0;
+    x[lane + 32] = v1;
+  }
+}
+
+// T = (I + A)^-1 for strictly lower A (64 x 64, fp32, leading dim LDA): 16 x 16
+// diagonal blocks by substitution, off-diagonal blocks by
+// T_ij = -T_ii sum_{j <= m < i} A_im T_mj, block diagonal by block diagonal.
+// Needs blockDim.x >= 128 and a multiple of 32 (all threads of the block call it).
+__device__ __forceinline__ void solve_unit_lower64(const float* A, float* T, float* Y,
+                                                   const int LDA = 65) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp < 4 && lane < 16) {
+    const int b0 = warp * 16, j = lane;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float v = (i == j) ? 1.f : 0.f;
+#pragma unroll
+      for (int l = 0; l < i; ++l) v = fmaf(-A[(b0 + i) * LDA + b0 + l], x[l], v);
+      x[i] = (i >= j) ? v : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) T[(b0 + i) * LDA + b0 + j] = x[i];
+  }
+  __syncthreads();
+  for (int d = 1; d <= 3; ++d) {
+    const int nb = 4 - d;
+    for (int e = tid; e < nb * 256; e += blockDim.x) {
+      const int bj = e >> 8, bi = bj + d, r = (e >> 4) & 15, c = e & 15;
+      float y = 0.f;
+      for (int m = bj * 16; m < bi * 16; ++m) y = fmaf(A[(bi * 16 + r) * LDA + m], T[m * LDA + bj * 16 + c], y);
+      Y[e] = y;
+    }
+    __syncthreads();
+    for (int e = tid; e < nb * 256; e += blockDim.x) {
+      const int bj = e >> 8, bi = bj + d, r = (e >> 4) & 15, c = e & 15;
+      float t = 0.f;
+#pragma unroll
+      for (int l = 0; l < 16; ++l) t = fmaf(T[(bi * 16 + r) * LDA + bi * 16 + l], Y[(bj << 8) + l * 16 + c], t);
+      T[(bi * 16 + r) * LDA + bj * 16 + c] = -t;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace tc
+}  // namespace gdn

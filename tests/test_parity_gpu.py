@@ -115,6 +115,44 @@ def test_fp32_fwd_bwd_matches_oracle(case):
     check_fwd_bwd(w, inp, segments=seg)
 
 
+BF16_SMALL = [
+    # name, B, T, Hqk, H, segments, h0_std, valid_len, stress
+    ("bf16_T1", 1, 1, 1, 2, 0, 0.1, None, True),
+    ("bf16_T63", 1, 63, 1, 2, 0, 0.1, None, True),
+    ("bf16_T64", 1, 64, 1, 2, 1, None, None, False),
+    ("bf16_T200_seg3", 2, 200, 1, 2, 3, 0.1, None, True),
+    ("bf16_T320_seg2", 1, 320, 2, 4, 2, 0.1, None, True),
+    ("bf16_padded", 2, 300, 1, 2, 2, 0.1, [300, 97], True),
+    ("bf16_r4_default_decay", 1, 256, 1, 4, 2, 0.1, None, False),
+]
+
+
+@pytest.mark.parametrize("case", BF16_SMALL, ids=[c[0] for c in BF16_SMALL])
+def test_bf16_small_fwd_bwd_matches_oracle(case):
+    name, B, T, Hqk, H, seg, h0s, vl, stress = case
+    w = gi.Workload(name, B=B, T=T, Hqk=Hqk, H=H, dk=128, dv=128, dtype=torch.bfloat16,
+                    h0_std=h0s, with_dHT=h0s is not None, valid_len=vl, decay_stress=stress,
+                    seed=17)
+    o, hT, g = check_fwd_bwd(w, gi.make_inputs(w), segments=seg)
+    if vl is not None:
+        for bi, Lb in enumerate(vl):
+            assert (o[bi, Lb:] == 0).all()
+
+
+def test_bf16_summary_matches_oracle():
+    w = gi.Workload("bf16_summary", B=2, T=190, Hqk=1, H=2, dk=128, dv=128, dtype=torch.bfloat16,
+                    decay_stress=True, valid_len=[190, 150], seed=18)
+    inp = gi.make_inputs(w)
+    n = np64(inp)
+    d = dev(inp)
+    M, S = gdn.gdn_summary(d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                           d["valid_len"])
+    rM, rS = oracle.summary(n["k"], n["v"], n["a"], n["b"], n["A_log"], n["dt_bias"],
+                            n["valid_len"])
+    assert_close("M", M, rM, torch.bfloat16)
+    assert_close("S", S, rS, torch.bfloat16)
+
+
 def test_segment_counts_agree_fp32():
     w = gi.Workload("segcount", B=1, T=640, Hqk=2, H=4, dk=32, dv=32, dtype=torch.float32,
                     h0_std=0.1, with_dHT=True, decay_stress=True, seed=12)
