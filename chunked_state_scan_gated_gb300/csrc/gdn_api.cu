@@ -1,14 +1,15 @@
 // gdn_api.cu -- the extern "C" entry points declared in include/gdn.h:
 // validation, workspace layout and the order of kernel launches.
 //
-// Forward with P segments (the pages' p2p / all_gather algebra of "linear
-// attention cp #1035", run on one GPU): chunk prologue -> summaries [M|S] of
-// segments 0..P-2 -> exclusive prefix H_in -> state pass of every segment from
-// its H_in (chunk-start states, V') -> chunk-parallel output.
-// Backward: prologue -> summaries + prefix (forward states recomputed, nothing
-// saved by the forward) -> state pass -> gradient summaries D of segments
-// 1..P-1 -> reverse prefix dH_out -> state-gradient pass of every segment ->
+// Segments follow the p2p / all_gather algebra of "linear attention cp #1035",
+// run on one GPU.  bf16 path (tensor cores): chunk prologue (norm factors,
+// gates, W, U, P tiles) -> summaries [M|S] of segments 0..P-2 -> exclusive
+// prefix H_in -> forward chain of every segment from its H_in (token output).
+// Backward: prologue -> summaries + prefix -> forward chain storing every
+// chunk-start state -> gradient summaries D of segments 1..P-1 -> reverse
+// prefix dH_out -> reverse chain storing every chunk-end state gradient ->
 // chunk-parallel local gradients -> Q/K head sum and norm chain.
+// fp32 path (CUDA cores): the same algebra with the kernels of gdn_simt.cu.
 #include <math.h>
 #include <string.h>
 
@@ -111,7 +112,16 @@ size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws) {
   const bool bwd = op == GDN_OP_BWD;
   const bool fwd = op == GDN_OP_FWD;
   w.status = (int*)take(64);
+  auto take_prep = [&]() {  // norm factors, gates and tile images of the tensor-core prologue
+    w.rqk = take(B * Hqk * NC * 128);
+    w.wim = take(B * H * NC * 4096);
+    w.uim = take(B * H * NC * 4096);
+    w.pim = take(B * H * NC * 2048);
+    w.gl = take(B * H * NC * 64);
+    if (bwd) w.tim = take(B * H * NC * 2048);
+  };
   if (tc_path(pr) && bwd) {
+    take_prep();
     if (P > 1) {
       w.Mseg = take(P * B * H * dk * dk);
       w.Sseg = take(P * B * H * dk * dv);
@@ -127,7 +137,7 @@ size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws) {
     return off;
   }
   if (tc_path(pr) && (fwd || op == GDN_OP_SUMMARY)) {
-    // the tensor-core scan keeps every chunk intermediate on chip
+    take_prep();
     if (fwd && P > 1) {
       w.Mseg = take(P * B * H * dk * dk);
       w.Sseg = take(P * B * H * dk * dv);
@@ -230,19 +240,20 @@ gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* 
   int64_t init_stride = 0;
   const int64_t sstride = pr.B * pr.H * pr.dk * pr.dv;
   if (tc_path(pr)) {
+    GDN_RUN(sc, "prep_tc", launch_prep_tc(pr, in, ws, st));
     if (pr.P > 1) {
-      GDN_RUN(sc, "summary_scan_tc",
-              launch_chunk_scan_tc(pr, in, ws, 1, 0, pr.P - 1, nullptr, 0, nullptr, nullptr,
-                                   ws.Mseg, ws.Sseg, sstride, nullptr, st));
+      GDN_RUN(sc, "summary_chain_tc",
+              launch_chain_tc(pr, in, ws, 1, 0, pr.P - 1, nullptr, 0, nullptr, nullptr, ws.Mseg,
+                              ws.Sseg, sstride, nullptr, st));
       GDN_RUN(sc, "prefix",
               launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Sseg, h0, ws.Hin,
                             nullptr, st));
       init = ws.Hin;
       init_stride = sstride;
     }
-    GDN_RUN(sc, "apply_scan_tc",
-            launch_chunk_scan_tc(pr, in, ws, 0, 0, pr.P, init, init_stride, o, hT, nullptr,
-                                 nullptr, 0, nullptr, st));
+    GDN_RUN(sc, "apply_chain_tc",
+            launch_chain_tc(pr, in, ws, 0, 0, pr.P, init, init_stride, o, hT, nullptr, nullptr,
+                            0, nullptr, st));
     return GDN_OK;
   }
   GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, false, st));
@@ -270,34 +281,35 @@ gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const
   if (tc_path(pr)) {
     const float* init = h0;
     int64_t init_stride = 0;
+    GDN_RUN(sc, "prep_tc", launch_prep_tc(pr, in, ws, st));
     if (pr.P > 1) {
-      GDN_RUN(sc, "summary_scan_tc",
-              launch_chunk_scan_tc(pr, in, ws, 1, 0, pr.P, nullptr, 0, nullptr, nullptr, ws.Mseg,
-                                   ws.Sseg, sstride, nullptr, st));
+      GDN_RUN(sc, "summary_chain_tc",
+              launch_chain_tc(pr, in, ws, 1, 0, pr.P, nullptr, 0, nullptr, nullptr, ws.Mseg,
+                              ws.Sseg, sstride, nullptr, st));
       GDN_RUN(sc, "prefix",
               launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Sseg, h0, ws.Hin,
                             nullptr, st));
       init = ws.Hin;
       init_stride = sstride;
     }
-    GDN_RUN(sc, "states_scan_tc",
-            launch_chunk_scan_tc(pr, in, ws, 2, 0, pr.P, init, init_stride, nullptr, nullptr,
-                                 nullptr, nullptr, 0, ws.hc16, st));
+    GDN_RUN(sc, "states_chain_tc",
+            launch_chain_tc(pr, in, ws, 2, 0, pr.P, init, init_stride, nullptr, nullptr, nullptr,
+                            nullptr, 0, ws.hc16, st));
     const float* dinit = dHT;
     int64_t dinit_stride = 0;
     if (pr.P > 1) {
-      GDN_RUN(sc, "grad_summary_scan_tc",
-              launch_dscan_tc(pr, in, ws, 1, 1, pr.P - 1, nullptr, 0, nullptr, nullptr, ws.Dseg,
-                              sstride, st));
+      GDN_RUN(sc, "grad_summary_chain_tc",
+              launch_dchain_tc(pr, in, ws, 1, 1, pr.P - 1, nullptr, 0, nullptr, nullptr, ws.Dseg,
+                               sstride, st));
       GDN_RUN(sc, "prefix_bwd",
               launch_prefix_bwd(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Dseg, dHT,
                                 ws.dHout, nullptr, st));
       dinit = ws.dHout;
       dinit_stride = sstride;
     }
-    GDN_RUN(sc, "dstate_scan_tc",
-            launch_dscan_tc(pr, in, ws, 0, 0, pr.P, dinit, dinit_stride, ws.dhc16, dH0, nullptr,
-                            0, st));
+    GDN_RUN(sc, "dstate_chain_tc",
+            launch_dchain_tc(pr, in, ws, 0, 0, pr.P, dinit, dinit_stride, ws.dhc16, dH0, nullptr,
+                             0, st));
     GDN_RUN(sc, "grad_tc", launch_grad_tc(pr, in, ws, ws.hc16, ws.dhc16, dv, dg, dbeta, st));
     GDN_RUN(sc, "qk_grad", launch_qk_grad(pr, in, ws, dq, dk, st));
     return GDN_OK;
@@ -528,8 +540,10 @@ gdn_status gdn_summary(const gdn_problem* p, const void* k, const void* v, const
   if ((s = prepare(p, GDN_OP_SUMMARY, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK)
     return s;
   if (tc_path(pr)) {
-    GDN_TRY(launch_chunk_scan_tc(pr, in, ws, 1, 0, 1, nullptr, 0, nullptr, nullptr, M, S, 0,
-                                 nullptr, st));
+    in.q = k;  // the prologue reads a q tile; a summary never uses it
+    GDN_TRY(launch_prep_tc(pr, in, ws, st));
+    GDN_TRY(launch_chain_tc(pr, in, ws, 1, 0, 1, nullptr, 0, nullptr, nullptr, M, S, 0, nullptr,
+                            st));
     return GDN_OK;
   }
   GDN_TRY(launch_prep(pr, in, ws, false, false, st));

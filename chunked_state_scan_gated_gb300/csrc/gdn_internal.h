@@ -47,6 +47,12 @@ struct WS {
   float* dHout; // [P][B][H][dk][dv]
   float* dqp;   // [B][Tp][H][dk]    per-V-head gradient of q_hat
   float* dkp;   // [B][Tp][H][dk]    per-V-head gradient of k_hat
+  float* rqk;   // [B][Hqk][NC][128] per-token norm factors rq = scale/|q|, then rk = 1/|k|
+  void* wim;    // [B][H][NC]   16 KB bf16 tile images of W (tensor-core path)
+  void* uim;    // [B][H][NC]   16 KB tile images of U
+  void* pim;    // [B][H][NC]   8 KB tile images of P = tril(Q K^T o Gamma)
+  void* tim;    // [B][H][NC]   8 KB tile images of T = (I + A)^-1 (backward)
+  float* gl;    // [B][H][NC][64] cumulative gate inside each chunk, log2 units
   void* hc16;   // [B][H][NC][dk][dv] bf16 chunk-start states (tensor-core backward)
   void* dhc16;  // [B][H][NC][dk][dv] bf16 chunk-end state gradients (tensor-core backward)
 };
@@ -97,21 +103,24 @@ cudaError_t launch_prefix_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, cons
 
 // ---- tensor-core (tcgen05) kernels, bf16 with dk = dv = 128 ----
 bool tc_path(const Prob& pr);
-// mode 0: forward over `nseg` segments from `init` (o, final state of the last
-// segment); mode 1: summaries of segments seg_first.. (M_out, S_out); mode 2:
-// forward states only, every chunk-start state to `hc` (bf16 [B][H][NC][dk][dv]).
-cudaError_t launch_chunk_scan_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode,
-                                 int seg_first, int nseg, const float* init,
-                                 int64_t init_seg_stride, void* o, float* final_out,
-                                 float* M_out, float* S_out, int64_t out_seg_stride,
-                                 void* hc, cudaStream_t st);
+// chunk-parallel prologue: norm factors, gates and the W, U, P (and T) tile images
+cudaError_t launch_prep_tc(const Prob& pr, const Inputs& in, const WS& ws, cudaStream_t st);
+// state chain over the prologue's tiles.  mode 0 (apply): o and the final state of
+// the last segment from `init`; mode 1 (summary): M_out, S_out of segments
+// seg_first..; mode 2 (states): every chunk-start state into `hc` (bf16).
+cudaError_t launch_chain_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode,
+                            int seg_first, int nseg, const float* init, int64_t init_seg_stride,
+                            void* o, float* final_out, float* M_out, float* S_out,
+                            int64_t out_seg_stride, void* hc, cudaStream_t st);
 
-// mode 0: reverse state-gradient scan storing every chunk-end gradient (bf16)
-// and the start gradient of segment 0; mode 1: gradient summaries from zero.
-cudaError_t launch_dscan_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode, int seg_first,
-                            int nseg, const float* init, int64_t init_seg_stride, void* dhc,
-                            float* start_out, float* D_out, int64_t out_seg_stride,
-                            cudaStream_t st);
+// reverse chain over the prologue's tiles: mode 0 stores every chunk-end state
+// gradient (bf16) and the start gradient of segment 0; mode 1 writes gradient
+// summaries D of segments seg_first..
+cudaError_t launch_dchain_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode,
+                             int seg_first, int nseg, const float* init, int64_t init_seg_stride,
+                             void* dhc, float* start_out, float* D_out, int64_t out_seg_stride,
+                             cudaStream_t st);
+
 // chunk-parallel gradients from chunk-start states and chunk-end state gradients
 cudaError_t launch_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, const void* hc,
                            const void* dhc, void* dv, float* dg, float* dbeta, cudaStream_t st);

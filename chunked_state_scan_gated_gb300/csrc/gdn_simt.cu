@@ -900,48 +900,78 @@ __global__ void __launch_bounds__(NT) k_compose(int64_t dk, int64_t dv, const fl
   }
 }
 
-// grid (n, ceil(dv / CS)); transpose = 0: forward prefix, 1: reverse with M^T.
+// Exclusive prefix over segments, grid (n, ceil(dv / PCS)), 256 threads.
+// transpose = 0: X <- M[s] X + S[s] for s = 0, 1, ...; transpose = 1: X <- M[s]^T X + S[s]
+// for s = P-1, P-2, ...  Each step stages M[s] (dk x dk) in shared memory with a
+// padded row stride (conflict-free for both orientations) and gives every thread
+// one row of X times PCS / 2 columns, so a step is one coalesced 64 KB read plus a
+// register-blocked fp32 product instead of strided global loads.
+constexpr int PCS = 16;          // state columns per prefix block
+constexpr int PLD = 129;         // shared-memory row stride of M
 __global__ void __launch_bounds__(NT) k_prefix(int64_t n, int64_t P, int64_t dk, int64_t dv,
                                               const float* __restrict__ M,
                                               const float* __restrict__ S,
                                               const float* __restrict__ x0, float* out_seq,
                                               float* out_last, int transpose) {
   extern __shared__ float sm[];
-  float* Xs = sm;            // [dk][CS]
-  float* Ys = Xs + dk * CS;  // [dk][CS]
+  float* Ms = sm;                  // [dk][PLD]
+  float* Xs = Ms + kMaxHeadDim * PLD;  // [dk][PCS]
   const int64_t e0 = blockIdx.x;
-  const int c0 = blockIdx.y * CS;
-  for (int e = threadIdx.x; e < dk * CS; e += NT) {
-    const int i = e / CS, col = c0 + e % CS;
-    Xs[e] = (x0 && col < dv) ? x0[(e0 * dk + i) * dv + col] : 0.f;
+  const int c0 = blockIdx.y * PCS;
+  const int tid = threadIdx.x;
+  const int i = tid >> 1;          // row of X owned by this thread
+  const int j0 = (tid & 1) * (PCS / 2);
+  const bool own = i < dk;
+  float x[PCS / 2];
+#pragma unroll
+  for (int j = 0; j < PCS / 2; ++j) {
+    const int col = c0 + j0 + j;
+    x[j] = (own && x0 && col < dv) ? x0[(e0 * dk + i) * dv + col] : 0.f;
   }
-  __syncthreads();
   for (int64_t step = 0; step < P; ++step) {
     const int64_t s = transpose ? P - 1 - step : step;
-    for (int e = threadIdx.x; e < dk * CS; e += NT) {
-      const int i = e / CS, col = c0 + e % CS;
-      if (col < dv) out_seq[((s * n + e0) * dk + i) * dv + col] = Xs[e];
+    if (own) {
+#pragma unroll
+      for (int j = 0; j < PCS / 2; ++j) {
+        const int col = c0 + j0 + j;
+        if (col < dv) out_seq[((s * n + e0) * dk + i) * dv + col] = x[j];
+      }
     }
     const bool apply = transpose ? (s > 0 || out_last) : (s < P - 1 || out_last);
     if (!apply) break;
-    const float* Ms = M + (s * n + e0) * dk * dk;
-    for (int e = threadIdx.x; e < dk * CS; e += NT) {
-      const int i = e / CS, col = c0 + e % CS;
-      Ys[e] = col < dv ? S[((s * n + e0) * dk + i) * dv + col] : 0.f;
+    const float* Mg = M + (s * n + e0) * dk * dk;
+    __syncthreads();  // previous step's readers of Ms / Xs are done
+    {  // warp-per-row copy: no integer division in the loop
+      const int ndk = (int)dk, warp = tid >> 5, lane = tid & 31;
+      for (int r = warp; r < ndk; r += NT / 32)
+        for (int l = lane; l < ndk; l += 32) Ms[r * PLD + l] = Mg[(int64_t)r * ndk + l];
     }
+#pragma unroll
+    for (int j = 0; j < PCS / 2; ++j)
+      if (own) Xs[i * PCS + j0 + j] = x[j];
     __syncthreads();
-    if (transpose)
-      blk_gemm((int)dk, CS, (int)dk, 1.f, Ms, 1, dk, Xs, CS, 1, true, Ys, CS, 1);
-    else
-      blk_gemm((int)dk, CS, (int)dk, 1.f, Ms, dk, 1, Xs, CS, 1, true, Ys, CS, 1);
-    __syncthreads();
-    for (int e = threadIdx.x; e < dk * CS; e += NT) Xs[e] = Ys[e];
-    __syncthreads();
+    float acc[PCS / 2];
+#pragma unroll
+    for (int j = 0; j < PCS / 2; ++j) {
+      const int col = c0 + j0 + j;
+      acc[j] = (own && col < dv) ? S[((s * n + e0) * dk + i) * dv + col] : 0.f;
+    }
+    if (own) {
+      const int sa_i = transpose ? 1 : PLD, sa_l = transpose ? PLD : 1, ndk = (int)dk;
+      for (int l = 0; l < ndk; ++l) {
+        const float a = Ms[i * sa_i + l * sa_l];
+#pragma unroll
+        for (int j = 0; j < PCS / 2; ++j) acc[j] = fmaf(a, Xs[l * PCS + j0 + j], acc[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < PCS / 2; ++j) x[j] = acc[j];
   }
-  if (out_last) {
-    for (int e = threadIdx.x; e < dk * CS; e += NT) {
-      const int i = e / CS, col = c0 + e % CS;
-      if (col < dv) out_last[(e0 * dk + i) * dv + col] = Xs[e];
+  if (out_last && own) {
+#pragma unroll
+    for (int j = 0; j < PCS / 2; ++j) {
+      const int col = c0 + j0 + j;
+      if (col < dv) out_last[(e0 * dk + i) * dv + col] = x[j];
     }
   }
 }
@@ -1098,8 +1128,8 @@ cudaError_t launch_prefix(int64_t n, int64_t P, int64_t dk, int64_t dv, const fl
                           const float* S, const float* h0, float* Hin, float* Hout,
                           cudaStream_t st) {
   if (n == 0 || P == 0) return cudaSuccess;
-  const size_t smem = sizeof(float) * (size_t)(2 * dk * CS);
-  dim3 grid((unsigned)n, (unsigned)((dv + CS - 1) / CS));
+  const size_t smem = sizeof(float) * (size_t)(kMaxHeadDim * PLD + kMaxHeadDim * PCS);
+  dim3 grid((unsigned)n, (unsigned)((dv + PCS - 1) / PCS));
   cudaError_t e;
   if ((e = set_smem(k_prefix, smem)) != cudaSuccess) return e;
   k_prefix<<<grid, NT, smem, st>>>(n, P, dk, dv, M, S, h0, Hin, Hout, 0);
@@ -1110,8 +1140,8 @@ cudaError_t launch_prefix_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, cons
                               const float* D, const float* dHT, float* dHout, float* dH0,
                               cudaStream_t st) {
   if (n == 0 || P == 0) return cudaSuccess;
-  const size_t smem = sizeof(float) * (size_t)(2 * dk * CS);
-  dim3 grid((unsigned)n, (unsigned)((dv + CS - 1) / CS));
+  const size_t smem = sizeof(float) * (size_t)(kMaxHeadDim * PLD + kMaxHeadDim * PCS);
+  dim3 grid((unsigned)n, (unsigned)((dv + PCS - 1) / PCS));
   cudaError_t e;
   if ((e = set_smem(k_prefix, smem)) != cudaSuccess) return e;
   k_prefix<<<grid, NT, smem, st>>>(n, P, dk, dv, M, D, dHT, dHout, dH0, 1);

@@ -1,17 +1,10 @@
-// gdn_tc_bwd.cu -- tensor-core (tcgen05) kernels of the bf16 backward.
+// gdn_tc_bwd.cu -- chunk-parallel local gradients of the bf16 backward (tcgen05).
 //
-// The backward of the chunked gated delta rule (notation of gdn_simt.cu), with
-// dS the gradient of the state at the end of a chunk:
-//
-//   dV'   = P^T dO + diag(exp(G_C - G)) K dS
-//   dS   <- gamma_C dS + (diag(gamma) Q)^T dO - W^T dV'          (state chain)
-//   local gradients of the chunk from S (chunk start), dS, V', dV'  (chunk-parallel)
-//
-// k_dscan_tc runs the state chain in reverse over the chunks of one segment of
-// one (batch row, V head), storing every dS (bf16) or, from dS = 0, returning
-// the segment's gradient summary D (the reverse-direction state-gradient pass
-// of "linear attention cp #1035", p2p mode).  Layout and phases mirror the
-// forward chunk scan of gdn_tc_fwd.cu.
+// Given every chunk's start state S and the gradient dS of its end state (both
+// bf16, produced by the forward and reverse state chains of gdn_tc_chain.cu),
+// each chunk's gradients are independent of every other chunk's; k_grad_tc
+// computes them one CTA per (chunk, V head) from the chunk's inputs, recomputing
+// the chunk-local intermediates (nothing per chunk is kept by the forward).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <string.h>
@@ -23,7 +16,7 @@
 
 namespace gdn {
 
-// Shared with gdn_tc_fwd.cu: tensor-map encoder for [B, Ts, heads, 128] bf16.
+// Tensor-map encoders of gdn_tc_maps.cu: [B, Ts, heads, 128] inputs and [n][128][128] states.
 bool tc_make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t Ts, int64_t heads);
 bool tc_make_state_map(CUtensorMap* m, const void* ptr, int64_t n);
 
@@ -32,38 +25,6 @@ namespace {
 using namespace tc;
 
 constexpr int FT = 256;
-constexpr uint32_t ATOM = 24576;                     // [W | Q | K] per 64-column atom
-constexpr uint32_t OFF_W = 0, OFF_Q = 8192, OFF_K = 16384;
-constexpr uint32_t OFF_DO = 49152, LBO_DO = 8192;    // dO tile
-constexpr uint32_t OFF_TA = 65536;                   // [T_u; T_w] (only T_w is used)
-constexpr uint32_t OFF_PZ = 81920;                   // [0; P]
-constexpr uint32_t OFF_DS = 98304, LBO_DS = 16384;   // dS bf16 (MN-major, 128 x 128)
-constexpr uint32_t OFF_NDV = 131072, LBO_NDV = 8192; // -dV' (64 x 128)
-constexpr uint32_t OFF_A = 131072;                   // fp32 A, T, Y of the solve (earlier)
-constexpr uint32_t OFF_T = OFF_A + 64 * LDA * 4;
-constexpr uint32_t OFF_Y = OFF_T + 64 * LDA * 4;
-constexpr uint32_t OFF_QKW1 = 172032;
-constexpr uint32_t OFF_SC = OFF_QKW1 + 2 * ATOM;
-constexpr uint32_t SMEM_BYTES = OFF_SC + 2048 + 1024;
-
-struct DscanArgs {
-  int64_t T, Ts, H, r, NC, CPS;
-  int l2norm;
-  float eps, scale;
-  const __nv_bfloat16* a;
-  const __nv_bfloat16* b;
-  const float* A_log;
-  const float* dt_bias;
-  const int32_t* valid_len;
-  const float* init;          // mode 0: dH_out per segment (or dHT); mode 1 unused
-  int64_t init_seg_stride;
-  __nv_bfloat16* dhc;         // mode 0: chunk-end state gradients [B][H][NC][128][128]
-  float* start_out;           // mode 0: gradient of segment 0's initial state
-  float* D_out;               // mode 1: gradient summaries [P][B][H][128][128]
-  int64_t out_seg_stride;
-  int* status;
-  int mode, seg_first, nseg;
-};
 
 #define PHASE_SYNC()            \
   do {                          \
@@ -74,351 +35,7 @@ struct DscanArgs {
     if (*s_abort) goto done;    \
   } while (0)
 
-__global__ void __launch_bounds__(FT, 1)
-    k_dscan_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-               const __grid_constant__ CUtensorMap mdo, DscanArgs ar) {
-  extern __shared__ uint8_t smraw[];
-  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
-  const uint32_t base = smem_u32(sm);
-  float* sG = (float*)(sm + OFF_SC);
-  float* sGam = sG + 64;
-  float* sBeta = sGam + 64;
-  float* sKt = sBeta + 64;
-  uint64_t* bar_qk = (uint64_t*)(sm + OFF_SC + 1536);
-  uint64_t* bar_do = bar_qk + 2;
-  uint64_t* bar_mma = bar_qk + 3;
-  uint32_t* s_tmem = (uint32_t*)(bar_qk + 4);
-  int* s_abort = (int*)(s_tmem + 1);
-  float* sA = (float*)(sm + OFF_A);
-  float* sT = (float*)(sm + OFF_T);
-  float* sY = (float*)(sm + OFF_Y);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, half = warp >> 2;
-  const int row = quad * 32 + lane;
-  const bool store = ar.mode == 0;
-  const int64_t h = blockIdx.y;
-  const int64_t b = blockIdx.z / ar.nseg;
-  const int seg = ar.seg_first + (int)(blockIdx.z % ar.nseg);
-  const int64_t hq = h / ar.r, bh = b * ar.H + h;
-  const int64_t cs = (int64_t)seg * ar.CPS;
-  const int64_t ce = cs + ar.CPS < ar.NC ? cs + ar.CPS : ar.NC;
-  int64_t L = ar.T;
-  if (ar.valid_len) {
-    L = ar.valid_len[b];
-    if (L < 0 || L > ar.T) L = L < 0 ? 0 : ar.T;
-  }
-
-  if (tid == 0) {
-    mbar_init(bar_qk, 1);
-    mbar_init(bar_qk + 1, 1);
-    mbar_init(bar_do, 1);
-    mbar_init(bar_mma, 1);
-    fence_barrier_init();
-    *s_abort = 0;
-  }
-  if (warp == 0) tmem_alloc(s_tmem, 512);
-  for (int e = tid; e < 512; e += FT) reinterpret_cast<uint4*>(sm + OFF_PZ)[e] = make_uint4(0, 0, 0, 0);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *s_tmem;
-  const uint32_t tX = tmem, tD3 = tmem + 256;
-  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-
-  float dS[64];  // gradient of the state at the end of the current chunk: row `row`, cols half*64..
-#pragma unroll
-  for (int j = 0; j < 64; ++j) {
-    const int col = half * 64 + j;
-    dS[j] = (store && ar.init) ? ar.init[seg * ar.init_seg_stride + (bh * 128 + row) * 128 + col] : 0.f;
-  }
-#pragma unroll
-  for (int cc = 0; cc < 8; ++cc) st_chunk(sm + OFF_DS, mnmaj_chunk(row, half * 8 + cc, LBO_DS), &dS[cc * 8]);
-
-  {
-    uint32_t ph_mma = 0;
-    const uint32_t id_qk = idesc_bf16(128, 64, 0, 0);
-    const uint32_t id_kn = idesc_bf16(128, 128, 0, 1);
-    const uint32_t id_mn = idesc_bf16(128, 128, 1, 1);
-    auto issue_qk = [&](int64_t c) {  // chunk c into buffer (ce-1-c) & 1
-      const int64_t kl = ce - 1 - c;
-      const uint32_t qb = (kl & 1) ? OFF_QKW1 : 0u;
-      uint64_t* bar = bar_qk + (kl & 1);
-      mbar_arrive_expect_tx(bar, 32768u);
-      for (int at = 0; at < 2; ++at) {
-        tma_load_4d(sm + qb + at * ATOM + OFF_Q, &mq, at * 64, (int)hq, (int)(c * 64), (int)b, bar);
-        tma_load_4d(sm + qb + at * ATOM + OFF_K, &mk, at * 64, (int)hq, (int)(c * 64), (int)b, bar);
-      }
-    };
-    auto issue_do = [&](int64_t c) {
-      mbar_arrive_expect_tx(bar_do, 16384u);
-      for (int at = 0; at < 2; ++at)
-        tma_load_4d(sm + OFF_DO + at * LBO_DO, &mdo, at * 64, (int)h, (int)(c * 64), (int)b, bar_do);
-    };
-    float a_next = 0.f, b_next = 0.f;
-    auto load_gates = [&](int64_t c) {
-      const int64_t t = c * 64 + tid;
-      if (tid < 64 && t < L) {
-        const int64_t gi = (b * ar.Ts + t) * ar.H + h;
-        a_next = __bfloat162float(ar.a[gi]);
-        b_next = __bfloat162float(ar.b[gi]);
-      }
-    };
-    if (cs < ce) {
-      if (tid == 0) {
-        issue_qk(ce - 1);
-        issue_do(ce - 1);
-      }
-      load_gates(ce - 1);
-    }
-    for (int64_t c = ce - 1; c >= cs; --c) {
-      const int64_t t0 = c * 64;
-      const int64_t kl = ce - 1 - c;
-      const uint32_t qkw = (kl & 1) ? OFF_QKW1 : 0u;
-      fence_proxy_async();
-      __syncthreads();
-      if (tid == 0 && c - 1 >= cs) issue_qk(c - 1);
-      if (tid < 64) {
-        const int64_t t = t0 + tid;
-        float g = 0.f, be = 0.f;
-        if (t < L) {
-          const float x = a_next + ar.dt_bias[h];
-          const float sp = x > 20.f ? x : log1pf(expf(x));
-          g = -expf(ar.A_log[h]) * sp;
-          be = 1.f / (1.f + expf(-b_next));
-        }
-        sG[tid] = g * kLog2e;
-        sBeta[tid] = be;
-      }
-      if (c - 1 >= cs) load_gates(c - 1);
-      if (store) {  // gradient of chunk c's end state, bf16 row-major [dk][dv]
-        uint4* dst = reinterpret_cast<uint4*>(ar.dhc + ((bh * ar.NC + c) * 128 + row) * 128 + half * 64);
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint4 pk;
-          pk.x = pack_bf16(dS[cc * 8 + 0], dS[cc * 8 + 1]);
-          pk.y = pack_bf16(dS[cc * 8 + 2], dS[cc * 8 + 3]);
-          pk.z = pack_bf16(dS[cc * 8 + 4], dS[cc * 8 + 5]);
-          pk.w = pack_bf16(dS[cc * 8 + 6], dS[cc * 8 + 7]);
-          dst[cc] = pk;
-        }
-      }
-      __syncthreads();
-      cumsum64f(sG);
-      __syncthreads();
-      if (tid < 64) {
-        sGam[tid] = exp2f(sG[tid]);
-        sKt[tid] = dexp_(sG[63], sG[tid]);
-      }
-      if (!mbar_wait(bar_qk + (kl & 1), (uint32_t)((kl >> 1) & 1), ar.status, kStatusTimeout)) *s_abort = 1;
-      if (!mbar_wait(bar_do, (uint32_t)(kl & 1), ar.status, kStatusTimeout)) *s_abort = 1;
-      // ---- row norms of q, k (in place); padded tokens get dO = 0
-      for (int it = 0; it < 8; ++it) {
-        const int rr = (tid >> 4) + 16 * it;
-        const bool isk = rr >= 64;
-        const int sub = tid & 15, at = sub >> 3, ch = sub & 7, r6 = rr & 63;
-        const uint32_t off = qkw + at * ATOM + (isk ? OFF_K : OFF_Q) + kmaj_chunk(r6, ch);
-        float x[8];
-        ld_chunk(sm, off, x);
-        float ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        float s = ar.l2norm ? rsqrtf(ss + ar.eps) : 1.f;
-        if (!isk) s *= ar.scale;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] *= s;
-        st_chunk(sm, off, x);
-      }
-      if (t0 + 64 > L) {
-        for (int idx = tid; idx < 1024; idx += FT) {
-          const int i = idx >> 4, cc = idx & 15;
-          if (t0 + i >= L) *reinterpret_cast<uint4*>(sm + OFF_DO + mnmaj_chunk(i, cc, LBO_DO)) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      PHASE_SYNC();
-      // ---- MMA1: [Q;K] K^T -> P (rows 0..63), K K^T (rows 64..127)
-      if (tid == 0) {
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t at = ks >> 2, kk = ks & 3;
-          mma_bf16(tX, sdesc(base + qkw + at * ATOM + OFF_Q + kk * 32, 16, 1024),
-                   sdesc(base + qkw + at * ATOM + OFF_K + kk * 32, 16, 1024), id_qk, ks > 0);
-        }
-        mma_commit(bar_mma);
-      }
-      if (!mbar_wait(bar_mma, ph_mma, ar.status, kStatusTimeout)) *s_abort = 1;
-      ph_mma ^= 1;
-      tc_fence_after();
-      {
-        float v[32];
-        tmem_ld32(tX + lane_off + half * 32, v);
-        if (row < 64) {
-          const int i = row;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            float p[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int j = half * 32 + cc * 8 + e;
-              p[e] = (j <= i) ? v[cc * 8 + e] * dexp_(sG[i], sG[j]) : 0.f;
-            }
-            st_chunk(sm + OFF_PZ, kmaj_chunk(64 + i, half * 4 + cc), p);
-          }
-        } else {
-          const int i = row - 64;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = half * 32 + e;
-            sA[i * LDA + j] = (j < i) ? sBeta[i] * v[e] * dexp_(sG[i], sG[j]) : 0.f;
-          }
-        }
-      }
-      PHASE_SYNC();
-      solve_unit_lower64(sA, sT, sY);
-      for (int q = 0; q < 2; ++q) {  // T_w = T diag(beta gamma) into rows 64..127
-        const int idx = tid + FT * q;
-        const int i = idx >> 3, cc = idx & 7;
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = cc * 8 + e;
-          x[e] = (j <= i) ? sT[i * LDA + j] * sBeta[j] * sGam[j] : 0.f;
-        }
-        st_chunk(sm + OFF_TA, kmaj_chunk(64 + i, cc), x);
-      }
-      PHASE_SYNC();
-      // ---- W = T_w K (rows 64..127 of X[0,128)); K dS (rows 64..127 of X[128,256));
-      //      P^T dO (rows 64..127 of D3)
-      if (tid == 0) {
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tX, sdesc(base + OFF_TA + ks * 32, 16, 1024),
-                   sdesc(base + qkw + OFF_K + ks * 2048, ATOM, 1024), id_kn, ks > 0);
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t at = ks >> 2, kk = ks & 3;
-          mma_bf16(tX + 128, sdesc(base + qkw + at * ATOM + OFF_Q + kk * 32, 16, 1024),
-                   sdesc(base + OFF_DS + ks * 2048, LBO_DS, 1024), id_kn, ks > 0);
-        }
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tD3, sdesc(base + OFF_PZ + ks * 2048, 8192, 1024),
-                   sdesc(base + OFF_DO + ks * 2048, LBO_DO, 1024), id_mn, ks > 0);
-        mma_commit(bar_mma);
-      }
-      if (!mbar_wait(bar_mma, ph_mma, ar.status, kStatusTimeout)) *s_abort = 1;
-      ph_mma ^= 1;
-      tc_fence_after();
-      if (quad >= 2) {
-        const int i = row - 64;
-        const float kt = sKt[i];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float w[32], kd[32], pd[32];
-          tmem_ld32(tX + lane_off + half * 64 + hh * 32, w);
-          tmem_ld32(tX + lane_off + 128 + half * 64 + hh * 32, kd);
-          tmem_ld32(tD3 + lane_off + half * 64 + hh * 32, pd);
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            st_chunk(sm + qkw + half * ATOM + OFF_W, kmaj_chunk(i, hh * 4 + cc), &w[cc * 8]);
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = -(kt * kd[cc * 8 + e] + pd[cc * 8 + e]);
-            st_chunk(sm + OFF_NDV, mnmaj_chunk(i, half * 8 + hh * 4 + cc, LBO_NDV), x);
-          }
-        }
-      }
-      // Q rows scaled by gamma (for (diag(gamma) Q)^T dO)
-      for (int q = 0; q < 4; ++q) {
-        const int idx = tid + FT * q;  // 64 rows x 16 chunks
-        const int i = idx >> 4, at = (idx >> 3) & 1, ch = idx & 7;
-        const uint32_t off = qkw + at * ATOM + OFF_Q + kmaj_chunk(i, ch);
-        float x[8];
-        ld_chunk(sm, off, x);
-        const float gm = sGam[i];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] *= gm;
-        st_chunk(sm, off, x);
-      }
-      PHASE_SYNC();
-      // ---- (diag(gamma) Q)^T dO + W^T (-dV') -> X[0,128)
-      if (tid == 0) {
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tX, sdesc(base + qkw + OFF_Q + ks * 2048, ATOM, 1024),
-                   sdesc(base + OFF_DO + ks * 2048, LBO_DO, 1024), id_mn, ks > 0);
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tX, sdesc(base + qkw + OFF_W + ks * 2048, ATOM, 1024),
-                   sdesc(base + OFF_NDV + ks * 2048, LBO_NDV, 1024), id_mn, 1);
-        mma_commit(bar_mma);
-      }
-      if (!mbar_wait(bar_mma, ph_mma, ar.status, kStatusTimeout)) *s_abort = 1;
-      ph_mma ^= 1;
-      tc_fence_after();
-      if (tid == 0 && c - 1 >= cs) issue_do(c - 1);  // dO(c) consumed
-      {
-        const float gC = sGam[63];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float v[32];
-          tmem_ld32(tX + lane_off + half * 64 + hh * 32, v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) dS[hh * 32 + e] = fmaf(gC, dS[hh * 32 + e], v[e]);
-        }
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          st_chunk(sm + OFF_DS, mnmaj_chunk(row, half * 8 + cc, LBO_DS), &dS[cc * 8]);
-      }
-      PHASE_SYNC();
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 64; ++j) {
-    const int col = half * 64 + j;
-    const int64_t off = (bh * 128 + row) * 128 + col;
-    if (store) {
-      if (ar.start_out && seg == 0) ar.start_out[off] = dS[j];
-    } else if (ar.D_out) {
-      ar.D_out[seg * ar.out_seg_stride + off] = dS[j];
-    }
-  }
-done:
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 512);
-}
-
 }  // namespace
-
-cudaError_t launch_dscan_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode, int seg_first,
-                            int nseg, const float* init, int64_t init_seg_stride, void* dhc,
-                            float* start_out, float* D_out, int64_t out_seg_stride,
-                            cudaStream_t st) {
-  if (nseg <= 0 || pr.B == 0 || pr.NC == 0) return cudaSuccess;
-  CUtensorMap mq, mk, mdo;
-  memset(&mq, 0, sizeof(mq));
-  memset(&mk, 0, sizeof(mk));
-  memset(&mdo, 0, sizeof(mdo));
-  if (!tc_make_map(&mq, in.q, pr.B, pr.T, pr.Ts, pr.Hqk) ||
-      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
-      !tc_make_map(&mdo, in.dO, pr.B, pr.T, pr.Ts, pr.H))
-    return cudaErrorInvalidValue;
-  DscanArgs ar;
-  ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.r = pr.r; ar.NC = pr.NC; ar.CPS = pr.CPS;
-  ar.l2norm = pr.l2norm; ar.eps = pr.eps; ar.scale = pr.scale;
-  ar.a = (const __nv_bfloat16*)in.a; ar.b = (const __nv_bfloat16*)in.b;
-  ar.A_log = in.A_log; ar.dt_bias = in.dt_bias; ar.valid_len = in.valid_len;
-  ar.init = init; ar.init_seg_stride = init_seg_stride;
-  ar.dhc = (__nv_bfloat16*)dhc; ar.start_out = start_out; ar.D_out = D_out;
-  ar.out_seg_stride = out_seg_stride; ar.status = ws.status;
-  ar.mode = mode; ar.seg_first = seg_first; ar.nseg = nseg;
-  cudaError_t e = cudaFuncSetAttribute(k_dscan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  dim3 grid(1, (unsigned)pr.H, (unsigned)(pr.B * nseg));
-  k_dscan_tc<<<grid, FT, SMEM_BYTES, st>>>(mq, mk, mdo, ar);
-  return cudaGetLastError();
-}
 
 // ============================================================================
 // k_grad_tc: every local gradient of one chunk and one V head, given S (the

@@ -1,0 +1,1015 @@
+// gdn_tc_chain.cu -- tensor-core (tcgen05) chunk prologue and forward state chain
+// of the bf16 path (dk = dv = 128, C = 64).
+//
+// The chunked gated delta rule (notation of gdn_simt.cu) splits into work that
+// depends only on one chunk's inputs and a short recurrence on the state:
+//
+//   chunk-local   G = cumsum(g), gamma = e^G, P = tril(Q K^T o Gamma),
+//                 A = tril(diag(beta) K K^T o Gamma, -1), T = (I + A)^-1,
+//                 W = T diag(beta gamma) K,  U = T diag(beta) V
+//   recurrence    V' = U - W S,  O = diag(gamma) Q S + P V',
+//                 S <- gamma_C S + K^T diag(e^{G_C - G}) V'
+//
+// k_prep_tc runs the chunk-local part once for every (chunk, V head) in
+// parallel and leaves its results in the workspace as bf16 "tile images": the
+// exact bytes of a 128-byte-swizzled K-major shared-memory tile, so that a
+// consumer fetches each with one plain bulk copy and hands it to tcgen05.mma
+// as is.  k_chain_tc then walks the chunks of one segment of one (batch row,
+// V head) with the state in fp32 registers and only the two state products
+// per chunk (W S, then K^T V2) on its critical path.  It produces segment
+// summaries (the "p2p" map H_out = M H_in + S of "linear attention cp #1035":
+// M from the identity with U = 0, S from zero), the token output from a given
+// initial state, or every chunk-start state for the backward.
+//
+// Tile images (bf16): a [64][128] matrix is two 8 KB atoms (columns 0..63,
+// 64..127); row r, 16-byte chunk c of an atom sits at r*128 + ((c ^ r) & 7)*16.
+// A [64][64] matrix is one atom.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <string.h>
+
+#include "gdn_internal.h"
+#include "gdn_tc_common.cuh"
+
+namespace gdn {
+
+bool tc_make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t Ts, int64_t heads);
+
+namespace {
+
+using namespace tc;
+
+constexpr uint32_t kImg = 16384;   // bytes of a [64][128] tile image
+constexpr uint32_t kImgP = 8192;   // bytes of a [64][64] tile image
+
+__device__ __forceinline__ uint32_t img_chunk(int r, int c16) {  // 16-byte chunk c16 (0..15) of row r
+  return (uint32_t)((c16 >> 3) * 8192) + kmaj_chunk(r, c16 & 7);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* x) {
+  uint4 v;
+  v.x = pack_bf16(x[0], x[1]);
+  v.y = pack_bf16(x[2], x[3]);
+  v.z = pack_bf16(x[4], x[5]);
+  v.w = pack_bf16(x[6], x[7]);
+  return v;
+}
+
+__device__ __forceinline__ int64_t clamp_len(const int32_t* valid_len, int64_t b, int64_t T,
+                                             int* status, bool report) {
+  if (!valid_len) return T;
+  int64_t L = valid_len[b];
+  if (L < 0 || L > T) {
+    if (report && status) atomicOr(status, kStatusClamped);
+    L = L < 0 ? 0 : T;
+  }
+  return L;
+}
+
+// ============================================================================
+// k_prep_tc: grid (NC, H, B), 256 threads.  Warp w reads TMEM lane quadrant
+// w & 3 (tile row `row`) and handles column half w >> 2 of that row.
+//
+// The q and k row norms come from the diagonal of one product [Q;K][Q;K]^T of
+// the raw tiles, so neither tile is rewritten: every later use of q_hat = rq q
+// and k_hat = rk k applies the per-token factors rq = scale / |q|, rk = 1 / |k|
+// (kept in the workspace) to an fp32 result or to a row of bf16 operands.
+// ============================================================================
+constexpr int PT = 256;
+constexpr uint32_t P_QK = 0;                   // atoms a at a*16384: [Q_a | K_a], raw, 8 KB each
+constexpr uint32_t P_V = 32768;                // V atoms at a*8192
+constexpr uint32_t P_TA = 49152;               // [T_u; T_w], 128 x 64 K-major
+constexpr uint32_t P_A = 65536;                // fp32 A [64][LDA]
+constexpr uint32_t P_T = P_A + 64 * LDA * 4;   // fp32 T [64][LDA]
+constexpr uint32_t P_Y = P_T + 64 * LDA * 4;   // solve scratch, 768 floats
+constexpr uint32_t P_SC = P_Y + 768 * 4;       // gates, row factors, barriers
+constexpr uint32_t P_SMEM = P_SC + 1280 + 64 + 1024;
+
+struct PrepArgs {
+  int64_t T, Ts, H, Hqk, r, NC;
+  int l2norm;
+  float eps, scale;
+  const __nv_bfloat16* a;
+  const __nv_bfloat16* b;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* valid_len;
+  float* rqk;    // [B][Hqk][NC][128]: rq of the chunk's 64 tokens, then rk
+  uint8_t* wim;  // [B][H][NC] images of W
+  uint8_t* uim;  // [B][H][NC] images of U
+  uint8_t* pim;  // [B][H][NC] images of P (64 x 64)
+  uint8_t* tim;  // [B][H][NC] images of T = (I + A)^-1 (64 x 64), or null
+  float* gl;     // [B][H][NC][64] cumulative gate in log2 units
+  int* status;
+};
+
+__global__ void __launch_bounds__(PT, 2)
+    k_prep_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+              const __grid_constant__ CUtensorMap mv, PrepArgs ar) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const uint32_t base = smem_u32(sm);
+  float* sG = (float*)(sm + P_SC);
+  float* sGam = sG + 64;
+  float* sBeta = sGam + 64;
+  float* sInv = sBeta + 64;  // [128]: rq (rows 0..63), rk (rows 64..127)
+  uint64_t* bar_qk = (uint64_t*)(sm + P_SC + 1280);
+  uint64_t* bar_v = bar_qk + 1;
+  uint64_t* bar_mma = bar_qk + 2;
+  uint32_t* s_tmem = (uint32_t*)(bar_qk + 3);
+  int* s_abort = (int*)(s_tmem + 1);
+  float* sA = (float*)(sm + P_A);
+  float* sT = (float*)(sm + P_T);
+  float* sY = (float*)(sm + P_Y);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int row = quad * 32 + lane;  // TMEM lane of this thread
+  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t hq = h / ar.r, bh = b * ar.H + h;
+  const int64_t t0 = c * 64;
+  const int64_t L = clamp_len(ar.valid_len, b, ar.T, ar.status, tid == 0 && c == 0 && h == 0);
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+
+  if (tid == 0) {
+    mbar_init(bar_qk, 1);
+    mbar_init(bar_v, 1);
+    mbar_init(bar_mma, 1);
+    fence_barrier_init();
+    *s_abort = 0;
+  }
+  if (warp == 0) tmem_alloc(s_tmem, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_qk, 32768u);
+    for (int at = 0; at < 2; ++at) {
+      tma_load_4d(sm + P_QK + at * 16384, &mq, at * 64, (int)hq, (int)t0, (int)b, bar_qk);
+      tma_load_4d(sm + P_QK + at * 16384 + 8192, &mk, at * 64, (int)hq, (int)t0, (int)b, bar_qk);
+    }
+    mbar_arrive_expect_tx(bar_v, 16384u);
+    for (int at = 0; at < 2; ++at)
+      tma_load_4d(sm + P_V + at * 8192, &mv, at * 64, (int)h, (int)t0, (int)b, bar_v);
+  }
+  if (tid < 64) {
+    const int64_t t = t0 + tid;
+    float g = 0.f, be = 0.f;
+    if (t < L) {
+      const int64_t gi = (b * ar.Ts + t) * ar.H + h;
+      const float x = __bfloat162float(ar.a[gi]) + ar.dt_bias[h];
+      const float sp = x > 20.f ? x : log1pf(expf(x));
+      g = -expf(ar.A_log[h]) * sp;
+      be = 1.f / (1.f + expf(-__bfloat162float(ar.b[gi])));
+    }
+    sG[tid] = g * kLog2e;
+    sBeta[tid] = be;
+  }
+  __syncthreads();
+  cumsum64f(sG);
+  __syncthreads();
+  if (tid < 64) {
+    sGam[tid] = exp2f(sG[tid]);
+    ar.gl[(bh * ar.NC + c) * 64 + tid] = sG[tid];
+  }
+  if (!mbar_wait(bar_qk, 0, ar.status, kStatusTimeout)) *s_abort = 1;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (*s_abort) goto done;
+  // ---- [Q; K] [Q; K]^T -> cols [0, 128): row norms on the diagonal, Q K^T and K K^T in cols 64..127
+  if (tid == 0) {
+    const uint32_t id = idesc_bf16(128, 128, 0, 0);
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t at = ks >> 2, kk = ks & 3;
+      const uint64_t d = sdesc(base + P_QK + at * 16384 + kk * 32, 16, 1024);
+      mma_bf16(tmem, d, d, id, ks > 0);
+    }
+    mma_commit(bar_mma);
+  }
+  if (!mbar_wait(bar_mma, 0, ar.status, kStatusTimeout)) *s_abort = 1;
+  tc_fence_after();
+  if (half == 0) {  // diagonal element (row, row) sits in column group `quad`, element `lane`
+    float d[32];
+    tmem_ld32(tmem + lane_off + 32 * quad, d);
+    float nrm = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) nrm = (e == lane) ? d[e] : nrm;
+    float inv = ar.l2norm ? rsqrtf(nrm + ar.eps) : 1.f;
+    if (row < 64) inv *= ar.scale;
+    sInv[row] = inv;
+  }
+  __syncthreads();
+  if (h % ar.r == 0 && tid < 128) ar.rqk[((b * ar.Hqk + hq) * ar.NC + c) * 128 + tid] = sInv[tid];
+  {
+    float v[32];  // row . k_j for j = 32*half + e
+    tmem_ld32(tmem + lane_off + 64 + 32 * half, v);
+    const int i = row & 63;
+    const float gi = sG[i], si = sInv[row];
+    if (row < 64) {
+      uint8_t* dst = ar.pim + (bh * ar.NC + c) * (int64_t)kImgP;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = half * 32 + cc * 8 + e;
+          p[e] = (j <= i) ? v[cc * 8 + e] * si * sInv[64 + j] * exp2f(gi - sG[j]) : 0.f;
+        }
+        *reinterpret_cast<uint4*>(dst + kmaj_chunk(i, half * 4 + cc)) = pack8(p);
+      }
+    } else {
+      const float bs = sBeta[i] * si;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = half * 32 + e;
+        sA[i * LDA + j] = (j < i) ? bs * v[e] * sInv[64 + j] * exp2f(gi - sG[j]) : 0.f;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  solve_unit_lower64(sA, sT, sY);
+  if (ar.tim) {  // T for the backward, bf16 image
+    uint8_t* dst = ar.tim + (bh * ar.NC + c) * (int64_t)kImgP;
+    for (int e = tid; e < 512; e += PT) {
+      const int i = e >> 3, cc = e & 7;
+      float x[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int j = cc * 8 + q;
+        x[q] = (j <= i) ? sT[i * LDA + j] : 0.f;
+      }
+      *reinterpret_cast<uint4*>(dst + kmaj_chunk(i, cc)) = pack8(x);
+    }
+  }
+  // [T_u; T_w] = [T diag(beta); T diag(beta gamma rk)] in bf16 (W is formed from raw k)
+  for (int e = tid; e < 1024; e += PT) {
+    const int rr = e >> 3, cc = e & 7, i = rr & 63;
+    const bool w = rr >= 64;
+    float x[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = cc * 8 + q;
+      x[q] = (j <= i) ? sT[i * LDA + j] * sBeta[j] * (w ? sGam[j] * sInv[64 + j] : 1.f) : 0.f;
+    }
+    st_chunk(sm + P_TA, kmaj_chunk(rr, cc), x);
+  }
+  if (!mbar_wait(bar_v, 0, ar.status, kStatusTimeout)) *s_abort = 1;
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (*s_abort) goto done;
+  // ---- [T_u; T_w] V -> cols [0,128) (U in rows 0..63); [T_u; T_w] K -> cols [128,256) (W in 64..127)
+  if (tid == 0) {
+    const uint32_t id = idesc_bf16(128, 128, 0, 1);
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t a = sdesc(base + P_TA + ks * 32, 16, 1024);
+      mma_bf16(tmem, a, sdesc(base + P_V + ks * 2048, 8192, 1024), id, ks > 0);
+      mma_bf16(tmem + 128, a, sdesc(base + P_QK + 8192 + ks * 2048, 16384, 1024), id, ks > 0);
+    }
+    mma_commit(bar_mma);
+  }
+  if (!mbar_wait(bar_mma, 1, ar.status, kStatusTimeout)) *s_abort = 1;
+  tc_fence_after();
+  {
+    const bool isw = row >= 64;
+    const int i = row & 63;
+    uint8_t* dst = (isw ? ar.wim : ar.uim) + (bh * ar.NC + c) * (int64_t)kImg;
+    const uint32_t src = tmem + lane_off + (isw ? 128 : 0) + 64 * half;
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      float v[32];
+      tmem_ld32(src + q2 * 32, v);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        *reinterpret_cast<uint4*>(dst + img_chunk(i, half * 8 + q2 * 4 + cc)) = pack8(&v[cc * 8]);
+    }
+  }
+done:
+  if (*s_abort && tid == 0) {  // let the loads still in flight land before the CTA exits
+    mbar_wait(bar_qk, 0, nullptr, 0);
+    mbar_wait(bar_v, 0, nullptr, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ============================================================================
+// k_chain_tc: grid (parts, H, B * nseg), 256 threads.  Warp w reads TMEM lane
+// quadrant w & 3 (state row `row`) and owns state columns (w >> 2) * 64 .. +63.
+// q and k tiles are the raw inputs (TMA); their norm factors rq, rk come from
+// the prologue and are applied to the rows of V2 and of the scaled q tile.
+// ============================================================================
+constexpr int CT = 256;
+enum { CH_APPLY = 0, CH_SUM = 1, CH_STATES = 2 };
+
+// Summary / states layout (one buffer; two CTAs fit on an SM).
+constexpr uint32_t S_XA = 0;        // atoms a at a*16384: [W_a | K_a]
+constexpr uint32_t S_U = 32768;     // U image
+constexpr uint32_t S_S = 49152;     // state, bf16, MN-major (column halves 16 KB apart)
+constexpr uint32_t S_V2 = 81920;    // V2 = diag(rk e^{G_C - G}) V', MN-major (halves 8 KB apart)
+constexpr uint32_t S_G = 98304;     // G of the chunk (64 floats), then rk (64 floats)
+constexpr uint32_t S_SC = 98816;    // barriers
+constexpr uint32_t S_SMEM = S_SC + 128 + 1024;
+
+// Apply layout ([W | Q | K] double-buffered; U, P single).
+constexpr uint32_t A_XA = 0;        // buffer x at x*49152; atoms a at a*24576: [W_a | Q_a | K_a]
+constexpr uint32_t A_U = 98304;
+constexpr uint32_t A_PZ = 114688;   // [0; P]: 64 zero rows then P, 128 x 64 K-major
+constexpr uint32_t A_S = 131072;
+constexpr uint32_t A_VP = 163840;   // V'
+constexpr uint32_t A_V2 = 180224;
+constexpr uint32_t A_G = 196608;    // buffer x at x*768: G (64 floats), rq (64), rk (64)
+constexpr uint32_t A_SC = 198144;
+constexpr uint32_t A_SMEM = A_SC + 128 + 1024;
+
+struct ChainArgs {
+  int64_t T, Ts, H, Hqk, r, NC, CPS;
+  int P;
+  const float* rqk;
+  const uint8_t* wim;
+  const uint8_t* uim;
+  const uint8_t* pim;
+  const float* gl;
+  const int32_t* valid_len;
+  const float* init;
+  int64_t init_seg_stride;
+  __nv_bfloat16* o;
+  float* final_out;
+  float* M_out;
+  float* S_out;
+  int64_t out_seg_stride;
+  __nv_bfloat16* hc;  // CH_STATES: chunk-start states [B][H][NC][128][128]
+  int* status;
+  int seg_first, nseg;
+};
+
+#define CHAIN_SYNC()            \
+  do {                          \
+    fence_proxy_async();        \
+    tc_fence_before();          \
+    __syncthreads();            \
+    tc_fence_after();           \
+    if (*s_abort) goto done;    \
+  } while (0)
+
+template <int MODE>
+__global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
+    k_chain_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+               ChainArgs ar) {
+  constexpr bool kApply = MODE == CH_APPLY;
+  constexpr uint32_t XSTR = kApply ? 24576 : 16384;  // atom stride in the [W | (Q) | K] block
+  constexpr uint32_t KOFF = kApply ? 16384 : 8192;   // K's offset inside an atom
+  constexpr uint32_t OFF_S = kApply ? A_S : S_S;
+  constexpr uint32_t OFF_U = kApply ? A_U : S_U;
+  constexpr uint32_t OFF_V2 = kApply ? A_V2 : S_V2;
+  constexpr uint32_t OFF_SC = kApply ? A_SC : S_SC;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const uint32_t base = smem_u32(sm);
+  // apply: xa0, xa1, u, p, mma; otherwise: w, k, u, -, mma
+  uint64_t* bars = (uint64_t*)(sm + OFF_SC);
+  uint64_t* bar_u = bars + 2;
+  uint64_t* bar_mma = bars + 4;
+  uint32_t* s_tmem = (uint32_t*)(bars + 6);
+  int* s_abort = (int*)(s_tmem + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int row = quad * 32 + lane;
+  const bool mpart = MODE == CH_SUM && blockIdx.x == 1;
+  const bool needU = !mpart;
+  const int64_t h = blockIdx.y;
+  const int64_t b = blockIdx.z / ar.nseg;
+  const int seg = ar.seg_first + (int)(blockIdx.z % ar.nseg);
+  const int64_t hq = h / ar.r, bh = b * ar.H + h;
+  const int64_t cs = (int64_t)seg * ar.CPS;
+  const int64_t ce = cs + ar.CPS < ar.NC ? cs + ar.CPS : ar.NC;
+  const int64_t L = clamp_len(ar.valid_len, b, ar.T, ar.status, false);
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  uint32_t pend = 0;  // tid 0: barriers with a copy or MMA in flight (drained on an abort)
+
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
+    fence_barrier_init();
+    *s_abort = 0;
+  }
+  if (warp == 0) tmem_alloc(s_tmem, 256);
+  if (kApply)  // zero rows of [0; P]
+    for (int e = tid; e < 512; e += CT) reinterpret_cast<uint4*>(sm + A_PZ)[e] = make_uint4(0, 0, 0, 0);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tA = tmem, tB = tmem + 128;
+
+  float S[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    const int col = half * 64 + j;
+    float x = 0.f;
+    if (MODE != CH_SUM) {
+      if (ar.init) x = ar.init[seg * ar.init_seg_stride + (bh * 128 + row) * 128 + col];
+    } else if (mpart) {
+      x = (row == col) ? 1.f : 0.f;
+    }
+    S[j] = x;
+  }
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) st_chunk(sm + OFF_S, mnmaj_chunk(row, half * 8 + cc, 16384), &S[cc * 8]);
+
+  {
+    const uint8_t* wsrc = ar.wim + bh * ar.NC * (int64_t)kImg;
+    const uint8_t* usrc = ar.uim + bh * ar.NC * (int64_t)kImg;
+    const uint8_t* psrc = ar.pim + bh * ar.NC * (int64_t)kImgP;
+    const float* gsrc = ar.gl + bh * ar.NC * 64;
+    const float* rsrc = ar.rqk + (b * ar.Hqk + hq) * ar.NC * 128;
+    // ---- load issue (tid 0 only)
+    auto issue_x = [&](int64_t c, uint64_t* bar, uint32_t xa, uint32_t gbuf) {
+      // apply: W, Q, K, G, rq, rk; otherwise W only
+      mbar_arrive_expect_tx(bar, kApply ? 3 * kImg + 768 : kImg);
+      for (int a = 0; a < 2; ++a) {
+        bulk_load(sm + xa + a * XSTR, wsrc + c * kImg + a * 8192, 8192, bar);
+        if (kApply) {
+          tma_load_4d(sm + xa + a * XSTR + 8192, &mq, a * 64, (int)hq, (int)(c * 64), (int)b, bar);
+          tma_load_4d(sm + xa + a * XSTR + KOFF, &mk, a * 64, (int)hq, (int)(c * 64), (int)b, bar);
+        }
+      }
+      if (kApply) {
+        bulk_load(sm + gbuf, gsrc + c * 64, 256, bar);
+        bulk_load(sm + gbuf + 256, rsrc + c * 128, 512, bar);
+      }
+    };
+    auto issue_k = [&](int64_t c) {  // summary / states: K, G, rk
+      mbar_arrive_expect_tx(bars + 1, kImg + 512);
+      for (int a = 0; a < 2; ++a)
+        tma_load_4d(sm + S_XA + a * XSTR + KOFF, &mk, a * 64, (int)hq, (int)(c * 64), (int)b, bars + 1);
+      bulk_load(sm + S_G, gsrc + c * 64, 256, bars + 1);
+      bulk_load(sm + S_G + 256, rsrc + c * 128 + 64, 256, bars + 1);
+    };
+    auto issue_u = [&](int64_t c) {
+      mbar_arrive_expect_tx(bar_u, kImg);
+      bulk_load(sm + OFF_U, usrc + c * kImg, kImg, bar_u);
+    };
+    auto issue_p = [&](int64_t c) {
+      mbar_arrive_expect_tx(bars + 3, kImgP);
+      bulk_load(sm + A_PZ + 8192, psrc + c * kImgP, kImgP, bars + 3);
+    };
+    if (tid == 0 && cs < ce) {
+      if (kApply) {
+        issue_x(cs, bars + 0, A_XA, A_G);
+        pend |= 1u;
+        if (cs + 1 < ce) {
+          issue_x(cs + 1, bars + 1, A_XA + 49152, A_G + 768);
+          pend |= 2u;
+        }
+        issue_u(cs);
+        issue_p(cs);
+        pend |= 4u | 8u;
+      } else {
+        issue_x(cs, bars + 0, S_XA, 0);
+        issue_k(cs);
+        pend |= 1u | 2u;
+        if (needU) {
+          issue_u(cs);
+          pend |= 4u;
+        }
+      }
+    }
+    for (int64_t c = cs; c < ce; ++c) {
+      const int64_t k = c - cs;
+      const int64_t t0 = c * 64;
+      const uint32_t par = (uint32_t)(k & 1);
+      const uint32_t bi = kApply ? (uint32_t)(k & 1) : 0u;
+      const uint32_t xa = kApply ? A_XA + bi * 49152 : S_XA;
+      // per-chunk vectors: G, then (apply) rq, then rk
+      const float* sGc = (const float*)(sm + (kApply ? A_G + bi * 768 : S_G));
+      const float* sRk = sGc + (kApply ? 128 : 64);
+      const uint32_t xpar = kApply ? (uint32_t)((k >> 1) & 1) : par;
+      uint64_t* bar_x = bars + (kApply ? bi : 0);
+      // ---- inputs of chunk c
+      if (!mbar_wait(bar_x, xpar, ar.status, kStatusTimeout)) *s_abort = 1;
+      if (tid == 0) pend &= kApply ? ~(1u << bi) : ~1u;
+      if (!kApply) {
+        if (!mbar_wait(bars + 1, par, ar.status, kStatusTimeout)) *s_abort = 1;
+        if (tid == 0) pend &= ~2u;
+      }
+      if (kApply) {  // q rows scaled by gamma_i rq_i (every chunk of a row shares the factor)
+        for (int e = tid; e < 1024; e += CT) {
+          const int r = e >> 4, at = (e >> 3) & 1, p = e & 7;
+          const uint32_t off = xa + at * XSTR + 8192 + r * 128 + p * 16;
+          float x[8];
+          ld_chunk(sm, off, x);
+          const float f = exp2f(sGc[r]) * sGc[64 + r];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x[q] *= f;
+          st_chunk(sm, off, x);
+        }
+      }
+      const float gC = exp2f(sGc[63]);
+      const float kt = exp2f(sGc[63] - sGc[row & 63]) * sRk[row & 63];
+      if (MODE == CH_STATES) {  // chunk-start state, bf16 row-major [dk][dv]
+        uint4* dst = reinterpret_cast<uint4*>(ar.hc + ((bh * ar.NC + c) * 128 + row) * 128 + half * 64);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) dst[cc] = pack8(&S[cc * 8]);
+      }
+      CHAIN_SYNC();
+      // ---- MMA_a: [W; Q or K] S -> tA (W S in rows 0..63)
+      if (tid == 0) {
+        const uint32_t id = idesc_bf16(128, 128, 0, 1);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t at = ks >> 2, kk = ks & 3;
+          mma_bf16(tA, sdesc(base + xa + at * XSTR + kk * 32, 16, 1024),
+                   sdesc(base + OFF_S + ks * 2048, 16384, 1024), id, ks > 0);
+        }
+        mma_commit(bar_mma);
+        pend |= 16u;
+      }
+      if (needU && quad < 2) {
+        if (!mbar_wait(bar_u, par, ar.status, kStatusTimeout)) *s_abort = 1;
+        if (tid == 0) pend &= ~4u;
+      }
+      if (!mbar_wait(bar_mma, 0, ar.status, kStatusTimeout)) *s_abort = 1;
+      if (tid == 0) pend &= ~16u;
+      tc_fence_after();
+      if (!kApply && tid == 0 && c + 1 < ce) {  // W(c) consumed
+        issue_x(c + 1, bars + 0, S_XA, 0);
+        pend |= 1u;
+      }
+      if (quad < 2) {  // V' = U - W S, V2 = rk e^{G_C - G} V'
+        const int i = row;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[32];
+          tmem_ld32(tA + lane_off + half * 64 + hh * 32, v);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int chn = half * 8 + hh * 4 + cc;
+            float u[8];
+            if (needU) {
+              ld_chunk(sm + OFF_U, img_chunk(i, chn), u);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) u[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) u[e] -= v[cc * 8 + e];
+            if (kApply) st_chunk(sm + A_VP, mnmaj_chunk(i, chn, 8192), u);
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = kt * u[e];
+            st_chunk(sm + OFF_V2, mnmaj_chunk(i, chn, 8192), x);
+          }
+        }
+      }
+      CHAIN_SYNC();
+      // ---- MMA_b: K^T V2 -> tB; apply: MMA_c: [0; P] V' accumulated into tA rows 64..127
+      if (tid == 0) {
+        if (needU && c + 1 < ce) {  // U(c) consumed
+          issue_u(c + 1);
+          pend |= 4u;
+        }
+        const uint32_t id = idesc_bf16(128, 128, 1, 1);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tB, sdesc(base + xa + KOFF + ks * 2048, XSTR, 1024),
+                   sdesc(base + OFF_V2 + ks * 2048, 8192, 1024), id, ks > 0);
+        if (kApply) {
+          if (!mbar_wait(bars + 3, par, ar.status, kStatusTimeout)) *s_abort = 1;
+          pend &= ~8u;
+          const uint32_t id2 = idesc_bf16(128, 128, 0, 1);
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tA, sdesc(base + A_PZ + ks * 32, 16, 1024),
+                     sdesc(base + A_VP + ks * 2048, 8192, 1024), id2, 1);
+        }
+        mma_commit(bar_mma);
+        pend |= 16u;
+      }
+      if (!mbar_wait(bar_mma, 1, ar.status, kStatusTimeout)) *s_abort = 1;
+      if (tid == 0) pend &= ~16u;
+      tc_fence_after();
+      if (tid == 0 && c + 1 < ce) {
+        if (kApply) {
+          issue_p(c + 1);  // P(c) consumed by MMA_c
+          pend |= 8u;
+          if (c + 2 < ce) {  // buffer bi free: MMA_a, MMA_b of chunk c are done
+            issue_x(c + 2, bars + bi, xa, A_G + bi * 768);
+            pend |= 1u << bi;
+          }
+        } else {
+          issue_k(c + 1);  // K(c) consumed by MMA_b; G(c), rk(c) already read
+          pend |= 2u;
+        }
+      }
+      {  // S <- gamma_C S + K^T V2
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[32];
+          tmem_ld32(tB + lane_off + half * 64 + hh * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) S[hh * 32 + e] = fmaf(gC, S[hh * 32 + e], v[e]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          st_chunk(sm + OFF_S, mnmaj_chunk(row, half * 8 + cc, 16384), &S[cc * 8]);
+      }
+      if (kApply && quad >= 2) {  // O = gamma Q S + P V' (rows 64..127 of tA)
+        const int i = row - 64;
+        const int64_t t = t0 + i;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[32];
+          tmem_ld32(tA + lane_off + half * 64 + hh * 32, v);
+          if (t < ar.T) {
+            uint4* dst = reinterpret_cast<uint4*>(ar.o + ((b * ar.Ts + t) * ar.H + h) * 128 + half * 64 + hh * 32);
+            if (t >= L) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = 0.f;
+            }
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) dst[cc] = pack8(&v[cc * 8]);
+          }
+        }
+      }
+      CHAIN_SYNC();
+    }
+  }
+  {  // ---- final state
+    float* dst = nullptr;
+    if (kApply) {
+      if (seg == ar.P - 1) dst = ar.final_out;
+    } else if (MODE == CH_SUM) {
+      dst = mpart ? ar.M_out : ar.S_out;
+      if (dst) dst += seg * ar.out_seg_stride;
+    }
+    if (dst) {
+      float4* d4 = reinterpret_cast<float4*>(dst + (bh * 128 + row) * 128 + half * 64);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) d4[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+    }
+  }
+done:
+  if (tid == 0 && pend) {  // abort: let every copy and MMA still in flight finish first
+    for (int i = 0; i < 5; ++i)
+      if (pend & (1u << i)) {
+        // one of the two parities is the phase in flight; the other returns at once
+        mbar_wait(bars + i, 0, nullptr, 0);
+        mbar_wait(bars + i, 1, nullptr, 0);
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ============================================================================
+// k_dchain_tc: the reverse chain of the backward, grid (1, H, B * nseg), 256
+// threads, chunks of one segment walked from the last to the first.  With dS
+// the gradient of the state at the end of a chunk:
+//
+//   dV' = P^T dO + diag(rk e^{G_C - G}) K dS
+//   dS <- gamma_C dS + (diag(gamma rq) Q)^T dO - W^T dV'
+//
+// mode 0 stores every chunk's dS (bf16) and the start gradient of segment 0;
+// mode 1 starts from dS = 0 and returns the segment's gradient summary D (the
+// reverse-direction state-gradient pass of "linear attention cp #1035").
+// ============================================================================
+constexpr uint32_t D_XA = 0;        // atoms a at a*16384: [Kt_a | Qg_a] (scaled k, scaled q)
+constexpr uint32_t D_W = 32768;     // W image
+constexpr uint32_t D_P = 49152;     // P image; the 64 rows after it (dO) stand in as junk A rows
+constexpr uint32_t D_DO = 57344;    // dO tile, later -dV' (MN-major, halves 8 KB apart)
+constexpr uint32_t D_DS = 73728;    // dS, bf16, MN-major (halves 16 KB apart)
+constexpr uint32_t D_G = 106496;    // G, rq, rk of the chunk (64 floats each)
+constexpr uint32_t D_SC = 107264;   // barriers
+constexpr uint32_t D_SMEM = D_SC + 128 + 1024;
+
+struct DchainArgs {
+  int64_t T, Ts, H, Hqk, r, NC, CPS;
+  const float* rqk;
+  const uint8_t* wim;
+  const uint8_t* pim;
+  const float* gl;
+  const int32_t* valid_len;
+  const float* init;          // mode 0: gradient at the end of each segment
+  int64_t init_seg_stride;
+  __nv_bfloat16* dhc;         // mode 0: chunk-end state gradients [B][H][NC][128][128]
+  float* start_out;           // mode 0: gradient at the start of segment 0
+  float* D_out;               // mode 1: gradient summaries
+  int64_t out_seg_stride;
+  int* status;
+  int mode, seg_first, nseg;
+};
+
+__global__ void __launch_bounds__(CT, 2)
+    k_dchain_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                const __grid_constant__ CUtensorMap mdo, DchainArgs ar) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const uint32_t base = smem_u32(sm);
+  uint64_t* bars = (uint64_t*)(sm + D_SC);  // a: K, Q, P, G/rq/rk; b: W, dO; mma
+  uint64_t* bar_a = bars, *bar_b = bars + 1, *bar_mma = bars + 2;
+  uint32_t* s_tmem = (uint32_t*)(bars + 4);
+  int* s_abort = (int*)(s_tmem + 1);
+  const float* sG = (const float*)(sm + D_G);
+  const float* sRq = sG + 64;
+  const float* sRk = sG + 128;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int row = quad * 32 + lane;
+  const bool store = ar.mode == 0;
+  const int64_t h = blockIdx.y;
+  const int64_t b = blockIdx.z / ar.nseg;
+  const int seg = ar.seg_first + (int)(blockIdx.z % ar.nseg);
+  const int64_t hq = h / ar.r, bh = b * ar.H + h;
+  const int64_t cs = (int64_t)seg * ar.CPS;
+  const int64_t ce = cs + ar.CPS < ar.NC ? cs + ar.CPS : ar.NC;
+  const int64_t L = clamp_len(ar.valid_len, b, ar.T, ar.status, false);
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  uint32_t pend = 0;
+
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(bars + i, 1);
+    fence_barrier_init();
+    *s_abort = 0;
+  }
+  if (warp == 0) tmem_alloc(s_tmem, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tV = tmem, tS = tmem + 128;
+
+  float dS[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    const int col = half * 64 + j;
+    dS[j] = (store && ar.init) ? ar.init[seg * ar.init_seg_stride + (bh * 128 + row) * 128 + col] : 0.f;
+  }
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) st_chunk(sm + D_DS, mnmaj_chunk(row, half * 8 + cc, 16384), &dS[cc * 8]);
+
+  {
+    const uint8_t* wsrc = ar.wim + bh * ar.NC * (int64_t)kImg;
+    const uint8_t* psrc = ar.pim + bh * ar.NC * (int64_t)kImgP;
+    const float* gsrc = ar.gl + bh * ar.NC * 64;
+    const float* rsrc = ar.rqk + (b * ar.Hqk + hq) * ar.NC * 128;
+    auto issue_a = [&](int64_t c) {
+      mbar_arrive_expect_tx(bar_a, 2 * kImg + kImgP + 768);
+      for (int a = 0; a < 2; ++a) {
+        tma_load_4d(sm + D_XA + a * 16384, &mk, a * 64, (int)hq, (int)(c * 64), (int)b, bar_a);
+        tma_load_4d(sm + D_XA + a * 16384 + 8192, &mq, a * 64, (int)hq, (int)(c * 64), (int)b, bar_a);
+      }
+      bulk_load(sm + D_P, psrc + c * kImgP, kImgP, bar_a);
+      bulk_load(sm + D_G, gsrc + c * 64, 256, bar_a);
+      bulk_load(sm + D_G + 256, rsrc + c * 128, 512, bar_a);
+    };
+    auto issue_b = [&](int64_t c) {
+      mbar_arrive_expect_tx(bar_b, 2 * kImg);
+      bulk_load(sm + D_W, wsrc + c * kImg, kImg, bar_b);
+      for (int a = 0; a < 2; ++a)
+        tma_load_4d(sm + D_DO + a * 8192, &mdo, a * 64, (int)h, (int)(c * 64), (int)b, bar_b);
+    };
+    if (tid == 0 && cs < ce) {
+      issue_a(ce - 1);
+      issue_b(ce - 1);
+      pend |= 3u;
+    }
+    for (int64_t c = ce - 1; c >= cs; --c) {
+      const int64_t k = ce - 1 - c;
+      const int64_t t0 = c * 64;
+      const uint32_t par = (uint32_t)(k & 1);
+      if (!mbar_wait(bar_a, par, ar.status, kStatusTimeout)) *s_abort = 1;
+      if (!mbar_wait(bar_b, par, ar.status, kStatusTimeout)) *s_abort = 1;
+      if (tid == 0) pend &= ~3u;
+      // ---- scale k rows by rk e^{G_C - G}, q rows by gamma rq; zero dO rows past valid_len
+      for (int e = tid; e < 2048; e += CT) {
+        const int isq = e >> 10, r = (e >> 4) & 63, at = (e >> 3) & 1, p = e & 7;
+        const uint32_t off = D_XA + at * 16384 + isq * 8192 + r * 128 + p * 16;
+        const float f = isq ? exp2f(sG[r]) * sRq[r] : exp2f(sG[63] - sG[r]) * sRk[r];
+        float x[8];
+        ld_chunk(sm, off, x);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] *= f;
+        st_chunk(sm, off, x);
+      }
+      if (t0 + 64 > L) {
+        for (int e = tid; e < 1024; e += CT) {
+          const int i = e >> 4, cc = e & 15;
+          if (t0 + i >= L)
+            *reinterpret_cast<uint4*>(sm + D_DO + mnmaj_chunk(i, cc, 8192)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      const float gC = exp2f(sG[63]);
+      if (store) {  // gradient of chunk c's end state, bf16 row-major [dk][dv]
+        uint4* dst = reinterpret_cast<uint4*>(ar.dhc + ((bh * ar.NC + c) * 128 + row) * 128 + half * 64);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) dst[cc] = pack8(&dS[cc * 8]);
+      }
+      CHAIN_SYNC();
+      // ---- P^T dO + Kt dS -> tV rows 0..63 (dV'); Qg^T dO -> tS
+      if (tid == 0) {
+        const uint32_t idmm = idesc_bf16(128, 128, 1, 1);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tV, sdesc(base + D_P + ks * 2048, 8192, 1024),
+                   sdesc(base + D_DO + ks * 2048, 8192, 1024), idmm, ks > 0);
+        const uint32_t idkm = idesc_bf16(128, 128, 0, 1);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t at = ks >> 2, kk = ks & 3;
+          mma_bf16(tV, sdesc(base + D_XA + at * 16384 + kk * 32, 16, 1024),
+                   sdesc(base + D_DS + ks * 2048, 16384, 1024), idkm, 1);
+        }
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tS, sdesc(base + D_XA + 8192 + ks * 2048, 16384, 1024),
+                   sdesc(base + D_DO + ks * 2048, 8192, 1024), idmm, ks > 0);
+        mma_commit(bar_mma);
+        pend |= 4u;
+      }
+      if (!mbar_wait(bar_mma, 0, ar.status, kStatusTimeout)) *s_abort = 1;
+      if (tid == 0) pend &= ~4u;
+      tc_fence_after();
+      if (tid == 0 && c - 1 >= cs) {  // K, Q, P, gates of chunk c consumed
+        issue_a(c - 1);
+        pend |= 1u;
+      }
+      if (quad < 2) {  // -dV' over the dO tile
+        const int i = row;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[32];
+          tmem_ld32(tV + lane_off + half * 64 + hh * 32, v);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = -v[cc * 8 + e];
+            st_chunk(sm + D_DO, mnmaj_chunk(i, half * 8 + hh * 4 + cc, 8192), x);
+          }
+        }
+      }
+      CHAIN_SYNC();
+      // ---- tS += W^T (-dV')
+      if (tid == 0) {
+        const uint32_t id = idesc_bf16(128, 128, 1, 1);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tS, sdesc(base + D_W + ks * 2048, 8192, 1024),
+                   sdesc(base + D_DO + ks * 2048, 8192, 1024), id, 1);
+        mma_commit(bar_mma);
+        pend |= 4u;
+      }
+      if (!mbar_wait(bar_mma, 1, ar.status, kStatusTimeout)) *s_abort = 1;
+      if (tid == 0) pend &= ~4u;
+      tc_fence_after();
+      if (tid == 0 && c - 1 >= cs) {  // W and the dO / -dV' tile consumed
+        issue_b(c - 1);
+        pend |= 2u;
+      }
+      {  // dS <- gamma_C dS + tS
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[32];
+          tmem_ld32(tS + lane_off + half * 64 + hh * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dS[hh * 32 + e] = fmaf(gC, dS[hh * 32 + e], v[e]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          st_chunk(sm + D_DS, mnmaj_chunk(row, half * 8 + cc, 16384), &dS[cc * 8]);
+      }
+      CHAIN_SYNC();
+    }
+  }
+  {
+    float* dst = nullptr;
+    if (store) {
+      if (seg == 0) dst = ar.start_out;
+    } else if (ar.D_out) {
+      dst = ar.D_out + seg * ar.out_seg_stride;
+    }
+    if (dst) {
+      float4* d4 = reinterpret_cast<float4*>(dst + (bh * 128 + row) * 128 + half * 64);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) d4[j] = make_float4(dS[4 * j], dS[4 * j + 1], dS[4 * j + 2], dS[4 * j + 3]);
+    }
+  }
+done:
+  if (tid == 0 && pend) {
+    for (int i = 0; i < 3; ++i)
+      if (pend & (1u << i)) {
+        mbar_wait(bars + i, 0, nullptr, 0);
+        mbar_wait(bars + i, 1, nullptr, 0);
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+template <typename K>
+cudaError_t smem_attr(K kern, uint32_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+cudaError_t launch_prep_tc(const Prob& pr, const Inputs& in, const WS& ws, cudaStream_t st) {
+  if (pr.B == 0 || pr.NC == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv;
+  memset(&mq, 0, sizeof(mq));
+  memset(&mk, 0, sizeof(mk));
+  memset(&mv, 0, sizeof(mv));
+  if (!tc_make_map(&mq, in.q, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mv, in.v, pr.B, pr.T, pr.Ts, pr.H))
+    return cudaErrorInvalidValue;
+  PrepArgs ar;
+  ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.Hqk = pr.Hqk; ar.r = pr.r; ar.NC = pr.NC;
+  ar.l2norm = pr.l2norm; ar.eps = pr.eps; ar.scale = pr.scale;
+  ar.a = (const __nv_bfloat16*)in.a; ar.b = (const __nv_bfloat16*)in.b;
+  ar.A_log = in.A_log; ar.dt_bias = in.dt_bias; ar.valid_len = in.valid_len;
+  ar.rqk = ws.rqk; ar.wim = (uint8_t*)ws.wim; ar.uim = (uint8_t*)ws.uim;
+  ar.pim = (uint8_t*)ws.pim; ar.tim = (uint8_t*)ws.tim; ar.gl = ws.gl;
+  ar.status = ws.status;
+  cudaError_t e = smem_attr(k_prep_tc, P_SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)pr.NC, (unsigned)pr.H, (unsigned)pr.B);
+  k_prep_tc<<<grid, PT, P_SMEM, st>>>(mq, mk, mv, ar);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chain_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode,
+                            int seg_first, int nseg, const float* init, int64_t init_seg_stride,
+                            void* o, float* final_out, float* M_out, float* S_out,
+                            int64_t out_seg_stride, void* hc, cudaStream_t st) {
+  if (nseg <= 0 || pr.B == 0 || pr.NC == 0) return cudaSuccess;
+  CUtensorMap mq, mk;
+  memset(&mq, 0, sizeof(mq));
+  memset(&mk, 0, sizeof(mk));
+  const void* qptr = in.q ? in.q : in.k;  // summaries and states never read q
+  if (!tc_make_map(&mq, qptr, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk))
+    return cudaErrorInvalidValue;
+  ChainArgs ar;
+  ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.Hqk = pr.Hqk; ar.r = pr.r; ar.NC = pr.NC;
+  ar.CPS = pr.CPS; ar.P = pr.P;
+  ar.rqk = ws.rqk;
+  ar.wim = (const uint8_t*)ws.wim; ar.uim = (const uint8_t*)ws.uim;
+  ar.pim = (const uint8_t*)ws.pim; ar.gl = ws.gl;
+  ar.valid_len = in.valid_len;
+  ar.init = init; ar.init_seg_stride = init_seg_stride;
+  ar.o = (__nv_bfloat16*)o; ar.final_out = final_out;
+  ar.M_out = M_out; ar.S_out = S_out; ar.out_seg_stride = out_seg_stride;
+  ar.hc = (__nv_bfloat16*)hc;
+  ar.status = ws.status;
+  ar.seg_first = seg_first; ar.nseg = nseg;
+  cudaError_t e;
+  dim3 grid(mode == CH_SUM ? 2 : 1, (unsigned)pr.H, (unsigned)(pr.B * nseg));
+  if (mode == CH_APPLY) {
+    if ((e = smem_attr(k_chain_tc<CH_APPLY>, A_SMEM)) != cudaSuccess) return e;
+    k_chain_tc<CH_APPLY><<<grid, CT, A_SMEM, st>>>(mq, mk, ar);
+  } else if (mode == CH_SUM) {
+    if ((e = smem_attr(k_chain_tc<CH_SUM>, S_SMEM)) != cudaSuccess) return e;
+    k_chain_tc<CH_SUM><<<grid, CT, S_SMEM, st>>>(mq, mk, ar);
+  } else {
+    if ((e = smem_attr(k_chain_tc<CH_STATES>, S_SMEM)) != cudaSuccess) return e;
+    k_chain_tc<CH_STATES><<<grid, CT, S_SMEM, st>>>(mq, mk, ar);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dchain_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode,
+                             int seg_first, int nseg, const float* init, int64_t init_seg_stride,
+                             void* dhc, float* start_out, float* D_out, int64_t out_seg_stride,
+                             cudaStream_t st) {
+  if (nseg <= 0 || pr.B == 0 || pr.NC == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mdo;
+  memset(&mq, 0, sizeof(mq));
+  memset(&mk, 0, sizeof(mk));
+  memset(&mdo, 0, sizeof(mdo));
+  if (!tc_make_map(&mq, in.q, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mdo, in.dO, pr.B, pr.T, pr.Ts, pr.H))
+    return cudaErrorInvalidValue;
+  DchainArgs ar;
+  ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.Hqk = pr.Hqk; ar.r = pr.r; ar.NC = pr.NC;
+  ar.CPS = pr.CPS;
+  ar.rqk = ws.rqk; ar.wim = (const uint8_t*)ws.wim; ar.pim = (const uint8_t*)ws.pim;
+  ar.gl = ws.gl; ar.valid_len = in.valid_len;
+  ar.init = init; ar.init_seg_stride = init_seg_stride;
+  ar.dhc = (__nv_bfloat16*)dhc; ar.start_out = start_out; ar.D_out = D_out;
+  ar.out_seg_stride = out_seg_stride; ar.status = ws.status;
+  ar.mode = mode; ar.seg_first = seg_first; ar.nseg = nseg;
+  cudaError_t e = smem_attr(k_dchain_tc, D_SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(1, (unsigned)pr.H, (unsigned)(pr.B * nseg));
+  k_dchain_tc<<<grid, CT, D_SMEM, st>>>(mq, mk, mdo, ar);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn
