@@ -131,8 +131,8 @@ size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws) {
     }
     w.hc16 = take(B * H * NC * dk * dv / 2);
     w.dhc16 = take(B * H * NC * dk * dv / 2);
-    w.dqp = take(B * Tp * H * dk);
-    w.dkp = take(B * Tp * H * dk);
+    w.dqp = take(B * Tp * H * dk / 2);  // bf16
+    w.dkp = take(B * Tp * H * dk / 2);
     if (ws) *ws = w;
     return off;
   }
@@ -311,7 +311,7 @@ gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const
             launch_dchain_tc(pr, in, ws, 0, 0, pr.P, dinit, dinit_stride, ws.dhc16, dH0, nullptr,
                              0, st));
     GDN_RUN(sc, "grad_tc", launch_grad_tc(pr, in, ws, ws.hc16, ws.dhc16, dv, dg, dbeta, st));
-    GDN_RUN(sc, "qk_grad", launch_qk_grad(pr, in, ws, dq, dk, st));
+    GDN_RUN(sc, "qk_grad_tc", launch_qk_grad_tc(pr, in, ws, dq, dk, st));
     return GDN_OK;
   }
   GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, true, st));

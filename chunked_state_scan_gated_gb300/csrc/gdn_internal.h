@@ -45,7 +45,7 @@ struct WS {
   float* dVn;   // [B][H][Tp][dv]    gradient of V'
   float* Dseg;  // [P][B][H][dk][dv]
   float* dHout; // [P][B][H][dk][dv]
-  float* dqp;   // [B][Tp][H][dk]    per-V-head gradient of q_hat
+  float* dqp;   // [B][Tp][H][dk]    per-V-head gradient of q_hat (bf16 on the tensor-core path)
   float* dkp;   // [B][Tp][H][dk]    per-V-head gradient of k_hat
   float* rqk;   // [B][Hqk][NC][128] per-token norm factors rq = scale/|q|, then rk = 1/|k|
   void* wim;    // [B][H][NC]   16 KB bf16 tile images of W (tensor-core path)
@@ -121,6 +121,9 @@ cudaError_t launch_dchain_tc(const Prob& pr, const Inputs& in, const WS& ws, int
                              void* dhc, float* start_out, float* D_out, int64_t out_seg_stride,
                              cudaStream_t st);
 
+// dq, dk (bf16) from the per-V-head bf16 gradients of q_hat, k_hat in ws.dqp / ws.dkp
+cudaError_t launch_qk_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, void* dq, void* dk,
+                              cudaStream_t st);
 // chunk-parallel gradients from chunk-start states and chunk-end state gradients
 cudaError_t launch_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, const void* hc,
                            const void* dhc, void* dv, float* dg, float* dbeta, cudaStream_t st);

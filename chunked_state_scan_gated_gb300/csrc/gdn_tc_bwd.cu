@@ -53,13 +53,13 @@ namespace {
 
 constexpr uint32_t G_Q = 0, G_K = 16384, G_W = 32768, G_V = 49152, G_DO = 65536;  // [64][128]
 constexpr uint32_t G_S = 81920, G_DS = 114688;      // [128][128], atoms of 16 KB
-constexpr uint32_t G_TU = 147456, G_TW = 155648;    // [64][64]; later U [64][128]
+constexpr uint32_t G_TU = 147456;                   // U [64][128] (prologue image)
 constexpr uint32_t G_P = 163840, G_TP = 172032;     // [64][64]; P later E; Y of the solve in TP
 constexpr uint32_t G_VP = 180224;                   // V' [64][128]; later dP o Gamma [64][64]
 constexpr uint32_t G_DV = 196608, G_DW = 212992;    // dV', dW [64][128]; earlier fp32 A, T
 constexpr uint32_t G_SC = 229376;                   // scalars
 constexpr uint32_t G_SMEM = G_SC + 1792 + 1024;
-constexpr int GLDA = 64;
+
 
 struct GradArgs {
   int64_t T, Ts, H, r, NC, Tp;
@@ -73,10 +73,23 @@ struct GradArgs {
   __nv_bfloat16* dv;   // [B, Ts, H, 128]
   float* dg;           // [B, Ts, H]
   float* dbeta;
-  float* dqp;          // [B][Tp][H][128] per-V-head gradient of q_hat
-  float* dkp;
+  __nv_bfloat16* dqp;  // [B][Tp][H][128] per-V-head gradient of q_hat (bf16)
+  __nv_bfloat16* dkp;
+  const uint8_t* wim;  // prologue tile images of the chunk: W, U, P, T
+  const uint8_t* uim;
+  const uint8_t* pim;
+  const uint8_t* tim;
   int* status;
 };
+
+__device__ __forceinline__ uint4 pack8g(const float* x) {
+  uint4 v;
+  v.x = pack_bf16(x[0], x[1]);
+  v.y = pack_bf16(x[2], x[3]);
+  v.z = pack_bf16(x[4], x[5]);
+  v.w = pack_bf16(x[6], x[7]);
+  return v;
+}
 
 // 64 consecutive fp32 accumulator columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -112,9 +125,6 @@ __global__ void __launch_bounds__(FT, 1)
   uint64_t* bar_mma = bar_ld + 1;
   uint32_t* s_tmem = (uint32_t*)(bar_ld + 2);
   int* s_abort = (int*)(s_tmem + 1);
-  float* sA = (float*)(sm + G_DV);
-  float* sT = (float*)(sm + G_DW);
-  float* sY = (float*)(sm + G_TP);
   float* sZ = (float*)(sm + G_S);      // fp32 64 x 64 after S is consumed
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -143,7 +153,13 @@ __global__ void __launch_bounds__(FT, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar_ld, 131072u);
+    // chunk tiles of the prologue: W, U (over T_u/T_w), P, T
+    const int64_t im = bh * ar.NC + c;
+    mbar_arrive_expect_tx(bar_ld, 131072u + 49152u);
+    bulk_load(sm + G_W, ar.wim + im * 16384, 16384, bar_ld);
+    bulk_load(sm + G_TU, ar.uim + im * 16384, 16384, bar_ld);
+    bulk_load(sm + G_P, ar.pim + im * 8192, 8192, bar_ld);
+    bulk_load(sm + G_TP, ar.tim + im * 8192, 8192, bar_ld);
     for (int at = 0; at < 2; ++at) {
       tma_load_4d(sm + G_Q + at * 8192, &mq, at * 64, (int)hq, (int)t0, (int)b, bar_ld);
       tma_load_4d(sm + G_K + at * 8192, &mk, at * 64, (int)hq, (int)t0, (int)b, bar_ld);
@@ -206,92 +222,11 @@ __global__ void __launch_bounds__(FT, 1)
   {
   uint32_t ph = 0;
   float dGacc = 0.f, dbacc = 0.f, sKacc = 0.f;  // this thread's half-row partial sums
-  float dq[64], dk[64], U[64];
+  float dq[64], dk[64];
   const uint32_t id64 = idesc_bf16(64, 64, 0, 0);
   const uint32_t id128kn = idesc_bf16(64, 128, 0, 1);
   const uint32_t id128kk = idesc_bf16(64, 128, 0, 0);
   const uint32_t id128mn = idesc_bf16(64, 128, 1, 1);
-  PHASE_SYNC();
-  // ---- RT1: Q K^T -> [0,64), K K^T -> [64,128)
-  if (tid == 0) {
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t at = ks >> 2, kk = ks & 3;
-      const uint64_t bk = sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024);
-      mma_bf16(tmem, sdesc(base + G_Q + at * 8192 + kk * 32, 16, 1024), bk, id64, ks > 0);
-      mma_bf16(tmem + 64, sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024), bk, id64, ks > 0);
-    }
-    mma_commit(bar_mma);
-  }
-  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
-  ph ^= 1;
-  tc_fence_after();
-  {
-    float qk[32], kk[32];
-    tmem_ld32(tmem + lane_off + half * 32, qk);
-    tmem_ld32(tmem + lane_off + 64 + half * 32, kk);
-    if (own) {
-      const int i = ri;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = half * 32 + cc * 8 + e;
-          p[e] = (j <= i) ? qk[cc * 8 + e] * dexp_(sG[i], sG[j]) : 0.f;
-        }
-        st_chunk(sm + G_P, kmaj_chunk(i, half * 4 + cc), p);
-      }
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = half * 32 + e;
-        sA[i * GLDA + j] = (j < i) ? sBeta[i] * kk[e] * dexp_(sG[i], sG[j]) : 0.f;
-      }
-    }
-  }
-  PHASE_SYNC();
-  solve_unit_lower64(sA, sT, sY, GLDA);
-  for (int q = 0; q < 2; ++q) {  // T_u, T_w and T into bf16 tiles
-    const int idx = tid + FT * q;
-    const int i = idx >> 3, cc = idx & 7;
-    float xu[8], xw[8], xp[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int j = cc * 8 + e;
-      const float t = (j <= i) ? sT[i * GLDA + j] : 0.f;
-      xp[e] = t;
-      xu[e] = t * sBeta[j];
-      xw[e] = xu[e] * sGam[j];
-    }
-    st_chunk(sm + G_TU, kmaj_chunk(i, cc), xu);
-    st_chunk(sm + G_TW, kmaj_chunk(i, cc), xw);
-    st_chunk(sm + G_TP, kmaj_chunk(i, cc), xp);
-  }
-  PHASE_SYNC();
-  // ---- RT2: W = T_w K -> [128,256), U = T_u V -> [256,384)
-  if (tid == 0) {
-    for (int ks = 0; ks < 4; ++ks) {
-      mma_bf16(tmem + 128, sdesc(base + G_TW + ks * 32, 16, 1024),
-               sdesc(base + G_K + ks * 2048, 8192, 1024), id128kn, ks > 0);
-      mma_bf16(tmem + 256, sdesc(base + G_TU + ks * 32, 16, 1024),
-               sdesc(base + G_V + ks * 2048, 8192, 1024), id128kn, ks > 0);
-    }
-    mma_commit(bar_mma);
-  }
-  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
-  ph ^= 1;
-  tc_fence_after();
-  {
-    float w[64];
-    tmem_ld64(tmem + lane_off + 128 + half * 64, w);
-    tmem_ld64(tmem + lane_off + 256 + half * 64, U);
-    if (own) {
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        st_chunk(sm + G_W + half * 8192, kmaj_chunk(ri, cc), &w[cc * 8]);
-        st_chunk(sm + G_TU + half * 8192, kmaj_chunk(ri, cc), &U[cc * 8]);  // U over T_u, T_w
-      }
-    }
-  }
   PHASE_SYNC();
   // ---- RT3: W S -> [384,512), K dS -> [0,128), P^T dO -> [128,256), dO S^T -> [256,384)
   if (tid == 0) {
@@ -336,8 +271,14 @@ __global__ void __launch_bounds__(FT, 1)
       const int i = ri;
       const float kt = sKt[i], gm = sGam[i];
 #pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {       // V' = U - W S (U image over T_u, T_w)
+        float u[8];
+        ld_chunk(sm + G_TU + half * 8192, kmaj_chunk(i, cc), u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ws[cc * 8 + e] = u[e] - ws[cc * 8 + e];
+      }
+#pragma unroll
       for (int j = 0; j < 64; ++j) {
-        ws[j] = U[j] - ws[j];                 // V'
         kd[j] = fmaf(kt, kd[j], pd[j]);       // dV'
         dq[j] *= gm;                          // diag(gamma) dO S^T
       }
@@ -490,15 +431,13 @@ __global__ void __launch_bounds__(FT, 1)
     }
     tmem_ld64(tmem + lane_off + 256 + half * 64, x);  // (dP o Gamma) K
     if (own && t < ar.Tp) {
-      float* dst = ar.dqp + ((b * ar.Tp + t) * ar.H + h) * 128 + half * 64;
+      uint4* dst = reinterpret_cast<uint4*>(ar.dqp + ((b * ar.Tp + t) * ar.H + h) * 128 + half * 64);
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
-        float4 v4;
-        v4.x = valid ? dq[j] + x[j] : 0.f;
-        v4.y = valid ? dq[j + 1] + x[j + 1] : 0.f;
-        v4.z = valid ? dq[j + 2] + x[j + 2] : 0.f;
-        v4.w = valid ? dq[j + 3] + x[j + 3] : 0.f;
-        *reinterpret_cast<float4*>(dst + j) = v4;
+      for (int j = 0; j < 64; j += 8) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = valid ? dq[j + e] + x[j + e] : 0.f;
+        dst[j >> 3] = pack8g(y);
       }
     }
   }
@@ -577,15 +516,13 @@ __global__ void __launch_bounds__(FT, 1)
     const int64_t t = t0 + i;
     if (own && t < ar.Tp) {
       const bool valid = t < L;
-      float* dst = ar.dkp + ((b * ar.Tp + t) * ar.H + h) * 128 + half * 64;
+      uint4* dst = reinterpret_cast<uint4*>(ar.dkp + ((b * ar.Tp + t) * ar.H + h) * 128 + half * 64);
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
-        float4 v4;
-        v4.x = valid ? dk[j] + x[j] : 0.f;
-        v4.y = valid ? dk[j + 1] + x[j + 1] : 0.f;
-        v4.z = valid ? dk[j + 2] + x[j + 2] : 0.f;
-        v4.w = valid ? dk[j + 3] + x[j + 3] : 0.f;
-        *reinterpret_cast<float4*>(dst + j) = v4;
+      for (int j = 0; j < 64; j += 8) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = valid ? dk[j + e] + x[j + e] : 0.f;
+        dst[j >> 3] = pack8g(y);
       }
     }
     if (own) {
@@ -648,6 +585,88 @@ done:
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// ============================================================================
+// k_qk_grad_tc: dq, dk from the per-V-head bf16 gradients of q_hat, k_hat:
+// summed over the r V heads of a Q/K head, then back through the scale and the
+// L2 norm (q_hat = s q / |q|: dq = s (g - u (u . g)) / |q| with u = q / |q|).
+// One warp per (row, token, Q/K head); lane l holds columns 4l .. 4l+3.
+// ============================================================================
+struct QkArgs {
+  int64_t B, T, Ts, Tp, Hqk, H, r;
+  int l2norm;
+  float eps, scale;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* dqp;
+  const __nv_bfloat16* dkp;
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+};
+
+__device__ __forceinline__ void ld4bf(const __nv_bfloat16* p, float* x) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+  const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+  x[0] = a.x; x[1] = a.y; x[2] = c.x; x[3] = c.y;
+}
+
+__global__ void __launch_bounds__(256) k_qk_grad_tc(QkArgs ar) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t rowid = (int64_t)blockIdx.x * 8 + warp;
+  if (rowid >= ar.B * ar.T * ar.Hqk) return;
+  const int64_t hq = rowid % ar.Hqk, t = (rowid / ar.Hqk) % ar.T, b = rowid / (ar.Hqk * ar.T);
+  const int64_t xo = ((b * ar.Ts + t) * ar.Hqk + hq) * 128 + lane * 4;
+  float xq[4], xk[4], gq[4] = {0.f, 0.f, 0.f, 0.f}, gk[4] = {0.f, 0.f, 0.f, 0.f};
+  ld4bf(ar.q + xo, xq);
+  ld4bf(ar.k + xo, xk);
+  for (int64_t h = hq * ar.r; h < (hq + 1) * ar.r; ++h) {
+    const int64_t po = ((b * ar.Tp + t) * ar.H + h) * 128 + lane * 4;
+    float a[4], c[4];
+    ld4bf(ar.dqp + po, a);
+    ld4bf(ar.dkp + po, c);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      gq[e] += a[e];
+      gk[e] += c[e];
+    }
+  }
+  float sq = 0.f, sk = 0.f, pq = 0.f, pk = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    sq = fmaf(xq[e], xq[e], sq);
+    sk = fmaf(xk[e], xk[e], sk);
+    pq = fmaf(xq[e], gq[e], pq);
+    pk = fmaf(xk[e], gk[e], pk);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    pq += __shfl_xor_sync(0xffffffffu, pq, o);
+    pk += __shfl_xor_sync(0xffffffffu, pk, o);
+  }
+  float rq = 1.f, rk = 1.f, prq = 0.f, prk = 0.f;
+  if (ar.l2norm) {
+    rq = rsqrtf(sq + ar.eps);
+    rk = rsqrtf(sk + ar.eps);
+    prq = pq * rq * rq;
+    prk = pk * rk * rk;
+  }
+  float oq[4], ok[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    oq[e] = ar.scale * (gq[e] - xq[e] * prq) * rq;
+    ok[e] = (gk[e] - xk[e] * prk) * rk;
+  }
+  uint2 vq, vk;
+  vq.x = pack_bf16(oq[0], oq[1]);
+  vq.y = pack_bf16(oq[2], oq[3]);
+  vk.x = pack_bf16(ok[0], ok[1]);
+  vk.y = pack_bf16(ok[2], ok[3]);
+  *reinterpret_cast<uint2*>(ar.dq + xo) = vq;
+  *reinterpret_cast<uint2*>(ar.dk + xo) = vk;
+}
+
 }  // namespace
 
 cudaError_t launch_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, const void* hc,
@@ -673,12 +692,28 @@ cudaError_t launch_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, const
   ar.a = (const __nv_bfloat16*)in.a; ar.b = (const __nv_bfloat16*)in.b;
   ar.A_log = in.A_log; ar.dt_bias = in.dt_bias; ar.valid_len = in.valid_len;
   ar.dv = (__nv_bfloat16*)dv; ar.dg = dg; ar.dbeta = dbeta;
-  ar.dqp = ws.dqp; ar.dkp = ws.dkp; ar.status = ws.status;
+  ar.dqp = (__nv_bfloat16*)ws.dqp; ar.dkp = (__nv_bfloat16*)ws.dkp; ar.status = ws.status;
+  ar.wim = (const uint8_t*)ws.wim; ar.uim = (const uint8_t*)ws.uim;
+  ar.pim = (const uint8_t*)ws.pim; ar.tim = (const uint8_t*)ws.tim;
   cudaError_t e = cudaFuncSetAttribute(k_grad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)G_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)pr.NC, (unsigned)pr.H, (unsigned)pr.B);
   k_grad_tc<<<grid, FT, G_SMEM, st>>>(mq, mk, mv, mdo, ms, mds, ar);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qk_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, void* dq, void* dk,
+                              cudaStream_t st) {
+  const int64_t rows = pr.B * pr.T * pr.Hqk;
+  if (rows == 0) return cudaSuccess;
+  QkArgs ar;
+  ar.B = pr.B; ar.T = pr.T; ar.Ts = pr.Ts; ar.Tp = pr.Tp; ar.Hqk = pr.Hqk; ar.H = pr.H;
+  ar.r = pr.r; ar.l2norm = pr.l2norm; ar.eps = pr.eps; ar.scale = pr.scale;
+  ar.q = (const __nv_bfloat16*)in.q; ar.k = (const __nv_bfloat16*)in.k;
+  ar.dqp = (const __nv_bfloat16*)ws.dqp; ar.dkp = (const __nv_bfloat16*)ws.dkp;
+  ar.dq = (__nv_bfloat16*)dq; ar.dk = (__nv_bfloat16*)dk;
+  k_qk_grad_tc<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(ar);
   return cudaGetLastError();
 }
 
