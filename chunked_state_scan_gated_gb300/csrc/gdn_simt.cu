@@ -902,77 +902,107 @@ __global__ void __launch_bounds__(NT) k_compose(int64_t dk, int64_t dv, const fl
 
 // Exclusive prefix over segments, grid (n, ceil(dv / PCS)), 256 threads.
 // transpose = 0: X <- M[s] X + S[s] for s = 0, 1, ...; transpose = 1: X <- M[s]^T X + S[s]
-// for s = P-1, P-2, ...  Each step stages M[s] (dk x dk) in shared memory with a
-// padded row stride (conflict-free for both orientations) and gives every thread
-// one row of X times PCS / 2 columns, so a step is one coalesced 64 KB read plus a
-// register-blocked fp32 product instead of strided global loads.
-constexpr int PCS = 16;          // state columns per prefix block
-constexpr int PLD = 129;         // shared-memory row stride of M
-__global__ void __launch_bounds__(NT) k_prefix(int64_t n, int64_t P, int64_t dk, int64_t dv,
-                                              const float* __restrict__ M,
-                                              const float* __restrict__ S,
-                                              const float* __restrict__ x0, float* out_seq,
-                                              float* out_last, int transpose) {
+// for s = P-1, P-2, ...  Each step multiplies a dk x dk map by the block's dk x PCS
+// slice of X in fp32: the map is staged in shared memory (padded rows, conflict-free
+// in both orientations; two buffers, the next map prefetched into registers while
+// the current one is used) and every thread accumulates a 4 x 4 register tile.
+constexpr int PCS = 32;          // state columns per prefix block
+constexpr int PLD = 129;         // shared-memory row stride of a map
+constexpr int PMAXR = kMaxHeadDim / (NT / 32);        // map rows per warp (16)
+constexpr int PMAXC = kMaxHeadDim / 32;               // map columns per lane (4)
+__global__ void __launch_bounds__(NT, 1) k_prefix(int64_t n, int64_t P, int64_t dk, int64_t dv,
+                                                 const float* __restrict__ M,
+                                                 const float* __restrict__ S,
+                                                 const float* __restrict__ x0, float* out_seq,
+                                                 float* out_last, int transpose) {
   extern __shared__ float sm[];
-  float* Ms = sm;                  // [dk][PLD]
-  float* Xs = Ms + kMaxHeadDim * PLD;  // [dk][PCS]
+  float* Ms0 = sm;                               // [2][dk][PLD]
+  float* Xs = sm + 2 * kMaxHeadDim * PLD;        // [dk][PCS]
   const int64_t e0 = blockIdx.x;
   const int c0 = blockIdx.y * PCS;
-  const int tid = threadIdx.x;
-  const int i = tid >> 1;          // row of X owned by this thread
-  const int j0 = (tid & 1) * (PCS / 2);
-  const bool own = i < dk;
-  float x[PCS / 2];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ndk = (int)dk;
+  const int rg = tid >> 3, cg = tid & 7;         // rows 4 rg .. +3, columns c0 + 4 cg .. +3
+  float x[4][4];
 #pragma unroll
-  for (int j = 0; j < PCS / 2; ++j) {
-    const int col = c0 + j0 + j;
-    x[j] = (own && x0 && col < dv) ? x0[(e0 * dk + i) * dv + col] : 0.f;
-  }
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = rg * 4 + r, col = c0 + cg * 4 + c;
+      x[r][c] = (x0 && i < ndk && col < dv) ? x0[(e0 * dk + i) * dv + col] : 0.f;
+    }
+  float pre[PMAXR][PMAXC];  // map prefetch: rows warp + 8 a, columns lane + 32 b
+  auto prefetch = [&](int64_t s) {
+    const float* Mg = M + (s * n + e0) * dk * dk;
+#pragma unroll
+    for (int a = 0; a < PMAXR; ++a)
+#pragma unroll
+      for (int bb = 0; bb < PMAXC; ++bb) {
+        const int r = warp + 8 * a, l = lane + 32 * bb;
+        pre[a][bb] = (r < ndk && l < ndk) ? Mg[(int64_t)r * ndk + l] : 0.f;
+      }
+  };
+  const int64_t s_first = transpose ? P - 1 : 0;
+  prefetch(s_first);
   for (int64_t step = 0; step < P; ++step) {
     const int64_t s = transpose ? P - 1 - step : step;
-    if (own) {
 #pragma unroll
-      for (int j = 0; j < PCS / 2; ++j) {
-        const int col = c0 + j0 + j;
-        if (col < dv) out_seq[((s * n + e0) * dk + i) * dv + col] = x[j];
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = rg * 4 + r, col = c0 + cg * 4 + c;
+        if (i < ndk && col < dv) out_seq[((s * n + e0) * dk + i) * dv + col] = x[r][c];
       }
-    }
     const bool apply = transpose ? (s > 0 || out_last) : (s < P - 1 || out_last);
     if (!apply) break;
-    const float* Mg = M + (s * n + e0) * dk * dk;
-    __syncthreads();  // previous step's readers of Ms / Xs are done
-    {  // warp-per-row copy: no integer division in the loop
-      const int ndk = (int)dk, warp = tid >> 5, lane = tid & 31;
-      for (int r = warp; r < ndk; r += NT / 32)
-        for (int l = lane; l < ndk; l += 32) Ms[r * PLD + l] = Mg[(int64_t)r * ndk + l];
-    }
+    float* Ms = Ms0 + (step & 1) * kMaxHeadDim * PLD;
 #pragma unroll
-    for (int j = 0; j < PCS / 2; ++j)
-      if (own) Xs[i * PCS + j0 + j] = x[j];
+    for (int a = 0; a < PMAXR; ++a)
+#pragma unroll
+      for (int bb = 0; bb < PMAXC; ++bb) Ms[(warp + 8 * a) * PLD + lane + 32 * bb] = pre[a][bb];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) Xs[(rg * 4 + r) * PCS + cg * 4 + c] = x[r][c];
     __syncthreads();
-    float acc[PCS / 2];
+    const int64_t s_next = transpose ? s - 1 : s + 1;
+    if (step + 1 < P) prefetch(s_next);
+    float acc[4][4];
 #pragma unroll
-    for (int j = 0; j < PCS / 2; ++j) {
-      const int col = c0 + j0 + j;
-      acc[j] = (own && col < dv) ? S[((s * n + e0) * dk + i) * dv + col] : 0.f;
-    }
-    if (own) {
-      const int sa_i = transpose ? 1 : PLD, sa_l = transpose ? PLD : 1, ndk = (int)dk;
-      for (int l = 0; l < ndk; ++l) {
-        const float a = Ms[i * sa_i + l * sa_l];
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int j = 0; j < PCS / 2; ++j) acc[j] = fmaf(a, Xs[l * PCS + j0 + j], acc[j]);
+      for (int c = 0; c < 4; ++c) {
+        const int i = rg * 4 + r, col = c0 + cg * 4 + c;
+        acc[r][c] = (i < ndk && col < dv) ? S[((s * n + e0) * dk + i) * dv + col] : 0.f;
+      }
+    const int sa_i = transpose ? 1 : PLD, sa_l = transpose ? PLD : 1;
+    for (int l = 0; l < ndk; ++l) {
+      const float4 xv = *reinterpret_cast<const float4*>(Xs + l * PCS + cg * 4);
+      float av[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) av[r] = Ms[(rg * 4 + r) * sa_i + l * sa_l];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        acc[r][0] = fmaf(av[r], xv.x, acc[r][0]);
+        acc[r][1] = fmaf(av[r], xv.y, acc[r][1]);
+        acc[r][2] = fmaf(av[r], xv.z, acc[r][2]);
+        acc[r][3] = fmaf(av[r], xv.w, acc[r][3]);
       }
     }
 #pragma unroll
-    for (int j = 0; j < PCS / 2; ++j) x[j] = acc[j];
-  }
-  if (out_last && own) {
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int j = 0; j < PCS / 2; ++j) {
-      const int col = c0 + j0 + j;
-      if (col < dv) out_last[(e0 * dk + i) * dv + col] = x[j];
-    }
+      for (int c = 0; c < 4; ++c) x[r][c] = acc[r][c];
+    __syncthreads();  // Xs is rewritten at the next step
+  }
+  if (out_last) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = rg * 4 + r, col = c0 + cg * 4 + c;
+        if (i < ndk && col < dv) out_last[(e0 * dk + i) * dv + col] = x[r][c];
+      }
   }
 }
 
@@ -1128,7 +1158,7 @@ cudaError_t launch_prefix(int64_t n, int64_t P, int64_t dk, int64_t dv, const fl
                           const float* S, const float* h0, float* Hin, float* Hout,
                           cudaStream_t st) {
   if (n == 0 || P == 0) return cudaSuccess;
-  const size_t smem = sizeof(float) * (size_t)(kMaxHeadDim * PLD + kMaxHeadDim * PCS);
+  const size_t smem = sizeof(float) * (size_t)(2 * kMaxHeadDim * PLD + kMaxHeadDim * PCS);
   dim3 grid((unsigned)n, (unsigned)((dv + PCS - 1) / PCS));
   cudaError_t e;
   if ((e = set_smem(k_prefix, smem)) != cudaSuccess) return e;
@@ -1140,7 +1170,7 @@ cudaError_t launch_prefix_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, cons
                               const float* D, const float* dHT, float* dHout, float* dH0,
                               cudaStream_t st) {
   if (n == 0 || P == 0) return cudaSuccess;
-  const size_t smem = sizeof(float) * (size_t)(kMaxHeadDim * PLD + kMaxHeadDim * PCS);
+  const size_t smem = sizeof(float) * (size_t)(2 * kMaxHeadDim * PLD + kMaxHeadDim * PCS);
   dim3 grid((unsigned)n, (unsigned)((dv + PCS - 1) / PCS));
   cudaError_t e;
   if ((e = set_smem(k_prefix, smem)) != cudaSuccess) return e;

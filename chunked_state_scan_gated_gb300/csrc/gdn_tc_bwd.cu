@@ -16,9 +16,8 @@
 
 namespace gdn {
 
-// Tensor-map encoders of gdn_tc_maps.cu: [B, Ts, heads, 128] inputs and [n][128][128] states.
+// Tensor-map encoder of gdn_tc_maps.cu for the [B, Ts, heads, 128] inputs.
 bool tc_make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t Ts, int64_t heads);
-bool tc_make_state_map(CUtensorMap* m, const void* ptr, int64_t n);
 
 namespace {
 
@@ -75,6 +74,8 @@ struct GradArgs {
   float* dbeta;
   __nv_bfloat16* dqp;  // [B][Tp][H][128] per-V-head gradient of q_hat (bf16)
   __nv_bfloat16* dkp;
+  const uint8_t* hc;   // chunk-start states, 32 KB tile images
+  const uint8_t* dhc;  // chunk-end state gradients, 32 KB tile images
   const uint8_t* wim;  // prologue tile images of the chunk: W, U, P, T
   const uint8_t* uim;
   const uint8_t* pim;
@@ -106,7 +107,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 __global__ void __launch_bounds__(FT, 1)
     k_grad_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-              const __grid_constant__ CUtensorMap ms, const __grid_constant__ CUtensorMap mds,
               GradArgs ar) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(FT, 1)
   uint64_t* bar_mma = bar_ld + 1;
   uint32_t* s_tmem = (uint32_t*)(bar_ld + 2);
   int* s_abort = (int*)(s_tmem + 1);
-  float* sZ = (float*)(sm + G_S);      // fp32 64 x 64 after S is consumed
+  float* sZ = (float*)(sm + G_S);      // fp32 64 x 64, row stride 65, after S is consumed
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
@@ -165,9 +165,10 @@ __global__ void __launch_bounds__(FT, 1)
       tma_load_4d(sm + G_K + at * 8192, &mk, at * 64, (int)hq, (int)t0, (int)b, bar_ld);
       tma_load_4d(sm + G_V + at * 8192, &mv, at * 64, (int)h, (int)t0, (int)b, bar_ld);
       tma_load_4d(sm + G_DO + at * 8192, &mdo, at * 64, (int)h, (int)t0, (int)b, bar_ld);
-      tma_load_4d(sm + G_S + at * 16384, &ms, at * 64, 0, (int)(bh * ar.NC + c), 0, bar_ld);
-      tma_load_4d(sm + G_DS + at * 16384, &mds, at * 64, 0, (int)(bh * ar.NC + c), 0, bar_ld);
     }
+    // chunk-start state and chunk-end state gradient: 32 KB tile images of the chains
+    bulk_load(sm + G_S, ar.hc + im * 32768, 32768, bar_ld);
+    bulk_load(sm + G_DS, ar.dhc + im * 32768, 32768, bar_ld);
   }
   if (tid < 64) {
     const int64_t t = t0 + tid;
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(FT, 1)
         for (int e = 0; e < 8; ++e) {
           const int j = half * 32 + cc * 8 + e;
           const float dpv = (j <= i) ? dp[cc * 8 + e] : 0.f;
-          sZ[i * 64 + j] = dpv * pv[cc * 8 + e];                   // dP o P
+          sZ[i * 65 + j] = dpv * pv[cc * 8 + e];                   // dP o P
           y[e] = (j <= i) ? dpv * dexp_(sG[i], sG[j]) : 0.f;       // dP o Gamma
         }
         st_chunk(sm + G_VP, kmaj_chunk(i, half * 4 + cc), y);     // over V' (consumed)
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(FT, 1)
   PHASE_SYNC();
   if (tid < 64) {  // gate terms of P: sum_j Z_ij - sum_j Z_ji
     float acc = 0.f;
-    for (int j = 0; j < 64; ++j) acc += sZ[tid * 64 + j] - sZ[j * 64 + tid];
+    for (int j = 0; j < 64; ++j) acc += sZ[tid * 65 + j] - sZ[j * 65 + tid];
     sDG[tid] += acc;
   }
   // ---- RT5: T^T dV' -> [0,128), T^T dW -> [128,256), (dP o Gamma) K -> [256,384)
@@ -479,7 +480,7 @@ __global__ void __launch_bounds__(FT, 1)
           const float dA = (j < i) ? -da[cc * 8 + e] : 0.f;
           const float kg = kk[cc * 8 + e] * gmm;
           part = fmaf(dA, kg, part);                 // dbeta: dA (k_i . k_j) Gamma
-          sZ[i * 64 + j] = dA * be * kg;             // dA o A
+          sZ[i * 65 + j] = dA * be * kg;             // dA o A
           ex[e] = dA * be * gmm;                     // E
         }
         st_chunk(sm + G_P, kmaj_chunk(i, half * 4 + cc), ex);   // E over P
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(FT, 1)
   PHASE_SYNC();
   if (tid < 64) {
     float acc = 0.f;
-    for (int j = 0; j < 64; ++j) acc += sZ[tid * 64 + j] - sZ[j * 64 + tid];
+    for (int j = 0; j < 64; ++j) acc += sZ[tid * 65 + j] - sZ[j * 65 + tid];
     sDG[tid] += acc;
   }
   // ---- RT7: dk += (dP o Gamma)^T Q + E K + E^T K -> [0,128)
@@ -672,19 +673,15 @@ __global__ void __launch_bounds__(256) k_qk_grad_tc(QkArgs ar) {
 cudaError_t launch_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, const void* hc,
                            const void* dhc, void* dv, float* dg, float* dbeta, cudaStream_t st) {
   if (pr.B == 0 || pr.NC == 0) return cudaSuccess;
-  CUtensorMap mq, mk, mv, mdo, ms, mds;
+  CUtensorMap mq, mk, mv, mdo;
   memset(&mq, 0, sizeof(mq));
   memset(&mk, 0, sizeof(mk));
   memset(&mv, 0, sizeof(mv));
   memset(&mdo, 0, sizeof(mdo));
-  memset(&ms, 0, sizeof(ms));
-  memset(&mds, 0, sizeof(mds));
-  const int64_t n = pr.B * pr.H * pr.NC;
   if (!tc_make_map(&mq, in.q, pr.B, pr.T, pr.Ts, pr.Hqk) ||
       !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
       !tc_make_map(&mv, in.v, pr.B, pr.T, pr.Ts, pr.H) ||
-      !tc_make_map(&mdo, in.dO, pr.B, pr.T, pr.Ts, pr.H) || !tc_make_state_map(&ms, hc, n) ||
-      !tc_make_state_map(&mds, dhc, n))
+      !tc_make_map(&mdo, in.dO, pr.B, pr.T, pr.Ts, pr.H))
     return cudaErrorInvalidValue;
   GradArgs ar;
   ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.r = pr.r; ar.NC = pr.NC; ar.Tp = pr.Tp;
@@ -693,13 +690,14 @@ cudaError_t launch_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, const
   ar.A_log = in.A_log; ar.dt_bias = in.dt_bias; ar.valid_len = in.valid_len;
   ar.dv = (__nv_bfloat16*)dv; ar.dg = dg; ar.dbeta = dbeta;
   ar.dqp = (__nv_bfloat16*)ws.dqp; ar.dkp = (__nv_bfloat16*)ws.dkp; ar.status = ws.status;
+  ar.hc = (const uint8_t*)hc; ar.dhc = (const uint8_t*)dhc;
   ar.wim = (const uint8_t*)ws.wim; ar.uim = (const uint8_t*)ws.uim;
   ar.pim = (const uint8_t*)ws.pim; ar.tim = (const uint8_t*)ws.tim;
   cudaError_t e = cudaFuncSetAttribute(k_grad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)G_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)pr.NC, (unsigned)pr.H, (unsigned)pr.B);
-  k_grad_tc<<<grid, FT, G_SMEM, st>>>(mq, mk, mv, mdo, ms, mds, ar);
+  k_grad_tc<<<grid, FT, G_SMEM, st>>>(mq, mk, mv, mdo, ar);
   return cudaGetLastError();
 }
 

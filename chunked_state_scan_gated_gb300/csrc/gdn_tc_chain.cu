@@ -325,7 +325,8 @@ constexpr uint32_t A_S = 131072;
 constexpr uint32_t A_VP = 163840;   // V'
 constexpr uint32_t A_V2 = 180224;
 constexpr uint32_t A_G = 196608;    // buffer x at x*768: G (64 floats), rq (64), rk (64)
-constexpr uint32_t A_SC = 198144;
+constexpr uint32_t A_O = 198656;    // output tile [64 tokens][128] (two K-major atoms), TMA-stored
+constexpr uint32_t A_SC = 215040;
 constexpr uint32_t A_SMEM = A_SC + 128 + 1024;
 
 struct ChainArgs {
@@ -344,7 +345,7 @@ struct ChainArgs {
   float* M_out;
   float* S_out;
   int64_t out_seg_stride;
-  __nv_bfloat16* hc;  // CH_STATES: chunk-start states [B][H][NC][128][128]
+  uint8_t* hc;        // CH_STATES: chunk-start states, [B][H][NC] 32 KB bf16 tile images
   int* status;
   int seg_first, nseg;
 };
@@ -361,7 +362,7 @@ struct ChainArgs {
 template <int MODE>
 __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
     k_chain_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-               ChainArgs ar) {
+               const __grid_constant__ CUtensorMap mo, ChainArgs ar) {
   constexpr bool kApply = MODE == CH_APPLY;
   constexpr uint32_t XSTR = kApply ? 24576 : 16384;  // atom stride in the [W | (Q) | K] block
   constexpr uint32_t KOFF = kApply ? 16384 : 8192;   // K's offset inside an atom
@@ -513,12 +514,11 @@ __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
       }
       const float gC = exp2f(sGc[63]);
       const float kt = exp2f(sGc[63] - sGc[row & 63]) * sRk[row & 63];
-      if (MODE == CH_STATES) {  // chunk-start state, bf16 row-major [dk][dv]
-        uint4* dst = reinterpret_cast<uint4*>(ar.hc + ((bh * ar.NC + c) * 128 + row) * 128 + half * 64);
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) dst[cc] = pack8(&S[cc * 8]);
-      }
       CHAIN_SYNC();
+      if (MODE == CH_STATES && tid == 0) {  // chunk-start state: the bf16 S tile image, as is
+        bulk_store(ar.hc + (bh * ar.NC + c) * (int64_t)(2 * kImg), sm + OFF_S, 2 * kImg);
+        bulk_commit();
+      }
       // ---- MMA_a: [W; Q or K] S -> tA (W S in rows 0..63)
       if (tid == 0) {
         const uint32_t id = idesc_bf16(128, 128, 0, 1);
@@ -567,6 +567,8 @@ __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
           }
         }
       }
+      // the S tile (states) and the previous O tile (apply) are rewritten below
+      if ((MODE == CH_STATES || kApply) && tid == 0) bulk_wait_read();
       CHAIN_SYNC();
       // ---- MMA_b: K^T V2 -> tB; apply: MMA_c: [0; P] V' accumulated into tA rows 64..127
       if (tid == 0) {
@@ -617,25 +619,28 @@ __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
         for (int cc = 0; cc < 8; ++cc)
           st_chunk(sm + OFF_S, mnmaj_chunk(row, half * 8 + cc, 16384), &S[cc * 8]);
       }
-      if (kApply && quad >= 2) {  // O = gamma Q S + P V' (rows 64..127 of tA)
+      if (kApply && quad >= 2) {  // O = gamma Q S + P V' (rows 64..127 of tA) -> staging tile
         const int i = row - 64;
         const int64_t t = t0 + i;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float v[32];
           tmem_ld32(tA + lane_off + half * 64 + hh * 32, v);
-          if (t < ar.T) {
-            uint4* dst = reinterpret_cast<uint4*>(ar.o + ((b * ar.Ts + t) * ar.H + h) * 128 + half * 64 + hh * 32);
-            if (t >= L) {
+          if (t >= L) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = 0.f;
-            }
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) dst[cc] = pack8(&v[cc * 8]);
+            for (int e = 0; e < 32; ++e) v[e] = 0.f;
           }
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            st_chunk(sm + A_O + half * 8192, kmaj_chunk(i, hh * 4 + cc), &v[cc * 8]);
         }
       }
       CHAIN_SYNC();
+      if (kApply && tid == 0) {  // tokens past T are clipped by the tensor map
+        tma_store_4d(&mo, sm + A_O, 0, (int)h, (int)t0, (int)b);
+        tma_store_4d(&mo, sm + A_O + 8192, 64, (int)h, (int)t0, (int)b);
+        bulk_commit();
+      }
     }
   }
   {  // ---- final state
@@ -653,6 +658,7 @@ __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
     }
   }
 done:
+  if (tid == 0) bulk_wait_all();  // stores read shared memory until they complete
   if (tid == 0 && pend) {  // abort: let every copy and MMA still in flight finish first
     for (int i = 0; i < 5; ++i)
       if (pend & (1u << i)) {
@@ -697,7 +703,7 @@ struct DchainArgs {
   const int32_t* valid_len;
   const float* init;          // mode 0: gradient at the end of each segment
   int64_t init_seg_stride;
-  __nv_bfloat16* dhc;         // mode 0: chunk-end state gradients [B][H][NC][128][128]
+  uint8_t* dhc;               // mode 0: chunk-end state gradients, [B][H][NC] 32 KB tile images
   float* start_out;           // mode 0: gradient at the start of segment 0
   float* D_out;               // mode 1: gradient summaries
   int64_t out_seg_stride;
@@ -806,12 +812,11 @@ __global__ void __launch_bounds__(CT, 2)
         }
       }
       const float gC = exp2f(sG[63]);
-      if (store) {  // gradient of chunk c's end state, bf16 row-major [dk][dv]
-        uint4* dst = reinterpret_cast<uint4*>(ar.dhc + ((bh * ar.NC + c) * 128 + row) * 128 + half * 64);
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) dst[cc] = pack8(&dS[cc * 8]);
-      }
       CHAIN_SYNC();
+      if (store && tid == 0) {  // gradient of chunk c's end state: the bf16 dS tile image, as is
+        bulk_store(ar.dhc + (bh * ar.NC + c) * (int64_t)(2 * kImg), sm + D_DS, 2 * kImg);
+        bulk_commit();
+      }
       // ---- P^T dO + Kt dS -> tV rows 0..63 (dV'); Qg^T dO -> tS
       if (tid == 0) {
         const uint32_t idmm = idesc_bf16(128, 128, 1, 1);
@@ -852,6 +857,7 @@ __global__ void __launch_bounds__(CT, 2)
           }
         }
       }
+      if (store && tid == 0) bulk_wait_read();  // the dS tile is rewritten below
       CHAIN_SYNC();
       // ---- tS += W^T (-dV')
       if (tid == 0) {
@@ -898,6 +904,7 @@ __global__ void __launch_bounds__(CT, 2)
     }
   }
 done:
+  if (tid == 0) bulk_wait_all();
   if (tid == 0 && pend) {
     for (int i = 0; i < 3; ++i)
       if (pend & (1u << i)) {
@@ -951,9 +958,13 @@ cudaError_t launch_chain_tc(const Prob& pr, const Inputs& in, const WS& ws, int 
   CUtensorMap mq, mk;
   memset(&mq, 0, sizeof(mq));
   memset(&mk, 0, sizeof(mk));
+  CUtensorMap mo;
+  memset(&mo, 0, sizeof(mo));
   const void* qptr = in.q ? in.q : in.k;  // summaries and states never read q
+  const void* optr = o ? o : in.k;        // only apply writes o
   if (!tc_make_map(&mq, qptr, pr.B, pr.T, pr.Ts, pr.Hqk) ||
-      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk))
+      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mo, optr, pr.B, pr.T, pr.Ts, o ? pr.H : pr.Hqk))
     return cudaErrorInvalidValue;
   ChainArgs ar;
   ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.Hqk = pr.Hqk; ar.r = pr.r; ar.NC = pr.NC;
@@ -965,20 +976,20 @@ cudaError_t launch_chain_tc(const Prob& pr, const Inputs& in, const WS& ws, int 
   ar.init = init; ar.init_seg_stride = init_seg_stride;
   ar.o = (__nv_bfloat16*)o; ar.final_out = final_out;
   ar.M_out = M_out; ar.S_out = S_out; ar.out_seg_stride = out_seg_stride;
-  ar.hc = (__nv_bfloat16*)hc;
+  ar.hc = (uint8_t*)hc;
   ar.status = ws.status;
   ar.seg_first = seg_first; ar.nseg = nseg;
   cudaError_t e;
   dim3 grid(mode == CH_SUM ? 2 : 1, (unsigned)pr.H, (unsigned)(pr.B * nseg));
   if (mode == CH_APPLY) {
     if ((e = smem_attr(k_chain_tc<CH_APPLY>, A_SMEM)) != cudaSuccess) return e;
-    k_chain_tc<CH_APPLY><<<grid, CT, A_SMEM, st>>>(mq, mk, ar);
+    k_chain_tc<CH_APPLY><<<grid, CT, A_SMEM, st>>>(mq, mk, mo, ar);
   } else if (mode == CH_SUM) {
     if ((e = smem_attr(k_chain_tc<CH_SUM>, S_SMEM)) != cudaSuccess) return e;
-    k_chain_tc<CH_SUM><<<grid, CT, S_SMEM, st>>>(mq, mk, ar);
+    k_chain_tc<CH_SUM><<<grid, CT, S_SMEM, st>>>(mq, mk, mo, ar);
   } else {
     if ((e = smem_attr(k_chain_tc<CH_STATES>, S_SMEM)) != cudaSuccess) return e;
-    k_chain_tc<CH_STATES><<<grid, CT, S_SMEM, st>>>(mq, mk, ar);
+    k_chain_tc<CH_STATES><<<grid, CT, S_SMEM, st>>>(mq, mk, mo, ar);
   }
   return cudaGetLastError();
 }
@@ -1002,7 +1013,7 @@ cudaError_t launch_dchain_tc(const Prob& pr, const Inputs& in, const WS& ws, int
   ar.rqk = ws.rqk; ar.wim = (const uint8_t*)ws.wim; ar.pim = (const uint8_t*)ws.pim;
   ar.gl = ws.gl; ar.valid_len = in.valid_len;
   ar.init = init; ar.init_seg_stride = init_seg_stride;
-  ar.dhc = (__nv_bfloat16*)dhc; ar.start_out = start_out; ar.D_out = D_out;
+  ar.dhc = (uint8_t*)dhc; ar.start_out = start_out; ar.D_out = D_out;
   ar.out_seg_stride = out_seg_stride; ar.status = ws.status;
   ar.mode = mode; ar.seg_first = seg_first; ar.nseg = nseg;
   cudaError_t e = smem_attr(k_dchain_tc, D_SMEM);

@@ -53,19 +53,6 @@ bool tc_make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t 
   return make_map(m, ptr, B, T, Ts, heads);
 }
 
-// [n][128][128] bf16 matrices (chunk states, state gradients), boxes of 128 rows x 64 columns.
-bool tc_make_state_map(CUtensorMap* m, const void* ptr, int64_t n) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc || n <= 0) return false;
-  cuuint64_t dims[4] = {128, 128, (cuuint64_t)n, 1};
-  cuuint64_t strides[3] = {256, 32768, (cuuint64_t)(n * 32768)};
-  cuuint32_t box[4] = {64, 128, 1, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool tc_path(const Prob& pr) {
   return pr.dtype == GDN_BF16 && pr.dk == 128 && pr.dv == 128 && pr.B > 0 && pr.NC > 0;
 }
