@@ -81,8 +81,8 @@ constexpr uint32_t P_V = 32768;                // V atoms at a*8192
 constexpr uint32_t P_TA = 49152;               // [T_u; T_w], 128 x 64 K-major
 constexpr uint32_t P_A = 65536;                // fp32 A [64][LDA]
 constexpr uint32_t P_T = P_A + 64 * LDA * 4;   // fp32 T [64][LDA]
-constexpr uint32_t P_Y = P_T + 64 * LDA * 4;   // solve scratch, 768 floats
-constexpr uint32_t P_SC = P_Y + 768 * 4;       // gates, row factors, barriers
+constexpr uint32_t P_Y = P_T + 64 * LDA * 4;   // solve scratch, 8 warps x 128 floats
+constexpr uint32_t P_SC = P_Y + 1024 * 4;      // gates, row factors, barriers
 constexpr uint32_t P_SMEM = P_SC + 1280 + 64 + 1024;
 
 struct PrepArgs {
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(PT, 2)
   }
   tc_fence_before();
   __syncthreads();
-  solve_unit_lower64(sA, sT, sY);
+  solve_unit_lower64_mma(sA, sT, sY, LDA);
   if (ar.tim) {  // T for the backward, bf16 image
     uint8_t* dst = ar.tim + (bh * ar.NC + c) * (int64_t)kImgP;
     for (int e = tid; e < 512; e += PT) {

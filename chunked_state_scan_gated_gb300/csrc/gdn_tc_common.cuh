@@ -298,5 +298,81 @@ __device__ __forceinline__ void solve_unit_lower64(const float* A, float* T, flo
   }
 }
 
+// One warp-level tensor-core step D = A B + D on a 16 x 8 tile, tf32 operands
+// (fp32 rounded to nearest), fp32 accumulation.  Fragment ownership (g = lane / 4,
+// t = lane % 4): a0 (g, t), a1 (g+8, t), a2 (g, t+4), a3 (g+8, t+4);
+// b0 (t, g), b1 (t+4, g); c0 (g, 2t), c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&c)[4], const float (&a)[4],
+                                                const float (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(to_tf32(a[0])), "r"(to_tf32(a[1])), "r"(to_tf32(a[2])), "r"(to_tf32(a[3])),
+        "r"(to_tf32(b[0])), "r"(to_tf32(b[1])));
+}
+
+// T = (I + A)^-1 for strictly lower A (64 x 64, fp32, leading dim lda).  The
+// 16 x 16 diagonal blocks come from forward substitution on CUDA cores; the
+// blocks below them, block diagonal by block diagonal, from
+// T_ij = -T_ii (sum_{j <= m < i} A_im T_mj) with warp-level tf32 MMAs (one warp
+// per 16 x 8 half block).  Y needs 8 warps x 128 floats.  Needs blockDim.x >= 256.
+__device__ __forceinline__ void solve_unit_lower64_mma(const float* A, float* T, float* Y,
+                                                       const int lda) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp < 4 && lane < 16) {
+    const int b0 = warp * 16, j = lane;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float v = (i == j) ? 1.f : 0.f;
+#pragma unroll
+      for (int l = 0; l < i; ++l) v = fmaf(-A[(b0 + i) * lda + b0 + l], x[l], v);
+      x[i] = (i >= j) ? v : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) T[(b0 + i) * lda + b0 + j] = x[i];
+  }
+  __syncthreads();
+  const int g = lane >> 2, t = lane & 3;
+  float* Yw = Y + warp * 128;  // [16][8] scratch of this warp
+  for (int d = 1; d <= 3; ++d) {
+    if (warp < 2 * (4 - d)) {
+      const int bj = warp >> 1, bi = bj + d, r0 = bi * 16, n0 = bj * 16 + (warp & 1) * 8;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int m = bj * 16; m < bi * 16; m += 8) {  // Y = A[bi, bj..bi) T[bj..bi, bj]
+        const float a[4] = {A[(r0 + g) * lda + m + t], A[(r0 + g + 8) * lda + m + t],
+                            A[(r0 + g) * lda + m + t + 4], A[(r0 + g + 8) * lda + m + t + 4]};
+        const float b[2] = {T[(m + t) * lda + n0 + g], T[(m + t + 4) * lda + n0 + g]};
+        mma_tf32_16x8x8(c, a, b);
+      }
+      Yw[g * 8 + 2 * t] = c[0];
+      Yw[g * 8 + 2 * t + 1] = c[1];
+      Yw[(g + 8) * 8 + 2 * t] = c[2];
+      Yw[(g + 8) * 8 + 2 * t + 1] = c[3];
+      __syncwarp();
+      float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 16; k += 8) {  // T_ij = -T_ii Y
+        const float a[4] = {T[(r0 + g) * lda + r0 + k + t], T[(r0 + g + 8) * lda + r0 + k + t],
+                            T[(r0 + g) * lda + r0 + k + t + 4],
+                            T[(r0 + g + 8) * lda + r0 + k + t + 4]};
+        const float b[2] = {Yw[(k + t) * 8 + g], Yw[(k + t + 4) * 8 + g]};
+        mma_tf32_16x8x8(e, a, b);
+      }
+      T[(r0 + g) * lda + n0 + 2 * t] = -e[0];
+      T[(r0 + g) * lda + n0 + 2 * t + 1] = -e[1];
+      T[(r0 + g + 8) * lda + n0 + 2 * t] = -e[2];
+      T[(r0 + g + 8) * lda + n0 + 2 * t + 1] = -e[3];
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace tc
 }  // namespace gdn
