@@ -430,10 +430,7 @@ def run_ours(args):
                 ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
                 key = ("fwd." if op == gdn.GDN_OP_FWD else "bwd.") + nm
                 tot[key] = ms
-        P = p.segments if p.segments > 0 else None
-        if P is None:
-            # the automatic segment count used by the library
-            P = _auto_segments(gdn, p)
+        P = gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD)
         dom = max(tot, key=tot.get)
         ms_dom = tot[dom]
         flops, byt = kernel_work(dom, w, P)
@@ -496,24 +493,6 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
-
-
-def _auto_segments(gdn, p):
-    # Mirrors the library's automatic choice through the workspace layout: the
-    # number of segments is visible as the count of kernel launches only, so ask
-    # the library for a problem copy with segments set explicitly until sizes match.
-    import ctypes
-    base = gdn.gdn_workspace_size(p, gdn.GDN_OP_BWD)
-    nc = max(1, math.ceil(p.T / C))
-    for P in (1, 2, 4, 8, 16, 32, 64):
-        if P > nc:
-            break
-        q = gdn.Problem()
-        ctypes.memmove(ctypes.byref(q), ctypes.byref(p), ctypes.sizeof(p))
-        q.segments = P
-        if gdn.gdn_workspace_size(q, gdn.GDN_OP_BWD) == base:
-            return P
-    return 1
 
 
 def main():

@@ -8,7 +8,8 @@ CPU fallback.
 The functions keep the C names (``gdn_fwd``, ``gdn_bwd``, ``gdn_summary``,
 ``gdn_summary_bwd``, ``gdn_compose``, ``gdn_prefix_compose``,
 ``gdn_prefix_compose_bwd``, ``gdn_apply_state``, ``gdn_apply_state_bwd``,
-``gdn_query_support``, ``gdn_workspace_size``, ``gdn_check_device_status``) and
+``gdn_query_support``, ``gdn_resolved_segments``, ``gdn_workspace_size``,
+``gdn_check_device_status``) and
 take torch tensors in the token-major layouts of the header: q, k
 [B,T,Hqk,dk]; v [B,T,H,dv]; a, b [B,T,H]; A_log, dt_bias [H] fp32; states
 [B,H,dk,dv] fp32.
@@ -32,7 +33,7 @@ GDN_OP_FWD, GDN_OP_BWD, GDN_OP_SUMMARY, GDN_OP_SUMMARY_BWD = range(4)
 # Every symbol include/gdn.h declares (checked by the CPU test suite).
 EXPORTS = (
     "gdn_status_string", "gdn_abi_version", "gdn_problem_init", "gdn_query_support",
-    "gdn_workspace_size", "gdn_fwd", "gdn_bwd", "gdn_summary", "gdn_summary_bwd",
+    "gdn_resolved_segments", "gdn_workspace_size", "gdn_fwd", "gdn_bwd", "gdn_summary", "gdn_summary_bwd",
     "gdn_compose", "gdn_prefix_compose", "gdn_prefix_compose_bwd", "gdn_apply_state",
     "gdn_apply_state_bwd", "gdn_check_device_status", "gdn_kernel_info", "gdn_fwd_kernel",
     "gdn_bwd_kernel", "gdn_fwd_noalloc",
@@ -81,6 +82,8 @@ def load_library(path: str | None = None):
             "gdn_query_support": ([_PP], ctypes.c_int),
             "gdn_workspace_size": ([_PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
                                    ctypes.c_int),
+            "gdn_resolved_segments": ([_PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
+                                      ctypes.c_int),
             "gdn_fwd": ([_PP] + [_VP] * 12 + [ctypes.c_size_t, _VP], ctypes.c_int),
             "gdn_apply_state": ([_PP] + [_VP] * 12 + [ctypes.c_size_t, _VP], ctypes.c_int),
             "gdn_bwd": ([_PP] + [_VP] * 18 + [ctypes.c_size_t, _VP], ctypes.c_int),
@@ -166,6 +169,14 @@ def gdn_workspace_size(problem: Problem, op: int) -> int:
     n = ctypes.c_size_t(0)
     _check("gdn_workspace_size",
            load_library().gdn_workspace_size(ctypes.byref(problem), op, ctypes.byref(n)))
+    return n.value
+
+
+def gdn_resolved_segments(problem: Problem, op: int) -> int:
+    """Segments the call of `op` splits T into (problem.segments, or the automatic choice)."""
+    n = ctypes.c_int32(0)
+    _check("gdn_resolved_segments",
+           load_library().gdn_resolved_segments(ctypes.byref(problem), op, ctypes.byref(n)))
     return n.value
 
 

@@ -38,10 +38,46 @@ bool ok_ptr(const void* p, int64_t numel) {
 }
 bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
 
+// SM count of the current device (152 on GB300 when no device can be queried).
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return n;
+}
+
+// Segment count of the tensor-core path: the P that minimises a model of the
+// forward + backward chain time.  Every chain pass runs ceil(CTAs / slots)
+// waves of ceil(NC / P) chunk steps (slots = SMs, or 2 x SMs for the passes that
+// fit two CTAs on an SM); the step times (us, GB300) are those of the chain
+// kernels measured at T = 32K, and each prefix step costs ~7 us.
+int auto_segments_tc(int64_t BH, int64_t NC, int sms) {
+  double best = 1e300;
+  int best_p = 1;
+  for (int64_t P = 1; P <= 64 && P <= NC; ++P) {
+    const int64_t cps = (NC + P - 1) / P, pe = (NC + cps - 1) / cps;
+    auto waves = [](int64_t n, int64_t slots) { return (double)((n + slots - 1) / slots); };
+    const double fwd = waves(2 * BH * (pe - 1), 2 * sms) * cps * 2.9 +
+                       waves(BH * pe, sms) * cps * 3.2 + (pe - 1) * 7.0;
+    const double bwd = waves(2 * BH * pe, 2 * sms) * cps * 2.9 +
+                       waves(BH * pe, 2 * sms) * cps * 4.4 +
+                       waves(BH * (pe - 1), 2 * sms) * cps * 4.6 +
+                       waves(BH * pe, 2 * sms) * cps * 5.7 + 2 * (pe - 1) * 7.0;
+    if (fwd + bwd < best - 1e-9) {
+      best = fwd + bwd;
+      best_p = (int)pe;
+    }
+  }
+  return best_p;
+}
+
 int auto_segments(int64_t B, int64_t H, int64_t dv, int64_t NC, bool tensor_core) {
   if (NC <= 1) return 1;
-  // The tensor-core scan runs one CTA per (row, head, segment) and holds a whole SM.
-  const int64_t per_seg = tensor_core ? B * H : B * H * ((dv + kScanCols - 1) / kScanCols);
+  if (tensor_core) return auto_segments_tc(B * H, NC, device_sms());
+  const int64_t per_seg = B * H * ((dv + kScanCols - 1) / kScanCols);
   int64_t want = (kTargetBlocks + per_seg - 1) / (per_seg > 0 ? per_seg : 1);
   int64_t P = 1;
   while (P < want) P <<= 1;
@@ -384,6 +420,15 @@ void gdn_problem_init(gdn_problem* p) {
 gdn_status gdn_query_support(const gdn_problem* p) {
   Prob pr;
   return resolve_op(p, GDN_OP_FWD, &pr);
+}
+
+gdn_status gdn_resolved_segments(const gdn_problem* p, int32_t op, int32_t* segments) {
+  if (!segments || op < GDN_OP_FWD || op > GDN_OP_SUMMARY_BWD) return GDN_ERR_INVALID_ARG;
+  Prob pr;
+  gdn_status s = resolve_op(p, op, &pr);
+  if (s != GDN_OK) return s;
+  *segments = pr.P;
+  return GDN_OK;
 }
 
 gdn_status gdn_workspace_size(const gdn_problem* p, int32_t op, size_t* bytes) {

@@ -117,6 +117,12 @@ void gdn_problem_init(gdn_problem* p);
  */
 gdn_status gdn_query_support(const gdn_problem* p);
 
+/* Number of sequence segments (*segments) a call of `op` on problem p splits T into:
+   p->segments when set, else the automatic choice for the current device (on the
+   tensor-core path, the count that minimises a model of the chain passes' time).
+   Summary calls always use 1. */
+gdn_status gdn_resolved_segments(const gdn_problem* p, int32_t op, int32_t* segments);
+
 /* Workspace bytes needed by `op` for problem p on the current device (writes *bytes).
    Always at least 256 (the device status word lives there). */
 gdn_status gdn_workspace_size(const gdn_problem* p, int32_t op, size_t* bytes);
