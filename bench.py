@@ -291,6 +291,31 @@ def run_reference(args):
     return 0
 
 
+# ---------------------------------------------------------------- rank helpers
+
+def ranks_barrier(world):
+    """Barrier over the process group (no-op for one rank)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def ranks_max(x, world, device):
+    """Max of a per-rank float over all ranks (the slowest replica's time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ms_max, tokens_per_rank, world):
+    """Whole-job tokens/s: every replica processed its own tokens within the slowest time."""
+    return world * tokens_per_rank / (ms_max / 1e3)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args):
@@ -308,15 +333,10 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        ranks_barrier(world)
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return ranks_max(x, world, "cuda")
 
     w = workload_of(args.workload, args.T)
     inp = gi.make_inputs(w, seed=w.seed + 1000 * rank)
@@ -374,7 +394,7 @@ def run_ours(args):
     ms_step = max_over_ranks(ms_step)
     ms_fwd = max_over_ranks(timed(fwd, args.steps))
     tokens = B * T
-    value = world * tokens / (ms_step / 1e3)
+    value = job_throughput(ms_step, tokens, world)
 
     nf = len(gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD))
     nb = len(gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD))
@@ -390,7 +410,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(w, args, world),
-        "fwd": {"ms": ms_fwd, "tokens_per_s": world * tokens / (ms_fwd / 1e3)},
+        "fwd": {"ms": ms_fwd, "tokens_per_s": job_throughput(ms_fwd, tokens, world)},
         "gpu_launches": args.steps * (nf + nb),
         "step_roofline": {
             "flops": alg["flops_step"], "bytes": alg["bytes_step"],
@@ -477,7 +497,7 @@ def run_ours(args):
 
         e2e_step()
         ms_e2e = max_over_ranks(timed(e2e_step, args.steps))
-        line["e2e"] = {"value": world * tokens / (ms_e2e / 1e3), "unit": UNIT,
+        line["e2e"] = {"value": job_throughput(ms_e2e, tokens, world), "unit": UNIT,
                        "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": ms_e2e}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

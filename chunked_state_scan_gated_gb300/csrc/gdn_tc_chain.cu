@@ -423,6 +423,8 @@ __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
   }
 #pragma unroll
   for (int cc = 0; cc < 8; ++cc) st_chunk(sm + OFF_S, mnmaj_chunk(row, half * 8 + cc, 16384), &S[cc * 8]);
+  fence_proxy_async();  // the first MMA_a reads the initial state tile
+  __syncthreads();
 
   {
     const uint8_t* wsrc = ar.wim + bh * ar.NC * (int64_t)kImg;
@@ -493,12 +495,33 @@ __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
       const float* sRk = sGc + (kApply ? 128 : 64);
       const uint32_t xpar = kApply ? (uint32_t)((k >> 1) & 1) : par;
       uint64_t* bar_x = bars + (kApply ? bi : 0);
-      // ---- inputs of chunk c
-      if (!mbar_wait(bar_x, xpar, ar.status, kStatusTimeout)) *s_abort = 1;
-      if (tid == 0) pend &= kApply ? ~(1u << bi) : ~1u;
-      if (!kApply) {
-        if (!mbar_wait(bars + 1, par, ar.status, kStatusTimeout)) *s_abort = 1;
-        if (tid == 0) pend &= ~2u;
+      // ---- inputs of chunk c: W (and q, k, gates for apply) before MMA_a
+      if (kApply || tid == 0) {
+        if (!mbar_wait(bar_x, xpar, ar.status, kStatusTimeout)) *s_abort = 1;
+        if (tid == 0) pend &= kApply ? ~(1u << bi) : ~1u;
+      }
+      if (tid == 0) {  // pull the tiles of the next loads into L2
+        if (!kApply && c + 1 < ce) {
+          l2_prefetch(wsrc + (c + 1) * kImg, kImg);
+          if (needU) l2_prefetch(usrc + (c + 1) * kImg, kImg);
+          l2_prefetch_tile(&mk, 0, (int)hq, (int)((c + 1) * 64), (int)b);
+          l2_prefetch_tile(&mk, 64, (int)hq, (int)((c + 1) * 64), (int)b);
+          l2_prefetch(gsrc + (c + 1) * 64, 256);
+          l2_prefetch(rsrc + (c + 1) * 128 + 64, 256);
+        }
+        if (kApply && c + 1 < ce) {
+          l2_prefetch(usrc + (c + 1) * kImg, kImg);
+          l2_prefetch(psrc + (c + 1) * kImgP, kImgP);
+        }
+        if (kApply && c + 2 < ce) {
+          l2_prefetch(wsrc + (c + 2) * kImg, kImg);
+          for (int a = 0; a < 2; ++a) {
+            l2_prefetch_tile(&mq, a * 64, (int)hq, (int)((c + 2) * 64), (int)b);
+            l2_prefetch_tile(&mk, a * 64, (int)hq, (int)((c + 2) * 64), (int)b);
+          }
+          l2_prefetch(gsrc + (c + 2) * 64, 256);
+          l2_prefetch(rsrc + (c + 2) * 128, 512);
+        }
       }
       if (kApply) {  // q rows scaled by gamma_i rq_i (every chunk of a row shares the factor)
         for (int e = tid; e < 1024; e += CT) {
@@ -512,16 +535,16 @@ __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
           st_chunk(sm, off, x);
         }
       }
-      const float gC = exp2f(sGc[63]);
-      const float kt = exp2f(sGc[63] - sGc[row & 63]) * sRk[row & 63];
-      CHAIN_SYNC();
+      // apply: the scaled q tile must be complete; otherwise the loop's last barrier
+      // already ordered the state tile S(c) before MMA_a
+      if (kApply) CHAIN_SYNC();
       if (MODE == CH_STATES && tid == 0) {  // chunk-start state: the bf16 S tile image, as is
         bulk_store(ar.hc + (bh * ar.NC + c) * (int64_t)(2 * kImg), sm + OFF_S, 2 * kImg);
         bulk_commit();
       }
-      // ---- MMA_a: [W; Q or K] S -> tA (W S in rows 0..63)
+      // ---- MMA_a: apply [W; Q] S -> tA (W S in rows 0..63); otherwise W S with M = 64
       if (tid == 0) {
-        const uint32_t id = idesc_bf16(128, 128, 0, 1);
+        const uint32_t id = idesc_bf16(kApply ? 128 : 64, 128, 0, 1);
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t at = ks >> 2, kk = ks & 3;
           mma_bf16(tA, sdesc(base + xa + at * XSTR + kk * 32, 16, 1024),
@@ -530,7 +553,16 @@ __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
         mma_commit(bar_mma);
         pend |= 16u;
       }
-      if (needU && quad < 2) {
+      if (!kApply) {  // k tile, gates and rk of chunk c: first needed for V2 and MMA_b
+        if (!mbar_wait(bars + 1, par, ar.status, kStatusTimeout)) *s_abort = 1;
+        if (tid == 0) pend &= ~2u;
+      }
+      const float gC = exp2f(sGc[63]);
+      // token row of V' owned by this thread: M = 128 (apply: quadrants 0, 1) or M = 64
+      // accumulator layout (row r in TMEM lane (r % 16) + 32 (r / 16): lanes 0..15)
+      const int vi = kApply ? row : quad * 16 + (lane & 15);
+      const float kt = exp2f(sGc[63] - sGc[vi & 63]) * sRk[vi & 63];
+      if (needU && (!kApply || quad < 2)) {
         if (!mbar_wait(bar_u, par, ar.status, kStatusTimeout)) *s_abort = 1;
         if (tid == 0) pend &= ~4u;
       }
@@ -541,12 +573,14 @@ __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
         issue_x(c + 1, bars + 0, S_XA, 0);
         pend |= 1u;
       }
-      if (quad < 2) {  // V' = U - W S, V2 = rk e^{G_C - G} V'
-        const int i = row;
+      if (!kApply || quad < 2) {  // V' = U - W S, V2 = rk e^{G_C - G} V'
+        const int i = vi;
+        const bool own = kApply || lane < 16;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float v[32];
           tmem_ld32(tA + lane_off + half * 64 + hh * 32, v);
+          if (!own) continue;
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             const int chn = half * 8 + hh * 4 + cc;
@@ -687,7 +721,7 @@ done:
 // ============================================================================
 constexpr uint32_t D_XA = 0;        // atoms a at a*16384: [Kt_a | Qg_a] (scaled k, scaled q)
 constexpr uint32_t D_W = 32768;     // W image
-constexpr uint32_t D_P = 49152;     // P image; the 64 rows after it (dO) stand in as junk A rows
+constexpr uint32_t D_P = 49152;     // P image (8 KB)
 constexpr uint32_t D_DO = 57344;    // dO tile, later -dV' (MN-major, halves 8 KB apart)
 constexpr uint32_t D_DS = 73728;    // dS, bf16, MN-major (halves 16 KB apart)
 constexpr uint32_t D_G = 106496;    // G, rq, rk of the chunk (64 floats each)
@@ -790,6 +824,18 @@ __global__ void __launch_bounds__(CT, 2)
       const int64_t k = ce - 1 - c;
       const int64_t t0 = c * 64;
       const uint32_t par = (uint32_t)(k & 1);
+      if (tid == 0 && c - 1 >= cs) {  // pull the tiles of chunk c-1 into L2
+        const int tp = (int)((c - 1) * 64);
+        for (int a = 0; a < 2; ++a) {
+          l2_prefetch_tile(&mk, a * 64, (int)hq, tp, (int)b);
+          l2_prefetch_tile(&mq, a * 64, (int)hq, tp, (int)b);
+          l2_prefetch_tile(&mdo, a * 64, (int)h, tp, (int)b);
+        }
+        l2_prefetch(psrc + (c - 1) * kImgP, kImgP);
+        l2_prefetch(wsrc + (c - 1) * kImg, kImg);
+        l2_prefetch(gsrc + (c - 1) * 64, 256);
+        l2_prefetch(rsrc + (c - 1) * 128, 512);
+      }
       if (!mbar_wait(bar_a, par, ar.status, kStatusTimeout)) *s_abort = 1;
       if (!mbar_wait(bar_b, par, ar.status, kStatusTimeout)) *s_abort = 1;
       if (tid == 0) pend &= ~3u;
@@ -817,13 +863,14 @@ __global__ void __launch_bounds__(CT, 2)
         bulk_store(ar.dhc + (bh * ar.NC + c) * (int64_t)(2 * kImg), sm + D_DS, 2 * kImg);
         bulk_commit();
       }
-      // ---- P^T dO + Kt dS -> tV rows 0..63 (dV'); Qg^T dO -> tS
+      // ---- P^T dO + Kt dS -> tV (dV', M = 64 layout); Qg^T dO -> tS
       if (tid == 0) {
-        const uint32_t idmm = idesc_bf16(128, 128, 1, 1);
+        const uint32_t idv = idesc_bf16(64, 128, 1, 1);
         for (int ks = 0; ks < 4; ++ks)
           mma_bf16(tV, sdesc(base + D_P + ks * 2048, 8192, 1024),
-                   sdesc(base + D_DO + ks * 2048, 8192, 1024), idmm, ks > 0);
-        const uint32_t idkm = idesc_bf16(128, 128, 0, 1);
+                   sdesc(base + D_DO + ks * 2048, 8192, 1024), idv, ks > 0);
+        const uint32_t idkm = idesc_bf16(64, 128, 0, 1);
+        const uint32_t idmm = idesc_bf16(128, 128, 1, 1);
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t at = ks >> 2, kk = ks & 3;
           mma_bf16(tV, sdesc(base + D_XA + at * 16384 + kk * 32, 16, 1024),
@@ -842,12 +889,13 @@ __global__ void __launch_bounds__(CT, 2)
         issue_a(c - 1);
         pend |= 1u;
       }
-      if (quad < 2) {  // -dV' over the dO tile
-        const int i = row;
+      {  // -dV' over the dO tile; row r of the M = 64 accumulator is in TMEM lane (r % 16) + 32 (r / 16)
+        const int i = quad * 16 + (lane & 15);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float v[32];
           tmem_ld32(tV + lane_off + half * 64 + hh * 32, v);
+          if (lane >= 16) continue;
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             float x[8];

@@ -96,6 +96,19 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Hints that pull global data into L2 ahead of a later load (no completion to wait on).
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void l2_prefetch_tile(const CUtensorMap* map, int c0, int c1, int c2,
+                                                 int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   (uint64_t)map),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 // Bulk copy of `bytes` from shared to global memory (same alignment rules), in
 // this thread's bulk group; bulk_commit() closes the group, bulk_wait_read()
 // waits until every committed group has finished reading shared memory.
