@@ -72,6 +72,7 @@ def _load():
             "oracle_compose": [ctypes.c_int64] * 3 + [_D] * 6,
             "oracle_prefix": [ctypes.c_int64] * 4 + [_D] * 5,
             "oracle_prefix_bwd": [ctypes.c_int64] * 4 + [_D] * 5,
+            "oracle_gate_param_bwd": [_P, _D, _D, _D, _D, _I, _D, _D, _D, _D, _D, _D],
         }.items():
             fn = getattr(lib, name)
             fn.argtypes = args
@@ -222,6 +223,22 @@ def summary_bwd(q, k, a, b, A_log, dt_bias, dO, valid_len=None, *, l2norm=True, 
                                       _ptr(A_log), _ptr(dt_bias), _ptr(vl), _ptr(dO), _ptr(D),
                                       nthreads), "summary_bwd")
     return D
+
+
+def gate_param_bwd(a, b, A_log, dt_bias, dg, dbeta, valid_len=None):
+    """Gradients of the gate parameters from dg, dbeta [B,T,H]: (da, db [B,T,H],
+    dA_log, ddt_bias [H]) through g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)."""
+    a, b, A_log, dt_bias = _f64(a), _f64(b), _f64(A_log), _f64(dt_bias)
+    dg, dbeta = _f64(dg), _f64(dbeta)
+    B, T, H = a.shape
+    p = _problem(np.zeros((B, T, H, 1)), np.zeros((B, T, H, 1)))
+    da, db = np.empty_like(a), np.empty_like(a)
+    dA, ddt = np.empty(H), np.empty(H)
+    _check(_load().oracle_gate_param_bwd(ctypes.byref(p), _ptr(a), _ptr(b), _ptr(A_log),
+                                         _ptr(dt_bias), _ptr(_vl(valid_len)), _ptr(dg),
+                                         _ptr(dbeta), _ptr(da), _ptr(db), _ptr(dA), _ptr(ddt)),
+           "gate_param_bwd")
+    return da, db, dA, ddt
 
 
 def compose(M2, S2, M1, S1):

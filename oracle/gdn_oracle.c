@@ -638,4 +638,50 @@ int oracle_prefix_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, const double
   return 0;
 }
 
+/* ------------------------------------------------- gate parameter gradients */
+
+/* Chain of dg, dbeta [B,T,H] to the gate parameters, from the prologue's
+ * definitions g = -exp(A_log[h]) softplus(a + dt_bias[h]), beta = sigmoid(b)
+ * (softplus' = sigmoid):
+ *   da_t       = dg_t * (-exp(A_log[h])) * sigmoid(a_t + dt_bias[h])
+ *   db_t       = dbeta_t * beta_t (1 - beta_t)
+ *   ddt_bias_h = sum_{b,t} da_t            dA_log_h = sum_{b,t} dg_t * g_t
+ * Padded tokens (t >= valid_len[b]) have g and beta fixed at 0, independent of
+ * a, b and the parameters: their da, db are 0 and they add nothing to the sums.
+ * Softplus is x for x > 20 in the forward; its derivative there is taken as 1. */
+int oracle_gate_param_bwd(const oracle_problem* p, const double* a, const double* b,
+                          const double* A_log, const double* dt_bias, const int32_t* valid_len,
+                          const double* dg, const double* dbeta, double* da, double* db,
+                          double* dA_log, double* ddt_bias) {
+  int rc = check_problem(p);
+  if (rc) return rc;
+  if ((rc = check_valid_len(p, valid_len))) return rc;
+  for (int64_t h = 0; h < p->H; ++h) {
+    dA_log[h] = 0.0;
+    ddt_bias[h] = 0.0;
+  }
+  for (int64_t bb = 0; bb < p->B; ++bb) {
+    const int64_t L = valid_length(p, valid_len, bb);
+    for (int64_t t = 0; t < p->T; ++t) {
+      for (int64_t h = 0; h < p->H; ++h) {
+        const int64_t gi = G_IDX(p, bb, t, h);
+        if (t >= L) {
+          da[gi] = 0.0;
+          db[gi] = 0.0;
+          continue;
+        }
+        const double x = a[gi] + dt_bias[h];
+        const double dsp = x > 20.0 ? 1.0 : sigmoid(x);
+        const double g = -exp(A_log[h]) * softplus(x);
+        const double be = sigmoid(b[gi]);
+        da[gi] = dg[gi] * (-exp(A_log[h])) * dsp;
+        db[gi] = dbeta[gi] * be * (1.0 - be);
+        ddt_bias[h] += da[gi];
+        dA_log[h] += dg[gi] * g;
+      }
+    }
+  }
+  return 0;
+}
+
 int oracle_abi_version(void) { return 1; }

@@ -353,6 +353,36 @@ def test_gate_gradients_chain_to_the_parameters():
             np.testing.assert_allclose(chain, fd, rtol=1e-5, atol=1e-8)
 
 
+@pytest.mark.parametrize("valid_len", [None, [4, 6]])
+def test_gate_parameter_gradients_match_finite_differences(valid_len):
+    """oracle.gate_param_bwd (da, db, dA_log, ddt_bias from dg, dbeta) against central
+    finite differences of the whole loss L = <dO, o> + <dHT, hT> in every gate input
+    and parameter, with and without trailing padding."""
+    B, T, Hqk, H, dk, dv = 2, 6, 1, 2, 4, 3
+    q, k, v = rand(B, T, Hqk, dk), rand(B, T, Hqk, dk), rand(B, T, H, dv)
+    a, b, A_log, dt_bias = _gates(B, T, H, slow=True)
+    dO, dHT = rand(B, T, H, dv), rand(B, H, dk, dv)
+    vl = None if valid_len is None else np.array(valid_len, dtype=np.int32)
+    _, _, _, dg, dbe, _ = oracle.bwd(q, k, v, a, b, A_log, dt_bias, dO, dHT, valid_len=vl)
+    da, db, dA, ddt = oracle.gate_param_bwd(a, b, A_log, dt_bias, dg, dbe, valid_len=vl)
+
+    def loss():
+        o, hT = oracle.fwd(q, k, v, a, b, A_log, dt_bias, valid_len=vl)
+        return float(np.sum(o * dO) + np.sum(hT * dHT))
+
+    eps = 1e-6
+    for x, grad in ((a, da), (b, db), (A_log, dA), (dt_bias, ddt)):
+        flat, gflat = x.reshape(-1), grad.reshape(-1)
+        for i in range(flat.size):
+            old = flat[i]
+            flat[i] = old + eps
+            lp = loss()
+            flat[i] = old - eps
+            lm = loss()
+            flat[i] = old
+            np.testing.assert_allclose(gflat[i], (lp - lm) / (2 * eps), rtol=1e-5, atol=1e-8)
+
+
 def test_gradient_summary_and_reverse_prefix_reproduce_dH0():
     """D of a segment = dH_in with dH_out = 0; the reverse prefix of (M^T, D) over
     segments gives the monolithic dH0, and per-segment backward from dH_out[i]
