@@ -44,7 +44,8 @@ constexpr int FT = 256;
 //   dq  = diag(gamma) dO S^T + (dP o Gamma) K,      dP = dO V'^T (lower)
 //   dk  = (dP o Gamma)^T Q + diag(kt) V' dS^T + diag(beta gamma) X_w + E K + E^T K
 //   dv  = diag(beta) X_v,  dW = -dV' S^T,
-//   dA  = -(X_v U^T + X_w W^T) (strictly lower),  E = dA o beta_i Gamma
+//   dA  = -(X_v U^T + X_w W^T) = -X_v V'^T (strictly lower; W S = U - V'),
+//   E = dA o beta_i Gamma
 //   dbeta, dG: row dots of the same pieces; dg = reverse cumsum of dG.
 // All MMAs are M = 64: row r of an accumulator lives in TMEM lane
 // (r % 16) + 32 (r / 16), so threads with lane < 16 of each warp own one row.
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(FT, 1)
   float* sKt = sBeta + 64;
   float* sDG = sKt + 64;               // dG terms computed row-wise by threads 0..63
   float* sMisc = sDG + 64;             // [8] block partials of <S, dS>
-  // half-row partial sums, [2][64] each, in the T tile's slot (free after RT5)
+  // half-row partial sums, [2][64] each, in the T tile's slot (free after R5)
   float* sRed = (float*)(sm + G_TP);   // dG
   float* sRedB = sRed + 128;           // dbeta
   float* sRedS = sRedB + 128;          // Kt terms
@@ -297,7 +298,8 @@ __global__ void __launch_bounds__(FT, 1)
     }
   }
   PHASE_SYNC();
-  // ---- RT4: dV' S^T -> [0,128), V' dS^T -> [128,256), dP = dO V'^T -> [384,448)
+  // ---- R4: dV' S^T -> [0,128), V' dS^T -> [128,256), X_v = T^T dV' -> [256,384),
+  //      dP = dO V'^T -> [384,448), K K^T -> [448,512)
   if (tid == 0) {
     for (int ks = 0; ks < 8; ++ks) {
       const uint32_t at = ks >> 2, kk = ks & 3;
@@ -307,13 +309,21 @@ __global__ void __launch_bounds__(FT, 1)
                sdesc(base + G_DS + at * 16384 + kk * 32, 16, 1024), id128kk, ks > 0);
       mma_bf16(tmem + 384, sdesc(base + G_DO + at * 8192 + kk * 32, 16, 1024),
                sdesc(base + G_VP + at * 8192 + kk * 32, 16, 1024), id64, ks > 0);
+      mma_bf16(tmem + 448, sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024), id64, ks > 0);
     }
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem + 256, sdesc(base + G_TP + ks * 2048, 8192, 1024),
+               sdesc(base + G_DV + ks * 2048, 8192, 1024), id128mn, ks > 0);
     mma_commit(bar_mma);
   }
   if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
   ph ^= 1;
   tc_fence_after();
   {
+    const int i = ri;
+    const int64_t t = t0 + i;
+    const bool valid = t < L;
     float x[64];
     tmem_ld64(tmem + lane_off + half * 64, x);   // dV' S^T = -dW
     if (own) {
@@ -324,7 +334,6 @@ __global__ void __launch_bounds__(FT, 1)
     }
     tmem_ld64(tmem + lane_off + 128 + half * 64, x);  // dKt = V' dS^T
     if (own) {
-      const int i = ri;
       const float kt = sKt[i];
       float part = 0.f;
 #pragma unroll
@@ -338,53 +347,7 @@ __global__ void __launch_bounds__(FT, 1)
 #pragma unroll
       for (int j = 0; j < 64; ++j) dk[j] = kt * x[j];
     }
-    float dp[32];
-    tmem_ld32(tmem + lane_off + 384 + half * 32, dp);
-    if (own) {
-      const int i = ri;
-      float pv[32];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) ld_chunk(sm + G_P, kmaj_chunk(i, half * 4 + cc), &pv[cc * 8]);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = half * 32 + cc * 8 + e;
-          const float dpv = (j <= i) ? dp[cc * 8 + e] : 0.f;
-          sZ[i * 65 + j] = dpv * pv[cc * 8 + e];                   // dP o P
-          y[e] = (j <= i) ? dpv * dexp_(sG[i], sG[j]) : 0.f;       // dP o Gamma
-        }
-        st_chunk(sm + G_VP, kmaj_chunk(i, half * 4 + cc), y);     // over V' (consumed)
-      }
-    }
-  }
-  PHASE_SYNC();
-  if (tid < 64) {  // gate terms of P: sum_j Z_ij - sum_j Z_ji
-    float acc = 0.f;
-    for (int j = 0; j < 64; ++j) acc += sZ[tid * 65 + j] - sZ[j * 65 + tid];
-    sDG[tid] += acc;
-  }
-  // ---- RT5: T^T dV' -> [0,128), T^T dW -> [128,256), (dP o Gamma) K -> [256,384)
-  if (tid == 0) {
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint64_t at = sdesc(base + G_TP + ks * 2048, 8192, 1024);
-      mma_bf16(tmem, at, sdesc(base + G_DV + ks * 2048, 8192, 1024), id128mn, ks > 0);
-      mma_bf16(tmem + 128, at, sdesc(base + G_DW + ks * 2048, 8192, 1024), id128mn, ks > 0);
-      mma_bf16(tmem + 256, sdesc(base + G_VP + ks * 32, 16, 1024),
-               sdesc(base + G_K + ks * 2048, 8192, 1024), id128kn, ks > 0);
-    }
-    mma_commit(bar_mma);
-  }
-  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
-  ph ^= 1;
-  tc_fence_after();
-  {
-    const int i = ri;
-    const int64_t t = t0 + i;
-    const bool valid = t < L;
-    float x[64];
-    tmem_ld64(tmem + lane_off + half * 64, x);    // X_v
+    tmem_ld64(tmem + lane_off + 256 + half * 64, x);    // X_v
     if (own) {
       const float be = sBeta[i];
       float part = 0.f;
@@ -404,16 +367,61 @@ __global__ void __launch_bounds__(FT, 1)
           float y[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) y[e] = valid ? be * x[cc * 8 + e] : 0.f;
-          uint4 pk;
-          pk.x = pack_bf16(y[0], y[1]);
-          pk.y = pack_bf16(y[2], y[3]);
-          pk.z = pack_bf16(y[4], y[5]);
-          pk.w = pack_bf16(y[6], y[7]);
-          dst[cc] = pk;
+          dst[cc] = pack8g(y);
         }
       }
     }
-    tmem_ld64(tmem + lane_off + 128 + half * 64, x);  // X_w
+    float dp[32];
+    tmem_ld32(tmem + lane_off + 384 + half * 32, dp);
+    if (own) {
+      float pv[32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) ld_chunk(sm + G_P, kmaj_chunk(i, half * 4 + cc), &pv[cc * 8]);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = half * 32 + cc * 8 + e;
+          const float dpv = (j <= i) ? dp[cc * 8 + e] : 0.f;
+          sZ[i * 65 + j] = dpv * pv[cc * 8 + e];                   // dP o P
+          y[e] = (j <= i) ? dpv * dexp_(sG[i], sG[j]) : 0.f;       // dP o Gamma
+        }
+        st_chunk(sm + G_W, kmaj_chunk(i, half * 4 + cc), y);      // over W (consumed)
+      }
+    }
+  }
+  PHASE_SYNC();
+  if (tid < 64) {  // gate terms of P: sum_j Z_ij - sum_j Z_ji
+    float acc = 0.f;
+    for (int j = 0; j < 64; ++j) acc += sZ[tid * 65 + j] - sZ[j * 65 + tid];
+    sDG[tid] += acc;
+  }
+  // ---- R5: X_w = T^T dW -> [0,128), (dP o Gamma) K -> [128,256),
+  //      dA' = X_v V'^T -> [256,320) (= X_v U^T + X_w W^T, since W S = U - V')
+  if (tid == 0) {
+    for (int ks = 0; ks < 4; ++ks) {
+      mma_bf16(tmem, sdesc(base + G_TP + ks * 2048, 8192, 1024),
+               sdesc(base + G_DW + ks * 2048, 8192, 1024), id128mn, ks > 0);
+      mma_bf16(tmem + 128, sdesc(base + G_W + ks * 32, 16, 1024),
+               sdesc(base + G_K + ks * 2048, 8192, 1024), id128kn, ks > 0);
+    }
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t at = ks >> 2, kk = ks & 3;
+      mma_bf16(tmem + 256, sdesc(base + G_DS + at * 8192 + kk * 32, 16, 1024),
+               sdesc(base + G_VP + at * 8192 + kk * 32, 16, 1024), id64, ks > 0);
+    }
+    mma_commit(bar_mma);
+  }
+  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
+  ph ^= 1;
+  tc_fence_after();
+  {
+    const int i = ri;
+    const int64_t t = t0 + i;
+    const bool valid = t < L;
+    float x[64];
+    tmem_ld64(tmem + lane_off + half * 64, x);  // X_w
     if (own) {
       const float be = sBeta[i], gm = sGam[i];
       float part = 0.f;
@@ -423,14 +431,13 @@ __global__ void __launch_bounds__(FT, 1)
         ld_chunk(sm + G_K + half * 8192, kmaj_chunk(i, cc), kx);
 #pragma unroll
         for (int e = 0; e < 8; ++e) part = fmaf(x[cc * 8 + e], kx[e], part);
-        st_chunk(sm + G_DS + 16384 + half * 8192, kmaj_chunk(i, cc), &x[cc * 8]);  // X_w
       }
       dbacc += gm * part;
       dGacc += be * gm * part;
 #pragma unroll
       for (int j = 0; j < 64; ++j) dk[j] = fmaf(be * gm, x[j], dk[j]);
     }
-    tmem_ld64(tmem + lane_off + 256 + half * 64, x);  // (dP o Gamma) K
+    tmem_ld64(tmem + lane_off + 128 + half * 64, x);  // (dP o Gamma) K
     if (own && t < ar.Tp) {
       uint4* dst = reinterpret_cast<uint4*>(ar.dqp + ((b * ar.Tp + t) * ar.H + h) * 128 + half * 64);
 #pragma unroll
@@ -441,33 +448,10 @@ __global__ void __launch_bounds__(FT, 1)
         dst[j >> 3] = pack8g(y);
       }
     }
-  }
-  PHASE_SYNC();
-  // ---- RT6: dA' = X_v U^T + X_w W^T -> [0,64), K K^T -> [64,128)
-  if (tid == 0) {
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t at = ks >> 2, kk = ks & 3;
-      mma_bf16(tmem, sdesc(base + G_DS + at * 8192 + kk * 32, 16, 1024),
-               sdesc(base + G_TU + at * 8192 + kk * 32, 16, 1024), id64, ks > 0);
-    }
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t at = ks >> 2, kk = ks & 3;
-      mma_bf16(tmem, sdesc(base + G_DS + 16384 + at * 8192 + kk * 32, 16, 1024),
-               sdesc(base + G_W + at * 8192 + kk * 32, 16, 1024), id64, 1);
-      mma_bf16(tmem + 64, sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024),
-               sdesc(base + G_K + at * 8192 + kk * 32, 16, 1024), id64, ks > 0);
-    }
-    mma_commit(bar_mma);
-  }
-  if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
-  ph ^= 1;
-  tc_fence_after();
-  {
     float da[32], kk[32];
-    tmem_ld32(tmem + lane_off + half * 32, da);
-    tmem_ld32(tmem + lane_off + 64 + half * 32, kk);
+    tmem_ld32(tmem + lane_off + 256 + half * 32, da);
+    tmem_ld32(tmem + lane_off + 448 + half * 32, kk);
     if (own) {
-      const int i = ri;
       const float be = sBeta[i];
       float part = 0.f;
 #pragma unroll
@@ -494,10 +478,10 @@ __global__ void __launch_bounds__(FT, 1)
     for (int j = 0; j < 64; ++j) acc += sZ[tid * 65 + j] - sZ[j * 65 + tid];
     sDG[tid] += acc;
   }
-  // ---- RT7: dk += (dP o Gamma)^T Q + E K + E^T K -> [0,128)
+  // ---- R6: dk += (dP o Gamma)^T Q + E K + E^T K -> [0,128)
   if (tid == 0) {
     for (int ks = 0; ks < 4; ++ks)
-      mma_bf16(tmem, sdesc(base + G_VP + ks * 2048, 8192, 1024),
+      mma_bf16(tmem, sdesc(base + G_W + ks * 2048, 8192, 1024),
                sdesc(base + G_Q + ks * 2048, 8192, 1024), id128mn, ks > 0);
     for (int ks = 0; ks < 4; ++ks)
       mma_bf16(tmem, sdesc(base + G_P + ks * 32, 16, 1024),
