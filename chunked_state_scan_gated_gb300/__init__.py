@@ -8,7 +8,7 @@ CPU fallback.
 The functions keep the C names (``gdn_fwd``, ``gdn_bwd``, ``gdn_summary``,
 ``gdn_summary_bwd``, ``gdn_compose``, ``gdn_prefix_compose``,
 ``gdn_prefix_compose_bwd``, ``gdn_apply_state``, ``gdn_apply_state_bwd``,
-``gdn_query_support``, ``gdn_resolved_segments``, ``gdn_workspace_size``,
+``gdn_gate_param_bwd``, ``gdn_query_support``, ``gdn_resolved_segments``, ``gdn_workspace_size``,
 ``gdn_check_device_status``) and
 take torch tensors in the token-major layouts of the header: q, k
 [B,T,Hqk,dk]; v [B,T,H,dv]; a, b [B,T,H]; A_log, dt_bias [H] fp32; states
@@ -33,7 +33,7 @@ GDN_OP_FWD, GDN_OP_BWD, GDN_OP_SUMMARY, GDN_OP_SUMMARY_BWD = range(4)
 # Every symbol include/gdn.h declares (checked by the CPU test suite).
 EXPORTS = (
     "gdn_status_string", "gdn_abi_version", "gdn_problem_init", "gdn_query_support",
-    "gdn_resolved_segments", "gdn_workspace_size", "gdn_fwd", "gdn_bwd", "gdn_summary", "gdn_summary_bwd",
+    "gdn_resolved_segments", "gdn_workspace_size", "gdn_fwd", "gdn_bwd", "gdn_gate_param_bwd", "gdn_summary", "gdn_summary_bwd",
     "gdn_compose", "gdn_prefix_compose", "gdn_prefix_compose_bwd", "gdn_apply_state",
     "gdn_apply_state_bwd", "gdn_check_device_status", "gdn_kernel_info", "gdn_fwd_kernel",
     "gdn_bwd_kernel", "gdn_fwd_noalloc",
@@ -84,6 +84,7 @@ def load_library(path: str | None = None):
                                    ctypes.c_int),
             "gdn_resolved_segments": ([_PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
                                       ctypes.c_int),
+            "gdn_gate_param_bwd": ([_PP] + [_VP] * 11 + [_VP], ctypes.c_int),
             "gdn_fwd": ([_PP] + [_VP] * 12 + [ctypes.c_size_t, _VP], ctypes.c_int),
             "gdn_apply_state": ([_PP] + [_VP] * 12 + [ctypes.c_size_t, _VP], ctypes.c_int),
             "gdn_bwd": ([_PP] + [_VP] * 18 + [ctypes.c_size_t, _VP], ctypes.c_int),
@@ -289,6 +290,28 @@ def gdn_apply_state_bwd(q, k, v, a, b, A_log, dt_bias, Hin, dO, dHout=None, vali
         raise ValueError("gdn_apply_state_bwd needs Hin")
     return _bwd_common("gdn_apply_state_bwd", q, k, v, a, b, A_log, dt_bias, Hin, valid_len, dO,
                        dHout, True, kw)
+
+
+def gdn_gate_param_bwd(a, b, A_log, dt_bias, dg, dbeta, valid_len=None, *, da=None, db=None,
+                       dA_log=None, ddt_bias=None, stream=None, problem=None):
+    """Gate-parameter gradients from dg, dbeta: (da, db [B,T,H] fp32, dA_log, ddt_bias [H] fp32)."""
+    B, T, H = a.shape
+    if problem is None:
+        d = 128 if a.dtype == torch.bfloat16 else 16
+        problem = Problem()
+        load_library().gdn_problem_init(ctypes.byref(problem))
+        problem.dtype = _dtype_code(a.dtype)
+        problem.B, problem.T, problem.Hqk, problem.H, problem.dk, problem.dv = B, T, H, H, d, d
+    f32 = dict(dtype=torch.float32, device=a.device)
+    da = da if da is not None else torch.empty((B, T, H), **f32)
+    db = db if db is not None else torch.empty((B, T, H), **f32)
+    dA_log = dA_log if dA_log is not None else torch.empty((H,), **f32)
+    ddt_bias = ddt_bias if ddt_bias is not None else torch.empty((H,), **f32)
+    _check("gdn_gate_param_bwd", load_library().gdn_gate_param_bwd(
+        ctypes.byref(problem), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(valid_len),
+        _ptr(dg), _ptr(dbeta), _ptr(da), _ptr(db), _ptr(dA_log), _ptr(ddt_bias),
+        _stream(stream)))
+    return da, db, dA_log, ddt_bias
 
 
 def gdn_summary(k, v, a, b, A_log, dt_bias, valid_len=None, *, l2norm=True, eps=1e-6, M=None,

@@ -569,6 +569,22 @@ gdn_status gdn_apply_state_bwd(const gdn_problem* p, const void* q, const void* 
                  dbeta, dHin, workspace, workspace_bytes, stream);
 }
 
+gdn_status gdn_gate_param_bwd(const gdn_problem* p, const void* a, const void* b,
+                              const float* A_log, const float* dt_bias, const int32_t* valid_len,
+                              const float* dg, const float* dbeta, float* da, float* db,
+                              float* dA_log, float* ddt_bias, void* stream) {
+  Prob pr;
+  gdn_status s = resolve_op(p, GDN_OP_BWD, &pr);
+  if (s != GDN_OK) return s;
+  const int64_t ng = pr.B * pr.T * pr.H;
+  if (!ok_ptr(a, ng) || !ok_ptr(b, ng) || !ok_ptr(dg, ng) || !ok_ptr(dbeta, ng) ||
+      !ok_ptr(da, ng) || !ok_ptr(db, ng) || !ok_ptr(A_log, pr.H) || !ok_ptr(dt_bias, pr.H) ||
+      !ok_ptr(dA_log, pr.H) || !ok_ptr(ddt_bias, pr.H) || !ok_opt(valid_len))
+    return GDN_ERR_INVALID_ARG;
+  return cuda_status(launch_gate_param_bwd(pr, a, b, A_log, dt_bias, valid_len, dg, dbeta, da, db,
+                                           dA_log, ddt_bias, (cudaStream_t)stream));
+}
+
 gdn_status gdn_summary(const gdn_problem* p, const void* k, const void* v, const void* a,
                        const void* b, const float* A_log, const float* dt_bias,
                        const int32_t* valid_len, float* M, float* S, void* workspace,

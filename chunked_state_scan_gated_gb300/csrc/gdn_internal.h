@@ -101,6 +101,13 @@ cudaError_t launch_prefix_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, cons
                               const float* D, const float* dHT, float* dHout, float* dH0,
                               cudaStream_t st);
 
+// gate-parameter gradients from dg, dbeta (both dtypes; one CTA per head, fixed-order sums)
+cudaError_t launch_gate_param_bwd(const Prob& pr, const void* a, const void* b,
+                                  const float* A_log, const float* dt_bias,
+                                  const int32_t* valid_len, const float* dg, const float* dbeta,
+                                  float* da, float* db, float* dA_log, float* ddt_bias,
+                                  cudaStream_t st);
+
 // ---- tensor-core (tcgen05) kernels, bf16 with dk = dv = 128 ----
 bool tc_path(const Prob& pr);
 // chunk-parallel prologue: norm factors, gates and the W, U, P (and T) tile images

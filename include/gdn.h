@@ -155,6 +155,20 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Gradients of the gate parameters from the core's dg, dbeta [B,T,H] fp32 (as
+ * returned by gdn_bwd).  The gates are g = -exp(A_log[h]) softplus(a + dt_bias[h])
+ * and beta = sigmoid(b) (the test report, section 4.1, checks every parameter
+ * gradient).  Writes da, db [B,T,H] fp32 (w.r.t. the a, b given to gdn_fwd;
+ * zero for padded tokens) and dA_log, ddt_bias [H] fp32 (sums over all rows and
+ * valid tokens, in a fixed order: deterministic).  a, b in p->dtype.  No
+ * workspace; one launch.
+ */
+gdn_status gdn_gate_param_bwd(const gdn_problem* p, const void* a, const void* b,
+                              const float* A_log, const float* dt_bias, const int32_t* valid_len,
+                              const float* dg, const float* dbeta, float* da, float* db,
+                              float* dA_log, float* ddt_bias, void* stream);
+
+/*
  * Segment summary (PR #1035, "p2p": H_out = M @ H_in + S for the local
  * segment).  The segment is tokens [0, T) of the given rows (pass pointers to
  * the segment's first token and T_stride = the full row length).

@@ -127,6 +127,60 @@ BF16_SMALL = [
 ]
 
 
+PARAM_CASES = [  # name, dtype, B, T, H, valid_len
+    ("fp32", torch.float32, 1, 130, 3, None),
+    ("bf16_padded", torch.bfloat16, 2, 300, 4, [300, 97]),
+    ("bf16_32k", torch.bfloat16, 1, 32768, 32, None),
+]
+
+
+@pytest.mark.parametrize("case", PARAM_CASES, ids=[c[0] for c in PARAM_CASES])
+def test_gate_param_grads_match_oracle(case):
+    """gdn_gate_param_bwd on given dg, dbeta (seeded, fp32) against the oracle's chain:
+    both sides read the same values, the kernel computes in fp32 (fp32 tolerance)."""
+    name, dtype, B, T, H, vl = case
+    gen = torch.Generator().manual_seed(41)
+    a = torch.randn(B, T, H, generator=gen).to(dtype)
+    b = torch.randn(B, T, H, generator=gen).to(dtype)
+    A_log = torch.log(torch.rand(H, generator=gen) * 15 + 1)
+    dt_bias = torch.randn(H, generator=gen)
+    dg = torch.randn(B, T, H, generator=gen)
+    dbeta = torch.randn(B, T, H, generator=gen)
+    vlt = None if vl is None else torch.tensor(vl, dtype=torch.int32)
+    got = gdn.gdn_gate_param_bwd(a.cuda(), b.cuda(), A_log.cuda(), dt_bias.cuda(), dg.cuda(),
+                                 dbeta.cuda(), None if vlt is None else vlt.cuda())
+    torch.cuda.synchronize()
+    ref = oracle.gate_param_bwd(to64(a), to64(b), to64(A_log), to64(dt_bias), to64(dg),
+                                to64(dbeta), None if vl is None else np.array(vl, np.int32))
+    for nm, g, r in zip(("da", "db", "dA_log", "ddt_bias"), got, ref):
+        assert_close(nm, g, r, torch.float32)
+    if vl is not None:
+        for bi, Lb in enumerate(vl):
+            assert (got[0][bi, Lb:] == 0).all() and (got[1][bi, Lb:] == 0).all()
+    again = gdn.gdn_gate_param_bwd(a.cuda(), b.cuda(), A_log.cuda(), dt_bias.cuda(), dg.cuda(),
+                                   dbeta.cuda(), None if vlt is None else vlt.cuda())
+    for x, y in zip(got, again):  # fixed-order sums: bitwise repeatable
+        assert torch.equal(x, y)
+
+
+def test_gate_param_grads_end_to_end_bf16():
+    """gdn_bwd -> gdn_gate_param_bwd against oracle.bwd -> oracle.gate_param_bwd."""
+    w = gi.Workload("params_e2e", B=2, T=300, Hqk=1, H=2, dk=128, dv=128,
+                    dtype=torch.bfloat16, h0_std=0.1, with_dHT=True, valid_len=[300, 150],
+                    decay_stress=True, seed=23)
+    inp = gi.make_inputs(w)
+    d, n = dev(inp), np64(inp)
+    grads = gpu_bwd(d)
+    got = gdn.gdn_gate_param_bwd(d["a"], d["b"], d["A_log"], d["dt_bias"], grads[3], grads[4],
+                                 d["valid_len"])
+    torch.cuda.synchronize()
+    rg = oracle_bwd(n)
+    ref = oracle.gate_param_bwd(n["a"], n["b"], n["A_log"], n["dt_bias"], rg[3], rg[4],
+                                n["valid_len"])
+    for nm, g, r in zip(("da", "db", "dA_log", "ddt_bias"), got, ref):
+        assert_close(nm, g, r, torch.bfloat16)
+
+
 @pytest.mark.parametrize("case", BF16_SMALL, ids=[c[0] for c in BF16_SMALL])
 def test_bf16_small_fwd_bwd_matches_oracle(case):
     name, B, T, Hqk, H, seg, h0s, vl, stress = case
