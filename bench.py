@@ -121,6 +121,15 @@ def kernel_work(name, w, P):
         f = 2 * (mm(C, dv, dk) + mm(dk, dv, C)) * ch * frac   # [M | S] parts
         byt = ch * frac * (3 * tile + C * 8) + 2 * (P - 1) * B * H * state
         return f, byt
+    if kname == "summary_pair_tc":   # [M | S] of every segment + gradient summaries
+        f1 = 2 * (mm(C, dv, dk) + mm(dk, dv, C)) * ch
+        b1 = ch * (3 * tile + C * 8) + 2 * P * B * H * state
+        f2, b2 = kernel_work("bwd.grad_summary_chain_tc", w, P)
+        return f1 + f2, b1 + b2
+    if kname == "states_pair_tc":    # chunk-start states + chunk-end state gradients
+        f1, b1 = kernel_work("bwd.states_chain_tc", w, P)
+        f2, b2 = kernel_work("bwd.dstate_chain_tc", w, P)
+        return f1 + f2, b1 + b2
     if kname == "apply_chain_tc":
         f = (2 * mm(C, dv, dk) + mm(dk, dv, C) + mm(C, dv, C)) * ch
         byt = ch * (5 * tile + tile_p + C * 12) + B * H * state * (1 + (1 if P > 1 or w.h0_std else 0))
@@ -142,6 +151,8 @@ def kernel_work(name, w, P):
         return 0.0, tok * (H * 2 * dk * 2 + Hqk * 2 * dk * 2 * 2)
     if kname in ("prefix", "prefix_bwd"):
         return mm(dk, dv, dk) * B * H * max(P - 1, 0), B * H * max(P - 1, 0) * 3 * state
+    if kname == "prefix_pair":
+        return 2 * mm(dk, dv, dk) * B * H * max(P - 1, 0), 2 * B * H * max(P - 1, 0) * 3 * state
     return 0.0, 0.0
 
 

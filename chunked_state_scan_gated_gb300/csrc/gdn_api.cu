@@ -318,34 +318,27 @@ gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const
     const float* init = h0;
     int64_t init_stride = 0;
     GDN_RUN(sc, "prep_tc", launch_prep_tc(pr, in, ws, st));
-    if (pr.P > 1) {
-      GDN_RUN(sc, "summary_chain_tc",
-              launch_chain_tc(pr, in, ws, 1, 0, pr.P, nullptr, 0, nullptr, nullptr, ws.Mseg,
-                              ws.Sseg, sstride, nullptr, st));
-      GDN_RUN(sc, "prefix",
-              launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Sseg, h0, ws.Hin,
-                            nullptr, st));
-      init = ws.Hin;
-      init_stride = sstride;
-    }
-    GDN_RUN(sc, "states_chain_tc",
-            launch_chain_tc(pr, in, ws, 2, 0, pr.P, init, init_stride, nullptr, nullptr, nullptr,
-                            nullptr, 0, ws.hc16, st));
     const float* dinit = dHT;
     int64_t dinit_stride = 0;
     if (pr.P > 1) {
-      GDN_RUN(sc, "grad_summary_chain_tc",
-              launch_dchain_tc(pr, in, ws, 1, 1, pr.P - 1, nullptr, 0, nullptr, nullptr, ws.Dseg,
-                               sstride, st));
-      GDN_RUN(sc, "prefix_bwd",
-              launch_prefix_bwd(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Dseg, dHT,
-                                ws.dHout, nullptr, st));
+      // forward summaries of every segment (M feeds both prefixes) with the gradient
+      // summaries of segments 1..P-1, then both prefixes in one launch
+      const ChainPass f{0, pr.P, nullptr, 0, ws.Mseg, ws.Sseg, sstride, nullptr};
+      const ReversePass r{1, pr.P - 1, nullptr, 0, nullptr, nullptr, ws.Dseg, sstride};
+      GDN_RUN(sc, "summary_pair_tc", launch_chain_pair_tc(pr, in, ws, 1, f, 1, r, st));
+      GDN_RUN(sc, "prefix_pair",
+              launch_prefix_pair(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Sseg, h0, ws.Hin,
+                                 ws.Dseg, dHT, ws.dHout, st));
+      init = ws.Hin;
+      init_stride = sstride;
       dinit = ws.dHout;
       dinit_stride = sstride;
     }
-    GDN_RUN(sc, "dstate_chain_tc",
-            launch_dchain_tc(pr, in, ws, 0, 0, pr.P, dinit, dinit_stride, ws.dhc16, dH0, nullptr,
-                             0, st));
+    {  // every chunk-start state with every chunk-end state gradient
+      const ChainPass f{0, pr.P, init, init_stride, nullptr, nullptr, 0, ws.hc16};
+      const ReversePass r{0, pr.P, dinit, dinit_stride, ws.dhc16, dH0, nullptr, 0};
+      GDN_RUN(sc, "states_pair_tc", launch_chain_pair_tc(pr, in, ws, 2, f, 0, r, st));
+    }
     GDN_RUN(sc, "grad_tc", launch_grad_tc(pr, in, ws, ws.hc16, ws.dhc16, dv, dg, dbeta, st));
     GDN_RUN(sc, "qk_grad_tc", launch_qk_grad_tc(pr, in, ws, dq, dk, st));
     return GDN_OK;

@@ -96,6 +96,10 @@ cudaError_t launch_compose(int64_t n, int64_t dk, int64_t dv, const float* M2, c
 cudaError_t launch_prefix(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
                           const float* S, const float* h0, float* Hin, float* Hout,
                           cudaStream_t st);
+// Both prefixes of the backward in one launch: Hin (forward, no Hout) and dHout (reverse, no dH0).
+cudaError_t launch_prefix_pair(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
+                               const float* S, const float* h0, float* Hin, const float* D,
+                               const float* dHT, float* dHout, cudaStream_t st);
 // dHout[s] for s >= 0 in reverse; applies M[s]^T . + D[s] only when s > 0 or dH0 != null.
 cudaError_t launch_prefix_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
                               const float* D, const float* dHT, float* dHout, float* dH0,
@@ -128,6 +132,29 @@ cudaError_t launch_dchain_tc(const Prob& pr, const Inputs& in, const WS& ws, int
                              void* dhc, float* start_out, float* D_out, int64_t out_seg_stride,
                              cudaStream_t st);
 
+// A forward chain pass (summary or states) and an independent reverse chain pass in one
+// launch (the CTAs of both share the GPU); either pass may be empty (nseg <= 0).
+struct ChainPass {
+  int seg_first, nseg;
+  const float* init;
+  int64_t init_seg_stride;
+  float* M_out;
+  float* S_out;
+  int64_t out_seg_stride;
+  void* hc;
+};
+struct ReversePass {
+  int seg_first, nseg;
+  const float* init;
+  int64_t init_seg_stride;
+  void* dhc;
+  float* start_out;
+  float* D_out;
+  int64_t out_seg_stride;
+};
+cudaError_t launch_chain_pair_tc(const Prob& pr, const Inputs& in, const WS& ws, int fmode,
+                                 const ChainPass& f, int rmode, const ReversePass& r,
+                                 cudaStream_t st);
 // dq, dk (bf16) from the per-V-head bf16 gradients of q_hat, k_hat in ws.dqp / ws.dkp
 cudaError_t launch_qk_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, void* dq, void* dk,
                               cudaStream_t st);

@@ -910,11 +910,11 @@ constexpr int PCS = 32;          // state columns per prefix block
 constexpr int PLD = 129;         // shared-memory row stride of a map
 constexpr int PMAXR = kMaxHeadDim / (NT / 32);        // map rows per warp (16)
 constexpr int PMAXC = kMaxHeadDim / 32;               // map columns per lane (4)
-__global__ void __launch_bounds__(NT, 1) k_prefix(int64_t n, int64_t P, int64_t dk, int64_t dv,
-                                                 const float* __restrict__ M,
-                                                 const float* __restrict__ S,
-                                                 const float* __restrict__ x0, float* out_seq,
-                                                 float* out_last, int transpose) {
+__device__ __forceinline__ void prefix_block(int64_t n, int64_t P, int64_t dk, int64_t dv,
+                                             const float* __restrict__ M,
+                                             const float* __restrict__ S,
+                                             const float* __restrict__ x0, float* out_seq,
+                                             float* out_last, int transpose) {
   extern __shared__ float sm[];
   float* Ms0 = sm;                               // [2][dk][PLD]
   float* Xs = sm + 2 * kMaxHeadDim * PLD;        // [dk][PCS]
@@ -1004,6 +1004,29 @@ __global__ void __launch_bounds__(NT, 1) k_prefix(int64_t n, int64_t P, int64_t 
         if (i < ndk && col < dv) out_last[(e0 * dk + i) * dv + col] = x[r][c];
       }
   }
+}
+
+__global__ void __launch_bounds__(NT, 1) k_prefix(int64_t n, int64_t P, int64_t dk, int64_t dv,
+                                                 const float* __restrict__ M,
+                                                 const float* __restrict__ S,
+                                                 const float* __restrict__ x0, float* out_seq,
+                                                 float* out_last, int transpose) {
+  prefix_block(n, P, dk, dv, M, S, x0, out_seq, out_last, transpose);
+}
+
+// The forward prefix (blockIdx.z = 0: H_in from M, S, h0) and the reverse prefix
+// (blockIdx.z = 1: dH_out from M^T, D, dHT) of the backward in one launch.
+__global__ void __launch_bounds__(NT, 1) k_prefix_pair(int64_t n, int64_t P, int64_t dk,
+                                                      int64_t dv, const float* __restrict__ M,
+                                                      const float* __restrict__ S,
+                                                      const float* __restrict__ h0, float* Hin,
+                                                      const float* __restrict__ D,
+                                                      const float* __restrict__ dHT,
+                                                      float* dHout) {
+  if (blockIdx.z == 0)
+    prefix_block(n, P, dk, dv, M, S, h0, Hin, nullptr, 0);
+  else
+    prefix_block(n, P, dk, dv, M, D, dHT, dHout, nullptr, 1);
 }
 
 template <typename K>
@@ -1175,6 +1198,18 @@ cudaError_t launch_prefix_bwd(int64_t n, int64_t P, int64_t dk, int64_t dv, cons
   cudaError_t e;
   if ((e = set_smem(k_prefix, smem)) != cudaSuccess) return e;
   k_prefix<<<grid, NT, smem, st>>>(n, P, dk, dv, M, D, dHT, dHout, dH0, 1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefix_pair(int64_t n, int64_t P, int64_t dk, int64_t dv, const float* M,
+                               const float* S, const float* h0, float* Hin, const float* D,
+                               const float* dHT, float* dHout, cudaStream_t st) {
+  if (n == 0 || P == 0) return cudaSuccess;
+  const size_t smem = sizeof(float) * (size_t)(2 * kMaxHeadDim * PLD + kMaxHeadDim * PCS);
+  dim3 grid((unsigned)n, (unsigned)((dv + PCS - 1) / PCS), 2);
+  cudaError_t e;
+  if ((e = set_smem(k_prefix_pair, smem)) != cudaSuccess) return e;
+  k_prefix_pair<<<grid, NT, smem, st>>>(n, P, dk, dv, M, S, h0, Hin, D, dHT, dHout);
   return cudaGetLastError();
 }
 

@@ -359,10 +359,11 @@ struct ChainArgs {
     if (*s_abort) goto done;    \
   } while (0)
 
+// One CTA of the chain: `part` (summary: 0 = S, 1 = M), head h, zi = row * nseg + segment.
 template <int MODE>
-__global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
-    k_chain_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-               const __grid_constant__ CUtensorMap mo, ChainArgs ar) {
+__device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorMap& mk,
+                                          const CUtensorMap& mo, const ChainArgs& ar, int part,
+                                          int64_t h, int64_t zi) {
   constexpr bool kApply = MODE == CH_APPLY;
   constexpr uint32_t XSTR = kApply ? 24576 : 16384;  // atom stride in the [W | (Q) | K] block
   constexpr uint32_t KOFF = kApply ? 16384 : 8192;   // K's offset inside an atom
@@ -383,11 +384,10 @@ __global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
   const int row = quad * 32 + lane;
-  const bool mpart = MODE == CH_SUM && blockIdx.x == 1;
+  const bool mpart = MODE == CH_SUM && part == 1;
   const bool needU = !mpart;
-  const int64_t h = blockIdx.y;
-  const int64_t b = blockIdx.z / ar.nseg;
-  const int seg = ar.seg_first + (int)(blockIdx.z % ar.nseg);
+  const int64_t b = zi / ar.nseg;
+  const int seg = ar.seg_first + (int)(zi % ar.nseg);
   const int64_t hq = h / ar.r, bh = b * ar.H + h;
   const int64_t cs = (int64_t)seg * ar.CPS;
   const int64_t ce = cs + ar.CPS < ar.NC ? cs + ar.CPS : ar.NC;
@@ -745,9 +745,10 @@ struct DchainArgs {
   int mode, seg_first, nseg;
 };
 
-__global__ void __launch_bounds__(CT, 2)
-    k_dchain_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                const __grid_constant__ CUtensorMap mdo, DchainArgs ar) {
+// One CTA of the reverse chain: head h, zi = row * nseg + segment.
+__device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensorMap& mk,
+                                           const CUtensorMap& mdo, const DchainArgs& ar,
+                                           int64_t h, int64_t zi) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t base = smem_u32(sm);
@@ -763,9 +764,8 @@ __global__ void __launch_bounds__(CT, 2)
   const int quad = warp & 3, half = warp >> 2;
   const int row = quad * 32 + lane;
   const bool store = ar.mode == 0;
-  const int64_t h = blockIdx.y;
-  const int64_t b = blockIdx.z / ar.nseg;
-  const int seg = ar.seg_first + (int)(blockIdx.z % ar.nseg);
+  const int64_t b = zi / ar.nseg;
+  const int seg = ar.seg_first + (int)(zi % ar.nseg);
   const int64_t hq = h / ar.r, bh = b * ar.H + h;
   const int64_t cs = (int64_t)seg * ar.CPS;
   const int64_t ce = cs + ar.CPS < ar.NC ? cs + ar.CPS : ar.NC;
@@ -966,6 +966,34 @@ done:
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+template <int MODE>
+__global__ void __launch_bounds__(CT, MODE == CH_APPLY ? 1 : 2)
+    k_chain_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mo, ChainArgs ar) {
+  chain_cta<MODE>(mq, mk, mo, ar, (int)blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+__global__ void __launch_bounds__(CT, 2)
+    k_dchain_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                const __grid_constant__ CUtensorMap mdo, DchainArgs ar) {
+  dchain_cta(mq, mk, mdo, ar, blockIdx.y, blockIdx.z);
+}
+
+// A forward chain pass and an independent reverse chain pass in one launch, so that
+// the CTAs of both fill the GPU together: z in [0, nf) runs the forward chain (with
+// `parts` parts per segment folded into z), z in [nf, nf + nr) the reverse chain.
+template <int MODE>
+__global__ void __launch_bounds__(CT, 2)
+    k_chain_pair_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mdo,
+                    ChainArgs fa, DchainArgs ra, int parts, int64_t nf) {
+  const int64_t z = blockIdx.z;
+  if (z < nf)
+    chain_cta<MODE>(mq, mk, mo, fa, (int)(z % parts), blockIdx.y, z / parts);
+  else
+    dchain_cta(mq, mk, mdo, ra, blockIdx.y, z - nf);
+}
+
 template <typename K>
 cudaError_t smem_attr(K kern, uint32_t bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -998,35 +1026,72 @@ cudaError_t launch_prep_tc(const Prob& pr, const Inputs& in, const WS& ws, cudaS
   return cudaGetLastError();
 }
 
+namespace {
+
+// Tensor maps and arguments of a forward chain pass.
+bool chain_setup(const Prob& pr, const Inputs& in, const WS& ws, int seg_first, int nseg,
+                 const float* init, int64_t init_seg_stride, void* o, float* final_out,
+                 float* M_out, float* S_out, int64_t out_seg_stride, void* hc, CUtensorMap* mq,
+                 CUtensorMap* mk, CUtensorMap* mo, ChainArgs* ar) {
+  memset(mq, 0, sizeof(*mq));
+  memset(mk, 0, sizeof(*mk));
+  memset(mo, 0, sizeof(*mo));
+  const void* qptr = in.q ? in.q : in.k;  // summaries and states never read q
+  const void* optr = o ? o : in.k;        // only apply writes o
+  if (!tc_make_map(mq, qptr, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(mo, optr, pr.B, pr.T, pr.Ts, o ? pr.H : pr.Hqk))
+    return false;
+  ar->T = pr.T; ar->Ts = pr.Ts; ar->H = pr.H; ar->Hqk = pr.Hqk; ar->r = pr.r; ar->NC = pr.NC;
+  ar->CPS = pr.CPS; ar->P = pr.P;
+  ar->rqk = ws.rqk;
+  ar->wim = (const uint8_t*)ws.wim; ar->uim = (const uint8_t*)ws.uim;
+  ar->pim = (const uint8_t*)ws.pim; ar->gl = ws.gl;
+  ar->valid_len = in.valid_len;
+  ar->init = init; ar->init_seg_stride = init_seg_stride;
+  ar->o = (__nv_bfloat16*)o; ar->final_out = final_out;
+  ar->M_out = M_out; ar->S_out = S_out; ar->out_seg_stride = out_seg_stride;
+  ar->hc = (uint8_t*)hc;
+  ar->status = ws.status;
+  ar->seg_first = seg_first; ar->nseg = nseg;
+  return true;
+}
+
+// Tensor maps and arguments of a reverse chain pass.
+bool dchain_setup(const Prob& pr, const Inputs& in, const WS& ws, int mode, int seg_first,
+                  int nseg, const float* init, int64_t init_seg_stride, void* dhc,
+                  float* start_out, float* D_out, int64_t out_seg_stride, CUtensorMap* mq,
+                  CUtensorMap* mk, CUtensorMap* mdo, DchainArgs* ar) {
+  memset(mq, 0, sizeof(*mq));
+  memset(mk, 0, sizeof(*mk));
+  memset(mdo, 0, sizeof(*mdo));
+  if (!tc_make_map(mq, in.q, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(mdo, in.dO, pr.B, pr.T, pr.Ts, pr.H))
+    return false;
+  ar->T = pr.T; ar->Ts = pr.Ts; ar->H = pr.H; ar->Hqk = pr.Hqk; ar->r = pr.r; ar->NC = pr.NC;
+  ar->CPS = pr.CPS;
+  ar->rqk = ws.rqk; ar->wim = (const uint8_t*)ws.wim; ar->pim = (const uint8_t*)ws.pim;
+  ar->gl = ws.gl; ar->valid_len = in.valid_len;
+  ar->init = init; ar->init_seg_stride = init_seg_stride;
+  ar->dhc = (uint8_t*)dhc; ar->start_out = start_out; ar->D_out = D_out;
+  ar->out_seg_stride = out_seg_stride; ar->status = ws.status;
+  ar->mode = mode; ar->seg_first = seg_first; ar->nseg = nseg;
+  return true;
+}
+
+}  // namespace
+
 cudaError_t launch_chain_tc(const Prob& pr, const Inputs& in, const WS& ws, int mode,
                             int seg_first, int nseg, const float* init, int64_t init_seg_stride,
                             void* o, float* final_out, float* M_out, float* S_out,
                             int64_t out_seg_stride, void* hc, cudaStream_t st) {
   if (nseg <= 0 || pr.B == 0 || pr.NC == 0) return cudaSuccess;
-  CUtensorMap mq, mk;
-  memset(&mq, 0, sizeof(mq));
-  memset(&mk, 0, sizeof(mk));
-  CUtensorMap mo;
-  memset(&mo, 0, sizeof(mo));
-  const void* qptr = in.q ? in.q : in.k;  // summaries and states never read q
-  const void* optr = o ? o : in.k;        // only apply writes o
-  if (!tc_make_map(&mq, qptr, pr.B, pr.T, pr.Ts, pr.Hqk) ||
-      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
-      !tc_make_map(&mo, optr, pr.B, pr.T, pr.Ts, o ? pr.H : pr.Hqk))
-    return cudaErrorInvalidValue;
+  CUtensorMap mq, mk, mo;
   ChainArgs ar;
-  ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.Hqk = pr.Hqk; ar.r = pr.r; ar.NC = pr.NC;
-  ar.CPS = pr.CPS; ar.P = pr.P;
-  ar.rqk = ws.rqk;
-  ar.wim = (const uint8_t*)ws.wim; ar.uim = (const uint8_t*)ws.uim;
-  ar.pim = (const uint8_t*)ws.pim; ar.gl = ws.gl;
-  ar.valid_len = in.valid_len;
-  ar.init = init; ar.init_seg_stride = init_seg_stride;
-  ar.o = (__nv_bfloat16*)o; ar.final_out = final_out;
-  ar.M_out = M_out; ar.S_out = S_out; ar.out_seg_stride = out_seg_stride;
-  ar.hc = (uint8_t*)hc;
-  ar.status = ws.status;
-  ar.seg_first = seg_first; ar.nseg = nseg;
+  if (!chain_setup(pr, in, ws, seg_first, nseg, init, init_seg_stride, o, final_out, M_out, S_out,
+                   out_seg_stride, hc, &mq, &mk, &mo, &ar))
+    return cudaErrorInvalidValue;
   cudaError_t e;
   dim3 grid(mode == CH_SUM ? 2 : 1, (unsigned)pr.H, (unsigned)(pr.B * nseg));
   if (mode == CH_APPLY) {
@@ -1048,26 +1113,47 @@ cudaError_t launch_dchain_tc(const Prob& pr, const Inputs& in, const WS& ws, int
                              cudaStream_t st) {
   if (nseg <= 0 || pr.B == 0 || pr.NC == 0) return cudaSuccess;
   CUtensorMap mq, mk, mdo;
-  memset(&mq, 0, sizeof(mq));
-  memset(&mk, 0, sizeof(mk));
-  memset(&mdo, 0, sizeof(mdo));
-  if (!tc_make_map(&mq, in.q, pr.B, pr.T, pr.Ts, pr.Hqk) ||
-      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
-      !tc_make_map(&mdo, in.dO, pr.B, pr.T, pr.Ts, pr.H))
-    return cudaErrorInvalidValue;
   DchainArgs ar;
-  ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.Hqk = pr.Hqk; ar.r = pr.r; ar.NC = pr.NC;
-  ar.CPS = pr.CPS;
-  ar.rqk = ws.rqk; ar.wim = (const uint8_t*)ws.wim; ar.pim = (const uint8_t*)ws.pim;
-  ar.gl = ws.gl; ar.valid_len = in.valid_len;
-  ar.init = init; ar.init_seg_stride = init_seg_stride;
-  ar.dhc = (uint8_t*)dhc; ar.start_out = start_out; ar.D_out = D_out;
-  ar.out_seg_stride = out_seg_stride; ar.status = ws.status;
-  ar.mode = mode; ar.seg_first = seg_first; ar.nseg = nseg;
+  if (!dchain_setup(pr, in, ws, mode, seg_first, nseg, init, init_seg_stride, dhc, start_out,
+                    D_out, out_seg_stride, &mq, &mk, &mdo, &ar))
+    return cudaErrorInvalidValue;
   cudaError_t e = smem_attr(k_dchain_tc, D_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(1, (unsigned)pr.H, (unsigned)(pr.B * nseg));
   k_dchain_tc<<<grid, CT, D_SMEM, st>>>(mq, mk, mdo, ar);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chain_pair_tc(const Prob& pr, const Inputs& in, const WS& ws, int fmode,
+                                 const ChainPass& f, int rmode, const ReversePass& r,
+                                 cudaStream_t st) {
+  if (f.nseg <= 0) return launch_dchain_tc(pr, in, ws, rmode, r.seg_first, r.nseg, r.init,
+                                           r.init_seg_stride, r.dhc, r.start_out, r.D_out,
+                                           r.out_seg_stride, st);
+  if (r.nseg <= 0) return launch_chain_tc(pr, in, ws, fmode, f.seg_first, f.nseg, f.init,
+                                          f.init_seg_stride, nullptr, nullptr, f.M_out, f.S_out,
+                                          f.out_seg_stride, f.hc, st);
+  if (pr.B == 0 || pr.NC == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mo, mq2, mk2, mdo;
+  ChainArgs fa;
+  DchainArgs ra;
+  if (!chain_setup(pr, in, ws, f.seg_first, f.nseg, f.init, f.init_seg_stride, nullptr, nullptr,
+                   f.M_out, f.S_out, f.out_seg_stride, f.hc, &mq, &mk, &mo, &fa) ||
+      !dchain_setup(pr, in, ws, rmode, r.seg_first, r.nseg, r.init, r.init_seg_stride, r.dhc,
+                    r.start_out, r.D_out, r.out_seg_stride, &mq2, &mk2, &mdo, &ra))
+    return cudaErrorInvalidValue;
+  const int parts = fmode == CH_SUM ? 2 : 1;
+  const int64_t nf = (int64_t)parts * pr.B * f.nseg, nr = pr.B * (int64_t)r.nseg;
+  const uint32_t smem = S_SMEM > D_SMEM ? S_SMEM : D_SMEM;
+  dim3 grid(1, (unsigned)pr.H, (unsigned)(nf + nr));
+  cudaError_t e;
+  if (fmode == CH_SUM) {
+    if ((e = smem_attr(k_chain_pair_tc<CH_SUM>, smem)) != cudaSuccess) return e;
+    k_chain_pair_tc<CH_SUM><<<grid, CT, smem, st>>>(mq, mk, mo, mdo, fa, ra, parts, nf);
+  } else {
+    if ((e = smem_attr(k_chain_pair_tc<CH_STATES>, smem)) != cudaSuccess) return e;
+    k_chain_pair_tc<CH_STATES><<<grid, CT, smem, st>>>(mq, mk, mo, mdo, fa, ra, parts, nf);
+  }
   return cudaGetLastError();
 }
 
