@@ -159,11 +159,7 @@ def kernel_work(name, w, P):
 # ncu-measured DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
 # a kernel at the bench workload, valid only for the source file it was taken from
 # (its SHA-256); the capture is summarised under profiles/.
-MEASURED_TRAFFIC = {
-    "bwd.grad_tc": {"T": 32768, "bytes_per_launch": 3098280192 + 855851776,
-                    "src": "chunked_state_scan_gated_gb300/csrc/gdn_tc_bwd.cu",
-                    "sha256": "b75fab54bd428690514dc12e069dd5372f5715f4d46ccda74d4b4780fb27a0a1"},
-}
+MEASURED_TRAFFIC = {}
 
 
 def _src_sha(rel):

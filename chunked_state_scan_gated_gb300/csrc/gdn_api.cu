@@ -339,7 +339,7 @@ gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const
       const ReversePass r{0, pr.P, dinit, dinit_stride, ws.dhc16, dH0, nullptr, 0};
       GDN_RUN(sc, "states_pair_tc", launch_chain_pair_tc(pr, in, ws, 2, f, 0, r, st));
     }
-    GDN_RUN(sc, "grad_tc", launch_grad_tc(pr, in, ws, ws.hc16, ws.dhc16, dv, dg, dbeta, st));
+    GDN_RUN(sc, "grad_tc", launch_grad2_tc(pr, in, ws, ws.hc16, ws.dhc16, dv, dg, dbeta, st));
     GDN_RUN(sc, "qk_grad_tc", launch_qk_grad_tc(pr, in, ws, dq, dk, st));
     return GDN_OK;
   }

@@ -158,8 +158,9 @@ cudaError_t launch_chain_pair_tc(const Prob& pr, const Inputs& in, const WS& ws,
 // dq, dk (bf16) from the per-V-head bf16 gradients of q_hat, k_hat in ws.dqp / ws.dkp
 cudaError_t launch_qk_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, void* dq, void* dk,
                               cudaStream_t st);
-// chunk-parallel gradients from chunk-start states and chunk-end state gradients
-cudaError_t launch_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, const void* hc,
-                           const void* dhc, void* dv, float* dg, float* dbeta, cudaStream_t st);
+// chunk-parallel local gradients from chunk-start states and chunk-end state gradients
+// (feature-major tcgen05 products); dq_hat / dk_hat partials into ws.dqp / ws.dkp (bf16)
+cudaError_t launch_grad2_tc(const Prob& pr, const Inputs& in, const WS& ws, const void* hc,
+                            const void* dhc, void* dv, float* dg, float* dbeta, cudaStream_t st);
 
 }  // namespace gdn
