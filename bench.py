@@ -159,7 +159,11 @@ def kernel_work(name, w, P):
 # ncu-measured DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
 # a kernel at the bench workload, valid only for the source file it was taken from
 # (its SHA-256); the capture is summarised under profiles/.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    "bwd.grad_tc": {"T": 32768, "bytes_per_launch": 3102593024 + 847667968,
+                    "src": "chunked_state_scan_gated_gb300/csrc/gdn_tc_grad.cu",
+                    "sha256": "47d381c5fd075af9b1dc5ed7a38e12631cf5c842ca22c77e69852b1e774ec439"},
+}
 
 
 def _src_sha(rel):
