@@ -13,6 +13,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -38,16 +39,29 @@ bool ok_ptr(const void* p, int64_t numel) {
 }
 bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
 
-// SM count of the current device (152 on GB300 when no device can be queried).
+}  // namespace
+
+// SM count of the current device (152 on GB300 when no device can be queried), cached
+// per device.
 int device_sms() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices] = {};
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return 152;
   }
+  if (dev >= 0 && dev < kMaxDevices && (n = cache[dev].load(std::memory_order_relaxed)) > 0)
+    return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
+
+namespace {
 
 // Segment count of the tensor-core path: the P that minimises a model of the
 // forward + backward chain time.  Every chain pass runs ceil(CTAs / slots)

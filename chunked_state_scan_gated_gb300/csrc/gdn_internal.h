@@ -112,6 +112,9 @@ cudaError_t launch_gate_param_bwd(const Prob& pr, const void* a, const void* b,
                                   float* da, float* db, float* dA_log, float* ddt_bias,
                                   cudaStream_t st);
 
+// number of SMs of the current device (cached per device)
+int device_sms();
+
 // ---- tensor-core (tcgen05) kernels, bf16 with dk = dv = 128 ----
 bool tc_path(const Prob& pr);
 // chunk-parallel prologue: norm factors, gates and the W, U, P (and T) tile images

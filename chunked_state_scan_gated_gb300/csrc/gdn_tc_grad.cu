@@ -265,6 +265,13 @@ __global__ void __launch_bounds__(GT, 1)
     }
   }
   {
+    // Descriptors of every operand tile: the start address sits in the low 14 bits
+    // (address >> 4), so a tile at byte offset `off` is the base descriptor + off / 16.
+    const uint64_t d16 = sdesc(base, 16, 1024), d8192 = sdesc(base, 8192, 1024),
+                   d16384 = sdesc(base, 16384, 1024);
+    auto dsc16 = [&](uint32_t off) { return d16 + (off >> 4); };
+    auto dsc8192 = [&](uint32_t off) { return d8192 + (off >> 4); };
+    auto dsc16384 = [&](uint32_t off) { return d16384 + (off >> 4); };
     uint32_t ph = 0;
     float dqT[16], dkT[16];  // this thread's feature row fr of dq_hat^T, dk_hat^T, tokens cb + e
     const uint32_t idA = idesc_bf16(128, 64, 1, 0);  // A MN-major (feature rows), B K-major
@@ -278,18 +285,18 @@ __global__ void __launch_bounds__(GT, 1)
       const uint32_t id64d = idesc_bf16(64, 64, 0, 0);
       for (int ks = 0; ks < 8; ++ks) {  // K = dk (S^T W^T, dS^T K^T, K K^T) or dv (S dO^T)
         const uint32_t at = ks >> 2, kk = ks & 3;
-        mma_bf16(tmem, sdesc(base + R_S + ks * 2048, 16384, 1024),
-                 sdesc(base + R_W + at * 8192 + kk * 32, 16, 1024), idA, ks > 0);
-        mma_bf16(tmem + 128, sdesc(base + R_DS + ks * 2048, 16384, 1024),
-                 sdesc(base + R_K + at * 8192 + kk * 32, 16, 1024), idA, ks > 0);
-        mma_bf16(tmem + 192, sdesc(base + R_S + at * 16384 + kk * 32, 16, 1024),
-                 sdesc(base + R_DO + at * 8192 + kk * 32, 16, 1024), idD, ks > 0);
-        mma_bf16(tmem + 256, sdesc(base + R_K + at * 8192 + kk * 32, 16, 1024),
-                 sdesc(base + R_K + at * 8192 + kk * 32, 16, 1024), id64d, ks > 0);
+        mma_bf16(tmem, dsc16384(R_S + ks * 2048),
+                 dsc16(R_W + at * 8192 + kk * 32), idA, ks > 0);
+        mma_bf16(tmem + 128, dsc16384(R_DS + ks * 2048),
+                 dsc16(R_K + at * 8192 + kk * 32), idA, ks > 0);
+        mma_bf16(tmem + 192, dsc16(R_S + at * 16384 + kk * 32),
+                 dsc16(R_DO + at * 8192 + kk * 32), idD, ks > 0);
+        mma_bf16(tmem + 256, dsc16(R_K + at * 8192 + kk * 32),
+                 dsc16(R_K + at * 8192 + kk * 32), id64d, ks > 0);
       }
       for (int ks = 0; ks < 4; ++ks)  // K = tokens
-        mma_bf16(tmem + 64, sdesc(base + R_DO + ks * 2048, 8192, 1024),
-                 sdesc(base + R_P + ks * 2048, 8192, 1024), idC, ks > 0);
+        mma_bf16(tmem + 64, dsc8192(R_DO + ks * 2048),
+                 dsc8192(R_P + ks * 2048), idC, ks > 0);
       mma_commit(bar_mma);
     }
     {  // <S, dS> (same tile layout): warp partials into sMisc
@@ -335,16 +342,16 @@ __global__ void __launch_bounds__(GT, 1)
       const uint32_t id64b = idesc_bf16(64, 64, 0, 1);
       for (int ks = 0; ks < 8; ++ks) {  // K = dv
         const uint32_t at = ks >> 2, kk = ks & 3;
-        mma_bf16(tmem, sdesc(base + R_S + at * 16384 + kk * 32, 16, 1024),
-                 sdesc(base + R_DVT + ks * 2048, 8192, 1024), idB, ks > 0);
-        mma_bf16(tmem + 64, sdesc(base + R_DS + at * 16384 + kk * 32, 16, 1024),
-                 sdesc(base + R_VT + ks * 2048, 8192, 1024), idB, ks > 0);
-        mma_bf16(tmem + 192, sdesc(base + R_DO + at * 8192 + kk * 32, 16, 1024),
-                 sdesc(base + R_VT + ks * 2048, 8192, 1024), id64b, ks > 0);
+        mma_bf16(tmem, dsc16(R_S + at * 16384 + kk * 32),
+                 dsc8192(R_DVT + ks * 2048), idB, ks > 0);
+        mma_bf16(tmem + 64, dsc16(R_DS + at * 16384 + kk * 32),
+                 dsc8192(R_VT + ks * 2048), idB, ks > 0);
+        mma_bf16(tmem + 192, dsc16(R_DO + at * 8192 + kk * 32),
+                 dsc8192(R_VT + ks * 2048), id64b, ks > 0);
       }
       for (int ks = 0; ks < 4; ++ks)  // K = tokens
-        mma_bf16(tmem + 128, sdesc(base + R_DVT + ks * 32, 16, 1024),
-                 sdesc(base + R_T + ks * 2048, 8192, 1024), idB, ks > 0);
+        mma_bf16(tmem + 128, dsc16(R_DVT + ks * 32),
+                 dsc8192(R_T + ks * 2048), idB, ks > 0);
       mma_commit(bar_mma);
     }
     {  // while round B runs: (diag(gamma) dO S^T)^T and q_t . (gamma_t S dO_t)
@@ -400,14 +407,14 @@ __global__ void __launch_bounds__(GT, 1)
     if (tid == 0) {
       const uint32_t id64c = idesc_bf16(64, 64, 1, 1);
       for (int ks = 0; ks < 4; ++ks) {  // K = tokens
-        mma_bf16(tmem + 320, sdesc(base + R_W + ks * 32, 16, 1024),
-                 sdesc(base + R_T + ks * 2048, 8192, 1024), idB, ks > 0);
-        mma_bf16(tmem + 384, sdesc(base + R_K + ks * 2048, 8192, 1024),
-                 sdesc(base + R_P + ks * 32, 16, 1024), idA, ks > 0);
+        mma_bf16(tmem + 320, dsc16(R_W + ks * 32),
+                 dsc8192(R_T + ks * 2048), idB, ks > 0);
+        mma_bf16(tmem + 384, dsc8192(R_K + ks * 2048),
+                 dsc16(R_P + ks * 32), idA, ks > 0);
       }
       for (int ks = 0; ks < 8; ++ks)  // K = dv
-        mma_bf16(tmem + 448, sdesc(base + R_U + ks * 2048, 8192, 1024),
-                 sdesc(base + R_VT + ks * 2048, 8192, 1024), id64c, ks > 0);
+        mma_bf16(tmem + 448, dsc8192(R_U + ks * 2048),
+                 dsc8192(R_VT + ks * 2048), id64c, ks > 0);
       mma_commit(bar_mma);
     }
     {  // while round C runs: Kt part of dk, dv, and the row dots of V' dS^T and X_v
@@ -478,14 +485,14 @@ __global__ void __launch_bounds__(GT, 1)
       tma_store_4d(&mdv, sm + R_DO + 8192, 64, (int)h, (int)t0, (int)b);
       bulk_commit();
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem, sdesc(base + R_Q + ks * 2048, 8192, 1024),
-                 sdesc(base + R_P + ks * 2048, 8192, 1024), idC, ks > 0);
+        mma_bf16(tmem, dsc8192(R_Q + ks * 2048),
+                 dsc8192(R_P + ks * 2048), idC, ks > 0);
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem, sdesc(base + R_K + ks * 2048, 8192, 1024),
-                 sdesc(base + R_T + ks * 32, 16, 1024), idA, 1);
+        mma_bf16(tmem, dsc8192(R_K + ks * 2048),
+                 dsc16(R_T + ks * 32), idA, 1);
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem, sdesc(base + R_K + ks * 2048, 8192, 1024),
-                 sdesc(base + R_T + ks * 2048, 8192, 1024), idC, 1);
+        mma_bf16(tmem, dsc8192(R_K + ks * 2048),
+                 dsc8192(R_T + ks * 2048), idC, 1);
       mma_commit(bar_mma);
     }
     {  // while round D runs: X_w part of dk, dq_hat staging, row dots of X_w
