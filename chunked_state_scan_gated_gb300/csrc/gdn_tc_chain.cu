@@ -109,6 +109,9 @@ __global__ void __launch_bounds__(PT, 2)
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t base = smem_u32(sm);
+  // operand descriptors: base descriptor + byte offset / 16 (the start address field)
+  const uint64_t d16 = sdesc(base, 16, 1024), d8192 = sdesc(base, 8192, 1024),
+                 d16384 = sdesc(base, 16384, 1024);
   float* sG = (float*)(sm + P_SC);
   float* sGam = sG + 64;
   float* sBeta = sGam + 64;
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(PT, 2)
     const uint32_t id = idesc_bf16(128, 128, 0, 0);
     for (int ks = 0; ks < 8; ++ks) {
       const uint32_t at = ks >> 2, kk = ks & 3;
-      const uint64_t d = sdesc(base + P_QK + at * 16384 + kk * 32, 16, 1024);
+      const uint64_t d = (d16 + ((P_QK + at * 16384 + kk * 32) >> 4));
       mma_bf16(tmem, d, d, id, ks > 0);
     }
     mma_commit(bar_mma);
@@ -266,9 +269,9 @@ __global__ void __launch_bounds__(PT, 2)
   if (tid == 0) {
     const uint32_t id = idesc_bf16(128, 128, 0, 1);
     for (int ks = 0; ks < 4; ++ks) {
-      const uint64_t a = sdesc(base + P_TA + ks * 32, 16, 1024);
-      mma_bf16(tmem, a, sdesc(base + P_V + ks * 2048, 8192, 1024), id, ks > 0);
-      mma_bf16(tmem + 128, a, sdesc(base + P_QK + 8192 + ks * 2048, 16384, 1024), id, ks > 0);
+      const uint64_t a = (d16 + ((P_TA + ks * 32) >> 4));
+      mma_bf16(tmem, a, (d8192 + ((P_V + ks * 2048) >> 4)), id, ks > 0);
+      mma_bf16(tmem + 128, a, (d16384 + ((P_QK + 8192 + ks * 2048) >> 4)), id, ks > 0);
     }
     mma_commit(bar_mma);
   }
@@ -374,6 +377,10 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t base = smem_u32(sm);
+  // operand descriptors: base descriptor + byte offset / 16 (the start address field)
+  const uint64_t d16 = sdesc(base, 16, 1024), d8192 = sdesc(base, 8192, 1024),
+                 d16384 = sdesc(base, 16384, 1024);
+  const uint64_t dxs = sdesc(base, XSTR, 1024);
   // apply: xa0, xa1, u, p, mma; otherwise: w, k, u, -, mma
   uint64_t* bars = (uint64_t*)(sm + OFF_SC);
   uint64_t* bar_u = bars + 2;
@@ -547,8 +554,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
         const uint32_t id = idesc_bf16(kApply ? 128 : 64, 128, 0, 1);
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t at = ks >> 2, kk = ks & 3;
-          mma_bf16(tA, sdesc(base + xa + at * XSTR + kk * 32, 16, 1024),
-                   sdesc(base + OFF_S + ks * 2048, 16384, 1024), id, ks > 0);
+          mma_bf16(tA, (d16 + ((xa + at * XSTR + kk * 32) >> 4)),
+                   (d16384 + ((OFF_S + ks * 2048) >> 4)), id, ks > 0);
         }
         mma_commit(bar_mma);
         pend |= 16u;
@@ -612,15 +619,15 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
         }
         const uint32_t id = idesc_bf16(128, 128, 1, 1);
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tB, sdesc(base + xa + KOFF + ks * 2048, XSTR, 1024),
-                   sdesc(base + OFF_V2 + ks * 2048, 8192, 1024), id, ks > 0);
+          mma_bf16(tB, (dxs + ((xa + KOFF + ks * 2048) >> 4)),
+                   (d8192 + ((OFF_V2 + ks * 2048) >> 4)), id, ks > 0);
         if (kApply) {
           if (!mbar_wait(bars + 3, par, ar.status, kStatusTimeout)) *s_abort = 1;
           pend &= ~8u;
           const uint32_t id2 = idesc_bf16(128, 128, 0, 1);
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tA, sdesc(base + A_PZ + ks * 32, 16, 1024),
-                     sdesc(base + A_VP + ks * 2048, 8192, 1024), id2, 1);
+            mma_bf16(tA, (d16 + ((A_PZ + ks * 32) >> 4)),
+                     (d8192 + ((A_VP + ks * 2048) >> 4)), id2, 1);
         }
         mma_commit(bar_mma);
         pend |= 16u;
@@ -752,6 +759,9 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t base = smem_u32(sm);
+  // operand descriptors: base descriptor + byte offset / 16 (the start address field)
+  const uint64_t d16 = sdesc(base, 16, 1024), d8192 = sdesc(base, 8192, 1024),
+                 d16384 = sdesc(base, 16384, 1024);
   uint64_t* bars = (uint64_t*)(sm + D_SC);  // a: K, Q, P, G/rq/rk; b: W, dO; mma
   uint64_t* bar_a = bars, *bar_b = bars + 1, *bar_mma = bars + 2;
   uint32_t* s_tmem = (uint32_t*)(bars + 4);
@@ -867,18 +877,18 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
       if (tid == 0) {
         const uint32_t idv = idesc_bf16(64, 128, 1, 1);
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tV, sdesc(base + D_P + ks * 2048, 8192, 1024),
-                   sdesc(base + D_DO + ks * 2048, 8192, 1024), idv, ks > 0);
+          mma_bf16(tV, (d8192 + ((D_P + ks * 2048) >> 4)),
+                   (d8192 + ((D_DO + ks * 2048) >> 4)), idv, ks > 0);
         const uint32_t idkm = idesc_bf16(64, 128, 0, 1);
         const uint32_t idmm = idesc_bf16(128, 128, 1, 1);
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t at = ks >> 2, kk = ks & 3;
-          mma_bf16(tV, sdesc(base + D_XA + at * 16384 + kk * 32, 16, 1024),
-                   sdesc(base + D_DS + ks * 2048, 16384, 1024), idkm, 1);
+          mma_bf16(tV, (d16 + ((D_XA + at * 16384 + kk * 32) >> 4)),
+                   (d16384 + ((D_DS + ks * 2048) >> 4)), idkm, 1);
         }
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tS, sdesc(base + D_XA + 8192 + ks * 2048, 16384, 1024),
-                   sdesc(base + D_DO + ks * 2048, 8192, 1024), idmm, ks > 0);
+          mma_bf16(tS, (d16384 + ((D_XA + 8192 + ks * 2048) >> 4)),
+                   (d8192 + ((D_DO + ks * 2048) >> 4)), idmm, ks > 0);
         mma_commit(bar_mma);
         pend |= 4u;
       }
@@ -911,8 +921,8 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
       if (tid == 0) {
         const uint32_t id = idesc_bf16(128, 128, 1, 1);
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tS, sdesc(base + D_W + ks * 2048, 8192, 1024),
-                   sdesc(base + D_DO + ks * 2048, 8192, 1024), id, 1);
+          mma_bf16(tS, (d8192 + ((D_W + ks * 2048) >> 4)),
+                   (d8192 + ((D_DO + ks * 2048) >> 4)), id, 1);
         mma_commit(bar_mma);
         pend |= 4u;
       }

@@ -17,7 +17,8 @@ using namespace tc;
 // k_qk_grad_tc: dq, dk from the per-V-head bf16 gradients of q_hat, k_hat:
 // summed over the r V heads of a Q/K head, then back through the scale and the
 // L2 norm (q_hat = s q / |q|: dq = s (g - u (u . g)) / |q| with u = q / |q|).
-// One warp per (row, token, Q/K head); lane l holds columns 4l .. 4l+3.
+// Sixteen lanes per (row, token, Q/K head); lane l of the group holds columns
+// 8l .. 8l+7, so every access is 16 bytes and a warp covers two rows.
 // ============================================================================
 struct QkArgs {
   int64_t B, T, Ts, Tp, Hqk, H, r;
@@ -31,47 +32,56 @@ struct QkArgs {
   __nv_bfloat16* dk;
 };
 
-__device__ __forceinline__ void ld4bf(const __nv_bfloat16* p, float* x) {
-  const uint2 v = *reinterpret_cast<const uint2*>(p);
-  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-  const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-  x[0] = a.x; x[1] = a.y; x[2] = c.x; x[3] = c.y;
+__device__ __forceinline__ void ld8bf(const __nv_bfloat16* p, float* x) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
 }
 
+constexpr int QK_ROWS = 16;  // rows per 256-thread block
+
 __global__ void __launch_bounds__(256) k_qk_grad_tc(QkArgs ar) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t rowid = (int64_t)blockIdx.x * 8 + warp;
-  if (rowid >= ar.B * ar.T * ar.Hqk) return;
+  const int sub = threadIdx.x & 15;
+  const int64_t rowid = (int64_t)blockIdx.x * QK_ROWS + (threadIdx.x >> 4);
+  if (rowid >= ar.B * ar.T * ar.Hqk) return;  // whole 16-lane groups leave together
+  const unsigned gmask = 0xffffu << (threadIdx.x & 16);
   const int64_t hq = rowid % ar.Hqk, t = (rowid / ar.Hqk) % ar.T, b = rowid / (ar.Hqk * ar.T);
-  const int64_t xo = ((b * ar.Ts + t) * ar.Hqk + hq) * 128 + lane * 4;
-  float xq[4], xk[4], gq[4] = {0.f, 0.f, 0.f, 0.f}, gk[4] = {0.f, 0.f, 0.f, 0.f};
-  ld4bf(ar.q + xo, xq);
-  ld4bf(ar.k + xo, xk);
-  for (int64_t h = hq * ar.r; h < (hq + 1) * ar.r; ++h) {
-    const int64_t po = ((b * ar.Tp + t) * ar.H + h) * 128 + lane * 4;
-    float a[4], c[4];
-    ld4bf(ar.dqp + po, a);
-    ld4bf(ar.dkp + po, c);
+  const int64_t xo = ((b * ar.Ts + t) * ar.Hqk + hq) * 128 + sub * 8;
+  const int64_t po0 = ((b * ar.Tp + t) * ar.H + hq * ar.r) * 128 + sub * 8;
+  float xq[8], xk[8], gq[8], gk[8];
+  ld8bf(ar.q + xo, xq);
+  ld8bf(ar.k + xo, xk);
+  ld8bf(ar.dqp + po0, gq);
+  ld8bf(ar.dkp + po0, gk);
+  for (int64_t j = 1; j < ar.r; ++j) {
+    float a[8], c[8];
+    ld8bf(ar.dqp + po0 + j * 128, a);
+    ld8bf(ar.dkp + po0 + j * 128, c);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 8; ++e) {
       gq[e] += a[e];
       gk[e] += c[e];
     }
   }
   float sq = 0.f, sk = 0.f, pq = 0.f, pk = 0.f;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
+  for (int e = 0; e < 8; ++e) {
     sq = fmaf(xq[e], xq[e], sq);
     sk = fmaf(xk[e], xk[e], sk);
     pq = fmaf(xq[e], gq[e], pq);
     pk = fmaf(xk[e], gk[e], pk);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    sk += __shfl_xor_sync(0xffffffffu, sk, o);
-    pq += __shfl_xor_sync(0xffffffffu, pq, o);
-    pk += __shfl_xor_sync(0xffffffffu, pk, o);
+  for (int o = 8; o > 0; o >>= 1) {
+    sq += __shfl_xor_sync(gmask, sq, o);
+    sk += __shfl_xor_sync(gmask, sk, o);
+    pq += __shfl_xor_sync(gmask, pq, o);
+    pk += __shfl_xor_sync(gmask, pk, o);
   }
   float rq = 1.f, rk = 1.f, prq = 0.f, prk = 0.f;
   if (ar.l2norm) {
@@ -80,19 +90,23 @@ __global__ void __launch_bounds__(256) k_qk_grad_tc(QkArgs ar) {
     prq = pq * rq * rq;
     prk = pk * rk * rk;
   }
-  float oq[4], ok[4];
+  float oq[8], ok[8];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
+  for (int e = 0; e < 8; ++e) {
     oq[e] = ar.scale * (gq[e] - xq[e] * prq) * rq;
     ok[e] = (gk[e] - xk[e] * prk) * rk;
   }
-  uint2 vq, vk;
+  uint4 vq, vk;
   vq.x = pack_bf16(oq[0], oq[1]);
   vq.y = pack_bf16(oq[2], oq[3]);
+  vq.z = pack_bf16(oq[4], oq[5]);
+  vq.w = pack_bf16(oq[6], oq[7]);
   vk.x = pack_bf16(ok[0], ok[1]);
   vk.y = pack_bf16(ok[2], ok[3]);
-  *reinterpret_cast<uint2*>(ar.dq + xo) = vq;
-  *reinterpret_cast<uint2*>(ar.dk + xo) = vk;
+  vk.z = pack_bf16(ok[4], ok[5]);
+  vk.w = pack_bf16(ok[6], ok[7]);
+  *reinterpret_cast<uint4*>(ar.dq + xo) = vq;
+  *reinterpret_cast<uint4*>(ar.dk + xo) = vk;
 }
 
 }  // namespace
@@ -107,7 +121,7 @@ cudaError_t launch_qk_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, vo
   ar.q = (const __nv_bfloat16*)in.q; ar.k = (const __nv_bfloat16*)in.k;
   ar.dqp = (const __nv_bfloat16*)ws.dqp; ar.dkp = (const __nv_bfloat16*)ws.dkp;
   ar.dq = (__nv_bfloat16*)dq; ar.dk = (__nv_bfloat16*)dk;
-  k_qk_grad_tc<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(ar);
+  k_qk_grad_tc<<<(unsigned)((rows + QK_ROWS - 1) / QK_ROWS), 256, 0, st>>>(ar);
   return cudaGetLastError();
 }
 
