@@ -83,7 +83,25 @@ constexpr uint32_t P_A = 65536;                // fp32 A [64][LDA]
 constexpr uint32_t P_T = P_A + 64 * LDA * 4;   // fp32 T [64][LDA]
 constexpr uint32_t P_Y = P_T + 64 * LDA * 4;   // solve scratch, 8 warps x 128 floats
 constexpr uint32_t P_SC = P_Y + 1024 * 4;      // gates, row factors, barriers
-constexpr uint32_t P_SMEM = P_SC + 1280 + 64 + 1024;
+constexpr uint32_t P_SMEM = P_SC + 1536 + 64 + 1024;
+
+// Writes T diag(beta) (rows 0..63) and T diag(beta gamma rk) (rows 64..127) of the
+// 128 x 64 K-major bf16 tile [T_u; T_w] as the solve finalises each entry of T.
+struct TaEmit {
+  uint8_t* tile;
+  const float* cu;  // beta
+  const float* cw;  // beta gamma rk
+  __device__ __forceinline__ void one(int i, int j, float x) const {
+    const uint32_t off = kmaj_chunk(i, j >> 3) + (j & 7) * 2;
+    *reinterpret_cast<__nv_bfloat16*>(tile + off) = __float2bfloat16_rn(x * cu[j]);
+    *reinterpret_cast<__nv_bfloat16*>(tile + 8192 + off) = __float2bfloat16_rn(x * cw[j]);
+  }
+  __device__ __forceinline__ void two(int i, int j, float x0, float x1) const {
+    const uint32_t off = kmaj_chunk(i, j >> 3) + (j & 7) * 2;
+    *reinterpret_cast<uint32_t*>(tile + off) = pack_bf16(x0 * cu[j], x1 * cu[j + 1]);
+    *reinterpret_cast<uint32_t*>(tile + 8192 + off) = pack_bf16(x0 * cw[j], x1 * cw[j + 1]);
+  }
+};
 
 struct PrepArgs {
   int64_t T, Ts, H, Hqk, r, NC;
@@ -116,7 +134,8 @@ __global__ void __launch_bounds__(PT, 2)
   float* sGam = sG + 64;
   float* sBeta = sGam + 64;
   float* sInv = sBeta + 64;  // [128]: rq (rows 0..63), rk (rows 64..127)
-  uint64_t* bar_qk = (uint64_t*)(sm + P_SC + 1280);
+  float* sCw = sInv + 128;   // [64]: beta gamma rk, the column factors of T_w
+  uint64_t* bar_qk = (uint64_t*)(sm + P_SC + 1536);
   uint64_t* bar_v = bar_qk + 1;
   uint64_t* bar_mma = bar_qk + 2;
   uint32_t* s_tmem = (uint32_t*)(bar_qk + 3);
@@ -142,6 +161,8 @@ __global__ void __launch_bounds__(PT, 2)
     *s_abort = 0;
   }
   if (warp == 0) tmem_alloc(s_tmem, 256);
+  for (int e = tid; e < 1024; e += PT)  // [T_u; T_w]: the solve writes only the lower triangle
+    reinterpret_cast<uint4*>(sm + P_TA)[e] = make_uint4(0, 0, 0, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -205,6 +226,7 @@ __global__ void __launch_bounds__(PT, 2)
   }
   __syncthreads();
   if (h % ar.r == 0 && tid < 128) ar.rqk[((b * ar.Hqk + hq) * ar.NC + c) * 128 + tid] = sInv[tid];
+  if (tid >= 128 && tid < 192) sCw[tid - 128] = sBeta[tid - 128] * sGam[tid - 128] * sInv[tid - 64];
   {
     float v[32];  // row . k_j for j = 32*half + e
     tmem_ld32(tmem + lane_off + 64 + 32 * half, v);
@@ -233,7 +255,9 @@ __global__ void __launch_bounds__(PT, 2)
   }
   tc_fence_before();
   __syncthreads();
-  solve_unit_lower64_mma(sA, sT, sY, LDA);
+  // T = (I + A)^-1, with [T_u; T_w] = [T diag(beta); T diag(beta gamma rk)] (bf16, W is
+  // formed from raw k) written as each entry of T is final
+  solve_unit_lower64_mma(sA, sT, sY, LDA, TaEmit{sm + P_TA, sBeta, sCw});
   if (ar.tim) {  // T for the backward, bf16 image
     uint8_t* dst = ar.tim + (bh * ar.NC + c) * (int64_t)kImgP;
     for (int e = tid; e < 512; e += PT) {
@@ -246,18 +270,6 @@ __global__ void __launch_bounds__(PT, 2)
       }
       *reinterpret_cast<uint4*>(dst + kmaj_chunk(i, cc)) = pack8(x);
     }
-  }
-  // [T_u; T_w] = [T diag(beta); T diag(beta gamma rk)] in bf16 (W is formed from raw k)
-  for (int e = tid; e < 1024; e += PT) {
-    const int rr = e >> 3, cc = e & 7, i = rr & 63;
-    const bool w = rr >= 64;
-    float x[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = cc * 8 + q;
-      x[q] = (j <= i) ? sT[i * LDA + j] * sBeta[j] * (w ? sGam[j] * sInv[64 + j] : 1.f) : 0.f;
-    }
-    st_chunk(sm + P_TA, kmaj_chunk(rr, cc), x);
   }
   if (!mbar_wait(bar_v, 0, ar.status, kStatusTimeout)) *s_abort = 1;
   fence_proxy_async();

@@ -330,13 +330,22 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&c)[4], const float (&a)[
         "r"(to_tf32(b[0])), "r"(to_tf32(b[1])));
 }
 
+// Receiver of the entries of T as the solve finalises them (nothing by default).
+struct NoEmit {
+  __device__ __forceinline__ void one(int, int, float) const {}
+  __device__ __forceinline__ void two(int, int, float, float) const {}
+};
+
 // T = (I + A)^-1 for strictly lower A (64 x 64, fp32, leading dim lda).  The
 // 16 x 16 diagonal blocks come from forward substitution on CUDA cores; the
 // blocks below them, block diagonal by block diagonal, from
 // T_ij = -T_ii (sum_{j <= m < i} A_im T_mj) with warp-level tf32 MMAs (one warp
 // per 16 x 8 half block).  Y needs 8 warps x 128 floats.  Needs blockDim.x >= 256.
+// Every entry on or below the diagonal is also handed to emit.one(i, j, t) or, for
+// the column pair j, j + 1 (j even), emit.two(i, j, t_j, t_j+1) once it is final.
+template <typename Emit = NoEmit>
 __device__ __forceinline__ void solve_unit_lower64_mma(const float* A, float* T, float* Y,
-                                                       const int lda) {
+                                                       const int lda, const Emit& emit = Emit()) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp < 4 && lane < 16) {
     const int b0 = warp * 16, j = lane;
@@ -349,7 +358,10 @@ __device__ __forceinline__ void solve_unit_lower64_mma(const float* A, float* T,
       x[i] = (i >= j) ? v : 0.f;
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) T[(b0 + i) * lda + b0 + j] = x[i];
+    for (int i = 0; i < 16; ++i) {
+      T[(b0 + i) * lda + b0 + j] = x[i];
+      if (i >= j) emit.one(b0 + i, b0 + j, x[i]);
+    }
   }
   __syncthreads();
   const int g = lane >> 2, t = lane & 3;
@@ -382,6 +394,8 @@ __device__ __forceinline__ void solve_unit_lower64_mma(const float* A, float* T,
       T[(r0 + g) * lda + n0 + 2 * t + 1] = -e[1];
       T[(r0 + g + 8) * lda + n0 + 2 * t] = -e[2];
       T[(r0 + g + 8) * lda + n0 + 2 * t + 1] = -e[3];
+      emit.two(r0 + g, n0 + 2 * t, -e[0], -e[1]);
+      emit.two(r0 + g + 8, n0 + 2 * t, -e[2], -e[3]);
     }
     __syncthreads();
   }
