@@ -232,24 +232,37 @@ __global__ void __launch_bounds__(PT, 2)
     tmem_ld32(tmem + lane_off + 64 + 32 * half, v);
     const int i = row & 63;
     const float gi = sG[i], si = sInv[row];
-    if (row < 64) {
+    // v[e] <- row . k_j rk_j e^{G_i - G_j} (j = 32 half + e), zero above the diagonal; a
+    // warp whose 32 columns all lie above its rows (half 1, rows 0..31) has nothing to do
+    const bool upper = half * 32 > i;  // uniform across the warp
+    if (!upper) {
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(sG + half * 32 + 4 * q4);
+        const float4 r4 = *reinterpret_cast<const float4*>(sInv + 64 + half * 32 + 4 * q4);
+        const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, rr[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = 4 * q4 + u, j = half * 32 + e;
+          v[e] = (j <= i) ? v[e] * rr[u] * exp2f(gi - gg[u]) : 0.f;
+        }
+      }
+    }
+    if (row < 64) {  // P = tril(Q K^T o Gamma) with the norm factors: bf16 image
       uint8_t* dst = ar.pim + (bh * ar.NC + c) * (int64_t)kImgP;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         float p[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = half * 32 + cc * 8 + e;
-          p[e] = (j <= i) ? v[cc * 8 + e] * si * sInv[64 + j] * exp2f(gi - sG[j]) : 0.f;
-        }
+        for (int e = 0; e < 8; ++e) p[e] = upper ? 0.f : si * v[cc * 8 + e];
         *reinterpret_cast<uint4*>(dst + kmaj_chunk(i, half * 4 + cc)) = pack8(p);
       }
-    } else {
+    } else if (!upper) {  // A = strictly lower part, times beta_i (the solve never reads above it)
       const float bs = sBeta[i] * si;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int j = half * 32 + e;
-        sA[i * LDA + j] = (j < i) ? bs * v[e] * sInv[64 + j] * exp2f(gi - sG[j]) : 0.f;
+        sA[i * LDA + j] = (j < i) ? bs * v[e] : 0.f;
       }
     }
   }

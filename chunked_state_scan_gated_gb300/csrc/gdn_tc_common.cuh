@@ -348,18 +348,20 @@ __device__ __forceinline__ void solve_unit_lower64_mma(const float* A, float* T,
                                                        const int lda, const Emit& emit = Emit()) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp < 4 && lane < 16) {
+    // column j of the block, by columns of A: once x[l] is final it is removed from every
+    // later row, so the dependent chain is 15 FMAs long and the loads of A do not wait
     const int b0 = warp * 16, j = lane;
     float x[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float v = (i == j) ? 1.f : 0.f;
+    for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
 #pragma unroll
-      for (int l = 0; l < i; ++l) v = fmaf(-A[(b0 + i) * lda + b0 + l], x[l], v);
-      x[i] = (i >= j) ? v : 0.f;
+    for (int l = 0; l < 15; ++l) {
+#pragma unroll
+      for (int i = l + 1; i < 16; ++i) x[i] = fmaf(-A[(b0 + i) * lda + b0 + l], x[l], x[i]);
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      T[(b0 + i) * lda + b0 + j] = x[i];
+      T[(b0 + i) * lda + b0 + j] = x[i];  // zero above the diagonal (x[i] = 0 for i < j)
       if (i >= j) emit.one(b0 + i, b0 + j, x[i]);
     }
   }
