@@ -37,26 +37,48 @@ namespace {
 using namespace tc;
 
 constexpr int GT = 512;
-// Shared-memory map (1024-byte aligned regions).
-constexpr uint32_t R_Q = 0;          // q_hat [tok][dk] (two 8 KB atoms), scale included
-constexpr uint32_t R_K = 16384;      // k_hat [tok][dk]
-constexpr uint32_t R_V = 32768;      // v [tok][dv]
-constexpr uint32_t R_DO = 49152;     // dO [tok][dv]; after round B: dv staging [tok][dv]
-constexpr uint32_t R_S = 65536;      // S image [dk rows][dv] (two [128][64] atoms); then Z scratch
-constexpr uint32_t R_DS = 98304;     // dS image; after round B: dq_hat, dk_hat staging
-constexpr uint32_t R_W = 131072;     // W [tok][dk]; after round A: dW^T [dk][tok]
-constexpr uint32_t R_U = 147456;     // U [tok][dv]; after round A: X_v^T [dv][tok]
-constexpr uint32_t R_P = 163840;     // P [i][j]; in round B's epilogue: dP o Gamma
-constexpr uint32_t R_T = 172032;     // T [i][j]; in round C's epilogue: E
-constexpr uint32_t R_VT = 180224;    // V'^T [dv][tok] ([128][64] atom)
-constexpr uint32_t R_DVT = 196608;   // dV'^T [dv][tok]
-constexpr uint32_t R_SC = 212992;    // scalars
-constexpr uint32_t SC_BYTES = 7 * 64 * 4 + 4 * 4 * 64 * 4 + 4 * 64 * 4 + 8 * 64 * 4 + 64;  // + 4 barriers
+// Shared memory: thirteen 16 KB slots (the state S always in slots 4-5; P and T share
+// slot 10) whose roles alternate between two layouts from one chunk to the next, so
+// that every input tile of the next chunk lands in a slot the current chunk has
+// already finished with (see k_grad2_tc), then the scalars.
+constexpr uint32_t SLOT = 16384;
+constexpr uint32_t R_SC = 13 * SLOT;  // scalars
+constexpr uint32_t SC_BYTES = 2 * 4 * 64 * 4 + 3 * 64 * 4 + 4 * 4 * 64 * 4 + 3 * 4 * 64 * 4 + 128;
 constexpr uint32_t GR_SMEM = R_SC + SC_BYTES + 1024;
 static_assert(GR_SMEM <= 232448, "shared memory of k_grad2_tc");
 
+// Byte offsets of the tiles of one chunk.  q, k: q_hat, k_hat [tok][dk] (two 8 KB atoms,
+// normalised in place); v, dO: [tok][dv] (dO later the dv staging); s: S image [dk][dv]
+// (two [128][64] atoms 16 KB apart); ds0, ds1: the two atoms of the dS image (later the
+// dq_hat and dk_hat staging); w: W [tok][dk], later dW^T [dk][tok]; u: U [tok][dv], later
+// X_v^T; p: P, later dP o Gamma; t: T, later E; vt, dvt: V'^T and dV'^T [dv][tok].
+struct Lay {
+  uint32_t q, k, v, dO, s, ds0, ds1, w, u, p, t, vt, dvt;
+};
+// Layout 0 (even chunks of a CTA) and 1 (odd chunks).  Going 0 -> 1 the next chunk's
+// dO goes where dV'^T was (free once round B is done), its U where V was (after round
+// B's epilogue), its dS where U and V'^T were and its W where dW^T was (after round C),
+// its V where the dv staging was (after the dv store); 1 -> 0 mirrors it.
+__device__ __forceinline__ Lay layout_of(int par) {
+  Lay L;
+  L.q = 0;
+  L.k = SLOT;
+  L.s = 4 * SLOT;
+  L.w = 8 * SLOT;
+  L.p = 10 * SLOT;
+  L.t = 10 * SLOT + 8192;
+  if (par == 0) {
+    L.v = 2 * SLOT; L.dO = 3 * SLOT; L.ds0 = 6 * SLOT; L.ds1 = 7 * SLOT;
+    L.u = 9 * SLOT; L.vt = 11 * SLOT; L.dvt = 12 * SLOT;
+  } else {
+    L.u = 2 * SLOT; L.v = 3 * SLOT; L.vt = 6 * SLOT; L.dvt = 7 * SLOT;
+    L.ds0 = 9 * SLOT; L.ds1 = 11 * SLOT; L.dO = 12 * SLOT;
+  }
+  return L;
+}
+
 struct Grad2Args {
-  int64_t T, Ts, H, r, NC, Tp;
+  int64_t T, Ts, H, r, NC, Tp, NW;  // NW = B * H * NC chunks of work
   int l2norm;
   float eps, scale;
   const __nv_bfloat16* a;
@@ -90,8 +112,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-// Transpose-reduce of p[16] over the warp: lanes l and l ^ 16 both end with the sum
-// over all 32 lanes of p[l & 15] (15 + 1 shuffles).
+// Transpose-reduce of p[16] within each 16-lane half of the warp: lane l ends with the
+// sum over its half of p[l & 15] (15 shuffles).
 template <int K>
 __device__ __forceinline__ void xr_stage(float (&p)[16], int lane) {
 #pragma unroll
@@ -102,21 +124,23 @@ __device__ __forceinline__ void xr_stage(float (&p)[16], int lane) {
     p[i] = keep + __shfl_xor_sync(0xffffffffu, send, K);
   }
 }
-__device__ __forceinline__ float xreduce16(float (&p)[16], int lane) {
+__device__ __forceinline__ float xreduce_half(float (&p)[16], int lane) {
   xr_stage<8>(p, lane);
   xr_stage<4>(p, lane);
   xr_stage<2>(p, lane);
   xr_stage<1>(p, lane);
-  return p[0] + __shfl_xor_sync(0xffffffffu, p[0], 16);
+  return p[0];
+}
+// Over the whole warp: lanes l and l ^ 16 both end with the sum of p[l & 15].
+__device__ __forceinline__ float xreduce16(float (&p)[16], int lane) {
+  const float x = xreduce_half(p, lane);
+  return x + __shfl_xor_sync(0xffffffffu, x, 16);
 }
 
 // Element (t, f) of a token-major [64][128] bf16 tile (two K-major atoms).
 __device__ __forceinline__ uint32_t tf_off(int t, int f) {
   return (uint32_t)((f >> 6) * 8192 + t * 128 + (((((f & 63) >> 3) ^ t) & 7) << 4) + (f & 7) * 2);
 }
-// Element (i, j) of a 64 x 64 fp32 scratch matrix (XOR-swizzled rows: a warp reading a
-// row or a column of it touches 32 distinct banks).
-__device__ __forceinline__ int zoff(int i, int j) { return i * 64 + (j ^ (i & 31)); }
 __device__ __forceinline__ float ld_bf(const uint8_t* p) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
 }
@@ -133,10 +157,12 @@ __device__ __forceinline__ void st_bf(uint8_t* p, float x) {
     if (*s_abort) goto done;    \
   } while (0)
 
-// 512 threads: warp w reads TMEM lane quadrant q = w & 3 and token columns
-// 16 (w >> 2) .. +15.  In an M = 128 result thread (q, lane) owns feature row
-// 32 q + lane; in an M = 64 result (row r in lane (r % 16) + 32 (r / 16)) lanes
-// 0..15 of quadrant q own token row 16 q + lane.
+// Persistent: grid min(NW, SMs) x 512 threads, one CTA per SM; CTA i takes chunks
+// i, i + gridDim.x, ... (chunk w: c = w % NC, h = (w / NC) % H, b = w / (NC H)) and,
+// while it works on one, copies the next one's tiles into the slots it has freed.
+// Warp w reads TMEM lane quadrant q = w & 3 and token columns 16 (w >> 2) .. +15.  In
+// an M = 128 result thread (q, lane) owns feature row 32 q + lane; in an M = 64 result
+// (row r in lane (r % 16) + 32 (r / 16)) lanes 0..15 of quadrant q own token row 16 q + lane.
 __global__ void __launch_bounds__(GT, 1)
     k_grad2_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -145,24 +171,20 @@ __global__ void __launch_bounds__(GT, 1)
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t base = smem_u32(sm);
-  float* sG = (float*)(sm + R_SC);     // cumulative gate (log2 units)
-  float* sGam = sG + 64;
-  float* sBeta = sGam + 64;
-  float* sKt = sBeta + 64;
-  float* sDB = sKt + 64;               // dbeta (final)
+  // per chunk, two buffers (chunk k uses buffer k & 1): cumulative gate G (log2 units),
+  // gamma = 2^G, beta, Kt = 2^(G_C - G)
+  float* sGate = (float*)(sm + R_SC);
+  float* sDB = sGate + 2 * 256;        // dbeta (final)
   float* sFin = sDB + 64;              // final dG
   float* sMisc = sFin + 64;            // [16] warp partials of <S, dS>
   float* sRed = sMisc + 64;            // [4 types][4 quadrants][64 tokens] column partials
   float* sDBh = sRed + 4 * 4 * 64;     // [4 column parts][64] dbeta terms of A
-  float* sPart = sDBh + 4 * 64;        // [8 parts][64] gate terms of P and A (row - column sums)
-  uint64_t* bar_qk = (uint64_t*)(sPart + 8 * 64);  // q, k tiles
-  uint64_t* bar_a = bar_qk + 1;                      // S, dS, W, dO, P (round A)
-  uint64_t* bar_b = bar_qk + 2;                      // U, V, T
-  uint64_t* bar_mma = bar_qk + 3;
-  uint32_t* s_tmem = (uint32_t*)(bar_qk + 4);
+  float* sZr = sDBh + 4 * 64;          // [4 column parts][64 rows] row sums of dP o P + dA o A
+  float* sZc = sZr + 4 * 64;           // [4 row quadrants][64 columns] their column sums
+  uint64_t* bars = (uint64_t*)(sZc + 4 * 64);  // per layout: q/k, round-A tiles, U/V/T; MMA
+  uint64_t* bar_mma = bars + 6;
+  uint32_t* s_tmem = (uint32_t*)(bars + 7);
   int* s_abort = (int*)(s_tmem + 1);
-  float* sZb = (float*)(sm + R_S);           // dP o P (round B), once S is consumed
-  float* sZc = (float*)(sm + R_S + 16384);   // dA o A (round C)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, part = warp >> 2;
@@ -171,21 +193,14 @@ __global__ void __launch_bounds__(GT, 1)
   const bool own64 = lane < 16;        // owns row ri of M = 64 results
   const int ri = quad * 16 + (lane & 15);
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int64_t hq = h / ar.r, bh = b * ar.H + h;
-  const int64_t t0 = c * 64;
-  int64_t L = ar.T;
-  if (ar.valid_len) {
-    L = ar.valid_len[b];
-    if (L < 0 || L > ar.T) L = L < 0 ? 0 : ar.T;
-  }
+  const bool issuer = warp < 4 && lane == 0;  // issues one product per MMA round
   enum { RQ = 0, RV = 1, RKW = 2, RKD = 3 };  // column-sum types
+  enum { GQK = 0, GA = 1, GB = 2 };            // load groups
+  uint32_t armed = 0;  // tid 0: bit 3 l + g: group g of layout l armed and not yet consumed
 
   if (tid == 0) {
-    mbar_init(bar_qk, 1);
-    mbar_init(bar_a, 1);
-    mbar_init(bar_b, 1);
-    mbar_init(bar_mma, 1);
+    for (int i = 0; i < 6; ++i) mbar_init(bars + i, 1);
+    mbar_init(bar_mma, 4);  // each round's products are issued from four warps (lane 0 of 0..3)
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -194,117 +209,218 @@ __global__ void __launch_bounds__(GT, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  if (tid == 0) {
-    const int64_t im = bh * ar.NC + c;
-    mbar_arrive_expect_tx(bar_qk, 2 * 16384u);
-    for (int at = 0; at < 2; ++at) {
-      tma_load_4d(sm + R_Q + at * 8192, &mq, at * 64, (int)hq, (int)t0, (int)b, bar_qk);
-      tma_load_4d(sm + R_K + at * 8192, &mk, at * 64, (int)hq, (int)t0, (int)b, bar_qk);
+  // Descriptors of every operand tile: the start address sits in the low 14 bits
+  // (address >> 4), so a tile at byte offset `off` is the base descriptor + off / 16.
+  const uint64_t d16 = sdesc(base, 16, 1024), d8192 = sdesc(base, 8192, 1024),
+                 d16384 = sdesc(base, 16384, 1024);
+  auto dsc16 = [&](uint32_t off) { return d16 + (off >> 4); };
+  auto dsc8192 = [&](uint32_t off) { return d8192 + (off >> 4); };
+  auto dsc16384 = [&](uint32_t off) { return d16384 + (off >> 4); };
+  const uint32_t idA = idesc_bf16(128, 64, 1, 0);  // A MN-major (feature rows), B K-major
+  const uint32_t idB = idesc_bf16(128, 64, 0, 1);  // A K-major, B MN-major
+  const uint32_t idC = idesc_bf16(128, 64, 1, 1);  // both MN-major
+  const uint32_t idD = idesc_bf16(128, 64, 0, 0);  // both K-major
+  uint32_t ph = 0;                                 // parity of bar_mma
+
+  // ---- tile copies of chunk w into layout `lay` (tid 0)
+  struct Item {
+    int64_t c, h, b, hq, im, t0;
+  };
+  auto item_of = [&](int64_t w) {
+    Item it;
+    it.c = w % ar.NC;
+    it.h = (w / ar.NC) % ar.H;
+    it.b = w / (ar.NC * ar.H);
+    it.hq = it.h / ar.r;
+    it.im = (it.b * ar.H + it.h) * ar.NC + it.c;
+    it.t0 = it.c * 64;
+    return it;
+  };
+  auto arm = [&](int l, int g, uint32_t bytes) {
+    mbar_arrive_expect_tx(bars + 3 * l + g, bytes);
+    armed |= 1u << (3 * l + g);
+  };
+  auto tile2 = [&](uint32_t dst, const CUtensorMap* m, int64_t head, const Item& it, uint64_t* bar) {
+    for (int at = 0; at < 2; ++at)
+      tma_load_4d(sm + dst + at * 8192, m, at * 64, (int)head, (int)it.t0, (int)it.b, bar);
+  };
+  auto ld_qk = [&](const Item& it, const Lay& L, int l) {
+    arm(l, GQK, 2 * 16384u);
+    tile2(L.q, &mq, it.hq, it, bars + 3 * l + GQK);
+    tile2(L.k, &mk, it.hq, it, bars + 3 * l + GQK);
+  };
+  auto ld_s = [&](const Item& it, const Lay& L, int l) {
+    bulk_load(sm + L.s, ar.hc + it.im * 32768, 32768, bars + 3 * l + GA);
+  };
+  auto ld_ds = [&](const Item& it, const Lay& L, int l) {
+    bulk_load(sm + L.ds0, ar.dhc + it.im * 32768, 16384, bars + 3 * l + GA);
+    bulk_load(sm + L.ds1, ar.dhc + it.im * 32768 + 16384, 16384, bars + 3 * l + GA);
+  };
+  auto ld_w = [&](const Item& it, const Lay& L, int l) {
+    bulk_load(sm + L.w, ar.wim + it.im * 16384, 16384, bars + 3 * l + GA);
+  };
+  auto ld_do = [&](const Item& it, const Lay& L, int l) { tile2(L.dO, &mdo, it.h, it, bars + 3 * l + GA); };
+  auto ld_p = [&](const Item& it, const Lay& L, int l) {
+    bulk_load(sm + L.p, ar.pim + it.im * 8192, 8192, bars + 3 * l + GA);
+  };
+  auto ld_u = [&](const Item& it, const Lay& L, int l) {
+    bulk_load(sm + L.u, ar.uim + it.im * 16384, 16384, bars + 3 * l + GB);
+  };
+  auto ld_t = [&](const Item& it, const Lay& L, int l) {
+    bulk_load(sm + L.t, ar.tim + it.im * 8192, 8192, bars + 3 * l + GB);
+  };
+  auto ld_v = [&](const Item& it, const Lay& L, int l) { tile2(L.v, &mv, it.h, it, bars + 3 * l + GB); };
+  constexpr uint32_t kBytesA = 32768u + 32768u + 16384u + 16384u + 8192u;  // S, dS, W, dO, P
+  constexpr uint32_t kBytesB = 16384u + 8192u + 16384u;                    // U, T, V
+
+  // Gates of chunk `it` into buffer dst (G, gamma, beta, Kt at 0, 64, 128, 192), by warps 2
+  // and 3 (token = tid - 64) while the rest of the CTA works.
+  auto gates = [&](const Item& it, float* dst) {
+    const int t = tid - 64;
+    int64_t Lg = ar.T;
+    if (ar.valid_len) {
+      Lg = ar.valid_len[it.b];
+      if (Lg < 0 || Lg > ar.T) Lg = Lg < 0 ? 0 : ar.T;
     }
-    mbar_arrive_expect_tx(bar_a, 2 * 32768u + 2 * 16384u + 8192u);
-    bulk_load(sm + R_S, ar.hc + im * 32768, 32768, bar_a);
-    bulk_load(sm + R_W, ar.wim + im * 16384, 16384, bar_a);
-    bulk_load(sm + R_DS, ar.dhc + im * 32768, 32768, bar_a);
-    for (int at = 0; at < 2; ++at)
-      tma_load_4d(sm + R_DO + at * 8192, &mdo, at * 64, (int)h, (int)t0, (int)b, bar_a);
-    bulk_load(sm + R_P, ar.pim + im * 8192, 8192, bar_a);
-    mbar_arrive_expect_tx(bar_b, 2 * 16384u + 8192u);
-    bulk_load(sm + R_U, ar.uim + im * 16384, 16384, bar_b);
-    bulk_load(sm + R_T, ar.tim + im * 8192, 8192, bar_b);
-    for (int at = 0; at < 2; ++at)
-      tma_load_4d(sm + R_V + at * 8192, &mv, at * 64, (int)h, (int)t0, (int)b, bar_b);
-  }
-  if (tid < 64) {
-    const int64_t t = t0 + tid;
     float g = 0.f, be = 0.f;
-    if (t < L) {
-      const int64_t gi = (b * ar.Ts + t) * ar.H + h;
-      const float x = __bfloat162float(ar.a[gi]) + ar.dt_bias[h];
+    if (it.t0 + t < Lg) {
+      const int64_t gi = (it.b * ar.Ts + it.t0 + t) * ar.H + it.h;
+      const float x = __bfloat162float(ar.a[gi]) + ar.dt_bias[it.h];
       const float sp = x > 20.f ? x : log1pf(expf(x));
-      g = -expf(ar.A_log[h]) * sp;
+      g = -expf(ar.A_log[it.h]) * sp;
       be = 1.f / (1.f + expf(-__bfloat162float(ar.b[gi])));
     }
-    sG[tid] = g * kLog2e;
-    sBeta[tid] = be;
-  }
-  __syncthreads();
-  cumsum64f(sG);
-  __syncthreads();
-  if (tid < 64) {
-    sGam[tid] = exp2f(sG[tid]);
-    sKt[tid] = dexp_(sG[63], sG[tid]);
-  }
-  if (!mbar_wait(bar_qk, 0, ar.status, kStatusTimeout)) *s_abort = 1;
-  // q, k rows normalised in place (16 threads per row); padded dO rows zeroed
-  for (int it = 0; it < 4; ++it) {
-    const int rr = (tid >> 4) + 32 * it;
-    const bool isk = rr >= 64;
-    const int sub = tid & 15, at = sub >> 3, ch = sub & 7, r6 = rr & 63;
-    const uint32_t off = (isk ? R_K : R_Q) + at * 8192 + kmaj_chunk(r6, ch);
-    float x[8];
-    ld_chunk(sm, off, x);
-    float ss = 0.f;
+    float v = g * kLog2e;  // inclusive scan over the 64 tokens
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    float s = ar.l2norm ? rsqrtf(ss + ar.eps) : 1.f;
-    if (!isk) s *= ar.scale;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] *= s;
-    st_chunk(sm, off, x);
-  }
-  if (!mbar_wait(bar_a, 0, ar.status, kStatusTimeout)) *s_abort = 1;
-  if (t0 + 64 > L) {
-    for (int idx = tid; idx < 1024; idx += GT) {
-      const int i = idx >> 4, cc = idx & 15;
-      if (t0 + i >= L)
-        *reinterpret_cast<uint4*>(sm + R_DO + (cc >> 3) * 8192 + kmaj_chunk(i, cc & 7)) = make_uint4(0, 0, 0, 0);
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
     }
+    if (t == 31) dst[255] = v;  // Kt slot of token 63: scratch for the first half's total
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    if (t >= 32) v += dst[255];
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    dst[t] = v;
+    dst[64 + t] = exp2f(v);
+    dst[128 + t] = be;
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    dst[192 + t] = dexp_(dst[63], v);
+  };
+
+  if (warp == 2 || warp == 3) gates(item_of(blockIdx.x), sGate);
+  if (tid == 0 && blockIdx.x < ar.NW) {  // every tile of the first chunk
+    const Item it = item_of(blockIdx.x);
+    const Lay L = layout_of(0);
+    ld_qk(it, L, 0);
+    arm(0, GA, kBytesA);
+    ld_s(it, L, 0);
+    ld_w(it, L, 0);
+    ld_ds(it, L, 0);
+    ld_do(it, L, 0);
+    ld_p(it, L, 0);
+    arm(0, GB, kBytesB);
+    ld_u(it, L, 0);
+    ld_t(it, L, 0);
+    ld_v(it, L, 0);
   }
-  {
-    // Descriptors of every operand tile: the start address sits in the low 14 bits
-    // (address >> 4), so a tile at byte offset `off` is the base descriptor + off / 16.
-    const uint64_t d16 = sdesc(base, 16, 1024), d8192 = sdesc(base, 8192, 1024),
-                   d16384 = sdesc(base, 16384, 1024);
-    auto dsc16 = [&](uint32_t off) { return d16 + (off >> 4); };
-    auto dsc8192 = [&](uint32_t off) { return d8192 + (off >> 4); };
-    auto dsc16384 = [&](uint32_t off) { return d16384 + (off >> 4); };
-    uint32_t ph = 0;
+
+  for (int64_t w = blockIdx.x, k = 0; w < ar.NW; w += gridDim.x, ++k) {
+    const int lc = (int)(k & 1), ln = lc ^ 1;
+    const uint32_t bpar = (uint32_t)((k >> 1) & 1);  // phase parity of this layout's barriers
+    const Lay L = layout_of(lc);
+    const Lay N = layout_of(ln);
+    const Item it = item_of(w);
+    const bool more = w + gridDim.x < ar.NW;
+    const Item nx = item_of(more ? w + gridDim.x : w);
+    const int64_t h = it.h, b = it.b, t0 = it.t0;
+    int64_t L_len = ar.T;
+    if (ar.valid_len) {
+      L_len = ar.valid_len[b];
+      if (L_len < 0 || L_len > ar.T) L_len = L_len < 0 ? 0 : ar.T;
+    }
+    const uint32_t dsl = L.ds1 - L.ds0;  // atom stride of the dS image
+    const uint64_t dds = sdesc(base, dsl, 1024);
+    auto dscDS = [&](uint32_t off) { return dds + (off >> 4); };
+
+    float* sG = sGate + lc * 256;  // this chunk's gates (written during the previous chunk)
+    float* sGam = sG + 64;
+    float* sBeta = sG + 128;
+    float* sKt = sG + 192;
+    __syncthreads();  // the previous chunk's scalars have been consumed, these gates written
+    if (tid == 0 && k > 0) {  // tiles of this chunk that waited for the previous stores
+      bulk_wait_read();  // the previous chunk's dv, dq, dk stores have read their slots
+      if (lc == 1)
+        ld_v(it, L, lc);  // where the dv staging was
+      else
+        ld_u(it, L, lc);  // where the dq staging was
+    }
+    if (!mbar_wait(bars + 3 * lc + GQK, bpar, ar.status, kStatusTimeout)) *s_abort = 1;
+    // q, k rows normalised in place (16 threads per row); padded dO rows zeroed
+    for (int i4 = 0; i4 < 4; ++i4) {
+      const int rr = (tid >> 4) + 32 * i4;
+      const bool isk = rr >= 64;
+      const int sub = tid & 15, at = sub >> 3, ch = sub & 7, r6 = rr & 63;
+      const uint32_t off = (isk ? L.k : L.q) + at * 8192 + kmaj_chunk(r6, ch);
+      float x[8];
+      ld_chunk(sm, off, x);
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      float sc = ar.l2norm ? rsqrtf(ss + ar.eps) : 1.f;
+      if (!isk) sc *= ar.scale;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] *= sc;
+      st_chunk(sm, off, x);
+    }
+    if (!mbar_wait(bars + 3 * lc + GA, bpar, ar.status, kStatusTimeout)) *s_abort = 1;
+    if (tid == 0) armed &= ~((1u << (3 * lc + GQK)) | (1u << (3 * lc + GA)));
+    if (t0 + 64 > L_len) {
+      for (int idx = tid; idx < 1024; idx += GT) {
+        const int i = idx >> 4, cc = idx & 15;
+        if (t0 + i >= L_len)
+          *reinterpret_cast<uint4*>(sm + L.dO + (cc >> 3) * 8192 + kmaj_chunk(i, cc & 7)) = make_uint4(0, 0, 0, 0);
+      }
+    }
     float dqT[16], dkT[16];  // this thread's feature row fr of dq_hat^T, dk_hat^T, tokens cb + e
-    const uint32_t idA = idesc_bf16(128, 64, 1, 0);  // A MN-major (feature rows), B K-major
-    const uint32_t idB = idesc_bf16(128, 64, 0, 1);  // A K-major, B MN-major
-    const uint32_t idC = idesc_bf16(128, 64, 1, 1);  // both MN-major
-    const uint32_t idD = idesc_bf16(128, 64, 0, 0);  // both K-major
     GRAD_SYNC();
     // ---- round A: S^T W^T -> [0,64), dO^T P -> [64,128), dS^T K^T -> [128,192),
     //      S dO^T -> [192,256), K K^T -> [256,320) (M = 64; read in round C's epilogue)
-    if (tid == 0) {
-      const uint32_t id64d = idesc_bf16(64, 64, 0, 0);
-      for (int ks = 0; ks < 8; ++ks) {  // K = dk (S^T W^T, dS^T K^T, K K^T) or dv (S dO^T)
-        const uint32_t at = ks >> 2, kk = ks & 3;
-        mma_bf16(tmem, dsc16384(R_S + ks * 2048),
-                 dsc16(R_W + at * 8192 + kk * 32), idA, ks > 0);
-        mma_bf16(tmem + 128, dsc16384(R_DS + ks * 2048),
-                 dsc16(R_K + at * 8192 + kk * 32), idA, ks > 0);
-        mma_bf16(tmem + 192, dsc16(R_S + at * 16384 + kk * 32),
-                 dsc16(R_DO + at * 8192 + kk * 32), idD, ks > 0);
-        mma_bf16(tmem + 256, dsc16(R_K + at * 8192 + kk * 32),
-                 dsc16(R_K + at * 8192 + kk * 32), id64d, ks > 0);
+    // (one thread per product: a single thread issues tcgen05.mma at a far lower rate than
+    // the tensor core retires these small shapes)
+    if (issuer) {
+      if (warp == 0) {
+        for (int ks = 0; ks < 8; ++ks)  // K = dk
+          mma_bf16(tmem, dsc16384(L.s + ks * 2048), dsc16(L.w + (ks >> 2) * 8192 + (ks & 3) * 32),
+                   idA, ks > 0);
+      } else if (warp == 1) {
+        for (int ks = 0; ks < 8; ++ks)  // K = dk
+          mma_bf16(tmem + 128, dscDS(L.ds0 + ks * 2048),
+                   dsc16(L.k + (ks >> 2) * 8192 + (ks & 3) * 32), idA, ks > 0);
+      } else if (warp == 2) {
+        for (int ks = 0; ks < 8; ++ks)  // K = dv
+          mma_bf16(tmem + 192, dsc16(L.s + (ks >> 2) * 16384 + (ks & 3) * 32),
+                   dsc16(L.dO + (ks >> 2) * 8192 + (ks & 3) * 32), idD, ks > 0);
+      } else {
+        const uint32_t id64d = idesc_bf16(64, 64, 0, 0);
+        for (int ks = 0; ks < 8; ++ks) {  // K = dk
+          const uint64_t d = dsc16(L.k + (ks >> 2) * 8192 + (ks & 3) * 32);
+          mma_bf16(tmem + 256, d, d, id64d, ks > 0);
+        }
+        for (int ks = 0; ks < 4; ++ks)  // K = tokens
+          mma_bf16(tmem + 64, dsc8192(L.dO + ks * 2048), dsc8192(L.p + ks * 2048), idC, ks > 0);
       }
-      for (int ks = 0; ks < 4; ++ks)  // K = tokens
-        mma_bf16(tmem + 64, dsc8192(R_DO + ks * 2048),
-                 dsc8192(R_P + ks * 2048), idC, ks > 0);
       mma_commit(bar_mma);
     }
     {  // <S, dS> (same tile layout): warp partials into sMisc
       float acc = 0.f;
       for (int q = tid; q < 2048; q += GT) {
         float x[8], y[8];
-        ld_chunk(sm + R_S, q * 16, x);
-        ld_chunk(sm + R_DS, q * 16, y);
+        ld_chunk(sm + L.s, q * 16, x);
+        ld_chunk(sm + ((q < 1024) ? L.ds0 : L.ds1) + (q & 1023) * 16, 0, y);
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc = fmaf(x[e], y[e], acc);
       }
@@ -312,7 +428,8 @@ __global__ void __launch_bounds__(GT, 1)
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (lane == 0) sMisc[warp] = acc;
     }
-    if (!mbar_wait(bar_b, 0, ar.status, kStatusTimeout)) *s_abort = 1;
+    if (!mbar_wait(bars + 3 * lc + GB, bpar, ar.status, kStatusTimeout)) *s_abort = 1;
+    if (tid == 0) armed &= ~(1u << (3 * lc + GB));
     if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
     ph ^= 1;
     tc_fence_after();
@@ -326,32 +443,37 @@ __global__ void __launch_bounds__(GT, 1)
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
-        ws[e] = ld_bf(sm + R_U + tf_off(t, f)) - ws[e];   // V'^T
-        a1[e] = fmaf(sKt[t], a2[e], a1[e]);                 // dV'^T
+        ws[e] = ld_bf(sm + L.u + tf_off(t, f)) - ws[e];   // V'^T
+        a1[e] = fmaf(sKt[t], a2[e], a1[e]);                // dV'^T
       }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        st_chunk(sm + R_VT, kmaj_chunk(f, 2 * part + cc), &ws[cc * 8]);
-        st_chunk(sm + R_DVT, kmaj_chunk(f, 2 * part + cc), &a1[cc * 8]);
+        st_chunk(sm + L.vt, kmaj_chunk(f, 2 * part + cc), &ws[cc * 8]);
+        st_chunk(sm + L.dvt, kmaj_chunk(f, 2 * part + cc), &a1[cc * 8]);
       }
     }
+    if (tid == 0) bulk_wait_read();  // the previous chunk's dq/dk/dv stores have read their slots
     GRAD_SYNC();
     // ---- round B: S dV'^T -> [0,64) (-dW^T), dS V'^T -> [64,128), dV'^T T -> [128,192) (X_v^T),
     //      dO V'^T -> [192,256) (dP, M = 64)
-    if (tid == 0) {
-      const uint32_t id64b = idesc_bf16(64, 64, 0, 1);
-      for (int ks = 0; ks < 8; ++ks) {  // K = dv
-        const uint32_t at = ks >> 2, kk = ks & 3;
-        mma_bf16(tmem, dsc16(R_S + at * 16384 + kk * 32),
-                 dsc8192(R_DVT + ks * 2048), idB, ks > 0);
-        mma_bf16(tmem + 64, dsc16(R_DS + at * 16384 + kk * 32),
-                 dsc8192(R_VT + ks * 2048), idB, ks > 0);
-        mma_bf16(tmem + 192, dsc16(R_DO + at * 8192 + kk * 32),
-                 dsc8192(R_VT + ks * 2048), id64b, ks > 0);
+    if (issuer) {
+      if (warp == 0) {
+        for (int ks = 0; ks < 8; ++ks)  // K = dv
+          mma_bf16(tmem, dsc16(L.s + (ks >> 2) * 16384 + (ks & 3) * 32),
+                   dsc8192(L.dvt + ks * 2048), idB, ks > 0);
+      } else if (warp == 1) {
+        for (int ks = 0; ks < 8; ++ks)  // K = dv
+          mma_bf16(tmem + 64, dsc16(((ks >> 2) ? L.ds1 : L.ds0) + (ks & 3) * 32),
+                   dsc8192(L.vt + ks * 2048), idB, ks > 0);
+      } else if (warp == 2) {
+        const uint32_t id64b = idesc_bf16(64, 64, 0, 1);
+        for (int ks = 0; ks < 8; ++ks)  // K = dv
+          mma_bf16(tmem + 192, dsc16(L.dO + (ks >> 2) * 8192 + (ks & 3) * 32),
+                   dsc8192(L.vt + ks * 2048), id64b, ks > 0);
+      } else {
+        for (int ks = 0; ks < 4; ++ks)  // K = tokens
+          mma_bf16(tmem + 128, dsc16(L.dvt + ks * 32), dsc8192(L.t + ks * 2048), idB, ks > 0);
       }
-      for (int ks = 0; ks < 4; ++ks)  // K = tokens
-        mma_bf16(tmem + 128, dsc16(R_DVT + ks * 32),
-                 dsc8192(R_T + ks * 2048), idB, ks > 0);
       mma_commit(bar_mma);
     }
     {  // while round B runs: (diag(gamma) dO S^T)^T and q_t . (gamma_t S dO_t)
@@ -361,7 +483,7 @@ __global__ void __launch_bounds__(GT, 1)
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
         dqT[e] *= sGam[t];
-        pq[e] = ld_bf(sm + R_Q + tf_off(t, f)) * dqT[e];
+        pq[e] = ld_bf(sm + L.q + tf_off(t, f)) * dqT[e];
       }
       const float red = xreduce16(pq, lane);
       if (lane < 16) sRed[(RQ * 4 + quad) * 64 + cb + lane] = red;
@@ -369,6 +491,11 @@ __global__ void __launch_bounds__(GT, 1)
     if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
     ph ^= 1;
     tc_fence_after();
+    if (tid == 0 && more) {  // S and dV'^T are consumed: the next chunk's S (and dO)
+      arm(ln, GA, kBytesA);
+      ld_s(nx, N, ln);
+      if (lc == 0) ld_do(nx, N, ln);
+    }
     {  // -dW^T, X_v^T and dP o Gamma: the operands of round C
       const int f = fr;
       float x[16];
@@ -376,46 +503,52 @@ __global__ void __launch_bounds__(GT, 1)
 #pragma unroll
       for (int e = 0; e < 16; ++e) x[e] = -x[e];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) st_chunk(sm + R_W, kmaj_chunk(f, 2 * part + cc), &x[cc * 8]);
+      for (int cc = 0; cc < 2; ++cc) st_chunk(sm + L.w, kmaj_chunk(f, 2 * part + cc), &x[cc * 8]);
       tmem_ld16(tmem + lane_off + 128 + cb, x);            // X_v^T
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) st_chunk(sm + R_U, kmaj_chunk(f, 2 * part + cc), &x[cc * 8]);
-      float dp[16];
+      for (int cc = 0; cc < 2; ++cc) st_chunk(sm + L.u, kmaj_chunk(f, 2 * part + cc), &x[cc * 8]);
+      float dp[16], z[16];
       tmem_ld16(tmem + lane_off + 192 + cb, dp);           // dP (M = 64 layout)
-      if (own64) {
-        const int i = ri;
-        float pv[16];
+      const int i = ri;
+      float pv[16];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) ld_chunk(sm + R_P, kmaj_chunk(i, 2 * part + cc), &pv[cc * 8]);
+      for (int cc = 0; cc < 2; ++cc) ld_chunk(sm + L.p, kmaj_chunk(i, 2 * part + cc), &pv[cc * 8]);
+      float zr = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          float y[8];
+      for (int cc = 0; cc < 2; ++cc) {
+        float y[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = cb + cc * 8 + e;
-            const float dpv = (j <= i) ? dp[cc * 8 + e] : 0.f;
-            sZb[zoff(i, j)] = dpv * pv[cc * 8 + e];                 // dP o P
-            y[e] = (j <= i) ? dpv * dexp_(sG[i], sG[j]) : 0.f;      // dP o Gamma
-          }
-          st_chunk(sm + R_P, kmaj_chunk(i, 2 * part + cc), y);       // over P (this thread's)
+        for (int e = 0; e < 8; ++e) {
+          const int j = cb + cc * 8 + e;
+          const float dpv = (own64 && j <= i) ? dp[cc * 8 + e] : 0.f;
+          z[cc * 8 + e] = dpv * pv[cc * 8 + e];                  // dP o P
+          zr += z[cc * 8 + e];
+          y[e] = (j <= i) ? dpv * dexp_(sG[i], sG[j]) : 0.f;    // dP o Gamma
         }
+        if (own64) st_chunk(sm + L.p, kmaj_chunk(i, 2 * part + cc), y);  // over P (this thread's)
+      }
+      const float zc = xreduce_half(z, lane);  // column cb + lane of dP o P over this quadrant's rows
+      if (own64) {
+        sZr[part * 64 + i] = zr;
+        sZc[quad * 64 + cb + lane] = zc;
       }
     }
     GRAD_SYNC();
     // ---- round C: dW^T T -> [320,384) (X_w^T), K^T (dP o Gamma)^T -> [384,448),
     //      X_v V'^T -> [448,512) (dA', M = 64); K K^T stays in [256,320)
-    if (tid == 0) {
-      const uint32_t id64c = idesc_bf16(64, 64, 1, 1);
-      for (int ks = 0; ks < 4; ++ks) {  // K = tokens
-        mma_bf16(tmem + 320, dsc16(R_W + ks * 32),
-                 dsc8192(R_T + ks * 2048), idB, ks > 0);
-        mma_bf16(tmem + 384, dsc8192(R_K + ks * 2048),
-                 dsc16(R_P + ks * 32), idA, ks > 0);
+    if (issuer) {
+      if (warp == 0) {
+        for (int ks = 0; ks < 4; ++ks)  // K = tokens
+          mma_bf16(tmem + 320, dsc16(L.w + ks * 32), dsc8192(L.t + ks * 2048), idB, ks > 0);
+      } else if (warp == 1) {
+        for (int ks = 0; ks < 4; ++ks)  // K = tokens
+          mma_bf16(tmem + 384, dsc8192(L.k + ks * 2048), dsc16(L.p + ks * 32), idA, ks > 0);
+      } else if (warp == 2) {
+        const uint32_t id64c = idesc_bf16(64, 64, 1, 1);
+        for (int ks = 0; ks < 8; ++ks)  // K = dv
+          mma_bf16(tmem + 448, dsc8192(L.u + ks * 2048), dsc8192(L.vt + ks * 2048), id64c, ks > 0);
       }
-      for (int ks = 0; ks < 8; ++ks)  // K = dv
-        mma_bf16(tmem + 448, dsc8192(R_U + ks * 2048),
-                 dsc8192(R_VT + ks * 2048), id64c, ks > 0);
-      mma_commit(bar_mma);
+      mma_commit(bar_mma);  // warp 3 has nothing to issue: its commit arrives at once
     }
     {  // while round C runs: Kt part of dk, dv, and the row dots of V' dS^T and X_v
       const int f = fr;
@@ -425,7 +558,7 @@ __global__ void __launch_bounds__(GT, 1)
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
         dkT[e] = sKt[t] * x[e];
-        pk[e] = ld_bf(sm + R_K + tf_off(t, f)) * x[e];    // k_t . (V' dS^T)_t
+        pk[e] = ld_bf(sm + L.k + tf_off(t, f)) * x[e];    // k_t . (V' dS^T)_t
       }
       float red = xreduce16(pk, lane);
       if (lane < 16) sRed[(RKD * 4 + quad) * 64 + cb + lane] = red;
@@ -433,67 +566,81 @@ __global__ void __launch_bounds__(GT, 1)
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
-        pk[e] = ld_bf(sm + R_V + tf_off(t, f)) * x[e];    // v_t . X_v,t
-        st_bf(sm + R_DO + tf_off(t, f), (t0 + t < L) ? sBeta[t] * x[e] : 0.f);  // dv staging
+        pk[e] = ld_bf(sm + L.v + tf_off(t, f)) * x[e];    // v_t . X_v,t
+        st_bf(sm + L.dO + tf_off(t, f), (t0 + t < L_len) ? sBeta[t] * x[e] : 0.f);  // dv staging
       }
       red = xreduce16(pk, lane);
       if (lane < 16) sRed[(RV * 4 + quad) * 64 + cb + lane] = red;
     }
-    {  // gate terms of P: sum_j Z_ij - sum_j Z_ji, 8 column parts of 8
-      const int i = tid & 63, p8 = tid >> 6;
-      float acc = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = p8 * 8 + e;
-        acc += sZb[zoff(i, j)] - sZb[zoff(j, i)];
-      }
-      sPart[p8 * 64 + i] = acc;
-    }
     if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
     ph ^= 1;
     tc_fence_after();
+    if (tid == 0 && more) {  // dW^T, X_v^T and V'^T (and dV'^T) are consumed: next W and dS
+      ld_w(nx, N, ln);
+      ld_ds(nx, N, ln);
+      if (lc == 1) {
+        arm(ln, GB, kBytesB);
+        ld_v(nx, N, ln);
+      }
+    }
     {  // E (operand of round D), dA o A, dbeta terms of A
-      float da[16], kk[16];
+      float da[16], kk[16], z[16];
       tmem_ld16(tmem + lane_off + 448 + cb, da);           // dA' (M = 64 layout)
       tmem_ld16(tmem + lane_off + 256 + cb, kk);           // K K^T (M = 64 layout)
-      if (own64) {
-        const int i = ri;
-        const float be = sBeta[i];
-        float pt = 0.f;
+      const int i = ri;
+      const float be = sBeta[i];
+      float pt = 0.f, zr = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          float ex[8];
+      for (int cc = 0; cc < 2; ++cc) {
+        float ex[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = cb + cc * 8 + e;
-            const float gmm = (j < i) ? dexp_(sG[i], sG[j]) : 0.f;
-            const float dA = (j < i) ? -da[cc * 8 + e] : 0.f;
-            const float kg = kk[cc * 8 + e] * gmm;
-            pt = fmaf(dA, kg, pt);                     // dbeta: dA (k_i . k_j) Gamma
-            sZc[zoff(i, j)] = dA * be * kg;            // dA o A
-            ex[e] = dA * be * gmm;                     // E
-          }
-          st_chunk(sm + R_T, kmaj_chunk(i, 2 * part + cc), ex);   // E over T
+        for (int e = 0; e < 8; ++e) {
+          const int j = cb + cc * 8 + e;
+          const bool lo = own64 && j < i;
+          const float gmm = lo ? dexp_(sG[i], sG[j]) : 0.f;
+          const float dA = lo ? -da[cc * 8 + e] : 0.f;
+          const float kg = kk[cc * 8 + e] * gmm;
+          pt = fmaf(dA, kg, pt);                       // dbeta: dA (k_i . k_j) Gamma
+          z[cc * 8 + e] = dA * be * kg;                // dA o A
+          zr += z[cc * 8 + e];
+          ex[e] = dA * be * gmm;                       // E
         }
+        if (own64) st_chunk(sm + L.t, kmaj_chunk(i, 2 * part + cc), ex);   // E over T
+      }
+      const float zc = xreduce_half(z, lane);
+      if (own64) {
         sDBh[part * 64 + i] = pt;
+        sZr[part * 64 + i] += zr;
+        sZc[quad * 64 + cb + lane] += zc;
       }
     }
     GRAD_SYNC();
-    // ---- round D: Q^T (dP o Gamma) + K^T E^T + K^T E -> [0,64)
+    // ---- round D: Q^T (dP o Gamma) -> [0,64), K^T E^T -> [64,128), K^T E -> [128,192)
+    //      (three products from three warps, summed in the epilogue)
     if (tid == 0) {
-      tma_store_4d(&mdv, sm + R_DO, 0, (int)h, (int)t0, (int)b);  // dv tile (clipped past T)
-      tma_store_4d(&mdv, sm + R_DO + 8192, 64, (int)h, (int)t0, (int)b);
+      tma_store_4d(&mdv, sm + L.dO, 0, (int)h, (int)t0, (int)b);  // dv tile (clipped past T)
+      tma_store_4d(&mdv, sm + L.dO + 8192, 64, (int)h, (int)t0, (int)b);
       bulk_commit();
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem, dsc8192(R_Q + ks * 2048),
-                 dsc8192(R_P + ks * 2048), idC, ks > 0);
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem, dsc8192(R_K + ks * 2048),
-                 dsc16(R_T + ks * 32), idA, 1);
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem, dsc8192(R_K + ks * 2048),
-                 dsc8192(R_T + ks * 2048), idC, 1);
+    }
+    if (issuer) {
+      if (warp == 0) {
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem, dsc8192(L.q + ks * 2048), dsc8192(L.p + ks * 2048), idC, ks > 0);
+      } else if (warp == 1) {
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + 64, dsc8192(L.k + ks * 2048), dsc16(L.t + ks * 32), idA, ks > 0);
+      } else if (warp == 2) {
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + 128, dsc8192(L.k + ks * 2048), dsc8192(L.t + ks * 2048), idC, ks > 0);
+      }
       mma_commit(bar_mma);
+    }
+    if (tid == 0) {
+      if (more && lc == 0) {  // V (read before the last barrier) is consumed: the next U
+        arm(ln, GB, kBytesB);
+        ld_u(nx, N, ln);
+      }
+      if (more && lc == 1) ld_do(nx, N, ln);  // ... and, the other way round, the next dO
     }
     {  // while round D runs: X_w part of dk, dq_hat staging, row dots of X_w
       const int f = fr;
@@ -504,7 +651,7 @@ __global__ void __launch_bounds__(GT, 1)
         const int t = cb + e;
         const float bg = sBeta[t] * sGam[t];
         dkT[e] = fmaf(bg, x[e], dkT[e]);
-        pk[e] = ld_bf(sm + R_K + tf_off(t, f)) * x[e];    // k_t . X_w,t
+        pk[e] = ld_bf(sm + L.k + tf_off(t, f)) * x[e];    // k_t . X_w,t
       }
       const float red = xreduce16(pk, lane);
       if (lane < 16) sRed[(RKW * 4 + quad) * 64 + cb + lane] = red;
@@ -512,41 +659,41 @@ __global__ void __launch_bounds__(GT, 1)
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
-        st_bf(sm + R_DS + tf_off(t, f), (t0 + t < L) ? dqT[e] + x[e] : 0.f);  // dq_hat staging
+        st_bf(sm + L.ds0 + tf_off(t, f), (t0 + t < L_len) ? dqT[e] + x[e] : 0.f);  // dq_hat staging
       }
-    }
-    {  // gate terms of A, added to this thread's slot of the P terms
-      const int i = tid & 63, p8 = tid >> 6;
-      float acc = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = p8 * 8 + e;
-        acc += sZc[zoff(i, j)] - sZc[zoff(j, i)];
-      }
-      sPart[p8 * 64 + i] += acc;
     }
     if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
     ph ^= 1;
     tc_fence_after();
+    if (tid == 0 && more) {  // P (dP o Gamma) and T (E) are consumed
+      ld_p(nx, N, ln);
+      ld_t(nx, N, ln);
+    }
     {
       const int f = fr;
-      float x[16];
+      float x[16], y[16];
       tmem_ld16(tmem + lane_off + cb, x);
+      tmem_ld16(tmem + lane_off + 64 + cb, y);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) dkT[e] += x[e] + y[e];
+      tmem_ld16(tmem + lane_off + 128 + cb, x);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
-        st_bf(sm + R_DS + 16384 + tf_off(t, f), (t0 + t < L) ? dkT[e] + x[e] : 0.f);  // dk_hat
+        st_bf(sm + L.ds1 + tf_off(t, f), (t0 + t < L_len) ? dkT[e] + x[e] : 0.f);  // dk_hat
       }
     }
     GRAD_SYNC();
     if (tid == 0) {
-      tma_store_4d(&mdqp, sm + R_DS, 0, (int)h, (int)t0, (int)b);  // dq_hat tile
-      tma_store_4d(&mdqp, sm + R_DS + 8192, 64, (int)h, (int)t0, (int)b);
-      tma_store_4d(&mdkp, sm + R_DS + 16384, 0, (int)h, (int)t0, (int)b);
-      tma_store_4d(&mdkp, sm + R_DS + 16384 + 8192, 64, (int)h, (int)t0, (int)b);
+      tma_store_4d(&mdqp, sm + L.ds0, 0, (int)h, (int)t0, (int)b);  // dq_hat tile
+      tma_store_4d(&mdqp, sm + L.ds0 + 8192, 64, (int)h, (int)t0, (int)b);
+      tma_store_4d(&mdkp, sm + L.ds1, 0, (int)h, (int)t0, (int)b);
+      tma_store_4d(&mdkp, sm + L.ds1 + 8192, 64, (int)h, (int)t0, (int)b);
       bulk_commit();
+      if (more) ld_qk(nx, N, ln);  // q and k are consumed (round D and the dots above)
     }
-    // ---- gate gradients: column sums of the four row dots, Kt terms, state term
+    // ---- gate gradients: column sums of the four row dots, Kt terms, state term; the
+    //      next chunk's gates meanwhile (warps 2, 3)
     if (tid < 64) {
       const int t = tid;
       float rq = 0.f, rv = 0.f, rkw = 0.f, rkd = 0.f, zp = 0.f;
@@ -556,9 +703,8 @@ __global__ void __launch_bounds__(GT, 1)
         rv += sRed[(RV * 4 + qd) * 64 + t];
         rkw += sRed[(RKW * 4 + qd) * 64 + t];
         rkd += sRed[(RKD * 4 + qd) * 64 + t];
+        zp += sZr[qd * 64 + t] - sZc[qd * 64 + t];  // row sums minus column sums of Z
       }
-#pragma unroll
-      for (int p8 = 0; p8 < 8; ++p8) zp += sPart[p8 * 64 + t];
       const float be = sBeta[t], gm = sGam[t];
       const float s_t = sKt[t] * rkd;                       // Kt term of dG_t
       float d = zp + rq + be * gm * rkw;
@@ -566,18 +712,19 @@ __global__ void __launch_bounds__(GT, 1)
       sFin[t] = d;
       sDB[t] = rv + gm * rkw + sDBh[t] + sDBh[64 + t] + sDBh[128 + t] + sDBh[192 + t];
       sRed[t] = (t < 63) ? s_t : 0.f;                       // reuse: Kt terms to sum into dG_C
+    } else if (more && (warp == 2 || warp == 3)) {
+      gates(nx, sGate + ln * 256);
     }
     __syncthreads();
-    if (tid == 0) {
-      float tot = 0.f;
-      for (int i = 0; i < 63; ++i) tot += sRed[i];
-      float sd = 0.f;
-      for (int w = 0; w < GT / 32; ++w) sd += sMisc[w];
-      sFin[63] += tot + sGam[63] * sd;
-    }
-    __syncthreads();
-    if (tid < 32) {  // dg_j = sum_{i >= j} dG_i (reverse cumsum, warp 0)
+    if (tid < 32) {  // dG_C gets the Kt terms and the state term; then dg_j = sum_{i >= j} dG_i
+      float tot = sRed[tid] + sRed[32 + tid], sd = tid < GT / 32 ? sMisc[tid] : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        sd += __shfl_xor_sync(0xffffffffu, sd, o);
+      }
       float v0 = sFin[63 - tid], v1 = sFin[31 - tid];
+      if (tid == 0) v0 += tot + sGam[63] * sd;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float y0 = __shfl_up_sync(0xffffffffu, v0, o);
@@ -588,7 +735,6 @@ __global__ void __launch_bounds__(GT, 1)
         }
       }
       v1 += __shfl_sync(0xffffffffu, v0, 31);
-      __syncwarp();
       sFin[63 - tid] = v0;
       sFin[31 - tid] = v1;
     }
@@ -597,7 +743,7 @@ __global__ void __launch_bounds__(GT, 1)
       const int64_t t = t0 + tid;
       if (t < ar.T) {
         const int64_t gi = (b * ar.Ts + t) * ar.H + h;
-        const bool valid = t < L;
+        const bool valid = t < L_len;
         ar.dg[gi] = valid ? sFin[tid] : 0.f;   // natural-log units (log2 only enters exponents)
         ar.dbeta[gi] = valid ? sDB[tid] : 0.f;
       }
@@ -605,10 +751,13 @@ __global__ void __launch_bounds__(GT, 1)
   }
 done:
   if (tid == 0) bulk_wait_all();
-  if (*s_abort && tid == 0) {  // let the loads still in flight land before the CTA exits
-    mbar_wait(bar_qk, 0, nullptr, 0);
-    mbar_wait(bar_a, 0, nullptr, 0);
-    mbar_wait(bar_b, 0, nullptr, 0);
+  if (tid == 0 && armed) {  // abort: let every copy still in flight land before the CTA exits
+    for (int i = 0; i < 6; ++i)
+      if (armed & (1u << i)) {
+        // one of the two parities is the phase in flight; the other returns at once
+        mbar_wait(bars + i, 0, nullptr, 0);
+        mbar_wait(bars + i, 1, nullptr, 0);
+      }
   }
   tc_fence_before();
   __syncthreads();
@@ -639,6 +788,7 @@ cudaError_t launch_grad2_tc(const Prob& pr, const Inputs& in, const WS& ws, cons
     return cudaErrorInvalidValue;
   Grad2Args ar;
   ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.r = pr.r; ar.NC = pr.NC; ar.Tp = pr.Tp;
+  ar.NW = pr.B * pr.H * pr.NC;
   ar.l2norm = pr.l2norm; ar.eps = pr.eps; ar.scale = pr.scale;
   ar.a = (const __nv_bfloat16*)in.a; ar.b = (const __nv_bfloat16*)in.b;
   ar.A_log = in.A_log; ar.dt_bias = in.dt_bias; ar.valid_len = in.valid_len;
@@ -649,8 +799,8 @@ cudaError_t launch_grad2_tc(const Prob& pr, const Inputs& in, const WS& ws, cons
   cudaError_t e = cudaFuncSetAttribute(k_grad2_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)GR_SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)pr.NC, (unsigned)pr.H, (unsigned)pr.B);
-  k_grad2_tc<<<grid, GT, GR_SMEM, st>>>(mq, mk, mv, mdo, mdv, mdqp, mdkp, ar);
+  const int64_t nblk = ar.NW < device_sms() ? ar.NW : device_sms();  // one CTA per SM
+  k_grad2_tc<<<(unsigned)nblk, GT, GR_SMEM, st>>>(mq, mk, mv, mdo, mdv, mdqp, mdkp, ar);
   return cudaGetLastError();
 }
 
