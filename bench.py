@@ -117,10 +117,14 @@ def kernel_work(name, w, P):
         if op == "bwd":
             wr += ch * tile_p
         return f * ch, rd + wr
-    if kname == "summary_chain_tc":
-        f = 2 * (mm(C, dv, dk) + mm(dk, dv, C)) * ch * frac   # [M | S] parts
-        byt = ch * frac * (3 * tile + C * 8) + 2 * (P - 1) * B * H * state
+    if kname == "summary_chain_tc":  # gdn_fwd_ctx: [M | S] parts of every segment
+        f = 2 * (mm(C, dv, dk) + mm(dk, dv, C)) * ch
+        byt = ch * (3 * tile + C * 8) + 2 * P * B * H * state
         return f, byt
+    if kname == "grad_summary_tc":   # gdn_bwd_ctx: gradient summaries of segments 1..P-1
+        return kernel_work("bwd.grad_summary_chain_tc", w, P)
+    if kname == "ctx_init":
+        return 0.0, 2 * B * H * state
     if kname == "summary_pair_tc":   # [M | S] of every segment + gradient summaries
         f1 = 2 * (mm(C, dv, dk) + mm(dk, dv, C)) * ch
         b1 = ch * (3 * tile + C * 8) + 2 * P * B * H * state
@@ -369,18 +373,33 @@ def run_ours(args):
     dH0 = torch.empty_like(hT)
     stream = torch.cuda.current_stream()
 
+    ctx = gdn.ctx_buffer(p)
+
     def fwd():
         gdn.gdn_fwd(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["h0"],
                     None, o=o, hT=hT, ws=wsf, problem=p, stream=stream)
 
-    def bwd():
+    def fwd_ctx():  # the training-step forward: also keeps the segment states for the backward
+        gdn.gdn_fwd_ctx(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                        d["h0"], None, ctx=ctx, o=o, hT=hT, ws=wsf, problem=p, stream=stream)
+
+    def bwd_ctx():
+        gdn.gdn_bwd_ctx(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], ctx,
+                        d["dO"], d["dHT"], None, dq=dq, dk=dkk, dv=dvv, dg=dg, dbeta=dbeta,
+                        dH0=dH0, ws=wsb, problem=p, stream=stream)
+
+    def bwd_recompute():  # gdn_bwd: recomputes the segment summaries and their prefix
         gdn.gdn_bwd(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["dO"],
                     d["dHT"], d["h0"], None, dq=dq, dk=dkk, dv=dvv, dg=dg, dbeta=dbeta, dH0=dH0,
                     ws=wsb, problem=p, stream=stream)
 
     def step():
+        fwd_ctx()
+        bwd_ctx()
+
+    def step_recompute():
         fwd()
-        bwd()
+        bwd_recompute()
 
     def timed(fn, steps):
         barrier()
@@ -408,11 +427,12 @@ def run_ours(args):
     clocks = sampler.stop()
     ms_step = max_over_ranks(ms_step)
     ms_fwd = max_over_ranks(timed(fwd, args.steps))
+    ms_recompute = max_over_ranks(timed(step_recompute, args.steps))
     tokens = B * T
     value = job_throughput(ms_step, tokens, world)
 
-    nf = len(gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD))
-    nb = len(gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD))
+    nf = len(gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD_CTX))
+    nb = len(gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD_CTX))
     peaks = load_peaks()
     alg = step_algorithmic(w)
     t_roof_step = max(alg["flops_step"] / (peaks["bf16_tflops_sustained"] * 1e12),
@@ -426,6 +446,10 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(w, args, world),
         "fwd": {"ms": ms_fwd, "tokens_per_s": job_throughput(ms_fwd, tokens, world)},
+        "step": "gdn_fwd_ctx + gdn_bwd_ctx (the backward reads the forward's segment states)",
+        "fwd_bwd_recompute": {"ms": ms_recompute,
+                              "tokens_per_s": job_throughput(ms_recompute, tokens, world),
+                              "calls": "gdn_fwd + gdn_bwd (no context)"},
         "gpu_launches": args.steps * (nf + nb),
         "step_roofline": {
             "flops": alg["flops_step"], "bytes": alg["bytes_step"],
@@ -438,32 +462,31 @@ def run_ours(args):
 
     # Per-kernel CUDA-event timing: K profiled steps made of single-kernel calls.
     if not args.no_kernel_profile:
-        names_f = gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD)
-        names_b = gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD)
+        names_f = gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD_CTX)
+        names_b = gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD_CTX)
         tot = {}
         reps = max(1, args.steps)
-        fwd()
-        bwd()
+        step()
         torch.cuda.synchronize()
-        for op, names in ((gdn.GDN_OP_FWD, names_f), (gdn.GDN_OP_BWD, names_b)):
+        for op, names in ((gdn.GDN_OP_FWD_CTX, names_f), (gdn.GDN_OP_BWD_CTX, names_b)):
             for i, nm in enumerate(names):
                 evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(reps)]
                 for e0, e1 in evs:
                     e0.record(stream)
-                    if op == gdn.GDN_OP_FWD:
-                        gdn.gdn_fwd_kernel(i, d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"],
-                                           d["dt_bias"], d["h0"], None, o, hT, wsf, problem=p,
-                                           stream=stream)
+                    if op == gdn.GDN_OP_FWD_CTX:
+                        gdn.gdn_fwd_ctx_kernel(i, d["q"], d["k"], d["v"], d["a"], d["b"],
+                                               d["A_log"], d["dt_bias"], d["h0"], None, o, hT,
+                                               ctx, wsf, problem=p, stream=stream)
                     else:
-                        gdn.gdn_bwd_kernel(i, d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"],
-                                           d["dt_bias"], d["h0"], None, d["dO"], d["dHT"], dq,
-                                           dkk, dvv, dg, dbeta, dH0, wsb, problem=p,
-                                           stream=stream)
+                        gdn.gdn_bwd_ctx_kernel(i, d["q"], d["k"], d["v"], d["a"], d["b"],
+                                               d["A_log"], d["dt_bias"], ctx, None, d["dO"],
+                                               d["dHT"], dq, dkk, dvv, dg, dbeta, dH0, wsb,
+                                               problem=p, stream=stream)
                     e1.record(stream)
                 torch.cuda.synchronize()
                 ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
-                key = ("fwd." if op == gdn.GDN_OP_FWD else "bwd.") + nm
+                key = ("fwd." if op == gdn.GDN_OP_FWD_CTX else "bwd.") + nm
                 tot[key] = ms
         P = gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD)
         dom = max(tot, key=tot.get)

@@ -28,7 +28,8 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA, \
     GDN_ERR_DEVICE_TIMEOUT = range(6)
 GDN_FP32, GDN_BF16 = 0, 1
-GDN_OP_FWD, GDN_OP_BWD, GDN_OP_SUMMARY, GDN_OP_SUMMARY_BWD = range(4)
+GDN_OP_FWD, GDN_OP_BWD, GDN_OP_SUMMARY, GDN_OP_SUMMARY_BWD, GDN_OP_FWD_CTX, GDN_OP_BWD_CTX = \
+    range(6)
 
 # Every symbol include/gdn.h declares (checked by the CPU test suite).
 EXPORTS = (
@@ -36,7 +37,8 @@ EXPORTS = (
     "gdn_resolved_segments", "gdn_workspace_size", "gdn_fwd", "gdn_bwd", "gdn_gate_param_bwd", "gdn_summary", "gdn_summary_bwd",
     "gdn_compose", "gdn_prefix_compose", "gdn_prefix_compose_bwd", "gdn_apply_state",
     "gdn_apply_state_bwd", "gdn_check_device_status", "gdn_kernel_info", "gdn_fwd_kernel",
-    "gdn_bwd_kernel", "gdn_fwd_noalloc",
+    "gdn_bwd_kernel", "gdn_fwd_noalloc", "gdn_ctx_size", "gdn_fwd_ctx", "gdn_bwd_ctx",
+    "gdn_fwd_ctx_kernel", "gdn_bwd_ctx_kernel",
 )
 
 
@@ -103,6 +105,15 @@ def load_library(path: str | None = None):
             "gdn_bwd_kernel": ([_PP, ctypes.c_int32] + [_VP] * 18 + [ctypes.c_size_t, _VP],
                                ctypes.c_int),
             "gdn_fwd_noalloc": ([_PP] + [_VP] * 12, ctypes.c_int),
+            "gdn_ctx_size": ([_PP, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+            "gdn_fwd_ctx": ([_PP] + [_VP] * 12 + [ctypes.c_size_t, _VP, ctypes.c_size_t, _VP],
+                            ctypes.c_int),
+            "gdn_bwd_ctx": ([_PP] + [_VP] * 8 + [ctypes.c_size_t] + [_VP] * 10
+                            + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_fwd_ctx_kernel": ([_PP, ctypes.c_int32] + [_VP] * 12
+                                   + [ctypes.c_size_t, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_bwd_ctx_kernel": ([_PP, ctypes.c_int32] + [_VP] * 8 + [ctypes.c_size_t]
+                                   + [_VP] * 10 + [ctypes.c_size_t, _VP], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -292,6 +303,70 @@ def gdn_apply_state_bwd(q, k, v, a, b, A_log, dt_bias, Hin, dO, dHout=None, vali
                        dHout, True, kw)
 
 
+def gdn_ctx_size(problem: Problem) -> int:
+    """Bytes of the forward context of gdn_fwd_ctx / gdn_bwd_ctx."""
+    n = ctypes.c_size_t(0)
+    _check("gdn_ctx_size", load_library().gdn_ctx_size(ctypes.byref(problem), ctypes.byref(n)))
+    return n.value
+
+
+def ctx_buffer(problem: Problem, device=None) -> torch.Tensor:
+    """A caller-owned forward context buffer (uint8)."""
+    return torch.empty(gdn_ctx_size(problem), dtype=torch.uint8, device=device or "cuda")
+
+
+def gdn_fwd_ctx(q, k, v, a, b, A_log, dt_bias, h0=None, valid_len=None, *, ctx=None,
+                segments=0, l2norm=True, eps=1e-6, scale=0.0, o=None, hT=None, want_hT=True,
+                ws=None, stream=None, problem=None):
+    """Forward that also keeps the segment transitions and start states:
+    returns (o, hT, ctx) with ctx for gdn_bwd_ctx."""
+    p = problem or make_problem(q, v, segments=segments, l2norm=l2norm, eps=eps, scale=scale)
+    B, T, H, dv = v.shape
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, q.shape[3], dv), dtype=torch.float32, device=q.device)
+    ctx = ctx if ctx is not None else ctx_buffer(p, q.device)
+    ws = _ws(p, GDN_OP_FWD, ws, q.device)
+    _check("gdn_fwd_ctx", load_library().gdn_fwd_ctx(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+        _ptr(dt_bias), _ptr(h0), _ptr(valid_len), _ptr(o), _ptr(hT), _ptr(ctx), ctx.numel(),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return o, hT, ctx
+
+
+def gdn_bwd_ctx(q, k, v, a, b, A_log, dt_bias, ctx, dO, dHT=None, valid_len=None, *,
+                want_dH0=True, **kw):
+    """Backward from a gdn_fwd_ctx context: returns (dq, dk, dv, dg, dbeta, dH0)."""
+    p = kw.pop("problem", None) or make_problem(q, v, segments=kw.pop("segments", 0),
+                                                 l2norm=kw.pop("l2norm", True),
+                                                 eps=kw.pop("eps", 1e-6),
+                                                 scale=kw.pop("scale", 0.0))
+    B, T, H, dv = v.shape
+    dq = kw.pop("dq", None)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = kw.pop("dk", None)
+    dk = torch.empty_like(k) if dk is None else dk
+    dv_ = kw.pop("dv", None)
+    dv_ = torch.empty_like(v) if dv_ is None else dv_
+    dg = kw.pop("dg", None)
+    dg = torch.empty((B, T, H), dtype=torch.float32, device=q.device) if dg is None else dg
+    dbeta = kw.pop("dbeta", None)
+    dbeta = torch.empty((B, T, H), dtype=torch.float32, device=q.device) if dbeta is None else dbeta
+    dH0 = kw.pop("dH0", None)
+    if dH0 is None and want_dH0:
+        dH0 = torch.empty((B, H, q.shape[3], dv), dtype=torch.float32, device=q.device)
+    ws = _ws(p, GDN_OP_BWD, kw.pop("ws", None), q.device)
+    _check("gdn_bwd_ctx", load_library().gdn_bwd_ctx(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+        _ptr(dt_bias), _ptr(ctx), ctx.numel(), _ptr(valid_len), _ptr(dO), _ptr(dHT), _ptr(dq),
+        _ptr(dk), _ptr(dv_), _ptr(dg), _ptr(dbeta), _ptr(dH0), _ptr(ws), ws.numel(),
+        _stream(kw.pop("stream", None))))
+    if kw:
+        raise TypeError(f"unexpected arguments {sorted(kw)}")
+    return dq, dk, dv_, dg, dbeta, dH0
+
+
 def gdn_gate_param_bwd(a, b, A_log, dt_bias, dg, dbeta, valid_len=None, *, da=None, db=None,
                        dA_log=None, ddt_bias=None, stream=None, problem=None):
     """Gate-parameter gradients from dg, dbeta: (da, db [B,T,H] fp32, dA_log, ddt_bias [H] fp32)."""
@@ -412,6 +487,25 @@ def gdn_bwd_kernel(index, q, k, v, a, b, A_log, dt_bias, h0, valid_len, dO, dHT,
         ctypes.byref(problem), index, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
         _ptr(dt_bias), _ptr(h0), _ptr(valid_len), _ptr(dO), _ptr(dHT), _ptr(dq), _ptr(dk),
         _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dH0), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def gdn_fwd_ctx_kernel(index, q, k, v, a, b, A_log, dt_bias, h0, valid_len, o, hT, ctx, ws, *,
+                       problem, stream=None):
+    """Launch only kernel `index` of gdn_fwd_ctx (after a full gdn_fwd_ctx)."""
+    _check("gdn_fwd_ctx_kernel", load_library().gdn_fwd_ctx_kernel(
+        ctypes.byref(problem), index, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+        _ptr(dt_bias), _ptr(h0), _ptr(valid_len), _ptr(o), _ptr(hT), _ptr(ctx), ctx.numel(),
+        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def gdn_bwd_ctx_kernel(index, q, k, v, a, b, A_log, dt_bias, ctx, valid_len, dO, dHT, dq, dk,
+                       dv, dg, dbeta, dH0, ws, *, problem, stream=None):
+    """Launch only kernel `index` of gdn_bwd_ctx (after a full gdn_bwd_ctx)."""
+    _check("gdn_bwd_ctx_kernel", load_library().gdn_bwd_ctx_kernel(
+        ctypes.byref(problem), index, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+        _ptr(dt_bias), _ptr(ctx), ctx.numel(), _ptr(valid_len), _ptr(dO), _ptr(dHT), _ptr(dq),
+        _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dH0), _ptr(ws), ws.numel(),
+        _stream(stream)))
 
 
 def gdn_check_device_status(ws, stream=None) -> int:

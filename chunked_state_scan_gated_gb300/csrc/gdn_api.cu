@@ -284,14 +284,50 @@ bool inputs_ok(const Prob& pr, const Inputs& in, bool need_q, bool need_v) {
   return true;
 }
 
+// Forward context (gdn_fwd_ctx / gdn_bwd_ctx): the transitions M of every segment and
+// the start states H_in of every segment, fp32, [P][B][H][dk][dk] then [P][B][H][dk][dv].
+struct Ctx {
+  float* M;
+  float* Hin;
+};
+size_t ctx_bytes(const Prob& pr) {
+  return (size_t)pr.P * pr.B * pr.H * (pr.dk * pr.dk + pr.dk * pr.dv) * sizeof(float);
+}
+Ctx ctx_of(const Prob& pr, void* base) {
+  Ctx c;
+  c.M = (float*)base;
+  c.Hin = c.M + (size_t)pr.P * pr.B * pr.H * pr.dk * pr.dk;
+  return c;
+}
+// H_in of the only segment: h0, or zero
+cudaError_t ctx_single(const Prob& pr, const float* h0, float* Hin, cudaStream_t st) {
+  const size_t n = (size_t)pr.B * pr.H * pr.dk * pr.dv * sizeof(float);
+  if (n == 0) return cudaSuccess;
+  return h0 ? cudaMemcpyAsync(Hin, h0, n, cudaMemcpyDeviceToDevice, st)
+            : cudaMemsetAsync(Hin, 0, n, st);
+}
+
 gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* o, float* hT,
-                       const WS& ws, cudaStream_t st, Sched& sc) {
+                       const WS& ws, cudaStream_t st, Sched& sc, const Ctx* cx = nullptr) {
   const float* init = h0;
   int64_t init_stride = 0;
   const int64_t sstride = pr.B * pr.H * pr.dk * pr.dv;
   if (tc_path(pr)) {
     GDN_RUN(sc, "prep_tc", launch_prep_tc(pr, in, ws, st));
-    if (pr.P > 1) {
+    if (cx) {  // summaries of every segment; the transitions and start states are kept
+      if (pr.P > 1) {
+        GDN_RUN(sc, "summary_chain_tc",
+                launch_chain_tc(pr, in, ws, 1, 0, pr.P, nullptr, 0, nullptr, nullptr, cx->M,
+                                ws.Sseg, sstride, nullptr, st));
+        GDN_RUN(sc, "prefix",
+                launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, cx->M, ws.Sseg, h0, cx->Hin,
+                              nullptr, st));
+      } else {
+        GDN_RUN(sc, "ctx_init", ctx_single(pr, h0, cx->Hin, st));
+      }
+      init = cx->Hin;
+      init_stride = sstride;
+    } else if (pr.P > 1) {
       GDN_RUN(sc, "summary_chain_tc",
               launch_chain_tc(pr, in, ws, 1, 0, pr.P - 1, nullptr, 0, nullptr, nullptr, ws.Mseg,
                               ws.Sseg, sstride, nullptr, st));
@@ -307,7 +343,20 @@ gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* 
     return GDN_OK;
   }
   GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, false, st));
-  if (pr.P > 1) {
+  if (cx) {
+    if (pr.P > 1) {
+      GDN_RUN(sc, "summary_scan",
+              launch_state_scan(pr, ws, 1, 0, pr.P, nullptr, 0, nullptr, nullptr, nullptr, cx->M,
+                                ws.Sseg, sstride, st));
+      GDN_RUN(sc, "prefix",
+              launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, cx->M, ws.Sseg, h0, cx->Hin,
+                            nullptr, st));
+    } else {
+      GDN_RUN(sc, "ctx_init", ctx_single(pr, h0, cx->Hin, st));
+    }
+    init = cx->Hin;
+    init_stride = sstride;
+  } else if (pr.P > 1) {
     GDN_RUN(sc, "summary_scan",
             launch_state_scan(pr, ws, 1, 0, pr.P - 1, nullptr, 0, nullptr, nullptr, nullptr,
                               ws.Mseg, ws.Sseg, sstride, st));
@@ -326,7 +375,7 @@ gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* 
 
 gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const float* dHT,
                         void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dH0,
-                        const WS& ws, cudaStream_t st, Sched& sc) {
+                        const WS& ws, cudaStream_t st, Sched& sc, const Ctx* cx = nullptr) {
   const int64_t sstride = pr.B * pr.H * pr.dk * pr.dv;
   if (tc_path(pr)) {
     const float* init = h0;
@@ -334,7 +383,20 @@ gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const
     GDN_RUN(sc, "prep_tc", launch_prep_tc(pr, in, ws, st));
     const float* dinit = dHT;
     int64_t dinit_stride = 0;
-    if (pr.P > 1) {
+    if (cx) {  // segment start states from the forward: only the reverse summaries and prefix
+      init = cx->Hin;
+      init_stride = sstride;
+      if (pr.P > 1) {
+        GDN_RUN(sc, "grad_summary_tc",
+                launch_dchain_tc(pr, in, ws, 1, 1, pr.P - 1, nullptr, 0, nullptr, nullptr,
+                                 ws.Dseg, sstride, st));
+        GDN_RUN(sc, "prefix_bwd",
+                launch_prefix_bwd(pr.B * pr.H, pr.P, pr.dk, pr.dv, cx->M, ws.Dseg, dHT,
+                                  ws.dHout, nullptr, st));
+        dinit = ws.dHout;
+        dinit_stride = sstride;
+      }
+    } else if (pr.P > 1) {
       // forward summaries of every segment (M feeds both prefixes) with the gradient
       // summaries of segments 1..P-1, then both prefixes in one launch
       const ChainPass f{0, pr.P, nullptr, 0, ws.Mseg, ws.Sseg, sstride, nullptr};
@@ -360,7 +422,10 @@ gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const
   GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, true, st));
   const float* init = h0;
   int64_t init_stride = 0;
-  if (pr.P > 1) {
+  if (cx) {
+    init = cx->Hin;
+    init_stride = sstride;
+  } else if (pr.P > 1) {
     GDN_RUN(sc, "summary_scan",
             launch_state_scan(pr, ws, 1, 0, pr.P, nullptr, 0, nullptr, nullptr, nullptr, ws.Mseg,
                               ws.Sseg, sstride, st));
@@ -380,8 +445,8 @@ gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const
             launch_dstate_scan(pr, in, ws, 1, 1, pr.P - 1, nullptr, 0, nullptr, ws.Dseg, sstride,
                                st));
     GDN_RUN(sc, "prefix_bwd",
-            launch_prefix_bwd(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Dseg, dHT, ws.dHout,
-                              nullptr, st));
+            launch_prefix_bwd(pr.B * pr.H, pr.P, pr.dk, pr.dv, cx ? cx->M : ws.Mseg, ws.Dseg,
+                              dHT, ws.dHout, nullptr, st));
     dinit = ws.dHout;
     dinit_stride = sstride;
   }
@@ -430,7 +495,9 @@ gdn_status gdn_query_support(const gdn_problem* p) {
 }
 
 gdn_status gdn_resolved_segments(const gdn_problem* p, int32_t op, int32_t* segments) {
-  if (!segments || op < GDN_OP_FWD || op > GDN_OP_SUMMARY_BWD) return GDN_ERR_INVALID_ARG;
+  if (!segments || op < GDN_OP_FWD || op > GDN_OP_BWD_CTX) return GDN_ERR_INVALID_ARG;
+  if (op == GDN_OP_FWD_CTX) op = GDN_OP_FWD;
+  if (op == GDN_OP_BWD_CTX) op = GDN_OP_BWD;
   Prob pr;
   gdn_status s = resolve_op(p, op, &pr);
   if (s != GDN_OK) return s;
@@ -439,7 +506,9 @@ gdn_status gdn_resolved_segments(const gdn_problem* p, int32_t op, int32_t* segm
 }
 
 gdn_status gdn_workspace_size(const gdn_problem* p, int32_t op, size_t* bytes) {
-  if (!bytes || op < GDN_OP_FWD || op > GDN_OP_SUMMARY_BWD) return GDN_ERR_INVALID_ARG;
+  if (!bytes || op < GDN_OP_FWD || op > GDN_OP_BWD_CTX) return GDN_ERR_INVALID_ARG;
+  if (op == GDN_OP_FWD_CTX) op = GDN_OP_FWD;
+  if (op == GDN_OP_BWD_CTX) op = GDN_OP_BWD;
   Prob pr;
   gdn_status s = resolve_op(p, op, &pr);
   if (s != GDN_OK) return s;
@@ -451,7 +520,8 @@ static gdn_status fwd_impl(const gdn_problem* p, const void* q, const void* k, c
                            const void* a, const void* b, const float* A_log,
                            const float* dt_bias, const float* h0, const int32_t* valid_len,
                            void* o, float* hT, void* workspace, size_t workspace_bytes,
-                           void* stream, Sched& sc) {
+                           void* stream, Sched& sc, void* ctx = nullptr,
+                           size_t ctx_size = 0, bool with_ctx = false) {
   Prob pr;
   gdn_status s = resolve_op(p, GDN_OP_FWD, &pr);
   if (s != GDN_OK) return s;
@@ -459,10 +529,15 @@ static gdn_status fwd_impl(const gdn_problem* p, const void* q, const void* k, c
   if (!inputs_ok(pr, in, true, true)) return GDN_ERR_INVALID_ARG;
   if (!ok_ptr(o, pr.B * pr.T * pr.H * pr.dv) || !ok_opt(h0) || !ok_opt(hT))
     return GDN_ERR_INVALID_ARG;
+  Ctx cx;
+  if (with_ctx) {
+    if (ctx == nullptr || !aligned16(ctx) || ctx_size < ctx_bytes(pr)) return GDN_ERR_INVALID_ARG;
+    cx = ctx_of(pr, ctx);
+  }
   WS ws;
   cudaStream_t st = (cudaStream_t)stream;
   if ((s = prepare(p, GDN_OP_FWD, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK) return s;
-  return run_forward(pr, in, h0, o, hT, ws, st, sc);
+  return run_forward(pr, in, h0, o, hT, ws, st, sc, with_ctx ? &cx : nullptr);
 }
 
 static gdn_status bwd_impl(const gdn_problem* p, const void* q, const void* k, const void* v,
@@ -470,7 +545,9 @@ static gdn_status bwd_impl(const gdn_problem* p, const void* q, const void* k, c
                            const float* dt_bias, const float* h0, const int32_t* valid_len,
                            const void* dO, const float* dHT, void* dq, void* dk, void* dv,
                            float* dg, float* dbeta, float* dH0, void* workspace,
-                           size_t workspace_bytes, void* stream, Sched& sc) {
+                           size_t workspace_bytes, void* stream, Sched& sc,
+                           const void* ctx = nullptr, size_t ctx_size = 0,
+                           bool with_ctx = false) {
   Prob pr;
   gdn_status s = resolve_op(p, GDN_OP_BWD, &pr);
   if (s != GDN_OK) return s;
@@ -482,10 +559,16 @@ static gdn_status bwd_impl(const gdn_problem* p, const void* q, const void* k, c
   if (!ok_ptr(dq, nqk) || !ok_ptr(dk, nqk) || !ok_ptr(dv, nv) || !ok_ptr(dg, ng) ||
       !ok_ptr(dbeta, ng))
     return GDN_ERR_INVALID_ARG;
+  Ctx cx;
+  if (with_ctx) {
+    if (ctx == nullptr || !aligned16(ctx) || ctx_size < ctx_bytes(pr)) return GDN_ERR_INVALID_ARG;
+    cx = ctx_of(pr, const_cast<void*>(ctx));
+  }
   WS ws;
   cudaStream_t st = (cudaStream_t)stream;
   if ((s = prepare(p, GDN_OP_BWD, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK) return s;
-  return run_backward(pr, in, h0, dHT, dq, dk, dv, dg, dbeta, dH0, ws, st, sc);
+  return run_backward(pr, in, h0, dHT, dq, dk, dv, dg, dbeta, dH0, ws, st, sc,
+                      with_ctx ? &cx : nullptr);
 }
 
 gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,
@@ -522,11 +605,69 @@ gdn_status gdn_bwd_kernel(const gdn_problem* p, int32_t index, const void* q, co
                   dbeta, dH0, workspace, workspace_bytes, stream, sc);
 }
 
+gdn_status gdn_ctx_size(const gdn_problem* p, size_t* bytes) {
+  if (!bytes) return GDN_ERR_INVALID_ARG;
+  Prob pr;
+  gdn_status s = resolve_op(p, GDN_OP_FWD, &pr);
+  if (s != GDN_OK) return s;
+  *bytes = ctx_bytes(pr);
+  return GDN_OK;
+}
+
+gdn_status gdn_fwd_ctx(const gdn_problem* p, const void* q, const void* k, const void* v,
+                       const void* a, const void* b, const float* A_log, const float* dt_bias,
+                       const float* h0, const int32_t* valid_len, void* o, float* hT, void* ctx,
+                       size_t ctx_bytes_, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  Sched sc;
+  return fwd_impl(p, q, k, v, a, b, A_log, dt_bias, h0, valid_len, o, hT, workspace,
+                  workspace_bytes, stream, sc, ctx, ctx_bytes_, true);
+}
+
+gdn_status gdn_bwd_ctx(const gdn_problem* p, const void* q, const void* k, const void* v,
+                       const void* a, const void* b, const float* A_log, const float* dt_bias,
+                       const void* ctx, size_t ctx_bytes_, const int32_t* valid_len,
+                       const void* dO, const float* dHT, void* dq, void* dk, void* dv, float* dg,
+                       float* dbeta, float* dH0, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  Sched sc;
+  return bwd_impl(p, q, k, v, a, b, A_log, dt_bias, nullptr, valid_len, dO, dHT, dq, dk, dv, dg,
+                  dbeta, dH0, workspace, workspace_bytes, stream, sc, ctx, ctx_bytes_, true);
+}
+
+gdn_status gdn_fwd_ctx_kernel(const gdn_problem* p, int32_t index, const void* q, const void* k,
+                              const void* v, const void* a, const void* b, const float* A_log,
+                              const float* dt_bias, const float* h0, const int32_t* valid_len,
+                              void* o, float* hT, void* ctx, size_t ctx_bytes_, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (index < 0) return GDN_ERR_INVALID_ARG;
+  Sched sc;
+  sc.only = index;
+  return fwd_impl(p, q, k, v, a, b, A_log, dt_bias, h0, valid_len, o, hT, workspace,
+                  workspace_bytes, stream, sc, ctx, ctx_bytes_, true);
+}
+
+gdn_status gdn_bwd_ctx_kernel(const gdn_problem* p, int32_t index, const void* q, const void* k,
+                              const void* v, const void* a, const void* b, const float* A_log,
+                              const float* dt_bias, const void* ctx, size_t ctx_bytes_,
+                              const int32_t* valid_len, const void* dO, const float* dHT,
+                              void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dH0,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (index < 0) return GDN_ERR_INVALID_ARG;
+  Sched sc;
+  sc.only = index;
+  return bwd_impl(p, q, k, v, a, b, A_log, dt_bias, nullptr, valid_len, dO, dHT, dq, dk, dv, dg,
+                  dbeta, dH0, workspace, workspace_bytes, stream, sc, ctx, ctx_bytes_, true);
+}
+
 gdn_status gdn_kernel_info(const gdn_problem* p, int32_t op, int32_t index, int32_t* count,
                            const char** name) {
-  if (op != GDN_OP_FWD && op != GDN_OP_BWD) return GDN_ERR_INVALID_ARG;
+  if (op != GDN_OP_FWD && op != GDN_OP_BWD && op != GDN_OP_FWD_CTX && op != GDN_OP_BWD_CTX)
+    return GDN_ERR_INVALID_ARG;
+  const bool fwd = op == GDN_OP_FWD || op == GDN_OP_FWD_CTX;
+  const bool with_ctx = op == GDN_OP_FWD_CTX || op == GDN_OP_BWD_CTX;
   Prob pr;
-  gdn_status s = resolve_op(p, op, &pr);
+  gdn_status s = resolve_op(p, fwd ? GDN_OP_FWD : GDN_OP_BWD, &pr);
   if (s != GDN_OK) return s;
   Sched sc;
   sc.dry = true;
@@ -534,11 +675,12 @@ gdn_status gdn_kernel_info(const gdn_problem* p, int32_t op, int32_t index, int3
   WS ws;
   memset(&ws, 0, sizeof(ws));
   Inputs in{};
-  if (op == GDN_OP_FWD)
-    run_forward(pr, in, nullptr, nullptr, nullptr, ws, nullptr, sc);
+  Ctx cx{nullptr, nullptr};
+  if (fwd)
+    run_forward(pr, in, nullptr, nullptr, nullptr, ws, nullptr, sc, with_ctx ? &cx : nullptr);
   else
     run_backward(pr, in, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                 ws, nullptr, sc);
+                 ws, nullptr, sc, with_ctx ? &cx : nullptr);
   if (count) *count = sc.idx;
   if (name) *name = sc.name;
   return (index >= 0 && index >= sc.idx) ? GDN_ERR_INVALID_ARG : GDN_OK;

@@ -75,7 +75,9 @@ typedef enum gdn_op {
   GDN_OP_FWD = 0,         /* gdn_fwd, gdn_apply_state */
   GDN_OP_BWD = 1,         /* gdn_bwd, gdn_apply_state_bwd */
   GDN_OP_SUMMARY = 2,     /* gdn_summary */
-  GDN_OP_SUMMARY_BWD = 3  /* gdn_summary_bwd */
+  GDN_OP_SUMMARY_BWD = 3, /* gdn_summary_bwd */
+  GDN_OP_FWD_CTX = 4,     /* gdn_fwd_ctx (workspace as GDN_OP_FWD) */
+  GDN_OP_BWD_CTX = 5      /* gdn_bwd_ctx (workspace as GDN_OP_BWD) */
 } gdn_op;
 
 /* Problem description.  Fill with gdn_problem_init, then set the sizes. */
@@ -153,6 +155,34 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
                    const float* h0, const int32_t* valid_len, const void* dO, const float* dHT,
                    void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dH0,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Forward context for a training step (no counterpart on the pages).  The forward
+ * splits T into P segments (P = gdn_resolved_segments(p, GDN_OP_FWD)) and computes
+ * every segment's transition M_s [dk,dk] (H_out = M_s H_in + S_s) and start state
+ * H_in,s [dk,dv]; gdn_bwd recomputes both.  gdn_fwd_ctx is gdn_fwd that also keeps
+ * them in `ctx`: M [P][B][H][dk][dk] then H_in [P][B][H][dk][dv], fp32, in a
+ * caller-owned, 16-byte aligned device buffer of at least gdn_ctx_size bytes
+ * (36 MiB at B=1, H=32, d=128, P=9).  gdn_bwd_ctx is gdn_bwd with h0 replaced by
+ * that context: it reads H_in (which already holds h0 as H_in,0) and M instead of
+ * recomputing the forward summaries and their prefix; every chunk intermediate is
+ * still recomputed.  The context is only valid for the same problem (same resolved
+ * P), inputs and h0; the library cannot check that.  Invalid pointer or size:
+ * GDN_ERR_INVALID_ARG.  gdn_fwd_ctx_kernel / gdn_bwd_ctx_kernel and the ops
+ * GDN_OP_FWD_CTX / GDN_OP_BWD_CTX of gdn_kernel_info are the profiling aids below
+ * for these two calls.
+ */
+gdn_status gdn_ctx_size(const gdn_problem* p, size_t* bytes);
+gdn_status gdn_fwd_ctx(const gdn_problem* p, const void* q, const void* k, const void* v,
+                       const void* a, const void* b, const float* A_log, const float* dt_bias,
+                       const float* h0, const int32_t* valid_len, void* o, float* hT, void* ctx,
+                       size_t ctx_bytes, void* workspace, size_t workspace_bytes, void* stream);
+gdn_status gdn_bwd_ctx(const gdn_problem* p, const void* q, const void* k, const void* v,
+                       const void* a, const void* b, const float* A_log, const float* dt_bias,
+                       const void* ctx, size_t ctx_bytes, const int32_t* valid_len,
+                       const void* dO, const float* dHT, void* dq, void* dk, void* dv, float* dg,
+                       float* dbeta, float* dH0, void* workspace, size_t workspace_bytes,
+                       void* stream);
 
 /*
  * Gradients of the gate parameters from the core's dg, dbeta [B,T,H] fp32 (as
@@ -242,7 +272,8 @@ gdn_status gdn_apply_state_bwd(const gdn_problem* p, const void* q, const void* 
  * Profiling aid (no counterpart on the pages): gdn_fwd and gdn_bwd are a short
  * sequence of kernel launches.  gdn_kernel_info gives, for `op` (GDN_OP_FWD or
  * GDN_OP_BWD) and problem p, the number of launches (*count, nullable) and the
- * name of launch `index` (*name, nullable; a static string).  gdn_fwd_kernel /
+ * name of launch `index` (*name, nullable; a static string); GDN_OP_FWD_CTX and
+ * GDN_OP_BWD_CTX list the launches of gdn_fwd_ctx and gdn_bwd_ctx.  gdn_fwd_kernel /
  * gdn_bwd_kernel take the arguments of gdn_fwd / gdn_bwd plus `index` and
  * launch only that kernel, so that a caller can time it alone with CUDA events.
  * They read the intermediates that the earlier kernels of the full call left in
@@ -263,6 +294,17 @@ gdn_status gdn_bwd_kernel(const gdn_problem* p, int32_t index, const void* q, co
                           const void* dO, const float* dHT, void* dq, void* dk, void* dv,
                           float* dg, float* dbeta, float* dH0, void* workspace,
                           size_t workspace_bytes, void* stream);
+gdn_status gdn_fwd_ctx_kernel(const gdn_problem* p, int32_t index, const void* q, const void* k,
+                              const void* v, const void* a, const void* b, const float* A_log,
+                              const float* dt_bias, const float* h0, const int32_t* valid_len,
+                              void* o, float* hT, void* ctx, size_t ctx_bytes, void* workspace,
+                              size_t workspace_bytes, void* stream);
+gdn_status gdn_bwd_ctx_kernel(const gdn_problem* p, int32_t index, const void* q, const void* k,
+                              const void* v, const void* a, const void* b, const float* A_log,
+                              const float* dt_bias, const void* ctx, size_t ctx_bytes,
+                              const int32_t* valid_len, const void* dO, const float* dHT,
+                              void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dH0,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Forward without a caller-provided workspace (no counterpart on the pages).

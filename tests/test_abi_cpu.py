@@ -153,3 +153,30 @@ def test_compose_prefix_validation(lib):
     assert lib.gdn_prefix_compose_bwd(2, 3, 4, 4, vp(A), vp(A + 4), None, vp(A), None,
                                       None) == gdn.GDN_ERR_INVALID_ARG
     assert lib.gdn_check_device_status(None, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_ctx_size_and_validation(lib):
+    """The forward context holds M and H_in of every resolved segment; a missing, short or
+    misaligned context is refused before any launch."""
+    for seg in (0, 1, 5):
+        p = problem(segments=seg)
+        P = gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD)
+        assert P == gdn.gdn_resolved_segments(p, gdn.GDN_OP_BWD)
+        assert P == gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD_CTX)
+        assert gdn.gdn_ctx_size(p) == P * 1 * 32 * (128 * 128 + 128 * 128) * 4
+    p = problem()
+    need = gdn.gdn_ctx_size(p)
+    vp = ctypes.c_void_p
+    fwd = [vp(A)] * 7 + [None, None, vp(A), None]      # q .. dt_bias, h0, valid_len, o, hT
+    for ctx, n in ((None, need), (A, need - 4), (A + 8, need)):
+        st = lib.gdn_fwd_ctx(ctypes.byref(p), *fwd, None if ctx is None else vp(ctx), n,
+                             vp(A), 1 << 40, None)
+        assert st == gdn.GDN_ERR_INVALID_ARG
+        st = lib.gdn_bwd_ctx(ctypes.byref(p), *[vp(A)] * 7, None if ctx is None else vp(ctx), n,
+                             None, vp(A), None, *[vp(A)] * 5, None, vp(A), 1 << 40, None)
+        assert st == gdn.GDN_ERR_INVALID_ARG
+    assert gdn.gdn_workspace_size(p, gdn.GDN_OP_FWD_CTX) == gdn.gdn_workspace_size(p, gdn.GDN_OP_FWD)
+    assert gdn.gdn_workspace_size(p, gdn.GDN_OP_BWD_CTX) == gdn.gdn_workspace_size(p, gdn.GDN_OP_BWD)
+    names = gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD_CTX)
+    assert "summary_pair_tc" not in names and "grad_tc" in names      # no forward summaries
+    assert gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD_CTX)[-1] == "apply_chain_tc"
