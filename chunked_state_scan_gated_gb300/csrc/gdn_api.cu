@@ -63,25 +63,26 @@ int device_sms() {
 
 namespace {
 
-// Segment count of the tensor-core path: the P that minimises a model of the
-// forward + backward chain time.  Every chain pass runs ceil(CTAs / slots)
-// waves of ceil(NC / P) chunk steps (slots = SMs, or 2 x SMs for the passes that
-// fit two CTAs on an SM); the step times (us, GB300) are those of the chain
-// kernels measured at T = 32K, and each prefix step costs ~7 us.
+// Segment count of the tensor-core path: the P that minimises a model of the chain
+// launches of a training step (gdn_fwd_ctx + gdn_bwd_ctx).  Every chain pass runs
+// ceil(CTAs / slots) waves of ceil(NC / P) chunk steps (slots = SMs, or 2 x SMs for the
+// passes that fit two CTAs on an SM) plus a fixed cost per wave; the step times (us,
+// GB300, T = 32K) are those of the forward summaries (3.3), the apply chain (3.3), the
+// gradient summaries (4.9) and the states + state-gradient pair (4.4), and each prefix
+// step costs ~7.7 us.  The model reproduces the measured best P at T = 8K, 32K, 64K.
 int auto_segments_tc(int64_t BH, int64_t NC, int sms) {
   double best = 1e300;
   int best_p = 1;
   for (int64_t P = 1; P <= 64 && P <= NC; ++P) {
     const int64_t cps = (NC + P - 1) / P, pe = (NC + cps - 1) / cps;
     auto waves = [](int64_t n, int64_t slots) { return (double)((n + slots - 1) / slots); };
-    const double fwd = waves(2 * BH * (pe - 1), 2 * sms) * cps * 2.9 +
-                       waves(BH * pe, sms) * cps * 3.2 + (pe - 1) * 7.0;
-    const double bwd = waves(2 * BH * pe, 2 * sms) * cps * 2.9 +
-                       waves(BH * pe, 2 * sms) * cps * 4.4 +
-                       waves(BH * (pe - 1), 2 * sms) * cps * 4.6 +
-                       waves(BH * pe, 2 * sms) * cps * 5.7 + 2 * (pe - 1) * 7.0;
-    if (fwd + bwd < best - 1e-9) {
-      best = fwd + bwd;
+    const double w_sum = waves(2 * BH * pe, 2 * sms), w_app = waves(BH * pe, sms);
+    const double w_gs = pe > 1 ? waves(BH * (pe - 1), 2 * sms) : 0.0;
+    const double w_st = waves(2 * BH * pe, 2 * sms);
+    const double t = cps * (w_sum * 3.34 + w_app * 3.25 + w_gs * 4.9 + w_st * 4.44) +
+                     15.0 * (w_sum + w_app + w_gs + w_st) + 2 * (pe - 1) * 7.7;
+    if (t < best - 1e-9) {
+      best = t;
       best_p = (int)pe;
     }
   }
