@@ -340,9 +340,10 @@ enum { CH_APPLY = 0, CH_SUM = 1, CH_STATES = 2 };
 constexpr uint32_t S_XA = 0;        // atoms a at a*16384: [W_a | K_a]
 constexpr uint32_t S_U = 32768;     // U image
 constexpr uint32_t S_S = 49152;     // state, bf16, MN-major (column halves 16 KB apart)
-constexpr uint32_t S_V2 = 81920;    // V2 = diag(rk e^{G_C - G}) V', MN-major (halves 8 KB apart)
-constexpr uint32_t S_G = 98304;     // G of the chunk (64 floats), then rk (64 floats)
-constexpr uint32_t S_SC = 98816;    // barriers
+constexpr uint32_t S_V2 = 81920;    // V2^T = (diag(rk e^{G_C - G}) V')^T [dv][tok], K-major
+constexpr uint32_t S_NI = 98304;    // -I (64 x 64 bf16): U^T (-I) = -U^T as an MMA term
+constexpr uint32_t S_G = 106496;    // G of the chunk (64 floats), then rk (64 floats)
+constexpr uint32_t S_SC = 107008;   // barriers
 constexpr uint32_t S_SMEM = S_SC + 128 + 1024;
 
 // Apply layout ([W | Q | K] double-buffered; U, P single).
@@ -435,6 +436,14 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
   if (warp == 0) tmem_alloc(s_tmem, 256);
   if (kApply)  // zero rows of [0; P]
     for (int e = tid; e < 512; e += CT) reinterpret_cast<uint4*>(sm + A_PZ)[e] = make_uint4(0, 0, 0, 0);
+  if (!kApply && needU)  // -I, the operand that adds -U^T to the first product
+    for (int e = tid; e < 512; e += CT) {
+      const int r = e >> 3, cc = e & 7;
+      float x[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) x[q] = (r == cc * 8 + q) ? -1.f : 0.f;
+      st_chunk(sm + S_NI, kmaj_chunk(r, cc), x);
+    }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -574,13 +583,28 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
         bulk_store(ar.hc + (bh * ar.NC + c) * (int64_t)(2 * kImg), sm + OFF_S, 2 * kImg);
         bulk_commit();
       }
-      // ---- MMA_a: apply [W; Q] S -> tA (W S in rows 0..63); otherwise W S with M = 64
+      // ---- MMA_a: apply [W; Q] S -> tA (W S in rows 0..63); otherwise, feature-major,
+      //      S^T W^T + U^T (-I) = -V'^T -> tA (M = 128 rows of dv, 64 token columns)
       if (tid == 0) {
-        const uint32_t id = idesc_bf16(kApply ? 128 : 64, 128, 0, 1);
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t at = ks >> 2, kk = ks & 3;
-          mma_bf16(tA, (d16 + ((xa + at * XSTR + kk * 32) >> 4)),
-                   (d16384 + ((OFF_S + ks * 2048) >> 4)), id, ks > 0);
+        if (kApply) {
+          const uint32_t id = idesc_bf16(128, 128, 0, 1);
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t at = ks >> 2, kk = ks & 3;
+            mma_bf16(tA, (d16 + ((xa + at * XSTR + kk * 32) >> 4)),
+                     (d16384 + ((OFF_S + ks * 2048) >> 4)), id, ks > 0);
+          }
+        } else {
+          const uint32_t id = idesc_bf16(128, 64, 1, 0);
+          for (int ks = 0; ks < 8; ++ks)  // K = dk
+            mma_bf16(tA, (d16384 + ((OFF_S + ks * 2048) >> 4)),
+                     (d16 + ((xa + (ks >> 2) * XSTR + (ks & 3) * 32) >> 4)), id, ks > 0);
+          if (needU) {
+            if (!mbar_wait(bar_u, par, ar.status, kStatusTimeout)) *s_abort = 1;
+            pend &= ~4u;
+            for (int ks = 0; ks < 4; ++ks)  // K = tokens
+              mma_bf16(tA, (d8192 + ((OFF_U + ks * 2048) >> 4)), (d16 + ((S_NI + ks * 32) >> 4)),
+                       id, 1);
+          }
         }
         mma_commit(bar_mma);
         pend |= 16u;
@@ -592,9 +616,9 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
       const float gC = exp2f(sGc[63]);
       // token row of V' owned by this thread: M = 128 (apply: quadrants 0, 1) or M = 64
       // accumulator layout (row r in TMEM lane (r % 16) + 32 (r / 16): lanes 0..15)
-      const int vi = kApply ? row : quad * 16 + (lane & 15);
+      const int vi = row;  // apply: token row of V' (quadrants 0, 1 of the M = 128 result)
       const float kt = exp2f(sGc[63] - sGc[vi & 63]) * sRk[vi & 63];
-      if (needU && (!kApply || quad < 2)) {
+      if (kApply && quad < 2) {
         if (!mbar_wait(bar_u, par, ar.status, kStatusTimeout)) *s_abort = 1;
         if (tid == 0) pend &= ~4u;
       }
@@ -605,9 +629,18 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
         issue_x(c + 1, bars + 0, S_XA, 0);
         pend |= 1u;
       }
-      if (!kApply || quad < 2) {  // V' = U - W S, V2 = rk e^{G_C - G} V'
+      if (!kApply) {  // V2^T = -rk e^{G_C - G} tA: thread row `row` (dv), tokens 32 half + e
+        float v[32];
+        tmem_ld32(tA + lane_off + half * 32, v);
+        const int tl = half * 32 + lane;
+        const float ktr = exp2f(sGc[63] - sGc[tl]) * sRk[tl];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] *= -__shfl_sync(0xffffffffu, ktr, e);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) st_chunk(sm + S_V2, kmaj_chunk(row, half * 4 + cc), &v[cc * 8]);
+      } else if (quad < 2) {  // V' = U - W S, V2 = rk e^{G_C - G} V'
         const int i = vi;
-        const bool own = kApply || lane < 16;
+        const bool own = true;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float v[32];
@@ -642,10 +675,11 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
           issue_u(c + 1);
           pend |= 4u;
         }
-        const uint32_t id = idesc_bf16(128, 128, 1, 1);
+        const uint32_t id = idesc_bf16(128, 128, 1, kApply ? 1 : 0);  // B: V2 (apply) or V2^T
         for (int ks = 0; ks < 4; ++ks)
           mma_bf16(tB, (dxs + ((xa + KOFF + ks * 2048) >> 4)),
-                   (d8192 + ((OFF_V2 + ks * 2048) >> 4)), id, ks > 0);
+                   kApply ? (d8192 + ((OFF_V2 + ks * 2048) >> 4)) : (d16 + ((S_V2 + ks * 32) >> 4)),
+                   id, ks > 0);
         if (kApply) {
           if (!mbar_wait(bars + 3, par, ar.status, kStatusTimeout)) *s_abort = 1;
           pend &= ~8u;
@@ -754,7 +788,7 @@ done:
 constexpr uint32_t D_XA = 0;        // atoms a at a*16384: [Kt_a | Qg_a] (scaled k, scaled q)
 constexpr uint32_t D_W = 32768;     // W image
 constexpr uint32_t D_P = 49152;     // P image (8 KB)
-constexpr uint32_t D_DO = 57344;    // dO tile, later -dV' (MN-major, halves 8 KB apart)
+constexpr uint32_t D_DO = 57344;    // dO tile [tok][dv]; later -dV'^T [dv][tok] (K-major)
 constexpr uint32_t D_DS = 73728;    // dS, bf16, MN-major (halves 16 KB apart)
 constexpr uint32_t D_G = 106496;    // G, rq, rk of the chunk (64 floats each)
 constexpr uint32_t D_SC = 107264;   // barriers
@@ -898,19 +932,18 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
         bulk_store(ar.dhc + (bh * ar.NC + c) * (int64_t)(2 * kImg), sm + D_DS, 2 * kImg);
         bulk_commit();
       }
-      // ---- P^T dO + Kt dS -> tV (dV', M = 64 layout); Qg^T dO -> tS
+      // ---- dV'^T = dO^T P + dS^T Kt^T -> tV (feature-major: M = 128 rows of dv, 64 token
+      //      columns); Qg^T dO -> tS
       if (tid == 0) {
-        const uint32_t idv = idesc_bf16(64, 128, 1, 1);
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tV, (d8192 + ((D_P + ks * 2048) >> 4)),
-                   (d8192 + ((D_DO + ks * 2048) >> 4)), idv, ks > 0);
-        const uint32_t idkm = idesc_bf16(64, 128, 0, 1);
+        const uint32_t idv = idesc_bf16(128, 64, 1, 1);
+        for (int ks = 0; ks < 4; ++ks)  // K = tokens i
+          mma_bf16(tV, (d8192 + ((D_DO + ks * 2048) >> 4)), (d8192 + ((D_P + ks * 2048) >> 4)),
+                   idv, ks > 0);
+        const uint32_t idk = idesc_bf16(128, 64, 1, 0);
+        for (int ks = 0; ks < 8; ++ks)  // K = dk
+          mma_bf16(tV, (d16384 + ((D_DS + ks * 2048) >> 4)),
+                   (d16 + ((D_XA + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4)), idk, 1);
         const uint32_t idmm = idesc_bf16(128, 128, 1, 1);
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t at = ks >> 2, kk = ks & 3;
-          mma_bf16(tV, (d16 + ((D_XA + at * 16384 + kk * 32) >> 4)),
-                   (d16384 + ((D_DS + ks * 2048) >> 4)), idkm, 1);
-        }
         for (int ks = 0; ks < 4; ++ks)
           mma_bf16(tS, (d16384 + ((D_XA + 8192 + ks * 2048) >> 4)),
                    (d8192 + ((D_DO + ks * 2048) >> 4)), idmm, ks > 0);
@@ -924,30 +957,22 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
         issue_a(c - 1);
         pend |= 1u;
       }
-      {  // -dV' over the dO tile; row r of the M = 64 accumulator is in TMEM lane (r % 16) + 32 (r / 16)
-        const int i = quad * 16 + (lane & 15);
+      {  // -dV'^T over the dO tile: thread row `row` (dv), tokens 32 half + e, K-major
+        float v[32];
+        tmem_ld32(tV + lane_off + half * 32, v);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float v[32];
-          tmem_ld32(tV + lane_off + half * 64 + hh * 32, v);
-          if (lane >= 16) continue;
+        for (int e = 0; e < 32; ++e) v[e] = -v[e];
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = -v[cc * 8 + e];
-            st_chunk(sm + D_DO, mnmaj_chunk(i, half * 8 + hh * 4 + cc, 8192), x);
-          }
-        }
+        for (int cc = 0; cc < 4; ++cc) st_chunk(sm + D_DO, kmaj_chunk(row, half * 4 + cc), &v[cc * 8]);
       }
       if (store && tid == 0) bulk_wait_read();  // the dS tile is rewritten below
       CHAIN_SYNC();
-      // ---- tS += W^T (-dV')
+      // ---- tS += W^T (-dV')  (B from the K-major -dV'^T tile)
       if (tid == 0) {
-        const uint32_t id = idesc_bf16(128, 128, 1, 1);
+        const uint32_t id = idesc_bf16(128, 128, 1, 0);
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tS, (d8192 + ((D_W + ks * 2048) >> 4)),
-                   (d8192 + ((D_DO + ks * 2048) >> 4)), id, 1);
+          mma_bf16(tS, (d8192 + ((D_W + ks * 2048) >> 4)), (d16 + ((D_DO + ks * 32) >> 4)), id,
+                   1);
         mma_commit(bar_mma);
         pend |= 4u;
       }
