@@ -429,7 +429,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
   uint32_t pend = 0;  // tid 0: barriers with a copy or MMA in flight (drained on an abort)
 
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bars + i, 1);
+    mbar_init(bar_mma, kApply ? 2 : 1);  // apply: MMA_b and MMA_c come from tid 0 and 32
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -608,6 +609,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
         }
         mma_commit(bar_mma);
         pend |= 16u;
+      } else if (kApply && tid == 32) {
+        mma_commit(bar_mma);  // nothing issued in this round: arrives at once
       }
       if (!kApply) {  // k tile, gates and rk of chunk c: first needed for V2 and MMA_b
         if (!mbar_wait(bars + 1, par, ar.status, kStatusTimeout)) *s_abort = 1;
@@ -680,19 +683,18 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
           mma_bf16(tB, (dxs + ((xa + KOFF + ks * 2048) >> 4)),
                    kApply ? (d8192 + ((OFF_V2 + ks * 2048) >> 4)) : (d16 + ((S_V2 + ks * 32) >> 4)),
                    id, ks > 0);
-        if (kApply) {
-          if (!mbar_wait(bars + 3, par, ar.status, kStatusTimeout)) *s_abort = 1;
-          pend &= ~8u;
-          const uint32_t id2 = idesc_bf16(128, 128, 0, 1);
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tA, (d16 + ((A_PZ + ks * 32) >> 4)),
-                     (d8192 + ((A_VP + ks * 2048) >> 4)), id2, 1);
-        }
         mma_commit(bar_mma);
         pend |= 16u;
+      } else if (kApply && tid == 32) {  // MMA_c into tA, in parallel with MMA_b
+        if (!mbar_wait(bars + 3, par, ar.status, kStatusTimeout)) *s_abort = 1;
+        const uint32_t id2 = idesc_bf16(128, 128, 0, 1);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tA, (d16 + ((A_PZ + ks * 32) >> 4)), (d8192 + ((A_VP + ks * 2048) >> 4)), id2,
+                   1);
+        mma_commit(bar_mma);
       }
       if (!mbar_wait(bar_mma, 1, ar.status, kStatusTimeout)) *s_abort = 1;
-      if (tid == 0) pend &= ~16u;
+      if (tid == 0) pend &= kApply ? ~(16u | 8u) : ~16u;  // (P consumed by tid 32's products)
       tc_fence_after();
       if (tid == 0 && c + 1 < ce) {
         if (kApply) {
