@@ -275,20 +275,36 @@ __global__ void __launch_bounds__(GT, 1)
 
   // Gates of chunk `it` into buffer dst (G, gamma, beta, Kt at 0, 64, 128, 192), by warps 2
   // and 3 (token = tid - 64) while the rest of the CTA works.
-  auto gates = [&](const Item& it, float* dst) {
+  // Gate inputs of chunk `it` for token tid - 64 (warps 2, 3): a + dt_bias and b, read early
+  // into registers so that their latency stays off the chunk's critical path.
+  struct GateIn {
+    float xa, xb;
+    bool live;
+  };
+  auto gate_in = [&](const Item& it) {
     const int t = tid - 64;
     int64_t Lg = ar.T;
     if (ar.valid_len) {
       Lg = ar.valid_len[it.b];
       if (Lg < 0 || Lg > ar.T) Lg = Lg < 0 ? 0 : ar.T;
     }
+    GateIn gi{0.f, 0.f, it.t0 + t < Lg};
+    if (gi.live) {
+      const int64_t ix = (it.b * ar.Ts + it.t0 + t) * ar.H + it.h;
+      gi.xa = __bfloat162float(ar.a[ix]) + ar.dt_bias[it.h];
+      gi.xb = __bfloat162float(ar.b[ix]);
+    }
+    return gi;
+  };
+  // Gates of a chunk of head h from its inputs into buffer dst (G, gamma, beta, Kt at 0, 64,
+  // 128, 192), by warps 2 and 3 (token = tid - 64) while the rest of the CTA works.
+  auto gates = [&](const GateIn& gi, int64_t h, float* dst) {
+    const int t = tid - 64;
     float g = 0.f, be = 0.f;
-    if (it.t0 + t < Lg) {
-      const int64_t gi = (it.b * ar.Ts + it.t0 + t) * ar.H + it.h;
-      const float x = __bfloat162float(ar.a[gi]) + ar.dt_bias[it.h];
-      const float sp = x > 20.f ? x : log1pf(expf(x));
-      g = -expf(ar.A_log[it.h]) * sp;
-      be = 1.f / (1.f + expf(-__bfloat162float(ar.b[gi])));
+    if (gi.live) {
+      const float sp = gi.xa > 20.f ? gi.xa : log1pf(expf(gi.xa));
+      g = -expf(ar.A_log[h]) * sp;
+      be = 1.f / (1.f + expf(-gi.xb));
     }
     float v = g * kLog2e;  // inclusive scan over the 64 tokens
 #pragma unroll
@@ -307,7 +323,11 @@ __global__ void __launch_bounds__(GT, 1)
     dst[192 + t] = dexp_(dst[63], v);
   };
 
-  if (warp == 2 || warp == 3) gates(item_of(blockIdx.x), sGate);
+  GateIn gnext{0.f, 0.f, false};  // warps 2, 3: inputs of the next chunk's gates
+  if (warp == 2 || warp == 3) {
+    const Item it0 = item_of(blockIdx.x);
+    gates(gate_in(it0), it0.h, sGate);
+  }
   if (tid == 0 && blockIdx.x < ar.NW) {  // every tile of the first chunk
     const Item it = item_of(blockIdx.x);
     const Lay L = layout_of(0);
@@ -476,6 +496,7 @@ __global__ void __launch_bounds__(GT, 1)
       }
       mma_commit(bar_mma);
     }
+    if (more && (warp == 2 || warp == 3)) gnext = gate_in(nx);  // lands before the tail
     {  // while round B runs: (diag(gamma) dO S^T)^T and q_t . (gamma_t S dO_t)
       const int f = fr;
       float pq[16];
@@ -713,7 +734,7 @@ __global__ void __launch_bounds__(GT, 1)
       sDB[t] = rv + gm * rkw + sDBh[t] + sDBh[64 + t] + sDBh[128 + t] + sDBh[192 + t];
       sRed[t] = (t < 63) ? s_t : 0.f;                       // reuse: Kt terms to sum into dG_C
     } else if (more && (warp == 2 || warp == 3)) {
-      gates(nx, sGate + ln * 256);
+      gates(gnext, nx.h, sGate + ln * 256);
     }
     __syncthreads();
     if (tid < 32) {  // dG_C gets the Kt terms and the state term; then dg_j = sum_{i >= j} dG_i
