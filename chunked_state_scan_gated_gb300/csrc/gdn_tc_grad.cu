@@ -193,14 +193,14 @@ __global__ void __launch_bounds__(GT, 1)
   const bool own64 = lane < 16;        // owns row ri of M = 64 results
   const int ri = quad * 16 + (lane & 15);
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const bool issuer = warp < 4 && lane == 0;  // issues one product per MMA round
+  const bool issuer = warp < 5 && lane == 0;  // issues one product per MMA round
   enum { RQ = 0, RV = 1, RKW = 2, RKD = 3 };  // column-sum types
   enum { GQK = 0, GA = 1, GB = 2 };            // load groups
   uint32_t armed = 0;  // tid 0: bit 3 l + g: group g of layout l armed and not yet consumed
 
   if (tid == 0) {
     for (int i = 0; i < 6; ++i) mbar_init(bars + i, 1);
-    mbar_init(bar_mma, 4);  // each round's products are issued from four warps (lane 0 of 0..3)
+    mbar_init(bar_mma, 5);  // each round's products are issued from five warps (lane 0 of 0..4)
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -409,8 +409,8 @@ __global__ void __launch_bounds__(GT, 1)
     GRAD_SYNC();
     // ---- round A: S^T W^T -> [0,64), dO^T P -> [64,128), dS^T K^T -> [128,192),
     //      S dO^T -> [192,256), K K^T -> [256,320) (M = 64; read in round C's epilogue)
-    // (one thread per product: a single thread issues tcgen05.mma at a far lower rate than
-    // the tensor core retires these small shapes)
+    // (one thread per product, five warps: a single thread issues tcgen05.mma at a far lower
+    // rate than the tensor core retires these small shapes)
     if (issuer) {
       if (warp == 0) {
         for (int ks = 0; ks < 8; ++ks)  // K = dk
@@ -424,12 +424,13 @@ __global__ void __launch_bounds__(GT, 1)
         for (int ks = 0; ks < 8; ++ks)  // K = dv
           mma_bf16(tmem + 192, dsc16(L.s + (ks >> 2) * 16384 + (ks & 3) * 32),
                    dsc16(L.dO + (ks >> 2) * 8192 + (ks & 3) * 32), idD, ks > 0);
-      } else {
+      } else if (warp == 3) {
         const uint32_t id64d = idesc_bf16(64, 64, 0, 0);
         for (int ks = 0; ks < 8; ++ks) {  // K = dk
           const uint64_t d = dsc16(L.k + (ks >> 2) * 8192 + (ks & 3) * 32);
           mma_bf16(tmem + 256, d, d, id64d, ks > 0);
         }
+      } else {
         for (int ks = 0; ks < 4; ++ks)  // K = tokens
           mma_bf16(tmem + 64, dsc8192(L.dO + ks * 2048), dsc8192(L.p + ks * 2048), idC, ks > 0);
       }
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(GT, 1)
         for (int ks = 0; ks < 8; ++ks)  // K = dv
           mma_bf16(tmem + 192, dsc16(L.dO + (ks >> 2) * 8192 + (ks & 3) * 32),
                    dsc8192(L.vt + ks * 2048), id64b, ks > 0);
-      } else {
+      } else if (warp == 3) {
         for (int ks = 0; ks < 4; ++ks)  // K = tokens
           mma_bf16(tmem + 128, dsc16(L.dvt + ks * 32), dsc8192(L.t + ks * 2048), idB, ks > 0);
       }
@@ -569,7 +570,7 @@ __global__ void __launch_bounds__(GT, 1)
         for (int ks = 0; ks < 8; ++ks)  // K = dv
           mma_bf16(tmem + 448, dsc8192(L.u + ks * 2048), dsc8192(L.vt + ks * 2048), id64c, ks > 0);
       }
-      mma_commit(bar_mma);  // warp 3 has nothing to issue: its commit arrives at once
+      mma_commit(bar_mma);  // warps 3, 4 have nothing to issue: their commits arrive at once
     }
     {  // while round C runs: Kt part of dk, dv, and the row dots of V' dS^T and X_v
       const int f = fr;
