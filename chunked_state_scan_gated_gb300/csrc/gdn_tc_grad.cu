@@ -194,9 +194,10 @@ __global__ void __launch_bounds__(GT, 1)
   const int ri = quad * 16 + (lane & 15);
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const bool issuer = warp < 5 && lane == 0;  // issues one product per MMA round
+  const bool mover = tid == 160;  // issues every tile copy and store (warp 5: no MMA issue)
   enum { RQ = 0, RV = 1, RKW = 2, RKD = 3 };  // column-sum types
   enum { GQK = 0, GA = 1, GB = 2 };            // load groups
-  uint32_t armed = 0;  // tid 0: bit 3 l + g: group g of layout l armed and not yet consumed
+  uint32_t armed = 0;  // mover: bit 3 l + g: group g of layout l armed and not yet consumed
 
   if (tid == 0) {
     for (int i = 0; i < 6; ++i) mbar_init(bars + i, 1);
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(GT, 1)
     const Item it0 = item_of(blockIdx.x);
     gates(gate_in(it0), it0.h, sGate);
   }
-  if (tid == 0 && blockIdx.x < ar.NW) {  // every tile of the first chunk
+  if (mover && blockIdx.x < ar.NW) {  // every tile of the first chunk
     const Item it = item_of(blockIdx.x);
     const Lay L = layout_of(0);
     ld_qk(it, L, 0);
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(GT, 1)
     float* sBeta = sG + 128;
     float* sKt = sG + 192;
     __syncthreads();  // the previous chunk's scalars have been consumed, these gates written
-    if (tid == 0 && k > 0) {  // tiles of this chunk that waited for the previous stores
+    if (mover && k > 0) {  // tiles of this chunk that waited for the previous stores
       bulk_wait_read();  // the previous chunk's dv, dq, dk stores have read their slots
       if (lc == 1)
         ld_v(it, L, lc);  // where the dv staging was
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(GT, 1)
       st_chunk(sm, off, x);
     }
     if (!mbar_wait(bars + 3 * lc + GA, bpar, ar.status, kStatusTimeout)) *s_abort = 1;
-    if (tid == 0) armed &= ~((1u << (3 * lc + GQK)) | (1u << (3 * lc + GA)));
+    armed &= ~((1u << (3 * lc + GQK)) | (1u << (3 * lc + GA)));
     if (t0 + 64 > L_len) {
       for (int idx = tid; idx < 1024; idx += GT) {
         const int i = idx >> 4, cc = idx & 15;
@@ -450,7 +451,7 @@ __global__ void __launch_bounds__(GT, 1)
       if (lane == 0) sMisc[warp] = acc;
     }
     if (!mbar_wait(bars + 3 * lc + GB, bpar, ar.status, kStatusTimeout)) *s_abort = 1;
-    if (tid == 0) armed &= ~(1u << (3 * lc + GB));
+    armed &= ~(1u << (3 * lc + GB));
     if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
     ph ^= 1;
     tc_fence_after();
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(GT, 1)
         st_chunk(sm + L.dvt, kmaj_chunk(f, 2 * part + cc), &a1[cc * 8]);
       }
     }
-    if (tid == 0) bulk_wait_read();  // the previous chunk's dq/dk/dv stores have read their slots
+    if (mover) bulk_wait_read();  // the previous chunk's dq/dk/dv stores have read their slots
     GRAD_SYNC();
     // ---- round B: S dV'^T -> [0,64) (-dW^T), dS V'^T -> [64,128), dV'^T T -> [128,192) (X_v^T),
     //      dO V'^T -> [192,256) (dP, M = 64)
@@ -513,7 +514,7 @@ __global__ void __launch_bounds__(GT, 1)
     if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
     ph ^= 1;
     tc_fence_after();
-    if (tid == 0 && more) {  // S and dV'^T are consumed: the next chunk's S (and dO)
+    if (mover && more) {  // S and dV'^T are consumed: the next chunk's S (and dO)
       arm(ln, GA, kBytesA);
       ld_s(nx, N, ln);
       if (lc == 0) ld_do(nx, N, ln);
@@ -597,7 +598,7 @@ __global__ void __launch_bounds__(GT, 1)
     if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
     ph ^= 1;
     tc_fence_after();
-    if (tid == 0 && more) {  // dW^T, X_v^T and V'^T (and dV'^T) are consumed: next W and dS
+    if (mover && more) {  // dW^T, X_v^T and V'^T (and dV'^T) are consumed: next W and dS
       ld_w(nx, N, ln);
       ld_ds(nx, N, ln);
       if (lc == 1) {
@@ -639,7 +640,7 @@ __global__ void __launch_bounds__(GT, 1)
     GRAD_SYNC();
     // ---- round D: Q^T (dP o Gamma) -> [0,64), K^T E^T -> [64,128), K^T E -> [128,192)
     //      (three products from three warps, summed in the epilogue)
-    if (tid == 0) {
+    if (mover) {
       tma_store_4d(&mdv, sm + L.dO, 0, (int)h, (int)t0, (int)b);  // dv tile (clipped past T)
       tma_store_4d(&mdv, sm + L.dO + 8192, 64, (int)h, (int)t0, (int)b);
       bulk_commit();
@@ -657,7 +658,7 @@ __global__ void __launch_bounds__(GT, 1)
       }
       mma_commit(bar_mma);
     }
-    if (tid == 0) {
+    if (mover) {
       if (more && lc == 0) {  // V (read before the last barrier) is consumed: the next U
         arm(ln, GB, kBytesB);
         ld_u(nx, N, ln);
@@ -687,7 +688,7 @@ __global__ void __launch_bounds__(GT, 1)
     if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
     ph ^= 1;
     tc_fence_after();
-    if (tid == 0 && more) {  // P (dP o Gamma) and T (E) are consumed
+    if (mover && more) {  // P (dP o Gamma) and T (E) are consumed
       ld_p(nx, N, ln);
       ld_t(nx, N, ln);
     }
@@ -706,7 +707,7 @@ __global__ void __launch_bounds__(GT, 1)
       }
     }
     GRAD_SYNC();
-    if (tid == 0) {
+    if (mover) {
       tma_store_4d(&mdqp, sm + L.ds0, 0, (int)h, (int)t0, (int)b);  // dq_hat tile
       tma_store_4d(&mdqp, sm + L.ds0 + 8192, 64, (int)h, (int)t0, (int)b);
       tma_store_4d(&mdkp, sm + L.ds1, 0, (int)h, (int)t0, (int)b);
@@ -772,8 +773,8 @@ __global__ void __launch_bounds__(GT, 1)
     }
   }
 done:
-  if (tid == 0) bulk_wait_all();
-  if (tid == 0 && armed) {  // abort: let every copy still in flight land before the CTA exits
+  if (mover) bulk_wait_all();
+  if (armed) {  // abort: let every copy still in flight land before the CTA exits
     for (int i = 0; i < 6; ++i)
       if (armed & (1u << i)) {
         // one of the two parities is the phase in flight; the other returns at once
