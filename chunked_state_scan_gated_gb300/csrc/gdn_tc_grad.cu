@@ -458,10 +458,8 @@ __global__ void __launch_bounds__(GT, 1)
     {  // V'^T and dV'^T: the operands of round B
       const int f = fr;
       float ws[16], a1[16], a2[16];
-      tmem_ld16(tmem + lane_off + cb, ws);
-      tmem_ld16(tmem + lane_off + 64 + cb, a1);
-      tmem_ld16(tmem + lane_off + 128 + cb, a2);
-      tmem_ld16(tmem + lane_off + 192 + cb, dqT);
+      tmem_ld16x4(tmem + lane_off + cb, tmem + lane_off + 64 + cb, tmem + lane_off + 128 + cb,
+                  tmem + lane_off + 192 + cb, ws, a1, a2, dqT);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
@@ -521,17 +519,16 @@ __global__ void __launch_bounds__(GT, 1)
     }
     {  // -dW^T, X_v^T and dP o Gamma: the operands of round C
       const int f = fr;
-      float x[16];
-      tmem_ld16(tmem + lane_off + cb, x);                  // S dV'^T = -dW^T
+      // S dV'^T = -dW^T, X_v^T and dP (M = 64 layout)
+      float x[16], xv[16], dp[16], z[16];
+      tmem_ld16x3(tmem + lane_off + cb, tmem + lane_off + 128 + cb, tmem + lane_off + 192 + cb, x,
+                  xv, dp);
 #pragma unroll
       for (int e = 0; e < 16; ++e) x[e] = -x[e];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) st_chunk(sm + L.w, kmaj_chunk(f, 2 * part + cc), &x[cc * 8]);
-      tmem_ld16(tmem + lane_off + 128 + cb, x);            // X_v^T
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) st_chunk(sm + L.u, kmaj_chunk(f, 2 * part + cc), &x[cc * 8]);
-      float dp[16], z[16];
-      tmem_ld16(tmem + lane_off + 192 + cb, dp);           // dP (M = 64 layout)
+      for (int cc = 0; cc < 2; ++cc) st_chunk(sm + L.u, kmaj_chunk(f, 2 * part + cc), &xv[cc * 8]);
       const int i = ri;
       float pv[16];
 #pragma unroll
@@ -575,8 +572,8 @@ __global__ void __launch_bounds__(GT, 1)
     }
     {  // while round C runs: Kt part of dk, dv, and the row dots of V' dS^T and X_v
       const int f = fr;
-      float x[16], pk[16];
-      tmem_ld16(tmem + lane_off + 64 + cb, x);             // (V' dS^T)^T
+      float x[16], xv[16], pk[16];
+      tmem_ld16x2(tmem + lane_off + 64 + cb, tmem + lane_off + 128 + cb, x, xv);  // (V' dS^T)^T, X_v^T
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
@@ -585,12 +582,11 @@ __global__ void __launch_bounds__(GT, 1)
       }
       float red = xreduce16(pk, lane);
       if (lane < 16) sRed[(RKD * 4 + quad) * 64 + cb + lane] = red;
-      tmem_ld16(tmem + lane_off + 128 + cb, x);            // X_v^T
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
-        pk[e] = ld_bf(sm + L.v + tf_off(t, f)) * x[e];    // v_t . X_v,t
-        st_bf(sm + L.dO + tf_off(t, f), (t0 + t < L_len) ? sBeta[t] * x[e] : 0.f);  // dv staging
+        pk[e] = ld_bf(sm + L.v + tf_off(t, f)) * xv[e];   // v_t . X_v,t
+        st_bf(sm + L.dO + tf_off(t, f), (t0 + t < L_len) ? sBeta[t] * xv[e] : 0.f);  // dv staging
       }
       red = xreduce16(pk, lane);
       if (lane < 16) sRed[(RV * 4 + quad) * 64 + cb + lane] = red;
@@ -608,8 +604,7 @@ __global__ void __launch_bounds__(GT, 1)
     }
     {  // E (operand of round D), dA o A, dbeta terms of A
       float da[16], kk[16], z[16];
-      tmem_ld16(tmem + lane_off + 448 + cb, da);           // dA' (M = 64 layout)
-      tmem_ld16(tmem + lane_off + 256 + cb, kk);           // K K^T (M = 64 layout)
+      tmem_ld16x2(tmem + lane_off + 448 + cb, tmem + lane_off + 256 + cb, da, kk);  // dA', K K^T (M = 64)
       const int i = ri;
       const float be = sBeta[i];
       float pt = 0.f, zr = 0.f;
@@ -667,8 +662,8 @@ __global__ void __launch_bounds__(GT, 1)
     }
     {  // while round D runs: X_w part of dk, dq_hat staging, row dots of X_w
       const int f = fr;
-      float x[16], pk[16];
-      tmem_ld16(tmem + lane_off + 320 + cb, x);            // X_w^T
+      float x[16], xd[16], pk[16];
+      tmem_ld16x2(tmem + lane_off + 320 + cb, tmem + lane_off + 384 + cb, x, xd);  // X_w^T, ((dP o Gamma) K)^T
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
@@ -678,11 +673,10 @@ __global__ void __launch_bounds__(GT, 1)
       }
       const float red = xreduce16(pk, lane);
       if (lane < 16) sRed[(RKW * 4 + quad) * 64 + cb + lane] = red;
-      tmem_ld16(tmem + lane_off + 384 + cb, x);            // (dP o Gamma) K, transposed
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
-        st_bf(sm + L.ds0 + tf_off(t, f), (t0 + t < L_len) ? dqT[e] + x[e] : 0.f);  // dq_hat staging
+        st_bf(sm + L.ds0 + tf_off(t, f), (t0 + t < L_len) ? dqT[e] + xd[e] : 0.f);  // dq_hat staging
       }
     }
     if (!mbar_wait(bar_mma, ph, ar.status, kStatusTimeout)) *s_abort = 1;
@@ -694,16 +688,13 @@ __global__ void __launch_bounds__(GT, 1)
     }
     {
       const int f = fr;
-      float x[16], y[16];
-      tmem_ld16(tmem + lane_off + cb, x);
-      tmem_ld16(tmem + lane_off + 64 + cb, y);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) dkT[e] += x[e] + y[e];
-      tmem_ld16(tmem + lane_off + 128 + cb, x);
+      float x[16], y[16], z3[16];
+      tmem_ld16x3(tmem + lane_off + cb, tmem + lane_off + 64 + cb, tmem + lane_off + 128 + cb, x, y,
+                  z3);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = cb + e;
-        st_bf(sm + L.ds1 + tf_off(t, f), (t0 + t < L_len) ? dkT[e] + x[e] : 0.f);  // dk_hat
+        st_bf(sm + L.ds1 + tf_off(t, f), (t0 + t < L_len) ? dkT[e] + x[e] + y[e] + z3[e] : 0.f);  // dk_hat
       }
     }
     GRAD_SYNC();
