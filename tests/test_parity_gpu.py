@@ -193,6 +193,37 @@ def test_bf16_small_fwd_bwd_matches_oracle(case):
             assert (o[bi, Lb:] == 0).all()
 
 
+@pytest.mark.parametrize("r, l2norm", [(1, True), (2, False), (4, False)],
+                         ids=["r1_l2norm", "r2_raw_qk", "r4_raw_qk"])
+def test_bf16_head_groups_and_raw_qk(r, l2norm):
+    """dq, dk summed over each Q/K head's r V heads (r = 1, 2, 4), with and without the
+    L2 norm of q and k (without it: q_hat = scale q, k_hat = k; the raw q, k are drawn
+    small so that the recurrence stays contractive)."""
+    w = gi.Workload(f"bf16_r{r}", B=2, T=200, Hqk=2, H=2 * r, dk=128, dv=128,
+                    dtype=torch.bfloat16, h0_std=0.1, with_dHT=True, valid_len=[200, 133],
+                    decay_stress=True, seed=41 + r)
+    inp = gi.make_inputs(w)
+    kw = {}
+    if not l2norm:
+        for nm in ("q", "k"):
+            inp[nm] = (inp[nm].float() * 0.07).to(torch.bfloat16)
+        kw = dict(l2norm=False, scale=0.5)
+    d = dev(inp)
+    o, hT = gdn.gdn_fwd(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                        d["h0"], d["valid_len"], segments=2, **kw)
+    grads = gdn.gdn_bwd(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                        d["dO"], d["dHT"], d["h0"], d["valid_len"], segments=2, **kw)
+    torch.cuda.synchronize()
+    n = np64(inp)
+    ro, rhT = oracle_fwd(n, **kw)
+    assert_close("o", o, ro, w.dtype)
+    assert_close("hT", hT, rhT, w.dtype)
+    for name, g, rg in zip(NAMES_BWD, grads, oracle_bwd(n, **kw)):
+        assert_close(name, g, rg, w.dtype)
+    for bi, Lb in enumerate(w.valid_len):  # padded tokens: zero dq, dk
+        assert (grads[0][bi, Lb:] == 0).all() and (grads[1][bi, Lb:] == 0).all()
+
+
 def test_bf16_summary_matches_oracle():
     w = gi.Workload("bf16_summary", B=2, T=190, Hqk=1, H=2, dk=128, dv=128, dtype=torch.bfloat16,
                     decay_stress=True, valid_len=[190, 150], seed=18)
