@@ -277,3 +277,7 @@ def prefix_bwd(M, D, dHT=None):
     _check(_load().oracle_prefix_bwd(n, P, dk, dv, _ptr(M), _ptr(D), _ptr(dHT), _ptr(dHout),
                                      _ptr(dH0)), "prefix_bwd")
     return dHout, dH0
+
+
+# The causal depthwise Conv1D + SiLU prologue (numpy, fp64): see oracle/conv.py.
+from .conv import conv_silu_bwd, conv_silu_fwd  # noqa: E402,F401
