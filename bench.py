@@ -522,6 +522,46 @@ def run_ours(args):
         line["kernel_roofline"] = kr
         line["kernel_ms"] = {k: round(v, 4) for k, v in tot.items()}
 
+    # The Conv1D + SiLU prologue over the projected q, k, v of this workload (C = 2 Hqk dk +
+    # H dv channels, K = 4 taps, a left halo, no bias): forward and backward, each timed
+    # alone with CUDA events, against the measured HBM bandwidth (both are bandwidth-bound:
+    # x read and y written; x, dy read and dx written).
+    if not args.no_kernel_profile:
+        Cc, Kc = 2 * w.Hqk * w.dk + w.H * w.dv, 4
+        ci = gi.make_conv_inputs(B, T, Cc, Kc, torch.bfloat16, seed=w.seed + 77, bias=False)
+        cd = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in ci.items()}
+        cp = gdn.make_conv_problem(cd["x"], Kc)
+        cy = torch.empty_like(cd["x"])
+        cdx = torch.empty_like(cd["x"])
+        cdw = torch.empty((Cc, Kc), dtype=torch.float32, device="cuda")
+        cdh = torch.empty_like(cd["halo"])
+        cws = torch.empty(gdn.gdn_conv_silu_bwd_workspace_size(cp), dtype=torch.uint8,
+                          device="cuda")
+
+        def conv_f():
+            gdn.gdn_conv_silu_fwd(cd["x"], cd["w"], None, cd["halo"], y=cy, problem=cp,
+                                  stream=stream)
+
+        def conv_b():
+            gdn.gdn_conv_silu_bwd(cd["x"], cd["w"], None, cd["halo"], cd["dy"], dx=cdx, dw=cdw,
+                                  dhalo=cdh, want_dbias=False, ws=cws, problem=cp, stream=stream)
+
+        for _ in range(3):
+            conv_f()
+            conv_b()
+        ms_cf, ms_cb = timed(conv_f, args.steps), timed(conv_b, args.steps)
+        el = B * T * Cc
+        bytes_f, bytes_b = 4 * el, 6 * el + B * (Kc - 1) * Cc * 4 + Cc * Kc * 4
+        line["conv1d_silu"] = {
+            "shape": f"B={B} T={T} C={Cc} K={Kc} bf16, halo, no bias",
+            "fwd_ms": ms_cf, "bwd_ms": ms_cb,
+            "fwd_gbs": bytes_f / (ms_cf / 1e3) / 1e9, "bwd_gbs": bytes_b / (ms_cb / 1e3) / 1e9,
+            "fwd_frac": bytes_f / (ms_cf / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "bwd_frac": bytes_b / (ms_cb / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "algorithmic_bytes": {"fwd": bytes_f, "bwd": bytes_b},
+            "peak": f"{peaks['hbm_gbs']} GB/s ({peaks['source']})"}
+        del cd, cy, cdx, cdw, cdh, cws
+
     # End to end: pinned host inputs copied in, fwd + bwd, result states read back, every
     # step.  As an input pipeline would, the inputs are double-buffered on the device: the
     # copies of step i + 1 (on E2E_COPY_STREAMS side streams) run while step i computes; the

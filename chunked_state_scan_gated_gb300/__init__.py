@@ -38,7 +38,8 @@ EXPORTS = (
     "gdn_compose", "gdn_prefix_compose", "gdn_prefix_compose_bwd", "gdn_apply_state",
     "gdn_apply_state_bwd", "gdn_check_device_status", "gdn_kernel_info", "gdn_fwd_kernel",
     "gdn_bwd_kernel", "gdn_fwd_noalloc", "gdn_ctx_size", "gdn_fwd_ctx", "gdn_bwd_ctx",
-    "gdn_fwd_ctx_kernel", "gdn_bwd_ctx_kernel",
+    "gdn_fwd_ctx_kernel", "gdn_bwd_ctx_kernel", "gdn_conv_silu_fwd",
+    "gdn_conv_silu_bwd_workspace_size", "gdn_conv_silu_bwd",
 )
 
 
@@ -58,11 +59,19 @@ class Problem(ctypes.Structure):
                 ("scale", ctypes.c_float), ("segments", ctypes.c_int32)]
 
 
+class ConvProblem(ctypes.Structure):
+    """Mirror of ``gdn_conv_problem`` (include/gdn.h)."""
+
+    _fields_ = [("dtype", ctypes.c_int32), ("K", ctypes.c_int32), ("B", ctypes.c_int64),
+                ("T", ctypes.c_int64), ("C", ctypes.c_int64), ("T_stride", ctypes.c_int64)]
+
+
 _lock = threading.Lock()
 _lib = None
 _VP = ctypes.c_void_p
 _PP = ctypes.POINTER(Problem)
 _I64 = ctypes.c_int64
+_CPP = ctypes.POINTER(ConvProblem)
 
 
 def load_library(path: str | None = None):
@@ -114,6 +123,10 @@ def load_library(path: str | None = None):
                                    + [ctypes.c_size_t, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
             "gdn_bwd_ctx_kernel": ([_PP, ctypes.c_int32] + [_VP] * 8 + [ctypes.c_size_t]
                                    + [_VP] * 10 + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_conv_silu_fwd": ([_CPP] + [_VP] * 6, ctypes.c_int),
+            "gdn_conv_silu_bwd_workspace_size": ([_CPP, ctypes.POINTER(ctypes.c_size_t)],
+                                                 ctypes.c_int),
+            "gdn_conv_silu_bwd": ([_CPP] + [_VP] * 10 + [ctypes.c_size_t, _VP], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -537,3 +550,55 @@ class GDNCore(torch.autograd.Function):
         # dg and dbeta are w.r.t. g and beta; the parameter chain to a, b,
         # A_log, dt_bias is not part of this operator.
         return dq, dk, dv, None, None, None, None, dH0, None, None
+
+
+# ------------------------------------------------ causal depthwise Conv1D + SiLU prologue
+
+def make_conv_problem(x: torch.Tensor, K: int, *, T: int | None = None,
+                      T_stride: int = 0) -> ConvProblem:
+    """Problem for x [B, T_stride, C] (tokens [0, T) of each row) and K taps."""
+    B, Tx, C = x.shape
+    p = ConvProblem()
+    p.dtype = _dtype_code(x.dtype)
+    p.K = K
+    p.B, p.T, p.C, p.T_stride = B, (Tx if T is None else T), C, T_stride
+    return p
+
+
+def gdn_conv_silu_bwd_workspace_size(problem: ConvProblem) -> int:
+    n = ctypes.c_size_t(0)
+    _check("gdn_conv_silu_bwd_workspace_size", load_library().gdn_conv_silu_bwd_workspace_size(
+        ctypes.byref(problem), ctypes.byref(n)))
+    return n.value
+
+
+def gdn_conv_silu_fwd(x, w, bias=None, halo=None, *, y=None, stream=None, problem=None):
+    """y = silu(causal depthwise conv of x with w [C, K] (+ bias [C]), the K - 1 tokens of
+    halo [B, K-1, C] before token 0).  x [B, T, C] bf16 or fp32; w, bias fp32."""
+    p = problem or make_conv_problem(x, w.shape[1])
+    y = y if y is not None else torch.empty_like(x)
+    _check("gdn_conv_silu_fwd", load_library().gdn_conv_silu_fwd(
+        ctypes.byref(p), _ptr(x), _ptr(w), _ptr(bias), _ptr(halo), _ptr(y), _stream(stream)))
+    return y
+
+
+def gdn_conv_silu_bwd(x, w, bias, halo, dy, *, want_dbias=True, want_dhalo=True, dx=None,
+                      dw=None, dbias=None, dhalo=None, ws=None, stream=None, problem=None):
+    """(dx [B,T,C], dw [C,K] fp32, dbias [C] fp32 or None, dhalo [B,K-1,C] or None)."""
+    p = problem or make_conv_problem(x, w.shape[1])
+    B, _, C = x.shape
+    K = w.shape[1]
+    f32 = dict(dtype=torch.float32, device=x.device)
+    dx = dx if dx is not None else torch.empty_like(x)
+    dw = dw if dw is not None else torch.empty((C, K), **f32)
+    if want_dbias and dbias is None:
+        dbias = torch.empty((C,), **f32)
+    if want_dhalo and dhalo is None and K > 1:
+        dhalo = torch.empty((B, K - 1, C), dtype=x.dtype, device=x.device)
+    if ws is None:
+        ws = torch.empty(max(gdn_conv_silu_bwd_workspace_size(p), 16), dtype=torch.uint8,
+                         device=x.device)
+    _check("gdn_conv_silu_bwd", load_library().gdn_conv_silu_bwd(
+        ctypes.byref(p), _ptr(x), _ptr(w), _ptr(bias), _ptr(halo), _ptr(dy), _ptr(dx), _ptr(dw),
+        _ptr(dbias), _ptr(dhalo), _ptr(ws), ws.numel(), _stream(stream)))
+    return dx, dw, dbias, dhalo

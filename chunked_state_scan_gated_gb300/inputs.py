@@ -119,3 +119,19 @@ def to_numpy64(inputs: dict) -> dict:
         else:
             res[key] = val.to(torch.float64).numpy()
     return res
+
+
+def make_conv_inputs(B: int, T: int, C: int, K: int, dtype=torch.bfloat16, *, seed: int = 0,
+                     halo: bool = True, bias: bool = True, T_stride: Optional[int] = None) -> dict:
+    """Seeded inputs of the Conv1D + SiLU prologue, on the CPU: x, dy [B, T_stride, C] in
+    `dtype` (T_stride >= T tokens per row, N(0, 1)), w [C, K] fp32 (N(0, 0.25)), bias [C]
+    fp32 (N(0, 0.01)) or None, halo [B, K-1, C] in `dtype` (N(0, 1)) or None.  C is the
+    channel count of the projected q, k, v the convolution runs over (2 Hqk dk + H dv)."""
+    Ts = T if T_stride is None else T_stride
+    gen = torch.Generator().manual_seed(seed)
+    out = {"x": _normal(gen, (B, Ts, C)).to(dtype),
+           "w": 0.5 * _normal(gen, (C, K)),
+           "bias": 0.1 * _normal(gen, (C,)) if bias else None,
+           "halo": _normal(gen, (B, K - 1, C)).to(dtype) if (halo and K > 1) else None,
+           "dy": _normal(gen, (B, Ts, C)).to(dtype)}
+    return out

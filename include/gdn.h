@@ -341,6 +341,41 @@ gdn_status gdn_fwd_noalloc(const gdn_problem* p, const void* q, const void* k, c
  */
 gdn_status gdn_check_device_status(void* workspace, void* stream);
 
+/*
+ * Causal depthwise Conv1D + SiLU over time: the step that feeds q, k, v to the core
+ * ("linear attention cp #1035", section "What does this PR do": the depthwise Conv1D
+ * runs before the Gated DeltaNet, and in its "p2p" mode each rank exchanges only the
+ * left halo that the Conv1D needs with its neighbour).  For row b and channel c, with
+ * x~ the row preceded by the K - 1 halo tokens (zeros when halo is null):
+ *   a[t] = bias[c] + sum_{i<K} w[c][i] x~[t - (K-1) + i],   y[t] = a[t] sigmoid(a[t]).
+ * Backward: dx and dhalo (the gradient of the halo tokens, for the rank that sent
+ * them), dw = sum_{b,t} ds x~, dbias = sum_{b,t} ds with ds = dy * silu'(a).
+ * Layouts (channel innermost): x, y, dy, dx [B][T_stride][C], the first T tokens of
+ * each row used; halo, dhalo [B][K-1][C]; w, dw [C][K] and bias, dbias [C] fp32.
+ * x, y, dy, dx, halo, dhalo are in p->dtype (GDN_BF16 or GDN_FP32); fp32 arithmetic;
+ * dw and dbias are summed in a fixed order (deterministic).  bias, halo (both calls)
+ * and dbias, dhalo (backward) may be null.  The caller owns every buffer; the calls
+ * are stream-ordered and never synchronise.  Errors: null required pointer, a pointer
+ * not 16-byte aligned, B or T < 0, C < 1, T_stride < T: GDN_ERR_INVALID_ARG; C times the
+ * element size not a multiple of 16 bytes (C % 8 for bf16, C % 4 for fp32) or K outside
+ * 1..4: GDN_ERR_UNSUPPORTED; workspace smaller than gdn_conv_silu_bwd_workspace_size:
+ * GDN_ERR_WORKSPACE.
+ */
+typedef struct {
+  int32_t dtype;    /* GDN_BF16 or GDN_FP32 */
+  int32_t K;        /* taps, 1..4 */
+  int64_t B, T, C;  /* rows, tokens, channels */
+  int64_t T_stride; /* tokens between the rows of x, y, dy, dx; 0 means T */
+} gdn_conv_problem;
+
+gdn_status gdn_conv_silu_fwd(const gdn_conv_problem* p, const void* x, const float* w,
+                             const float* bias, const void* halo, void* y, void* stream);
+gdn_status gdn_conv_silu_bwd_workspace_size(const gdn_conv_problem* p, size_t* bytes);
+gdn_status gdn_conv_silu_bwd(const gdn_conv_problem* p, const void* x, const float* w,
+                             const float* bias, const void* halo, const void* dy, void* dx,
+                             float* dw, float* dbias, void* dhalo, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -180,3 +180,48 @@ def test_ctx_size_and_validation(lib):
     names = gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD_CTX)
     assert "summary_pair_tc" not in names and "grad_tc" in names      # no forward summaries
     assert gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD_CTX)[-1] == "apply_chain_tc"
+
+
+def test_conv_validation_and_workspace(lib):
+    """Host-side checks of the Conv1D + SiLU calls (no launch reaches CUDA)."""
+    A = 1 << 20  # a 16-byte-aligned fake device address; validation fails before any use
+
+    def prob(**kw):
+        p = gdn.ConvProblem()
+        p.dtype, p.K, p.B, p.T, p.C, p.T_stride = gdn.GDN_BF16, 4, 2, 300, 256, 0
+        for k, v in kw.items():
+            setattr(p, k, v)
+        return p
+
+    n = ctypes.c_size_t(0)
+    assert lib.gdn_conv_silu_bwd_workspace_size(ctypes.byref(prob()), ctypes.byref(n)) == 0
+    assert n.value == 2 * 3 * 256 * 5 * 4  # 2 rows x 3 tiles of 128 tokens x C x (K + 1) fp32
+    assert lib.gdn_conv_silu_bwd_workspace_size(ctypes.byref(prob()), None) == \
+        gdn.GDN_ERR_INVALID_ARG
+    vp = ctypes.c_void_p
+    for kw, status in (({"K": 5}, gdn.GDN_ERR_UNSUPPORTED), ({"K": 0}, gdn.GDN_ERR_UNSUPPORTED),
+                       ({"C": 6}, gdn.GDN_ERR_UNSUPPORTED), ({"C": 12}, gdn.GDN_ERR_UNSUPPORTED),
+                       ({"C": 0}, gdn.GDN_ERR_INVALID_ARG),
+                       ({"T": -1}, gdn.GDN_ERR_INVALID_ARG),
+                       ({"T_stride": 10}, gdn.GDN_ERR_INVALID_ARG),
+                       ({"dtype": 7}, gdn.GDN_ERR_INVALID_ARG)):
+        p = prob(**kw)
+        assert lib.gdn_conv_silu_fwd(ctypes.byref(p), vp(A), vp(A), None, None, vp(A),
+                                     None) == status, kw
+        assert lib.gdn_conv_silu_bwd(ctypes.byref(p), vp(A), vp(A), None, None, vp(A), vp(A),
+                                     vp(A), None, None, vp(A), 1 << 30, None) == status, kw
+    p = prob()
+    # null or misaligned required pointers
+    assert lib.gdn_conv_silu_fwd(ctypes.byref(p), None, vp(A), None, None, vp(A), None) == \
+        gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_conv_silu_fwd(ctypes.byref(p), vp(A + 8), vp(A), None, None, vp(A), None) == \
+        gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_conv_silu_fwd(ctypes.byref(p), vp(A), None, None, None, vp(A), None) == \
+        gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_conv_silu_bwd(ctypes.byref(p), vp(A), vp(A), None, None, None, vp(A), vp(A),
+                                 None, None, vp(A), 1 << 30, None) == gdn.GDN_ERR_INVALID_ARG
+    # workspace too small or missing
+    assert lib.gdn_conv_silu_bwd(ctypes.byref(p), vp(A), vp(A), None, None, vp(A), vp(A), vp(A),
+                                 None, None, vp(A), n.value - 16, None) == gdn.GDN_ERR_WORKSPACE
+    assert lib.gdn_conv_silu_bwd(ctypes.byref(p), vp(A), vp(A), None, None, vp(A), vp(A), vp(A),
+                                 None, None, None, 0, None) == gdn.GDN_ERR_WORKSPACE
