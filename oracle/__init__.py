@@ -281,3 +281,5 @@ def prefix_bwd(M, D, dHT=None):
 
 # The causal depthwise Conv1D + SiLU prologue (numpy, fp64): see oracle/conv.py.
 from .conv import conv_silu_bwd, conv_silu_fwd  # noqa: E402,F401
+# The gated RMSNorm epilogue on o (numpy, fp64): see oracle/rmsnorm.py.
+from .rmsnorm import rmsnorm_gated_bwd, rmsnorm_gated_fwd  # noqa: E402,F401
