@@ -562,6 +562,38 @@ def run_ours(args):
             "peak": f"{peaks['hbm_gbs']} GB/s ({peaks['source']})"}
         del cd, cy, cdx, cdw, cdh, cws
 
+        # The gated RMSNorm epilogue on o (rows = B T H, D = dv), forward and backward.
+        ri = gi.make_rmsnorm_inputs((B, T, H, dv), torch.bfloat16, seed=w.seed + 78)
+        rd = {k: v.cuda() for k, v in ri.items()}
+        rp = gdn.make_rmsnorm_problem(rd["o"])
+        ry, rdo, rdz = (torch.empty_like(rd["o"]) for _ in range(3))
+        rdw = torch.empty((dv,), dtype=torch.float32, device="cuda")
+        rws = torch.empty(gdn.gdn_rmsnorm_gated_bwd_workspace_size(rp), dtype=torch.uint8,
+                          device="cuda")
+
+        def rms_f():
+            gdn.gdn_rmsnorm_gated_fwd(rd["o"], rd["z"], rd["w"], y=ry, problem=rp, stream=stream)
+
+        def rms_b():
+            gdn.gdn_rmsnorm_gated_bwd(rd["o"], rd["z"], rd["w"], rd["dy"], d_o=rdo, dz=rdz, dw=rdw,
+                                      ws=rws, problem=rp, stream=stream)
+
+        for _ in range(3):
+            rms_f()
+            rms_b()
+        ms_rf, ms_rb = timed(rms_f, args.steps), timed(rms_b, args.steps)
+        el = B * T * H * dv
+        bytes_f, bytes_b = 6 * el, 10 * el
+        line["rmsnorm_gated"] = {
+            "shape": f"rows={B * T * H} D={dv} bf16",
+            "fwd_ms": ms_rf, "bwd_ms": ms_rb,
+            "fwd_gbs": bytes_f / (ms_rf / 1e3) / 1e9, "bwd_gbs": bytes_b / (ms_rb / 1e3) / 1e9,
+            "fwd_frac": bytes_f / (ms_rf / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "bwd_frac": bytes_b / (ms_rb / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "algorithmic_bytes": {"fwd": bytes_f, "bwd": bytes_b},
+            "peak": f"{peaks['hbm_gbs']} GB/s ({peaks['source']})"}
+        del rd, ry, rdo, rdz, rdw, rws
+
     # End to end: pinned host inputs copied in, fwd + bwd, result states read back, every
     # step.  As an input pipeline would, the inputs are double-buffered on the device: the
     # copies of step i + 1 (on E2E_COPY_STREAMS side streams) run while step i computes; the

@@ -39,7 +39,8 @@ EXPORTS = (
     "gdn_apply_state_bwd", "gdn_check_device_status", "gdn_kernel_info", "gdn_fwd_kernel",
     "gdn_bwd_kernel", "gdn_fwd_noalloc", "gdn_ctx_size", "gdn_fwd_ctx", "gdn_bwd_ctx",
     "gdn_fwd_ctx_kernel", "gdn_bwd_ctx_kernel", "gdn_conv_silu_fwd",
-    "gdn_conv_silu_bwd_workspace_size", "gdn_conv_silu_bwd",
+    "gdn_conv_silu_bwd_workspace_size", "gdn_conv_silu_bwd", "gdn_rmsnorm_gated_fwd",
+    "gdn_rmsnorm_gated_bwd_workspace_size", "gdn_rmsnorm_gated_bwd",
 )
 
 
@@ -66,12 +67,20 @@ class ConvProblem(ctypes.Structure):
                 ("T", ctypes.c_int64), ("C", ctypes.c_int64), ("T_stride", ctypes.c_int64)]
 
 
+class RmsNormProblem(ctypes.Structure):
+    """Mirror of ``gdn_rmsnorm_problem`` (include/gdn.h)."""
+
+    _fields_ = [("dtype", ctypes.c_int32), ("D", ctypes.c_int32), ("rows", ctypes.c_int64),
+                ("eps", ctypes.c_float)]
+
+
 _lock = threading.Lock()
 _lib = None
 _VP = ctypes.c_void_p
 _PP = ctypes.POINTER(Problem)
 _I64 = ctypes.c_int64
 _CPP = ctypes.POINTER(ConvProblem)
+_RPP = ctypes.POINTER(RmsNormProblem)
 
 
 def load_library(path: str | None = None):
@@ -127,6 +136,10 @@ def load_library(path: str | None = None):
             "gdn_conv_silu_bwd_workspace_size": ([_CPP, ctypes.POINTER(ctypes.c_size_t)],
                                                  ctypes.c_int),
             "gdn_conv_silu_bwd": ([_CPP] + [_VP] * 10 + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_rmsnorm_gated_fwd": ([_RPP] + [_VP] * 5, ctypes.c_int),
+            "gdn_rmsnorm_gated_bwd_workspace_size": ([_RPP, ctypes.POINTER(ctypes.c_size_t)],
+                                                     ctypes.c_int),
+            "gdn_rmsnorm_gated_bwd": ([_RPP] + [_VP] * 8 + [ctypes.c_size_t, _VP], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -602,3 +615,49 @@ def gdn_conv_silu_bwd(x, w, bias, halo, dy, *, want_dbias=True, want_dhalo=True,
         ctypes.byref(p), _ptr(x), _ptr(w), _ptr(bias), _ptr(halo), _ptr(dy), _ptr(dx), _ptr(dw),
         _ptr(dbias), _ptr(dhalo), _ptr(ws), ws.numel(), _stream(stream)))
     return dx, dw, dbias, dhalo
+
+
+# ------------------------------------------------------- gated RMSNorm epilogue on o
+
+def make_rmsnorm_problem(o: torch.Tensor, eps: float = 1e-6) -> RmsNormProblem:
+    """Problem for o [..., D]: every leading index is a row."""
+    p = RmsNormProblem()
+    p.dtype = _dtype_code(o.dtype)
+    p.D = o.shape[-1]
+    p.rows = o.numel() // max(o.shape[-1], 1)
+    p.eps = eps
+    return p
+
+
+def gdn_rmsnorm_gated_bwd_workspace_size(problem: RmsNormProblem) -> int:
+    n = ctypes.c_size_t(0)
+    _check("gdn_rmsnorm_gated_bwd_workspace_size",
+           load_library().gdn_rmsnorm_gated_bwd_workspace_size(ctypes.byref(problem),
+                                                                ctypes.byref(n)))
+    return n.value
+
+
+def gdn_rmsnorm_gated_fwd(o, z, w, eps=1e-6, *, y=None, stream=None, problem=None):
+    """y = o / sqrt(mean(o^2) + eps) * w * silu(z) over the last dim; o, z bf16 or fp32."""
+    p = problem or make_rmsnorm_problem(o, eps)
+    y = y if y is not None else torch.empty_like(o)
+    _check("gdn_rmsnorm_gated_fwd", load_library().gdn_rmsnorm_gated_fwd(
+        ctypes.byref(p), _ptr(o), _ptr(z), _ptr(w), _ptr(y), _stream(stream)))
+    return y
+
+
+def gdn_rmsnorm_gated_bwd(o, z, w, dy, eps=1e-6, *, d_o=None, dz=None, dw=None, ws=None,
+                          stream=None, problem=None):
+    """(do, dz in o's dtype, dw [D] fp32)."""
+    p = problem or make_rmsnorm_problem(o, eps)
+    d_o = d_o if d_o is not None else torch.empty_like(o)
+    dz = dz if dz is not None else torch.empty_like(z)
+    dw = dw if dw is not None else torch.empty((o.shape[-1],), dtype=torch.float32,
+                                               device=o.device)
+    if ws is None:
+        ws = torch.empty(max(gdn_rmsnorm_gated_bwd_workspace_size(p), 16), dtype=torch.uint8,
+                         device=o.device)
+    _check("gdn_rmsnorm_gated_bwd", load_library().gdn_rmsnorm_gated_bwd(
+        ctypes.byref(p), _ptr(o), _ptr(z), _ptr(w), _ptr(dy), _ptr(d_o), _ptr(dz), _ptr(dw),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return d_o, dz, dw

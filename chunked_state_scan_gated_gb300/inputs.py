@@ -135,3 +135,11 @@ def make_conv_inputs(B: int, T: int, C: int, K: int, dtype=torch.bfloat16, *, se
            "halo": _normal(gen, (B, K - 1, C)).to(dtype) if (halo and K > 1) else None,
            "dy": _normal(gen, (B, Ts, C)).to(dtype)}
     return out
+
+
+def make_rmsnorm_inputs(shape, dtype=torch.bfloat16, *, seed: int = 0) -> dict:
+    """Seeded inputs of the gated RMSNorm epilogue, on the CPU: o, z, dy of `shape`
+    ([B, T, H, dv]) in `dtype`, N(0, 1); w [dv] fp32, 1 + N(0, 0.1^2)."""
+    gen = torch.Generator().manual_seed(seed)
+    return {"o": _normal(gen, shape).to(dtype), "z": _normal(gen, shape).to(dtype),
+            "w": 1.0 + 0.1 * _normal(gen, (shape[-1],)), "dy": _normal(gen, shape).to(dtype)}

@@ -376,6 +376,34 @@ gdn_status gdn_conv_silu_bwd(const gdn_conv_problem* p, const void* x, const flo
                              float* dw, float* dbias, void* dhalo, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/*
+ * Gated RMSNorm on the core's output: the step after the core ("linear attention cp
+ * #1035", section "What does this PR do": the output goes through RMSNorm, the gate and
+ * the output projection; the test report names the module "RMSNormGated").  For every
+ * row of D elements (one token and V head of o [B,T,H,dv]: rows = B*T*H, D = dv), with
+ * r = 1 / sqrt(mean(o^2) + eps):   y = o r w silu(z).
+ * Backward: do = r (dn - (o r) mean(dn o r)) with dn = dy w silu(z); dz = dy o r w silu'(z);
+ * dw = sum over rows of dy o r silu(z) (fixed-order sum: deterministic).
+ * Layouts: o, z, y, dy, do, dz [rows][D] contiguous in p->dtype (GDN_BF16 or GDN_FP32);
+ * w, dw [D] fp32.  fp32 arithmetic.  The caller owns every buffer; stream-ordered, no
+ * synchronisation.  Errors: null or not 16-byte aligned pointer, rows < 0, D < 1,
+ * eps < 0: GDN_ERR_INVALID_ARG; D not a multiple of 4 or above 512: GDN_ERR_UNSUPPORTED;
+ * workspace smaller than gdn_rmsnorm_gated_bwd_workspace_size: GDN_ERR_WORKSPACE.
+ */
+typedef struct {
+  int32_t dtype;  /* GDN_BF16 or GDN_FP32 */
+  int32_t D;      /* elements per row, a multiple of 4, at most 512 */
+  int64_t rows;
+  float eps;      /* 1e-6 in the layers the pages test */
+} gdn_rmsnorm_problem;
+
+gdn_status gdn_rmsnorm_gated_fwd(const gdn_rmsnorm_problem* p, const void* o, const void* z,
+                                 const float* w, void* y, void* stream);
+gdn_status gdn_rmsnorm_gated_bwd_workspace_size(const gdn_rmsnorm_problem* p, size_t* bytes);
+gdn_status gdn_rmsnorm_gated_bwd(const gdn_rmsnorm_problem* p, const void* o, const void* z,
+                                 const float* w, const void* dy, void* d_o, void* dz, float* dw,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

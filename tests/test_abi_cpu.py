@@ -225,3 +225,36 @@ def test_conv_validation_and_workspace(lib):
                                  None, None, vp(A), n.value - 16, None) == gdn.GDN_ERR_WORKSPACE
     assert lib.gdn_conv_silu_bwd(ctypes.byref(p), vp(A), vp(A), None, None, vp(A), vp(A), vp(A),
                                  None, None, None, 0, None) == gdn.GDN_ERR_WORKSPACE
+
+
+def test_rmsnorm_validation_and_workspace(lib):
+    """Host-side checks of the gated RMSNorm calls (no launch reaches CUDA)."""
+    A = 1 << 20
+    vp = ctypes.c_void_p
+
+    def prob(**kw):
+        p = gdn.RmsNormProblem()
+        p.dtype, p.D, p.rows, p.eps = gdn.GDN_BF16, 128, 1000, 1e-6
+        for k, v in kw.items():
+            setattr(p, k, v)
+        return p
+
+    n = ctypes.c_size_t(0)
+    assert lib.gdn_rmsnorm_gated_bwd_workspace_size(ctypes.byref(prob()), ctypes.byref(n)) == 0
+    assert n.value == 8 * 128 * 4  # ceil(1000 / 128 rows per CTA) CTAs x D fp32
+    for kw, status in (({"D": 6}, gdn.GDN_ERR_UNSUPPORTED), ({"D": 516}, gdn.GDN_ERR_UNSUPPORTED),
+                       ({"D": 0}, gdn.GDN_ERR_INVALID_ARG), ({"rows": -1}, gdn.GDN_ERR_INVALID_ARG),
+                       ({"eps": -1.0}, gdn.GDN_ERR_INVALID_ARG),
+                       ({"dtype": 9}, gdn.GDN_ERR_INVALID_ARG)):
+        p = prob(**kw)
+        assert lib.gdn_rmsnorm_gated_fwd(ctypes.byref(p), vp(A), vp(A), vp(A), vp(A),
+                                         None) == status, kw
+        assert lib.gdn_rmsnorm_gated_bwd(ctypes.byref(p), vp(A), vp(A), vp(A), vp(A), vp(A),
+                                         vp(A), vp(A), vp(A), 1 << 30, None) == status, kw
+    p = prob()
+    assert lib.gdn_rmsnorm_gated_fwd(ctypes.byref(p), vp(A), None, vp(A), vp(A), None) == \
+        gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_rmsnorm_gated_fwd(ctypes.byref(p), vp(A), vp(A + 4), vp(A), vp(A), None) == \
+        gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_rmsnorm_gated_bwd(ctypes.byref(p), vp(A), vp(A), vp(A), vp(A), vp(A), vp(A),
+                                     vp(A), vp(A), n.value - 16, None) == gdn.GDN_ERR_WORKSPACE
