@@ -22,6 +22,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -201,7 +202,8 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        out = os.environ.get("GDN_BENCH_CLOCKS_DIR", tempfile.gettempdir())
+        self.path = os.path.join(out, f"gdn_bench_clocks_gpu{gpu_index}_{os.getpid()}.csv")
 
     def start(self):
         try:
@@ -239,6 +241,10 @@ class ClockSampler:
                 for nm, val in zip(names, parts[5:9]):
                     if val.lower().startswith("active"):
                         reasons.add(nm)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
