@@ -37,7 +37,8 @@ EXPORTS = (
     "gdn_resolved_segments", "gdn_workspace_size", "gdn_fwd", "gdn_bwd", "gdn_gate_param_bwd", "gdn_summary", "gdn_summary_bwd",
     "gdn_compose", "gdn_prefix_compose", "gdn_prefix_compose_bwd", "gdn_apply_state",
     "gdn_apply_state_bwd", "gdn_check_device_status", "gdn_kernel_info", "gdn_fwd_kernel",
-    "gdn_bwd_kernel", "gdn_fwd_noalloc", "gdn_ctx_size", "gdn_fwd_ctx", "gdn_bwd_ctx",
+    "gdn_bwd_kernel", "gdn_fwd_noalloc", "gdn_noalloc_check_device_status", "gdn_ctx_size",
+    "gdn_fwd_ctx", "gdn_bwd_ctx",
     "gdn_fwd_ctx_kernel", "gdn_bwd_ctx_kernel", "gdn_conv_silu_fwd",
     "gdn_conv_silu_bwd_workspace_size", "gdn_conv_silu_bwd", "gdn_rmsnorm_gated_fwd",
     "gdn_rmsnorm_gated_bwd_workspace_size", "gdn_rmsnorm_gated_bwd",
@@ -115,6 +116,7 @@ def load_library(path: str | None = None):
             "gdn_prefix_compose": ([_I64] * 4 + [_VP] * 6, ctypes.c_int),
             "gdn_prefix_compose_bwd": ([_I64] * 4 + [_VP] * 6, ctypes.c_int),
             "gdn_check_device_status": ([_VP, _VP], ctypes.c_int),
+            "gdn_noalloc_check_device_status": ([_VP], ctypes.c_int),
             "gdn_kernel_info": ([_PP, ctypes.c_int32, ctypes.c_int32,
                                  ctypes.POINTER(ctypes.c_int32),
                                  ctypes.POINTER(ctypes.c_char_p)], ctypes.c_int),
@@ -532,6 +534,11 @@ def gdn_bwd_ctx_kernel(index, q, k, v, a, b, A_log, dt_bias, ctx, valid_len, dO,
         _ptr(dt_bias), _ptr(ctx), ctx.numel(), _ptr(valid_len), _ptr(dO), _ptr(dHT), _ptr(dq),
         _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dH0), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def gdn_noalloc_check_device_status(stream=None) -> int:
+    """Synchronise, read and clear the status word of gdn_fwd_noalloc's static scratch."""
+    return load_library().gdn_noalloc_check_device_status(_stream(stream))
 
 
 def gdn_check_device_status(ws, stream=None) -> int:

@@ -853,6 +853,13 @@ gdn_status gdn_fwd_noalloc(const gdn_problem* p, const void* q, const void* k, c
                   (size_t)GDN_NOALLOC_SCRATCH_BYTES, stream, sc);
 }
 
+gdn_status gdn_noalloc_check_device_status(void* stream) {
+  void* scratch = nullptr;
+  gdn_status s = noalloc_scratch(&scratch);
+  if (s != GDN_OK) return s;
+  return gdn_check_device_status(scratch, stream);
+}
+
 gdn_status gdn_check_device_status(void* workspace, void* stream) {
   if (workspace == nullptr || ((uintptr_t)workspace & 255u) != 0) return GDN_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;

@@ -325,13 +325,23 @@ gdn_status gdn_bwd_ctx_kernel(const gdn_problem* p, int32_t index, const void* q
  * zero (its status word) and overwrites the rest before reading it.  Calls that
  * can run at the same time on one GPU (on different streams, or issued from
  * host threads without an order between them) race on the array: the caller
- * must order them.  gdn_check_device_status does not apply to this call.
+ * must order them.  Faults that its kernels find (a valid_len outside [0, T], an
+ * exhausted bounded wait) are recorded in the status word at the start of the
+ * array and read with gdn_noalloc_check_device_status.
  */
 #define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
 gdn_status gdn_fwd_noalloc(const gdn_problem* p, const void* q, const void* k, const void* v,
                            const void* a, const void* b, const float* A_log,
                            const float* dt_bias, const float* h0, const int32_t* valid_len,
                            void* o, float* hT, void* stream);
+
+/*
+ * gdn_check_device_status for gdn_fwd_noalloc (no counterpart on the pages):
+ * synchronises `stream`, reads the status word of this device's static scratch
+ * array, clears it and returns what gdn_check_device_status would.  The first
+ * call on a device looks up the array's address, as gdn_fwd_noalloc does.
+ */
+gdn_status gdn_noalloc_check_device_status(void* stream);
 
 /*
  * Synchronises `stream`, reads the device status word of `workspace` (written by

@@ -448,6 +448,77 @@ def test_cfg3_segment_path_matches_monolithic_bf16():
     ro, rhT = oracle_fwd(n)
     assert_close("o segmented vs oracle", o_seg[:, :, hq * r:(hq + 1) * r], ro, torch.bfloat16)
     assert_close("hT segmented vs oracle", Hout[:, hq * r:(hq + 1) * r], rhT, torch.bfloat16)
+    # the segmented backward against the oracle's monolithic gradients, element by element
+    rg = oracle_bwd(n)
+    vs = slice(hq * r, (hq + 1) * r)
+    for j, name in enumerate(NAMES_BWD[:5]):
+        cat = torch.cat([g[j] for g in grads], dim=1)
+        got = cat[:, :, hq:hq + 1] if name in ("dq", "dk") else cat[:, :, vs]
+        assert_close(f"{name} segmented vs oracle", got, rg[j], torch.bfloat16)
+    assert_close("dH0 segmented vs oracle", dH0[:, vs], rg[5], torch.bfloat16)
+    assert_close("dHin of segment 0 vs oracle dH0", grads[0][5][:, vs], rg[5], torch.bfloat16)
+    # every segment's gradient summary D against the oracle's
+    for i in range(P):
+        nl = {k: (n[k][:, i * L:(i + 1) * L] if k in keys else n[k]) for k in n}
+        rD = oracle.summary_bwd(nl["q"], nl["k"], nl["a"], nl["b"], nl["A_log"], nl["dt_bias"],
+                                nl["dO"])
+        assert_close(f"D seg{i} vs oracle", Ds[i][:, vs], rD, torch.bfloat16)
+
+
+def test_bf16_summary_bwd_matches_oracle():
+    """The gradient summary D of a short bf16 segment (three chunks, a ragged tail)
+    against the oracle, with slow decay so every chunk contributes."""
+    w = gi.Workload("sumbwd", B=1, T=190, Hqk=1, H=2, dk=128, dv=128, decay_stress=True,
+                    seed=41)
+    inp = gi.make_inputs(w)
+    n = np64(inp)
+    d = dev(inp)
+    D = gdn.gdn_summary_bwd(d["q"], d["k"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["dO"])
+    rD = oracle.summary_bwd(n["q"], n["k"], n["a"], n["b"], n["A_log"], n["dt_bias"], n["dO"])
+    assert_close("D", D, rD, torch.bfloat16)
+
+
+def test_bf16_segmented_bwd_small_matches_oracle():
+    """Two bf16 segments through the public summary / prefix / apply calls, forward
+    and backward, compared with the oracle on every element (T = 190: a ragged tail)."""
+    w = gi.Workload("segbwd", B=1, T=190, Hqk=1, H=2, dk=128, dv=128, h0_std=0.1,
+                    with_dHT=True, decay_stress=True, seed=42)
+    inp = gi.make_inputs(w)
+    n = np64(inp)
+    d = dev(inp)
+    cuts = [0, 128, 190]
+    keys = ("q", "k", "v", "a", "b", "dO")
+    segs = [{k: d[k][:, s0:s1].contiguous() for k in keys} for s0, s1 in zip(cuts[:-1], cuts[1:])]
+    Ms, Ss, Ds = [], [], []
+    for s in segs:
+        M, S = gdn.gdn_summary(s["k"], s["v"], s["a"], s["b"], d["A_log"], d["dt_bias"])
+        Ms.append(M)
+        Ss.append(S)
+        Ds.append(gdn.gdn_summary_bwd(s["q"], s["k"], s["a"], s["b"], d["A_log"], d["dt_bias"],
+                                      s["dO"]))
+    Mst, Sst, Dst = torch.stack(Ms), torch.stack(Ss), torch.stack(Ds)
+    Hin, Hout = gdn.gdn_prefix_compose(Mst, Sst, d["h0"])
+    dHout, dH0 = gdn.gdn_prefix_compose_bwd(Mst, Dst, d["dHT"])
+    outs, grads = [], []
+    for i, s in enumerate(segs):
+        outs.append(gdn.gdn_apply_state(s["q"], s["k"], s["v"], s["a"], s["b"], d["A_log"],
+                                        d["dt_bias"], Hin[i].contiguous(), want_hT=False)[0])
+        grads.append(gdn.gdn_apply_state_bwd(s["q"], s["k"], s["v"], s["a"], s["b"],
+                                             d["A_log"], d["dt_bias"], Hin[i].contiguous(),
+                                             s["dO"], dHout[i].contiguous()))
+    ro, rhT = oracle_fwd(n)
+    rg = oracle_bwd(n)
+    assert_close("o", torch.cat(outs, dim=1), ro, torch.bfloat16)
+    assert_close("hT", Hout, rhT, torch.bfloat16)
+    for j, name in enumerate(NAMES_BWD[:5]):
+        assert_close(name, torch.cat([g[j] for g in grads], dim=1), rg[j], torch.bfloat16)
+    assert_close("dH0", dH0, rg[5], torch.bfloat16)
+    assert_close("dHin of segment 0", grads[0][5], rg[5], torch.bfloat16)
+    for i, (s0, s1) in enumerate(zip(cuts[:-1], cuts[1:])):
+        nl = {k: (n[k][:, s0:s1] if k in keys else n[k]) for k in n}
+        rD = oracle.summary_bwd(nl["q"], nl["k"], nl["a"], nl["b"], nl["A_log"], nl["dt_bias"],
+                                nl["dO"])
+        assert_close(f"D seg{i}", Ds[i], rD, torch.bfloat16)
 
 
 def test_cfg4a_padded_batch_bf16():

@@ -67,3 +67,25 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     d = {"q": q, "k": q, "v": v, "a": v, "b": v, "A_log": v, "dt_bias": v, "h0": None,
          "valid_len": None}
     assert call_noalloc(p, d, v, None) == gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_noalloc_device_status_reports_a_clamped_valid_len():
+    """A valid_len outside [0, T] (a bad input made on the host, not a fault) is
+    clamped by the kernels and recorded in the static scratch's status word, which
+    gdn_noalloc_check_device_status reads and clears."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = gi.Workload("noalloc_flag", B=1, T=64, Hqk=1, H=1, dk=16, dv=16, dtype=torch.float32,
+                    seed=33)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in gi.make_inputs(w).items()}
+    p = gdn.make_problem(d["q"], d["v"])
+    o = torch.empty_like(d["v"])
+    hT = torch.empty(1, 1, 16, 16, device="cuda")
+    assert gdn.gdn_noalloc_check_device_status() == gdn.GDN_OK   # clears earlier calls' word
+    d["valid_len"] = torch.tensor([100], dtype=torch.int32, device="cuda")
+    assert call_noalloc(p, d, o, hT) == gdn.GDN_OK
+    assert gdn.gdn_noalloc_check_device_status() == gdn.GDN_ERR_INVALID_ARG
+    assert gdn.gdn_noalloc_check_device_status() == gdn.GDN_OK   # cleared by the read
+    d["valid_len"] = torch.tensor([64], dtype=torch.int32, device="cuda")
+    assert call_noalloc(p, d, o, hT) == gdn.GDN_OK
+    assert gdn.gdn_noalloc_check_device_status() == gdn.GDN_OK
