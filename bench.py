@@ -373,7 +373,6 @@ def run_ours(args):
     d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
     p = gdn.make_problem(d["q"], d["v"])
     wsf = gdn.workspace(p, gdn.GDN_OP_FWD)
-    wsfc = gdn.workspace(p, gdn.GDN_OP_FWD_CTX)
     wsb = gdn.workspace(p, gdn.GDN_OP_BWD)
     B, T, H, dv = d["v"].shape
     dk = d["q"].shape[3]
@@ -393,7 +392,7 @@ def run_ours(args):
 
     def fwd_ctx():  # the training-step forward: also keeps the segment states for the backward
         gdn.gdn_fwd_ctx(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
-                        d["h0"], None, ctx=ctx, o=o, hT=hT, ws=wsfc, problem=p, stream=stream)
+                        d["h0"], None, ctx=ctx, o=o, hT=hT, ws=wsf, problem=p, stream=stream)
 
     def bwd_ctx():
         gdn.gdn_bwd_ctx(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], ctx,
@@ -489,7 +488,7 @@ def run_ours(args):
                     if op == gdn.GDN_OP_FWD_CTX:
                         gdn.gdn_fwd_ctx_kernel(i, d["q"], d["k"], d["v"], d["a"], d["b"],
                                                d["A_log"], d["dt_bias"], d["h0"], None, o, hT,
-                                               ctx, wsfc, problem=p, stream=stream)
+                                               ctx, wsf, problem=p, stream=stream)
                     else:
                         gdn.gdn_bwd_ctx_kernel(i, d["q"], d["k"], d["v"], d["a"], d["b"],
                                                d["A_log"], d["dt_bias"], ctx, None, d["dO"],
@@ -645,7 +644,7 @@ def run_ours(args):
 
         def run_step(x):
             gdn.gdn_fwd_ctx(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"], x["dt_bias"],
-                            x["h0"], None, ctx=ctx, o=o, hT=hT, ws=wsfc, problem=p, stream=stream)
+                            x["h0"], None, ctx=ctx, o=o, hT=hT, ws=wsf, problem=p, stream=stream)
             gdn.gdn_bwd_ctx(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"], x["dt_bias"], ctx,
                             x["dO"], x["dHT"], None, dq=dq, dk=dkk, dv=dvv, dg=dg, dbeta=dbeta,
                             dH0=dH0, ws=wsb, problem=p, stream=stream)

@@ -89,35 +89,6 @@ int auto_segments_tc(int64_t BH, int64_t NC, int sms) {
   return best_p;
 }
 
-// Segment count of the fused tensor-core forward (gdn_fwd): launch 1 runs the summaries
-// (S and M) of segments 0..P-2 -- and the output of segment 0 when every CTA still gets
-// its own SM -- launch 2 the output of the remaining segments from their start states.
-// Per-chunk times (us, GB300): summary 0.85, output 1.0; 10 us per launch and prefix.
-int auto_segments_fwd(int64_t BH, int64_t NC, int sms) {
-  auto waves = [](int64_t n, int64_t slots) { return (double)((n + slots - 1) / slots); };
-  double best = 1e300;
-  int best_p = 1;
-  for (int64_t P = 1; P <= 24 && P <= NC; ++P) {
-    const int64_t cps = (NC + P - 1) / P, pe = (NC + cps - 1) / cps;
-    double t;
-    if (pe == 1) {
-      t = waves(BH, sms) * cps * 1.0;
-    } else {
-      const int64_t n1 = 2 * (pe - 1) * BH;
-      const bool with0 = n1 + BH <= sms;
-      double t1 = waves(n1, sms) * cps * 0.85;
-      if (with0 && cps * 1.0 > t1) t1 = cps * 1.0;
-      const double t2 = waves((pe - (with0 ? 1 : 0)) * BH, sms) * cps * 1.0;
-      t = t1 + t2 + 20.0;
-    }
-    if (t < best - 1e-9) {
-      best = t;
-      best_p = (int)pe;
-    }
-  }
-  return best_p;
-}
-
 int auto_segments(int64_t B, int64_t H, int64_t dv, int64_t NC, bool tensor_core) {
   if (NC <= 1) return 1;
   if (tensor_core) return auto_segments_tc(B * H, NC, device_sms());
@@ -167,11 +138,7 @@ gdn_status resolve_op(const gdn_problem* p, int op, Prob* out) {
   const int64_t maxP = r.NC > 1 ? r.NC : 1;
   if (p->segments > maxP) return GDN_ERR_INVALID_ARG;
   const bool tcp = r.dtype == GDN_BF16 && r.dk == 128 && r.dv == 128 && r.B > 0 && r.NC > 0;
-  // gdn_fwd picks its own count on the tensor-core path; the training-step pair
-  // (GDN_OP_FWD_CTX, the backward) shares the backward's, which the context is built for
-  int P = p->segments > 0 ? p->segments
-          : (tcp && op == GDN_OP_FWD && r.NC > 1) ? auto_segments_fwd(r.B * r.H, r.NC, device_sms())
-                                                  : auto_segments(r.B, r.H, r.dv, r.NC, tcp);
+  int P = p->segments > 0 ? p->segments : auto_segments(r.B, r.H, r.dv, r.NC, tcp);
   if (op == GDN_OP_SUMMARY || op == GDN_OP_SUMMARY_BWD) P = 1;
   r.CPS = r.NC > 0 ? (r.NC + P - 1) / P : 0;
   r.P = r.CPS > 0 ? (int)((r.NC + r.CPS - 1) / r.CPS) : 1;
@@ -193,8 +160,8 @@ size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws) {
   };
   const size_t B = pr.B, H = pr.H, Hqk = pr.Hqk, dk = pr.dk, dv = pr.dv, Tp = pr.Tp,
                NC = pr.NC, P = pr.P;
-  const bool bwd = op == GDN_OP_BWD || op == GDN_OP_BWD_CTX;
-  const bool fwd = op == GDN_OP_FWD || op == GDN_OP_FWD_CTX;
+  const bool bwd = op == GDN_OP_BWD;
+  const bool fwd = op == GDN_OP_FWD;
   w.status = (int*)take(64);
   auto take_prep = [&]() {  // norm factors, gates and tile images of the tensor-core prologue
     w.rqk = take(B * Hqk * NC * 128);
@@ -221,7 +188,7 @@ size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws) {
     return off;
   }
   if (tc_path(pr) && (fwd || op == GDN_OP_SUMMARY)) {
-    w.tu = take(H * B * NC * fwd_record_bytes() / 4);  // one record per (chunk, V head)
+    take_prep();
     if (fwd && P > 1) {
       w.Mseg = take(P * B * H * dk * dk);
       w.Sseg = take(P * B * H * dk * dv);
@@ -347,41 +314,33 @@ gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* 
   int64_t init_stride = 0;
   const int64_t sstride = pr.B * pr.H * pr.dk * pr.dv;
   if (tc_path(pr)) {
-    // fused forward: T diag(beta) per chunk, then chain launches that form every other
-    // chunk intermediate on chip (gdn_tc_fwd.cu)
-    GDN_RUN(sc, "tsolve_tc", launch_tsolve_tc(pr, in, ws, st));
-    FwdWork out;  // the token-output items
-    out.init0 = h0;
-    out.o = o;
-    out.final_out = hT;
-    if (pr.P > 1) {
-      FwdWork sum;
-      sum.S_out = ws.Sseg;
-      sum.M_out = cx ? cx->M : ws.Mseg;
-      sum.out_stride = sstride;
-      for (int s = 0; s < pr.P - 1; ++s) sum.add(1, s);
-      for (int s = 0; s < (cx ? pr.P : pr.P - 1); ++s) sum.add(2, s);
-      // segment 0 needs no incoming state: it shares the first launch when every CTA
-      // of that launch still has an SM of its own
-      const bool with0 = !cx && (int64_t)(sum.nitems + 1) * pr.B * pr.H <= device_sms();
-      if (with0) {
-        sum.add(0, 0);
-        sum.init0 = h0;
-        sum.o = o;
+    GDN_RUN(sc, "prep_tc", launch_prep_tc(pr, in, ws, st));
+    if (cx) {  // summaries of every segment; the transitions and start states are kept
+      if (pr.P > 1) {
+        GDN_RUN(sc, "summary_chain_tc",
+                launch_chain_tc(pr, in, ws, 1, 0, pr.P, nullptr, 0, nullptr, nullptr, cx->M,
+                                ws.Sseg, sstride, nullptr, st));
+        GDN_RUN(sc, "prefix",
+                launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, cx->M, ws.Sseg, h0, cx->Hin,
+                              nullptr, st));
+      } else {
+        GDN_RUN(sc, "ctx_init", ctx_single(pr, h0, cx->Hin, st));
       }
-      GDN_RUN(sc, "fwd_sum_tc", launch_fwd_tc(pr, in, ws, sum, st));
-      float* Hin = cx ? cx->Hin : ws.Hin;
+      init = cx->Hin;
+      init_stride = sstride;
+    } else if (pr.P > 1) {
+      GDN_RUN(sc, "summary_chain_tc",
+              launch_chain_tc(pr, in, ws, 1, 0, pr.P - 1, nullptr, 0, nullptr, nullptr, ws.Mseg,
+                              ws.Sseg, sstride, nullptr, st));
       GDN_RUN(sc, "prefix",
-              launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, sum.M_out, ws.Sseg, h0, Hin, nullptr,
-                            st));
-      out.init = Hin;
-      out.init_stride = sstride;
-      for (int s = with0 ? 1 : 0; s < pr.P; ++s) out.add(0, s);
-    } else {
-      if (cx) GDN_RUN(sc, "ctx_init", ctx_single(pr, h0, cx->Hin, st));
-      out.add(0, 0);
+              launch_prefix(pr.B * pr.H, pr.P, pr.dk, pr.dv, ws.Mseg, ws.Sseg, h0, ws.Hin,
+                            nullptr, st));
+      init = ws.Hin;
+      init_stride = sstride;
     }
-    GDN_RUN(sc, "fwd_apply_tc", launch_fwd_tc(pr, in, ws, out, st));
+    GDN_RUN(sc, "apply_chain_tc",
+            launch_chain_tc(pr, in, ws, 0, 0, pr.P, init, init_stride, o, hT, nullptr, nullptr,
+                            0, nullptr, st));
     return GDN_OK;
   }
   GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, false, st));
@@ -538,6 +497,7 @@ gdn_status gdn_query_support(const gdn_problem* p) {
 
 gdn_status gdn_resolved_segments(const gdn_problem* p, int32_t op, int32_t* segments) {
   if (!segments || op < GDN_OP_FWD || op > GDN_OP_BWD_CTX) return GDN_ERR_INVALID_ARG;
+  if (op == GDN_OP_FWD_CTX) op = GDN_OP_FWD;
   if (op == GDN_OP_BWD_CTX) op = GDN_OP_BWD;
   Prob pr;
   gdn_status s = resolve_op(p, op, &pr);
@@ -548,6 +508,7 @@ gdn_status gdn_resolved_segments(const gdn_problem* p, int32_t op, int32_t* segm
 
 gdn_status gdn_workspace_size(const gdn_problem* p, int32_t op, size_t* bytes) {
   if (!bytes || op < GDN_OP_FWD || op > GDN_OP_BWD_CTX) return GDN_ERR_INVALID_ARG;
+  if (op == GDN_OP_FWD_CTX) op = GDN_OP_FWD;
   if (op == GDN_OP_BWD_CTX) op = GDN_OP_BWD;
   Prob pr;
   gdn_status s = resolve_op(p, op, &pr);
@@ -563,8 +524,7 @@ static gdn_status fwd_impl(const gdn_problem* p, const void* q, const void* k, c
                            void* stream, Sched& sc, void* ctx = nullptr,
                            size_t ctx_size = 0, bool with_ctx = false) {
   Prob pr;
-  const int op = with_ctx ? GDN_OP_FWD_CTX : GDN_OP_FWD;
-  gdn_status s = resolve_op(p, op, &pr);
+  gdn_status s = resolve_op(p, GDN_OP_FWD, &pr);
   if (s != GDN_OK) return s;
   Inputs in{q, k, v, a, b, A_log, dt_bias, valid_len, nullptr};
   if (!inputs_ok(pr, in, true, true)) return GDN_ERR_INVALID_ARG;
@@ -577,7 +537,7 @@ static gdn_status fwd_impl(const gdn_problem* p, const void* q, const void* k, c
   }
   WS ws;
   cudaStream_t st = (cudaStream_t)stream;
-  if ((s = prepare(p, op, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK) return s;
+  if ((s = prepare(p, GDN_OP_FWD, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK) return s;
   return run_forward(pr, in, h0, o, hT, ws, st, sc, with_ctx ? &cx : nullptr);
 }
 
@@ -649,7 +609,7 @@ gdn_status gdn_bwd_kernel(const gdn_problem* p, int32_t index, const void* q, co
 gdn_status gdn_ctx_size(const gdn_problem* p, size_t* bytes) {
   if (!bytes) return GDN_ERR_INVALID_ARG;
   Prob pr;
-  gdn_status s = resolve_op(p, GDN_OP_FWD_CTX, &pr);
+  gdn_status s = resolve_op(p, GDN_OP_FWD, &pr);
   if (s != GDN_OK) return s;
   *bytes = ctx_bytes(pr);
   return GDN_OK;
@@ -708,7 +668,7 @@ gdn_status gdn_kernel_info(const gdn_problem* p, int32_t op, int32_t index, int3
   const bool fwd = op == GDN_OP_FWD || op == GDN_OP_FWD_CTX;
   const bool with_ctx = op == GDN_OP_FWD_CTX || op == GDN_OP_BWD_CTX;
   Prob pr;
-  gdn_status s = resolve_op(p, fwd ? op : GDN_OP_BWD, &pr);
+  gdn_status s = resolve_op(p, fwd ? GDN_OP_FWD : GDN_OP_BWD, &pr);
   if (s != GDN_OK) return s;
   Sched sc;
   sc.dry = true;
@@ -791,13 +751,10 @@ gdn_status gdn_summary(const gdn_problem* p, const void* k, const void* v, const
   if ((s = prepare(p, GDN_OP_SUMMARY, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK)
     return s;
   if (tc_path(pr)) {
-    GDN_TRY(launch_tsolve_tc(pr, in, ws, st));
-    FwdWork w;
-    w.S_out = S;
-    w.M_out = M;
-    w.add(1, 0);
-    w.add(2, 0);
-    GDN_TRY(launch_fwd_tc(pr, in, ws, w, st));
+    in.q = k;  // the prologue reads a q tile; a summary never uses it
+    GDN_TRY(launch_prep_tc(pr, in, ws, st));
+    GDN_TRY(launch_chain_tc(pr, in, ws, 1, 0, 1, nullptr, 0, nullptr, nullptr, M, S, 0, nullptr,
+                            st));
     return GDN_OK;
   }
   GDN_TRY(launch_prep(pr, in, ws, false, false, st));

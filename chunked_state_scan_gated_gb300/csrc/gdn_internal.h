@@ -55,8 +55,6 @@ struct WS {
   float* gl;    // [B][H][NC][64] cumulative gate inside each chunk, log2 units
   void* hc16;   // [B][H][NC][dk][dv] bf16 chunk-start states (tensor-core backward)
   void* dhc16;  // [B][H][NC][dk][dv] bf16 chunk-end state gradients (tensor-core backward)
-  void* tu;     // [H][B*NC]    chunk records of the fused forward (fwd_record_bytes() each):
-                //              T diag(beta) image, T = (I + A)^-1, then per-token factors
 };
 
 // Raw inputs of a call (device pointers; type of q..dO is Prob::dtype).
@@ -160,36 +158,6 @@ struct ReversePass {
 cudaError_t launch_chain_pair_tc(const Prob& pr, const Inputs& in, const WS& ws, int fmode,
                                  const ChainPass& f, int rmode, const ReversePass& r,
                                  cudaStream_t st);
-// ---- fused tensor-core forward (gdn_tc_fwd.cu) ----
-// bytes of one chunk record in ws.tu
-size_t fwd_record_bytes();
-// T diag(beta) and the per-token factors of every (chunk, V head) into ws.tu
-cudaError_t launch_tsolve_tc(const Prob& pr, const Inputs& in, const WS& ws, cudaStream_t st);
-// Work items of one launch of the fused chain kernel: mode 0 = token output and final
-// state from a start state (APPLY), 1 = state reached from zero (S of a summary),
-// 2 = transition M of a segment; each for one segment, every (row, V head).
-struct FwdWork {
-  static constexpr int kMax = 48;
-  int nitems = 0;
-  int mode[kMax];
-  int seg[kMax];
-  const float* init = nullptr;   // APPLY of segment s > 0: start state init + s * init_stride
-  int64_t init_stride = 0;
-  const float* init0 = nullptr;  // APPLY of segment 0: start state (null: zero)
-  void* o = nullptr;
-  float* final_out = nullptr;    // APPLY of segment P - 1: final state (nullable)
-  float* S_out = nullptr;        // summaries: S of segment s at S_out + s * out_stride
-  float* M_out = nullptr;        // transitions: M of segment s at M_out + s * out_stride
-  int64_t out_stride = 0;
-  void add(int m, int s) {
-    mode[nitems] = m;
-    seg[nitems] = s;
-    ++nitems;
-  }
-};
-cudaError_t launch_fwd_tc(const Prob& pr, const Inputs& in, const WS& ws, const FwdWork& w,
-                          cudaStream_t st);
-
 // dq, dk (bf16) from the per-V-head bf16 gradients of q_hat, k_hat in ws.dqp / ws.dkp
 cudaError_t launch_qk_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, void* dq, void* dk,
                               cudaStream_t st);

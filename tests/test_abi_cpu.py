@@ -160,10 +160,9 @@ def test_ctx_size_and_validation(lib):
     misaligned context is refused before any launch."""
     for seg in (0, 1, 5):
         p = problem(segments=seg)
-        P = gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD_CTX)
-        assert P == gdn.gdn_resolved_segments(p, gdn.GDN_OP_BWD)   # the pair shares its split
-        if seg:
-            assert P == gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD) == seg
+        P = gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD)
+        assert P == gdn.gdn_resolved_segments(p, gdn.GDN_OP_BWD)
+        assert P == gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD_CTX)
         assert gdn.gdn_ctx_size(p) == P * 1 * 32 * (128 * 128 + 128 * 128) * 4
     p = problem()
     need = gdn.gdn_ctx_size(p)
@@ -176,11 +175,11 @@ def test_ctx_size_and_validation(lib):
         st = lib.gdn_bwd_ctx(ctypes.byref(p), *[vp(A)] * 7, None if ctx is None else vp(ctx), n,
                              None, vp(A), None, *[vp(A)] * 5, None, vp(A), 1 << 40, None)
         assert st == gdn.GDN_ERR_INVALID_ARG
+    assert gdn.gdn_workspace_size(p, gdn.GDN_OP_FWD_CTX) == gdn.gdn_workspace_size(p, gdn.GDN_OP_FWD)
     assert gdn.gdn_workspace_size(p, gdn.GDN_OP_BWD_CTX) == gdn.gdn_workspace_size(p, gdn.GDN_OP_BWD)
     names = gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD_CTX)
     assert "summary_pair_tc" not in names and "grad_tc" in names      # no forward summaries
-    names = gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD_CTX)
-    assert names[0] == "tsolve_tc" and names[-1] == "fwd_apply_tc"
+    assert gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD_CTX)[-1] == "apply_chain_tc"
 
 
 def test_conv_validation_and_workspace(lib):
