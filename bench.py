@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kernel-profile", action="store_true")
+    ap.add_argument("--no-lengths", action="store_true",
+                    help="skip the 8K/16K/32K/64K sequence-length matrix")
     ap.add_argument("--T", type=int, default=0,
                     help="override the sequence length (smaller cases for profiling)")
     return ap.parse_args()
@@ -95,13 +97,52 @@ def step_algorithmic(w):
             "bytes_step": fwd_bytes + bwd_bytes}
 
 
+def kernel_alg(name, w):
+    """(flops, bytes) of the method's algorithmic work owned by one launch of `name`.
+
+    The per-token figures of step_algorithmic, split over the launches that own them:
+    each input or output tensor of a pass is counted once, at the launch that reads or
+    writes it; each contraction of the method once, at the launch that performs it.
+    Forward: the prologue reads q, k, v, a, b and forms K K^T, Q K^T, T K, T V and the
+    solve; the output chain owns the three state products and P V', writes o and h_T and
+    reads h0.  Backward: the reverse chain owns the state-gradient recurrence (K~ dS,
+    W^T dV': 4 dk dv per token and head) and the state tensors h0, dH_T, dH0; the
+    gradient kernel owns every other gradient contraction, reads the forward inputs
+    again and dO, and writes dv, dg, dbeta; the Q/K head sum writes dq, dk.  Summaries,
+    prefixes and recomputation (the recomputing backward's prologue) are overhead of the
+    design: no algorithmic work.
+    """
+    op, kname = name.split(".", 1)
+    dk, dv, H, Hqk, B = w.dk, w.dv, w.H, w.Hqk, w.B
+    tok = B * w.T
+    e = 2
+    state = B * H * dk * dv * 4
+    f_local = 2 * C * (3 * dk + dv) + C * C / 3   # K K^T, Q K^T, T K, T V, the solve
+    f_chain = 6 * dk * dv + 2 * C * dv            # W S, Q S, K~^T V', P V'
+    f_fwd = f_local + f_chain
+    f_rev = 4 * dk * dv
+    in_fwd = tok * (2 * Hqk * dk * e + H * dv * e + 2 * H * e)
+    if kname == "prep_tc":
+        return (f_local * tok * H, in_fwd) if op == "fwd" else (0.0, 0.0)
+    if kname == "apply_chain_tc":
+        return f_chain * tok * H, tok * H * dv * e + state * (2 if w.h0_std else 1)
+    if kname == "states_pair_tc":
+        return f_rev * tok * H, state * ((1 if w.h0_std else 0) + (1 if w.with_dHT else 0) + 1)
+    if kname == "grad_tc":
+        return (2 * f_fwd - f_rev) * tok * H, in_fwd + tok * (H * dv * e + H * dv * e + 2 * H * 4)
+    if kname == "qk_grad_tc":
+        return 0.0, tok * 2 * Hqk * dk * e
+    return 0.0, 0.0
+
+
 def kernel_work(name, w, P):
-    """(flops, bytes) of algorithmic work of one launch of kernel `name`.
+    """(flops, bytes) the design itself moves and computes in one launch of `name`
+    (its intermediates included): the "model" figures beside the algorithmic ones.
 
     name is "<fwd|bwd>.<kernel>" as listed by gdn_kernel_info.  Flops count each
-    contraction the kernel must perform once per (chunk, V head) at its natural
-    size (C = 64, dk = dv = 128); bytes count every tensor the kernel must read
-    or write in HBM once (bf16 tiles, fp32 states and gates).
+    contraction the kernel performs once per (chunk, V head) at its natural size
+    (C = 64, dk = dv = 128); bytes count every tensor the kernel reads or writes
+    in HBM once (bf16 tiles, fp32 states and gates).
     """
     op, kname = name.split(".", 1)
     dk, dv, H, Hqk, B = w.dk, w.dv, w.H, w.Hqk, w.B
@@ -116,9 +157,9 @@ def kernel_work(name, w, P):
     if kname == "prep_tc":
         f = 2 * mm(C, C, dk) + C ** 3 / 3 + mm(C, dk, C) + mm(C, dv, C)
         rd = tok * (2 * Hqk * dk * 2 + H * dv * 2 + 2 * H * 2)
-        wr = ch * (2 * tile + tile_p + C * 4) + B * Hqk * NC * 2 * C * 4
-        if op == "bwd":
-            wr += ch * tile_p
+        # W, U, P and T images, gates, norm factors (the T images are written for the
+        # backward: by gdn_fwd_ctx into its context, by gdn_bwd's own prologue)
+        wr = ch * (2 * tile + 2 * tile_p + C * 4) + B * Hqk * NC * 2 * C * 4
         return f * ch, rd + wr
     if kname == "summary_chain_tc":  # gdn_fwd_ctx: [M | S] parts of every segment
         f = 2 * (mm(C, dv, dk) + mm(dk, dv, C)) * ch
@@ -251,6 +292,86 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- per-call statistics
+
+def stats_ms(xs):
+    """median, min and p90 (nearest rank) of per-call times in ms."""
+    ys = sorted(xs)
+    p90 = ys[min(len(ys) - 1, max(0, math.ceil(0.9 * len(ys)) - 1))]
+    return {"median": statistics.median(ys), "min": ys[0], "p90": p90, "n": len(ys)}
+
+
+LENGTHS = (8192, 16384, 32768, 65536)
+
+
+def measure_lengths(gdn, gi, torch, stream, peaks, args, per_step):
+    """The sequence-length matrix: B = 1, Hqk = 16, H = 32, dk = dv = 128, bf16, stateful.
+
+    Per length: gdn_fwd, the context pair (gdn_fwd_ctx + gdn_bwd_ctx) and the recompute
+    pair (gdn_fwd + gdn_bwd), every call timed alone with CUDA events on the launching
+    stream (median, min, p90 over --steps calls after 3 warm-up calls), tokens/s of the
+    median, the fraction of the algorithmic roofline (sustained bf16 peak, measured HBM
+    bandwidth) that the median reaches, and the incremental peak device memory of one
+    call that allocates its own outputs, context and workspace.
+    """
+    import dataclasses
+    out = {}
+    steps = max(args.steps, 5)
+    for T in LENGTHS:
+        w = dataclasses.replace(gi.STATEFUL_32K, T=T, name=f"fwdbwd_bf16_T{T}_h16x32_d128_stateful")
+        inp = gi.make_inputs(w)
+        d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+        fwd_in = (d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"])
+        p = gdn.make_problem(d["q"], d["v"])
+        alg = step_algorithmic(w)
+        t_fwd = max(alg["flops_fwd"] / (peaks["bf16_tflops_sustained"] * 1e12),
+                    alg["bytes_fwd"] / (peaks["hbm_gbs"] * 1e9))
+        t_step = max(alg["flops_step"] / (peaks["bf16_tflops_sustained"] * 1e12),
+                     alg["bytes_step"] / (peaks["hbm_gbs"] * 1e9))
+
+        def call_fwd():
+            return gdn.gdn_fwd(*fwd_in, d["h0"], None, problem=p, stream=stream)
+
+        def call_ctx():
+            ctx = gdn.ctx_buffer(p)
+            o, hT, _ = gdn.gdn_fwd_ctx(*fwd_in, d["h0"], None, ctx=ctx, problem=p, stream=stream)
+            return gdn.gdn_bwd_ctx(*fwd_in, ctx, d["dO"], d["dHT"], None, problem=p,
+                                   stream=stream), o, hT
+
+        def call_recompute():
+            o, hT = gdn.gdn_fwd(*fwd_in, d["h0"], None, problem=p, stream=stream)
+            return gdn.gdn_bwd(*fwd_in, d["dO"], d["dHT"], d["h0"], None, problem=p,
+                               stream=stream), o, hT
+
+        def peak_bytes(fn):
+            torch.cuda.synchronize()
+            base = torch.cuda.memory_allocated()
+            torch.cuda.reset_peak_memory_stats()
+            r = fn()
+            torch.cuda.synchronize()
+            peak = torch.cuda.max_memory_allocated() - base
+            del r
+            return peak
+
+        row = {"tokens": T}
+        for name, fn, t_roof in (("fwd", call_fwd, t_fwd), ("fwd_bwd_ctx", call_ctx, t_step),
+                                 ("fwd_bwd_recompute", call_recompute, t_step)):
+            for _ in range(3):
+                fn()
+            st = stats_ms(per_step(fn, steps))
+            row[name] = {"ms": st, "tokens_per_s": T / (st["median"] / 1e3),
+                         "roofline_frac": 1e3 * t_roof / st["median"],
+                         "t_roof_ms": 1e3 * t_roof,
+                         "peak_mem_bytes": peak_bytes(fn)}
+        out[str(T)] = row
+        del d, inp, p
+        torch.cuda.empty_cache()
+    return {"rows": out, "timing": "each call alone, CUDA events on the launching stream; "
+                                   "outputs, context and workspace allocated per call",
+            "peak_mem": "torch max_memory_allocated over one call minus the bytes held "
+                        "before it (inputs excluded)"}
+
+
 # ---------------------------------------------------------------- CPU baseline
 
 def oracle_sample(w, T_sample, nthreads):
@@ -273,6 +394,46 @@ def cpu_threads():
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count() or 1
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu model")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(w, T_sample=8192, runs=3):
+    """The fp64 oracle on the host cores: median of `runs` fwd + bwd over the first T_sample
+    tokens of every head (all cores, one OpenMP thread per (batch, V head) at most), plus one
+    single-thread run over one Q/K head group (H/Hqk V heads) of T_sample tokens."""
+    import dataclasses
+    threads = min(cpu_threads(), w.B * w.H)
+    secs = [oracle_sample(w, T_sample, threads) for _ in range(runs)]
+    med = statistics.median(secs)
+    one = dataclasses.replace(w, Hqk=1, H=w.H // w.Hqk)
+    s1 = oracle_sample(one, T_sample, 1)
+    return {"value": T_sample * w.B / med, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "host_cores": cpu_threads(), "cpu_model": cpu_model(),
+            "runs_s": [round(x, 3) for x in secs],
+            "sample": f"first {T_sample} tokens of all {w.H} V heads, fp64 C oracle fwd+bwd "
+                      f"(OpenMP, {threads} threads), median of {runs} runs",
+            "single_thread": {"tokens_per_s": T_sample * w.B / s1, "seconds": round(s1, 3),
+                              "sample": f"{T_sample} tokens of one Q/K head group "
+                                        f"({w.H // w.Hqk} V heads), 1 thread"}}
 
 
 def workload_of(name, T=0):
@@ -299,7 +460,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = workload_of(args.workload, args.T)
-    threads = min(cpu_threads(), w.B * w.Hqk)
+    threads = min(cpu_threads(), w.B * w.H)
     T_sample = 1024
     for _ in range(args.warmup):
         oracle_sample(w, T_sample, threads)
@@ -313,6 +474,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, args, 1),
         "cpu_baseline": {"kind": "oracle", "value": value, "unit": UNIT, "cores": threads,
+                         "host_cores": cpu_threads(), "cpu_model": cpu_model(),
                          "sample": f"first {T_sample} tokens of all {w.H} V heads per step, "
                                    f"fp64 C oracle fwd+bwd (OpenMP)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -374,6 +536,8 @@ def run_ours(args):
     p = gdn.make_problem(d["q"], d["v"])
     wsf = gdn.workspace(p, gdn.GDN_OP_FWD)
     wsb = gdn.workspace(p, gdn.GDN_OP_BWD)
+    wsfc = gdn.workspace(p, gdn.GDN_OP_FWD_CTX)
+    wsbc = gdn.workspace(p, gdn.GDN_OP_BWD_CTX)
     B, T, H, dv = d["v"].shape
     dk = d["q"].shape[3]
     o = torch.empty_like(d["v"])
@@ -392,12 +556,12 @@ def run_ours(args):
 
     def fwd_ctx():  # the training-step forward: also keeps the segment states for the backward
         gdn.gdn_fwd_ctx(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"],
-                        d["h0"], None, ctx=ctx, o=o, hT=hT, ws=wsf, problem=p, stream=stream)
+                        d["h0"], None, ctx=ctx, o=o, hT=hT, ws=wsfc, problem=p, stream=stream)
 
     def bwd_ctx():
         gdn.gdn_bwd_ctx(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], ctx,
                         d["dO"], d["dHT"], None, dq=dq, dk=dkk, dv=dvv, dg=dg, dbeta=dbeta,
-                        dH0=dH0, ws=wsb, problem=p, stream=stream)
+                        dH0=dH0, ws=wsbc, problem=p, stream=stream)
 
     def bwd_recompute():  # gdn_bwd: recomputes the segment summaries and their prefix
         gdn.gdn_bwd(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["dO"],
@@ -425,10 +589,22 @@ def run_ours(args):
         barrier()
         return ev0.elapsed_time(ev1) / steps
 
+    def per_step(fn, steps):
+        """ms of each of `steps` calls (CUDA events on the launching stream)."""
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
-    assert gdn.gdn_check_device_status(wsb) == gdn.GDN_OK
+    assert gdn.gdn_check_device_status(wsbc) == gdn.GDN_OK
 
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     gpu_id = vis.split(",")[local].strip() if vis else str(local)
@@ -437,7 +613,9 @@ def run_ours(args):
     ms_step = timed(step, args.steps)
     clocks = sampler.stop()
     ms_step = max_over_ranks(ms_step)
+    step_stats = stats_ms(per_step(step, args.steps))
     ms_fwd = max_over_ranks(timed(fwd, args.steps))
+    fwd_stats = stats_ms(per_step(fwd, args.steps))
     ms_recompute = max_over_ranks(timed(step_recompute, args.steps))
     tokens = B * T
     value = job_throughput(ms_step, tokens, world)
@@ -456,8 +634,10 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(w, args, world),
-        "fwd": {"ms": ms_fwd, "tokens_per_s": job_throughput(ms_fwd, tokens, world)},
+        "fwd": {"ms": ms_fwd, "tokens_per_s": job_throughput(ms_fwd, tokens, world),
+                "per_call": fwd_stats},
         "step": "gdn_fwd_ctx + gdn_bwd_ctx (the backward reads the forward's segment states)",
+        "step_per_call": step_stats,
         "fwd_bwd_recompute": {"ms": ms_recompute,
                               "tokens_per_s": job_throughput(ms_recompute, tokens, world),
                               "calls": "gdn_fwd + gdn_bwd (no context)"},
@@ -488,11 +668,11 @@ def run_ours(args):
                     if op == gdn.GDN_OP_FWD_CTX:
                         gdn.gdn_fwd_ctx_kernel(i, d["q"], d["k"], d["v"], d["a"], d["b"],
                                                d["A_log"], d["dt_bias"], d["h0"], None, o, hT,
-                                               ctx, wsf, problem=p, stream=stream)
+                                               ctx, wsfc, problem=p, stream=stream)
                     else:
                         gdn.gdn_bwd_ctx_kernel(i, d["q"], d["k"], d["v"], d["a"], d["b"],
                                                d["A_log"], d["dt_bias"], ctx, None, d["dO"],
-                                               d["dHT"], dq, dkk, dvv, dg, dbeta, dH0, wsb,
+                                               d["dHT"], dq, dkk, dvv, dg, dbeta, dH0, wsbc,
                                                problem=p, stream=stream)
                     e1.record(stream)
                 torch.cuda.synchronize()
@@ -502,7 +682,8 @@ def run_ours(args):
         P = gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD)
         dom = max(tot, key=tot.get)
         ms_dom = tot[dom]
-        flops, byt = kernel_work(dom, w, P)
+        flops, byt = kernel_alg(dom, w)
+        mflops, mbyt = kernel_work(dom, w, P)
         # the kernel is timed alone: burst peaks
         t_f = flops / (peaks["bf16_tflops"] * 1e12)
         t_b = byt / (peaks["hbm_gbs"] * 1e9)
@@ -512,21 +693,42 @@ def run_ours(args):
         else:
             bound, peak, punit = "hbm", peaks["hbm_gbs"], "GB/s"
             achieved = byt / (ms_dom / 1e3) / 1e9
+        traffic = measured_traffic(dom, w.T)
         line["roofline"] = {
             "kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": punit,
-            "frac": achieved / peak, "traffic": measured_traffic(dom, w.T),
+            "frac": achieved / peak, "traffic": traffic,
+            "traffic_over_algorithmic": (traffic / byt) if (traffic and byt) else None,
             "ms_per_launch": ms_dom, "algorithmic_flops_per_launch": flops,
             "algorithmic_bytes_per_launch": byt,
+            "algorithmic": "the method's own contractions and input/output tensors owned by "
+                           "this launch (per-token work of step_roofline, split by launch)",
+            "model_flops_per_launch": mflops, "model_bytes_per_launch": mbyt,
+            "model": "what the design computes and moves, its intermediates included",
             "timing": f"CUDA events around each launch, mean of {reps} launches",
             "peak_source": f"{peaks['source']} (burst: kernel timed alone)",
         }
         kr = {}
         for k, v in tot.items():
-            fl, by = kernel_work(k, w, P)
-            kr[k] = {"ms": round(v, 4), "tflops": round(fl / (v / 1e3) / 1e12, 1),
-                     "gbs": round(by / (v / 1e3) / 1e9, 1)}
+            fl, by = kernel_alg(k, w)
+            mfl, mby = kernel_work(k, w, P)
+            kr[k] = {"ms": round(v, 4),
+                     "alg_frac": round(max(fl / (peaks["bf16_tflops"] * 1e12),
+                                           by / (peaks["hbm_gbs"] * 1e9)) / (v / 1e3), 4),
+                     "model_tflops": round(mfl / (v / 1e3) / 1e12, 1),
+                     "model_gbs": round(mby / (v / 1e3) / 1e9, 1)}
         line["kernel_roofline"] = kr
         line["kernel_ms"] = {k: round(v, 4) for k, v in tot.items()}
+        if traffic is not None:
+            line["step_roofline"]["traffic_over_algorithmic_note"] = (
+                "ncu DRAM bytes of the dominant kernel only; see profiles/ for the launch list")
+
+    # Every sequence length of the measurement matrix (B = 1, H = 32, d = 128, stateful):
+    # forward, training step (context pair) and gdn_fwd + gdn_bwd, each call timed alone
+    # with CUDA events (median, min, p90), the roofline fraction of the median, and the
+    # incremental peak device memory of one call that allocates its own outputs and
+    # workspace.
+    if not args.no_lengths and world == 1:
+        line["lengths"] = measure_lengths(gdn, gi, torch, stream, peaks, args, per_step)
 
     # The Conv1D + SiLU prologue over the projected q, k, v of this workload (C = 2 Hqk dk +
     # H dv channels, K = 4 taps, a left halo, no bias): forward and backward, each timed
@@ -644,10 +846,10 @@ def run_ours(args):
 
         def run_step(x):
             gdn.gdn_fwd_ctx(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"], x["dt_bias"],
-                            x["h0"], None, ctx=ctx, o=o, hT=hT, ws=wsf, problem=p, stream=stream)
+                            x["h0"], None, ctx=ctx, o=o, hT=hT, ws=wsfc, problem=p, stream=stream)
             gdn.gdn_bwd_ctx(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"], x["dt_bias"], ctx,
                             x["dO"], x["dHT"], None, dq=dq, dk=dkk, dv=dvv, dg=dg, dbeta=dbeta,
-                            dH0=dH0, ws=wsb, problem=p, stream=stream)
+                            dH0=dH0, ws=wsbc, problem=p, stream=stream)
 
         def e2e_step():
             cur, nxt = bufs[pipe["i"] % 2], bufs[(pipe["i"] + 1) % 2]
@@ -673,13 +875,7 @@ def run_ours(args):
                                  "first timed step's copies are exposed"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        threads = min(cpu_threads(), w.B * w.Hqk)
-        T_sample = min(w.T, 32768)
-        secs = oracle_sample(w, T_sample, threads)
-        line["cpu_baseline"] = {"value": T_sample * w.B / secs, "unit": UNIT, "cores": threads,
-                                "kind": "oracle",
-                                "sample": f"first {T_sample} tokens of all {w.H} V heads, "
-                                          f"fp64 C oracle fwd+bwd, {secs:.1f} s"}
+        line["cpu_baseline"] = cpu_baseline(w, T_sample=min(w.T, 8192))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

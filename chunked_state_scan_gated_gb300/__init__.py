@@ -355,7 +355,7 @@ def gdn_fwd_ctx(q, k, v, a, b, A_log, dt_bias, h0=None, valid_len=None, *, ctx=N
     if hT is None and want_hT:
         hT = torch.empty((B, H, q.shape[3], dv), dtype=torch.float32, device=q.device)
     ctx = ctx if ctx is not None else ctx_buffer(p, q.device)
-    ws = _ws(p, GDN_OP_FWD, ws, q.device)
+    ws = _ws(p, GDN_OP_FWD_CTX, ws, q.device)
     _check("gdn_fwd_ctx", load_library().gdn_fwd_ctx(
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
         _ptr(dt_bias), _ptr(h0), _ptr(valid_len), _ptr(o), _ptr(hT), _ptr(ctx), ctx.numel(),
@@ -384,7 +384,7 @@ def gdn_bwd_ctx(q, k, v, a, b, A_log, dt_bias, ctx, dO, dHT=None, valid_len=None
     dH0 = kw.pop("dH0", None)
     if dH0 is None and want_dH0:
         dH0 = torch.empty((B, H, q.shape[3], dv), dtype=torch.float32, device=q.device)
-    ws = _ws(p, GDN_OP_BWD, kw.pop("ws", None), q.device)
+    ws = _ws(p, GDN_OP_BWD_CTX, kw.pop("ws", None), q.device)
     _check("gdn_bwd_ctx", load_library().gdn_bwd_ctx(
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
         _ptr(dt_bias), _ptr(ctx), ctx.numel(), _ptr(valid_len), _ptr(dO), _ptr(dHT), _ptr(dq),

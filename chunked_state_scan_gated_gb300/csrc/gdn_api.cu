@@ -160,9 +160,29 @@ size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws) {
   };
   const size_t B = pr.B, H = pr.H, Hqk = pr.Hqk, dk = pr.dk, dv = pr.dv, Tp = pr.Tp,
                NC = pr.NC, P = pr.P;
+  // With a forward context on the tensor-core path the prologue's outputs live in the
+  // context (written by gdn_fwd_ctx, read by gdn_bwd_ctx), not in the workspace.
+  const bool in_ctx = (op == GDN_OP_FWD_CTX || op == GDN_OP_BWD_CTX) && tc_path(pr);
+  if (op == GDN_OP_FWD_CTX) op = GDN_OP_FWD;
+  if (op == GDN_OP_BWD_CTX) op = GDN_OP_BWD;
   const bool bwd = op == GDN_OP_BWD;
   const bool fwd = op == GDN_OP_FWD;
   w.status = (int*)take(64);
+  if (in_ctx) {
+    if (fwd && P > 1) w.Sseg = take(P * B * H * dk * dv);
+    if (bwd) {
+      if (P > 1) {
+        w.Dseg = take(P * B * H * dk * dv);
+        w.dHout = take(P * B * H * dk * dv);
+      }
+      w.hc16 = take(B * H * NC * dk * dv / 2);
+      w.dhc16 = take(B * H * NC * dk * dv / 2);
+      w.dqp = take(B * Tp * H * dk / 2);  // bf16
+      w.dkp = take(B * Tp * H * dk / 2);
+    }
+    if (ws) *ws = w;
+    return off;
+  }
   auto take_prep = [&]() {  // norm factors, gates and tile images of the tensor-core prologue
     w.rqk = take(B * Hqk * NC * 128);
     w.wim = take(B * H * NC * 4096);
@@ -286,19 +306,53 @@ bool inputs_ok(const Prob& pr, const Inputs& in, bool need_q, bool need_v) {
 }
 
 // Forward context (gdn_fwd_ctx / gdn_bwd_ctx): the transitions M of every segment and
-// the start states H_in of every segment, fp32, [P][B][H][dk][dk] then [P][B][H][dk][dv].
+// the start states H_in of every segment, fp32, [P][B][H][dk][dk] then [P][B][H][dk][dv];
+// on the tensor-core path then the chunk prologue's outputs (norm factors, gates and the
+// W, U, P, T tile images), which the backward reads instead of recomputing them.
 struct Ctx {
   float* M;
   float* Hin;
+  WS pro;  // rqk, wim, uim, pim, tim, gl (tensor-core path), else all null
 };
-size_t ctx_bytes(const Prob& pr) {
-  return (size_t)pr.P * pr.B * pr.H * (pr.dk * pr.dk + pr.dk * pr.dv) * sizeof(float);
+size_t ctx_layout(const Prob& pr, void* base, Ctx* c) {
+  Ctx x;
+  memset(&x, 0, sizeof(x));
+  char* b = (char*)base;
+  size_t off = 0;
+  auto take = [&](size_t nfloat) -> float* {
+    float* ptr = base ? (float*)(b + off) : nullptr;
+    off = align_up(off + nfloat * sizeof(float));
+    return ptr;
+  };
+  const size_t B = pr.B, H = pr.H, Hqk = pr.Hqk, NC = pr.NC, P = pr.P;
+  x.M = take(P * B * H * pr.dk * pr.dk);
+  x.Hin = take(P * B * H * pr.dk * pr.dv);
+  if (tc_path(pr)) {
+    x.pro.rqk = take(B * Hqk * NC * 128);
+    x.pro.wim = take(B * H * NC * 4096);
+    x.pro.uim = take(B * H * NC * 4096);
+    x.pro.pim = take(B * H * NC * 2048);
+    x.pro.tim = take(B * H * NC * 2048);
+    x.pro.gl = take(B * H * NC * 64);
+  }
+  if (c) *c = x;
+  return off;
 }
+size_t ctx_bytes(const Prob& pr) { return ctx_layout(pr, nullptr, nullptr); }
 Ctx ctx_of(const Prob& pr, void* base) {
   Ctx c;
-  c.M = (float*)base;
-  c.Hin = c.M + (size_t)pr.P * pr.B * pr.H * pr.dk * pr.dk;
+  ctx_layout(pr, base, &c);
   return c;
+}
+// The prologue outputs of a context call: the workspace pointers redirected into the context.
+void use_ctx_prologue(const Prob& pr, const Ctx& cx, WS* ws) {
+  if (!tc_path(pr)) return;
+  ws->rqk = cx.pro.rqk;
+  ws->wim = cx.pro.wim;
+  ws->uim = cx.pro.uim;
+  ws->pim = cx.pro.pim;
+  ws->tim = cx.pro.tim;
+  ws->gl = cx.pro.gl;
 }
 // H_in of the only segment: h0, or zero
 cudaError_t ctx_single(const Prob& pr, const float* h0, float* Hin, cudaStream_t st) {
@@ -381,7 +435,7 @@ gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const
   if (tc_path(pr)) {
     const float* init = h0;
     int64_t init_stride = 0;
-    GDN_RUN(sc, "prep_tc", launch_prep_tc(pr, in, ws, st));
+    if (!cx) GDN_RUN(sc, "prep_tc", launch_prep_tc(pr, in, ws, st));  // else kept by the forward
     const float* dinit = dHT;
     int64_t dinit_stride = 0;
     if (cx) {  // segment start states from the forward: only the reverse summaries and prefix
@@ -508,8 +562,6 @@ gdn_status gdn_resolved_segments(const gdn_problem* p, int32_t op, int32_t* segm
 
 gdn_status gdn_workspace_size(const gdn_problem* p, int32_t op, size_t* bytes) {
   if (!bytes || op < GDN_OP_FWD || op > GDN_OP_BWD_CTX) return GDN_ERR_INVALID_ARG;
-  if (op == GDN_OP_FWD_CTX) op = GDN_OP_FWD;
-  if (op == GDN_OP_BWD_CTX) op = GDN_OP_BWD;
   Prob pr;
   gdn_status s = resolve_op(p, op, &pr);
   if (s != GDN_OK) return s;
@@ -537,7 +589,10 @@ static gdn_status fwd_impl(const gdn_problem* p, const void* q, const void* k, c
   }
   WS ws;
   cudaStream_t st = (cudaStream_t)stream;
-  if ((s = prepare(p, GDN_OP_FWD, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK) return s;
+  if ((s = prepare(p, with_ctx ? GDN_OP_FWD_CTX : GDN_OP_FWD, workspace, workspace_bytes, st,
+                   &pr, &ws)) != GDN_OK)
+    return s;
+  if (with_ctx) use_ctx_prologue(pr, cx, &ws);
   return run_forward(pr, in, h0, o, hT, ws, st, sc, with_ctx ? &cx : nullptr);
 }
 
@@ -567,7 +622,10 @@ static gdn_status bwd_impl(const gdn_problem* p, const void* q, const void* k, c
   }
   WS ws;
   cudaStream_t st = (cudaStream_t)stream;
-  if ((s = prepare(p, GDN_OP_BWD, workspace, workspace_bytes, st, &pr, &ws)) != GDN_OK) return s;
+  if ((s = prepare(p, with_ctx ? GDN_OP_BWD_CTX : GDN_OP_BWD, workspace, workspace_bytes, st,
+                   &pr, &ws)) != GDN_OK)
+    return s;
+  if (with_ctx) use_ctx_prologue(pr, cx, &ws);
   return run_backward(pr, in, h0, dHT, dq, dk, dv, dg, dbeta, dH0, ws, st, sc,
                       with_ctx ? &cx : nullptr);
 }
@@ -676,7 +734,8 @@ gdn_status gdn_kernel_info(const gdn_problem* p, int32_t op, int32_t index, int3
   WS ws;
   memset(&ws, 0, sizeof(ws));
   Inputs in{};
-  Ctx cx{nullptr, nullptr};
+  Ctx cx;
+  memset(&cx, 0, sizeof(cx));
   if (fwd)
     run_forward(pr, in, nullptr, nullptr, nullptr, ws, nullptr, sc, with_ctx ? &cx : nullptr);
   else

@@ -76,8 +76,8 @@ typedef enum gdn_op {
   GDN_OP_BWD = 1,         /* gdn_bwd, gdn_apply_state_bwd */
   GDN_OP_SUMMARY = 2,     /* gdn_summary */
   GDN_OP_SUMMARY_BWD = 3, /* gdn_summary_bwd */
-  GDN_OP_FWD_CTX = 4,     /* gdn_fwd_ctx (workspace as GDN_OP_FWD) */
-  GDN_OP_BWD_CTX = 5      /* gdn_bwd_ctx (workspace as GDN_OP_BWD) */
+  GDN_OP_FWD_CTX = 4,     /* gdn_fwd_ctx (a GDN_OP_FWD-sized workspace also suffices) */
+  GDN_OP_BWD_CTX = 5      /* gdn_bwd_ctx (a GDN_OP_BWD-sized workspace also suffices) */
 } gdn_op;
 
 /* Problem description.  Fill with gdn_problem_init, then set the sizes. */
@@ -162,13 +162,18 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
  * every segment's transition M_s [dk,dk] (H_out = M_s H_in + S_s) and start state
  * H_in,s [dk,dv]; gdn_bwd recomputes both.  gdn_fwd_ctx is gdn_fwd that also keeps
  * them in `ctx`: M [P][B][H][dk][dk] then H_in [P][B][H][dk][dv], fp32, in a
- * caller-owned, 16-byte aligned device buffer of at least gdn_ctx_size bytes
- * (36 MiB at B=1, H=32, d=128, P=9).  gdn_bwd_ctx is gdn_bwd with h0 replaced by
- * that context: it reads H_in (which already holds h0 as H_in,0) and M instead of
- * recomputing the forward summaries and their prefix; every chunk intermediate is
- * still recomputed.  The context is only valid for the same problem (same resolved
- * P), inputs and h0; the library cannot check that.  Invalid pointer or size:
- * GDN_ERR_INVALID_ARG.  gdn_fwd_ctx_kernel / gdn_bwd_ctx_kernel and the ops
+ * caller-owned, 16-byte aligned device buffer of at least gdn_ctx_size bytes.  On
+ * the bf16 tensor-core path (dk = dv = 128) the context also keeps the outputs of
+ * the chunk prologue (per-token norm factors, cumulative gates, and bf16 tile images
+ * of W = T diag(beta gamma) K, U = T diag(beta) V, P = tril(Q K^T o Gamma) and
+ * T = (I + A)^-1 for every chunk and V head): ~24.8 KB per token at H = 32, d = 128
+ * (812 MiB at T = 32K, P = 9), against 36 MiB without them; the workspaces of
+ * GDN_OP_FWD_CTX and GDN_OP_BWD_CTX shrink by the same images.  gdn_bwd_ctx is
+ * gdn_bwd with h0 replaced by that context: it reads H_in (which already holds h0 as
+ * H_in,0), M and the prologue outputs instead of recomputing the forward summaries,
+ * their prefix and the prologue.  The context is only valid for the same problem
+ * (same resolved P), inputs and h0; the library cannot check that.  Invalid pointer
+ * or size: GDN_ERR_INVALID_ARG.  gdn_fwd_ctx_kernel / gdn_bwd_ctx_kernel and the ops
  * GDN_OP_FWD_CTX / GDN_OP_BWD_CTX of gdn_kernel_info are the profiling aids below
  * for these two calls.
  */

@@ -156,14 +156,27 @@ def test_compose_prefix_validation(lib):
 
 
 def test_ctx_size_and_validation(lib):
-    """The forward context holds M and H_in of every resolved segment; a missing, short or
-    misaligned context is refused before any launch."""
+    """The forward context holds M and H_in of every resolved segment and, on the bf16
+    tensor-core path, the chunk prologue's outputs per chunk: rq/rk (Hqk x 128 fp32), and per
+    V head the W, U images (16 KB each), the P, T images (8 KB each) and 64 fp32 gates; a
+    missing, short or misaligned context is refused before any launch."""
+    NC = 8192 // 64
+    pro = NC * (16 * 128 * 4 + 32 * (16384 + 16384 + 8192 + 8192 + 64 * 4))
     for seg in (0, 1, 5):
         p = problem(segments=seg)
         P = gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD)
         assert P == gdn.gdn_resolved_segments(p, gdn.GDN_OP_BWD)
         assert P == gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD_CTX)
-        assert gdn.gdn_ctx_size(p) == P * 1 * 32 * (128 * 128 + 128 * 128) * 4
+        assert gdn.gdn_ctx_size(p) == P * 1 * 32 * (128 * 128 + 128 * 128) * 4 + pro
+        # the prologue images move from the workspaces into the context
+        for op, op_ctx in ((gdn.GDN_OP_FWD, gdn.GDN_OP_FWD_CTX),
+                           (gdn.GDN_OP_BWD, gdn.GDN_OP_BWD_CTX)):
+            assert gdn.gdn_workspace_size(p, op_ctx) < gdn.gdn_workspace_size(p, op)
+        p32 = problem(segments=seg, dtype=gdn.GDN_FP32)
+        P32 = gdn.gdn_resolved_segments(p32, gdn.GDN_OP_FWD)
+        assert gdn.gdn_ctx_size(p32) == P32 * 1 * 32 * (128 * 128 + 128 * 128) * 4
+        assert gdn.gdn_workspace_size(p32, gdn.GDN_OP_FWD_CTX) == \
+            gdn.gdn_workspace_size(p32, gdn.GDN_OP_FWD)
     p = problem()
     need = gdn.gdn_ctx_size(p)
     vp = ctypes.c_void_p
@@ -175,10 +188,10 @@ def test_ctx_size_and_validation(lib):
         st = lib.gdn_bwd_ctx(ctypes.byref(p), *[vp(A)] * 7, None if ctx is None else vp(ctx), n,
                              None, vp(A), None, *[vp(A)] * 5, None, vp(A), 1 << 40, None)
         assert st == gdn.GDN_ERR_INVALID_ARG
-    assert gdn.gdn_workspace_size(p, gdn.GDN_OP_FWD_CTX) == gdn.gdn_workspace_size(p, gdn.GDN_OP_FWD)
-    assert gdn.gdn_workspace_size(p, gdn.GDN_OP_BWD_CTX) == gdn.gdn_workspace_size(p, gdn.GDN_OP_BWD)
     names = gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD_CTX)
     assert "summary_pair_tc" not in names and "grad_tc" in names      # no forward summaries
+    assert "prep_tc" not in names                                      # nor the prologue
+    assert "prep_tc" in gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD)
     assert gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD_CTX)[-1] == "apply_chain_tc"
 
 
