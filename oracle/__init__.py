@@ -283,3 +283,75 @@ def prefix_bwd(M, D, dHT=None):
 from .conv import conv_silu_bwd, conv_silu_fwd  # noqa: E402,F401
 # The gated RMSNorm epilogue on o (numpy, fp64): see oracle/rmsnorm.py.
 from .rmsnorm import rmsnorm_gated_bwd, rmsnorm_gated_fwd  # noqa: E402,F401
+
+
+# ------------------------------------------------------------ packed variable-length rows
+#
+# The test report of "Linear Attention CP 融合算子 PR #1114" (section 5.2) covers
+# variable-length training samples through trailing padding of each batch row.  Packing
+# several samples into one row generalises it: sequence i is the tokens
+# cu_seqlens[i] .. cu_seqlens[i+1]-1 of the row and runs the gated delta rule on its own,
+# from its own initial state h0[i] (zero when h0 is None), exactly as if it were a batch
+# row of its own; nothing flows across a boundary.  These functions are that definition:
+# one call of the single-sequence oracle above per packed sequence.
+
+
+def seq_bounds(cu_seqlens, T):
+    """[(start, end)] of every packed sequence; cu_seqlens: N + 1 non-decreasing offsets
+    from 0 to T."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64).ravel()
+    if cu.size < 1 or cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must run from 0 to T without decreasing")
+    return [(int(cu[i]), int(cu[i + 1])) for i in range(cu.size - 1)]
+
+
+def _one(x, i):
+    return None if x is None else x[i:i + 1]
+
+
+def core_fwd_varlen(qh, kh, v, g, beta, cu_seqlens, h0=None, nthreads=0):
+    """Packed rows (B = 1) over prepared q_hat, k_hat, g, beta: (o [1,T,H,dv],
+    h_T [N,H,dk,dv]) with h0 [N,H,dk,dv] or None."""
+    qh, kh, v, g, beta, h0 = map(_f64, (qh, kh, v, g, beta, h0))
+    _, T, H, dv = v.shape
+    bounds = seq_bounds(cu_seqlens, T)
+    o = np.empty_like(v)
+    hT = np.empty((len(bounds), H, qh.shape[3], dv))
+    for i, (s, e) in enumerate(bounds):
+        o[:, s:e], hT[i:i + 1] = core_fwd(qh[:, s:e], kh[:, s:e], v[:, s:e], g[:, s:e],
+                                          beta[:, s:e], _one(h0, i), nthreads=nthreads)
+    return o, hT
+
+
+def fwd_varlen(q, k, v, a, b, A_log, dt_bias, cu_seqlens, h0=None, *, l2norm=True, eps=1e-6,
+               scale=None, nthreads=0):
+    """Packed rows (B = 1) from raw inputs: (o [1,T,H,dv], h_T [N,H,dk,dv])."""
+    q, k, v, a, b, A_log, dt_bias, h0 = map(_f64, (q, k, v, a, b, A_log, dt_bias, h0))
+    _, T, H, dv = v.shape
+    bounds = seq_bounds(cu_seqlens, T)
+    o = np.empty_like(v)
+    hT = np.empty((len(bounds), H, q.shape[3], dv))
+    for i, (s, e) in enumerate(bounds):
+        o[:, s:e], hT[i:i + 1] = fwd(q[:, s:e], k[:, s:e], v[:, s:e], a[:, s:e], b[:, s:e],
+                                     A_log, dt_bias, h0=_one(h0, i), l2norm=l2norm, eps=eps,
+                                     scale=scale, nthreads=nthreads)
+    return o, hT
+
+
+def bwd_varlen(q, k, v, a, b, A_log, dt_bias, cu_seqlens, dO, dHT=None, h0=None, *,
+               l2norm=True, eps=1e-6, scale=None, nthreads=0):
+    """Gradients of sum_t <dO_t, o_t> + sum_i <dHT[i], h_T[i]> over packed rows:
+    (dq, dk [1,T,Hqk,dk], dv [1,T,H,dv], dg, dbeta [1,T,H], dH0 [N,H,dk,dv])."""
+    q, k, v, a, b, A_log, dt_bias, h0, dO, dHT = map(
+        _f64, (q, k, v, a, b, A_log, dt_bias, h0, dO, dHT))
+    _, T, H, dv = v.shape
+    bounds = seq_bounds(cu_seqlens, T)
+    dq, dk, dv_ = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    dg, dbe = np.empty_like(a), np.empty_like(a)
+    dH0 = np.empty((len(bounds), H, q.shape[3], dv))
+    for i, (s, e) in enumerate(bounds):
+        r = bwd(q[:, s:e], k[:, s:e], v[:, s:e], a[:, s:e], b[:, s:e], A_log, dt_bias,
+                dO[:, s:e], _one(dHT, i), h0=_one(h0, i), l2norm=l2norm, eps=eps, scale=scale,
+                nthreads=nthreads)
+        dq[:, s:e], dk[:, s:e], dv_[:, s:e], dg[:, s:e], dbe[:, s:e], dH0[i:i + 1] = r
+    return dq, dk, dv_, dg, dbe, dH0
