@@ -6,9 +6,12 @@
 //   dn = dy w silu(z),  do = r (dn - n mean(dn n)),  dz = dy n w silu'(z),
 //   dw = sum over rows of dy n silu(z)
 // A warp owns a row (4 adjacent elements per lane and 128-element chunk, one 8- or
-// 16-byte access each); the row's sums are warp reductions.  Bandwidth-bound.  dw: each
-// warp of the backward walks 16 rows and keeps its lane's dw terms in registers; per-CTA
-// partials (8 warps in a fixed order), then one pass over the CTAs in a fixed order (fp64).
+// 16-byte access each); the row's sums are warp reductions.  Bandwidth-bound.  The
+// backward runs a fixed grid of at most RN_BCTAS CTAs (4 per SM of a 152-SM GPU, all
+// resident at once for D <= 128) whose warps stride over the rows two at a time (the loads of both
+// rows issued together) and keep their lane's dw terms in registers; per-CTA partials
+// (8 warps in a fixed order), then a column-parallel fp64 sum over the CTAs in a fixed
+// order.  The CTA count depends only on the row count, so dw is deterministic.
 #include <cuda_bf16.h>
 #include <string.h>
 
@@ -21,8 +24,9 @@ namespace {
 using namespace vec;
 
 constexpr int RN_NT = 256;      // 8 warps
-constexpr int RN_FROWS = 2;     // rows per warp, forward (their loads issued together)
-constexpr int RN_BROWS = 16;    // rows per warp, backward
+constexpr int RN_FROWS = 4;     // rows per warp, forward (their loads issued together)
+constexpr int RN_BROWS = 2;     // rows per warp and step, backward (loads issued together)
+constexpr int RN_BCTAS = 608;   // CTAs of the backward at most
 constexpr int RN_MAXD = 512;    // 4 chunks of 128 elements
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -90,10 +94,10 @@ __global__ void __launch_bounds__(RN_NT) k_rmsnorm_gated_fwd(RnArgs ar) {
 }
 
 template <int NV, typename T>
-__global__ void __launch_bounds__(RN_NT) k_rmsnorm_gated_bwd(RnArgs ar) {
+__global__ void __launch_bounds__(RN_NT, NV == 1 ? 4 : 1) k_rmsnorm_gated_bwd(RnArgs ar) {
   __shared__ float red[RN_NT / 32][RN_MAXD];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t r0 = ((int64_t)blockIdx.x * (RN_NT / 32) + warp) * RN_BROWS;
+  const int64_t step = (int64_t)gridDim.x * (RN_NT / 32) * RN_BROWS;
   float dwa[NV][4], w[NV][4];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
@@ -102,52 +106,59 @@ __global__ void __launch_bounds__(RN_NT) k_rmsnorm_gated_bwd(RnArgs ar) {
     for (int j = 0; j < 4; ++j) dwa[k][j] = w[k][j] = 0.f;
     if (e < ar.D) ld4(ar.w + e, w[k]);
   }
-  for (int q = 0; q < RN_BROWS; ++q) {
-    const int64_t row = r0 + q;
-    if (row >= ar.rows) break;
-    float o[NV][4], z[NV][4], g[NV][4];
+  for (int64_t r0 = ((int64_t)blockIdx.x * (RN_NT / 32) + warp) * RN_BROWS; r0 < ar.rows;
+       r0 += step) {
+    float o[RN_BROWS][NV][4], z[RN_BROWS][NV][4], g[RN_BROWS][NV][4];
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const int e = k * 128 + lane * 4;
+    for (int q = 0; q < RN_BROWS; ++q)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o[k][j] = z[k][j] = g[k][j] = 0.f;
-      if (e < ar.D) {
+      for (int k = 0; k < NV; ++k) {
+        const int e = k * 128 + lane * 4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[q][k][j] = z[q][k][j] = g[q][k][j] = 0.f;
+        if (r0 + q < ar.rows && e < ar.D) {
+          const int64_t off = (r0 + q) * ar.D + e;
+          ld4(reinterpret_cast<const T*>(ar.o) + off, o[q][k]);
+          ld4(reinterpret_cast<const T*>(ar.z) + off, z[q][k]);
+          ld4(reinterpret_cast<const T*>(ar.dy) + off, g[q][k]);
+        }
+      }
+#pragma unroll
+    for (int q = 0; q < RN_BROWS; ++q) {
+      const int64_t row = r0 + q;
+      if (row >= ar.rows) break;
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ss = fmaf(o[q][k][j], o[q][k][j], ss);
+      const float r = rsqrtf(warp_sum(ss) / (float)ar.D + ar.eps);
+      // n = o r (kept in o), dn = dy w silu(z) (kept in g); dz needs dy n w silu'(z)
+      float dzv[NV][4], dot = 0.f;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float n = o[q][k][j] * r, zz = z[q][k][j], s = sigm(zz), sl = zz * s,
+                      dy = g[q][k][j];
+          dwa[k][j] = fmaf(dy * n, sl, dwa[k][j]);
+          dzv[k][j] = dy * n * w[k][j] * s * (1.f + zz * (1.f - s));
+          o[q][k][j] = n;
+          g[q][k][j] = dy * w[k][j] * sl;
+          dot = fmaf(g[q][k][j], n, dot);
+        }
+      const float m = warp_sum(dot) / (float)ar.D;
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int e = k * 128 + lane * 4;
+        if (e >= ar.D) continue;
+        float d[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d[j] = r * (g[q][k][j] - o[q][k][j] * m);
         const int64_t off = row * ar.D + e;
-        ld4(reinterpret_cast<const T*>(ar.o) + off, o[k]);
-        ld4(reinterpret_cast<const T*>(ar.z) + off, z[k]);
-        ld4(reinterpret_cast<const T*>(ar.dy) + off, g[k]);
+        st4(reinterpret_cast<T*>(ar.out0) + off, d);
+        st4(reinterpret_cast<T*>(ar.out1) + off, dzv[k]);
       }
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) ss = fmaf(o[k][j], o[k][j], ss);
-    const float r = rsqrtf(warp_sum(ss) / (float)ar.D + ar.eps);
-    // n = o r (kept in o), dn = dy w silu(z) (kept in g); dz needs dy n w silu'(z)
-    float dzv[NV][4], dot = 0.f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float n = o[k][j] * r, zz = z[k][j], s = sigm(zz), sl = zz * s, dy = g[k][j];
-        dwa[k][j] = fmaf(dy * n, sl, dwa[k][j]);
-        dzv[k][j] = dy * n * w[k][j] * s * (1.f + zz * (1.f - s));
-        o[k][j] = n;
-        g[k][j] = dy * w[k][j] * sl;
-        dot = fmaf(g[k][j], n, dot);
-      }
-    const float m = warp_sum(dot) / (float)ar.D;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const int e = k * 128 + lane * 4;
-      if (e >= ar.D) continue;
-      float d[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) d[j] = r * (g[k][j] - o[k][j] * m);
-      const int64_t off = row * ar.D + e;
-      st4(reinterpret_cast<T*>(ar.out0) + off, d);
-      st4(reinterpret_cast<T*>(ar.out1) + off, dzv[k]);
     }
   }
   // this CTA's dw: its 8 warps added in order
@@ -167,14 +178,25 @@ __global__ void __launch_bounds__(RN_NT) k_rmsnorm_gated_bwd(RnArgs ar) {
   }
 }
 
+// dw[e] = sum over the n_part CTA partials, in fp64: 32 columns per CTA, warp w adds the
+// partials w, w + 8, ... in order, then warp 0 adds the 8 warp sums in order.
 __global__ void __launch_bounds__(256) k_rmsnorm_reduce(int64_t n_part, int D,
                                                         const float* __restrict__ part,
                                                         float* dw) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= D) return;
+  __shared__ double acc[8][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
   double s = 0.0;
-  for (int64_t p = 0; p < n_part; ++p) s += part[p * D + e];
-  dw[e] = (float)s;
+  if (e < D)
+    for (int64_t p = warp; p < n_part; p += 8) s += part[p * D + e];
+  acc[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && e < D) {
+    double t = 0.0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) t += acc[q][lane];
+    dw[e] = (float)t;
+  }
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -190,7 +212,8 @@ gdn_status check_problem(const gdn_rmsnorm_problem* p) {
 
 int64_t bwd_ctas(const gdn_rmsnorm_problem* p) {
   const int64_t per = (RN_NT / 32) * RN_BROWS;
-  return (p->rows + per - 1) / per;
+  const int64_t n = (p->rows + per - 1) / per;
+  return n < RN_BCTAS ? n : RN_BCTAS;
 }
 
 template <typename T, int NV>
@@ -293,8 +316,8 @@ gdn_status gdn_rmsnorm_gated_bwd(const gdn_rmsnorm_problem* p, const void* o, co
     e = p->dtype == GDN_BF16 ? launch_bwd_t<__nv_bfloat16>(ar, ctas, st)
                              : launch_bwd_t<float>(ar, ctas, st);
   if (e != cudaSuccess) return GDN_ERR_CUDA;
-  k_rmsnorm_reduce<<<(unsigned)((p->D + 255) / 256), 256, 0, st>>>(ctas, p->D,
-                                                                  (const float*)workspace, dw);
+  k_rmsnorm_reduce<<<(unsigned)((p->D + 31) / 32), 256, 0, st>>>(ctas, p->D,
+                                                                 (const float*)workspace, dw);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

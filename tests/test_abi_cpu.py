@@ -254,7 +254,12 @@ def test_rmsnorm_validation_and_workspace(lib):
 
     n = ctypes.c_size_t(0)
     assert lib.gdn_rmsnorm_gated_bwd_workspace_size(ctypes.byref(prob()), ctypes.byref(n)) == 0
-    assert n.value == 8 * 128 * 4  # ceil(1000 / 128 rows per CTA) CTAs x D fp32
+    assert n.value == 63 * 128 * 4  # ceil(1000 / 16 rows per CTA step) CTAs x D fp32
+    # the backward's grid is capped (a fixed count: dw does not depend on the device)
+    big = ctypes.c_size_t(0)
+    assert lib.gdn_rmsnorm_gated_bwd_workspace_size(ctypes.byref(prob(rows=1 << 20)),
+                                                     ctypes.byref(big)) == 0
+    assert big.value == 608 * 128 * 4
     for kw, status in (({"D": 6}, gdn.GDN_ERR_UNSUPPORTED), ({"D": 516}, gdn.GDN_ERR_UNSUPPORTED),
                        ({"D": 0}, gdn.GDN_ERR_INVALID_ARG), ({"rows": -1}, gdn.GDN_ERR_INVALID_ARG),
                        ({"eps": -1.0}, gdn.GDN_ERR_INVALID_ARG),
@@ -271,3 +276,40 @@ def test_rmsnorm_validation_and_workspace(lib):
         gdn.GDN_ERR_INVALID_ARG
     assert lib.gdn_rmsnorm_gated_bwd(ctypes.byref(p), vp(A), vp(A), vp(A), vp(A), vp(A), vp(A),
                                      vp(A), vp(A), n.value - 16, None) == gdn.GDN_ERR_WORKSPACE
+
+
+def test_varlen_validation_and_workspace(lib):
+    """Host-side checks of the packed variable-length calls (no launch reaches CUDA)."""
+    A = 1 << 20
+    vp = ctypes.c_void_p
+    p = problem(T=500, Hqk=1, H=2)
+
+    def ws(cu, op, prob=p):
+        arr = (ctypes.c_int32 * len(cu))(*cu)
+        n = ctypes.c_size_t(0)
+        st = lib.gdn_varlen_workspace_size(ctypes.byref(prob), arr, len(cu) - 1, op,
+                                           ctypes.byref(n))
+        return st, n.value
+
+    cu = [0, 1, 64, 64, 129, 319, 500]
+    st_f, nf = ws(cu, gdn.GDN_OP_FWD)
+    st_b, nb = ws(cu, gdn.GDN_OP_BWD)
+    assert st_f == gdn.GDN_OK and st_b == gdn.GDN_OK and nb > nf > 0
+    # the padded batch [6, 190] of the inputs and output is inside the workspace
+    assert nf >= 6 * 190 * (2 * 128 + 2 * 128 + 2 + 2 + 2 * 128) * 2
+    for bad in ([1, 500], [0, 400], [0, 300, 200, 500], [0, 501]):
+        assert ws(bad, gdn.GDN_OP_FWD)[0] == gdn.GDN_ERR_INVALID_ARG, bad
+    assert ws(cu, gdn.GDN_OP_SUMMARY)[0] == gdn.GDN_ERR_INVALID_ARG
+    assert ws(cu, gdn.GDN_OP_FWD, problem(B=2, T=500, Hqk=1, H=2))[0] == gdn.GDN_ERR_INVALID_ARG
+    assert ws([0], gdn.GDN_OP_FWD, problem(T=0, Hqk=1, H=2))[0] == gdn.GDN_OK
+    # an unsupported shape fails as it does for gdn_fwd
+    assert ws(cu, gdn.GDN_OP_FWD, problem(T=500, Hqk=1, H=2, dk=64))[0] == \
+        gdn.GDN_ERR_UNSUPPORTED
+    arr = (ctypes.c_int32 * 3)(0, 300, 200)
+    st = lib.gdn_fwd_varlen(ctypes.byref(problem(T=200, Hqk=1, H=2)), vp(A), arr, 2,
+                            *[vp(A)] * 5, vp(A), vp(A), None, vp(A), None, vp(A), 1 << 40, None)
+    assert st == gdn.GDN_ERR_INVALID_ARG
+    arr = (ctypes.c_int32 * 3)(0, 100, 200)
+    st = lib.gdn_fwd_varlen(ctypes.byref(problem(T=200, Hqk=1, H=2)), vp(A), arr, 2,
+                            *[vp(A)] * 5, vp(A), vp(A), None, vp(A), None, vp(A), 16, None)
+    assert st == gdn.GDN_ERR_WORKSPACE
