@@ -42,6 +42,8 @@ EXPORTS = (
     "gdn_fwd_ctx_kernel", "gdn_bwd_ctx_kernel", "gdn_conv_silu_fwd",
     "gdn_conv_silu_bwd_workspace_size", "gdn_conv_silu_bwd", "gdn_rmsnorm_gated_fwd",
     "gdn_rmsnorm_gated_bwd_workspace_size", "gdn_rmsnorm_gated_bwd",
+    "gdn_varlen_workspace_size", "gdn_fwd_varlen", "gdn_bwd_varlen",
+    "gdn_varlen_check_device_status",
 )
 
 
@@ -142,6 +144,14 @@ def load_library(path: str | None = None):
             "gdn_rmsnorm_gated_bwd_workspace_size": ([_RPP, ctypes.POINTER(ctypes.c_size_t)],
                                                      ctypes.c_int),
             "gdn_rmsnorm_gated_bwd": ([_RPP] + [_VP] * 8 + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_varlen_workspace_size": ([_PP, _VP, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+            "gdn_fwd_varlen": ([_PP, _VP, _VP, ctypes.c_int32] + [_VP] * 11
+                               + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_bwd_varlen": ([_PP, _VP, _VP, ctypes.c_int32] + [_VP] * 17
+                               + [ctypes.c_size_t, _VP], ctypes.c_int),
+            "gdn_varlen_check_device_status": ([_VP, _PP, _VP, ctypes.c_int32, ctypes.c_int32,
+                                                _VP], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -668,3 +678,87 @@ def gdn_rmsnorm_gated_bwd(o, z, w, dy, eps=1e-6, *, d_o=None, dz=None, dw=None, 
         ctypes.byref(p), _ptr(o), _ptr(z), _ptr(w), _ptr(dy), _ptr(d_o), _ptr(dz), _ptr(dw),
         _ptr(ws), ws.numel(), _stream(stream)))
     return d_o, dz, dw
+
+
+# ------------------------------------------------------------ packed variable-length rows
+
+class Varlen:
+    """The offsets of a packed row: a host int32 copy (sizes the launches) and a device
+    copy (read by the kernels), both [N + 1], from 0 to T."""
+
+    def __init__(self, cu_seqlens, device="cuda"):
+        host = torch.as_tensor(cu_seqlens, dtype=torch.int32).reshape(-1).cpu().contiguous()
+        self.host = host
+        self.n = int(host.numel()) - 1
+        if self.n < 0:
+            raise ValueError("cu_seqlens needs at least one offset")
+        self.dev = host.to(device)
+
+    def host_ptr(self):
+        return ctypes.c_void_p(self.host.data_ptr())
+
+
+def _varlen_of(cu_seqlens, device):
+    return cu_seqlens if isinstance(cu_seqlens, Varlen) else Varlen(cu_seqlens, device)
+
+
+def gdn_varlen_workspace_size(problem: Problem, cu: Varlen, op: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("gdn_varlen_workspace_size", load_library().gdn_varlen_workspace_size(
+        ctypes.byref(problem), cu.host_ptr(), cu.n, op, ctypes.byref(n)))
+    return n.value
+
+
+def varlen_workspace(problem: Problem, cu: Varlen, op: int, device=None) -> torch.Tensor:
+    n = gdn_varlen_workspace_size(problem, cu, op)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device or "cuda")
+
+
+def gdn_fwd_varlen(q, k, v, a, b, A_log, dt_bias, cu_seqlens, h0=None, *, segments=0,
+                   l2norm=True, eps=1e-6, scale=0.0, o=None, hT=None, want_hT=True, ws=None,
+                   stream=None, problem=None):
+    """Packed rows (B = 1): q, k [1,T,Hqk,dk], v [1,T,H,dv], a, b [1,T,H]; sequence i is
+    tokens cu_seqlens[i] .. cu_seqlens[i+1]-1, run from h0[i] ([N,H,dk,dv] or None).
+    Returns (o [1,T,H,dv], hT [N,H,dk,dv] fp32 or None)."""
+    cu = _varlen_of(cu_seqlens, q.device)
+    p = problem or make_problem(q, v, segments=segments, l2norm=l2norm, eps=eps, scale=scale)
+    _, T, H, dv = v.shape
+    if o is None:
+        o = torch.empty((1, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_hT:
+        hT = torch.empty((cu.n, H, q.shape[3], dv), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = varlen_workspace(p, cu, GDN_OP_FWD, q.device)
+    _check("gdn_fwd_varlen", load_library().gdn_fwd_varlen(
+        ctypes.byref(p), _ptr(cu.dev), cu.host_ptr(), cu.n, _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+        _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(o), _ptr(hT), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return o, hT
+
+
+def gdn_bwd_varlen(q, k, v, a, b, A_log, dt_bias, cu_seqlens, dO, dHT=None, h0=None, *,
+                   segments=0, l2norm=True, eps=1e-6, scale=0.0, want_dH0=True, ws=None,
+                   stream=None, problem=None):
+    """Backward of gdn_fwd_varlen: (dq, dk, dv, dg, dbeta, dH0 [N,H,dk,dv] or None)."""
+    cu = _varlen_of(cu_seqlens, q.device)
+    p = problem or make_problem(q, v, segments=segments, l2norm=l2norm, eps=eps, scale=scale)
+    _, T, H, dv = v.shape
+    dq, dk, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg = torch.empty((1, T, H), dtype=torch.float32, device=q.device)
+    dbeta = torch.empty_like(dg)
+    dH0 = torch.empty((cu.n, H, q.shape[3], dv), dtype=torch.float32,
+                      device=q.device) if want_dH0 else None
+    if ws is None:
+        ws = varlen_workspace(p, cu, GDN_OP_BWD, q.device)
+    _check("gdn_bwd_varlen", load_library().gdn_bwd_varlen(
+        ctypes.byref(p), _ptr(cu.dev), cu.host_ptr(), cu.n, _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+        _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(dO), _ptr(dHT), _ptr(dq), _ptr(dk),
+        _ptr(dv_), _ptr(dg), _ptr(dbeta), _ptr(dH0), _ptr(ws), ws.numel(), _stream(stream)))
+    return dq, dk, dv_, dg, dbeta, dH0
+
+
+def gdn_varlen_check_device_status(ws, problem: Problem, cu: Varlen, op: int,
+                                   stream=None) -> int:
+    """Synchronises and reads/clears the status words of a varlen call's workspace."""
+    return load_library().gdn_varlen_check_device_status(
+        _ptr(ws), ctypes.byref(problem), cu.host_ptr(), cu.n, op, _stream(stream))

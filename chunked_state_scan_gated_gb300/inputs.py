@@ -108,13 +108,48 @@ def make_inputs(w: Workload, *, T: Optional[int] = None, H: Optional[int] = None
     return out
 
 
+def make_varlen_inputs(w: Workload, lengths, *, seed: Optional[int] = None) -> dict:
+    """A packed row of len(lengths) sequences: q, k, v, a, b, dO of one row (B = 1) of
+    T = sum(lengths) tokens as in make_inputs, h0 and dHT [N,H,dk,dv] (one per sequence,
+    when the workload has them) and cu_seqlens int32 [N + 1] (the running offsets)."""
+    import dataclasses
+    lengths = [int(x) for x in lengths]
+    T = sum(lengths)
+    w1 = dataclasses.replace(w, B=1, T=T, valid_len=None)
+    out = make_inputs(w1, seed=seed)
+    seed = w.seed if seed is None else seed
+    gen = torch.Generator().manual_seed(seed + 7919)
+    N = len(lengths)
+    out["h0"] = (w.h0_std * _normal(gen, (N, w.H, w.dk, w.dv))) if w.h0_std else None
+    if w.with_dHT:
+        dHT = _normal(gen, (N, w.H, w.dk, w.dv))
+        out["dHT"] = dHT / (dHT.numel() ** 0.5) if w.grad_scale == "numel" else dHT
+    cu = [0]
+    for x in lengths:
+        cu.append(cu[-1] + x)
+    out["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32)
+    return out
+
+
+def length_mix(total: int, n: int, *, seed: int = 0, min_len: int = 1) -> list:
+    """n sequence lengths that sum to total, drawn around total / n (uniform cut points of
+    the row, at least min_len each): a packed batch of training samples of mixed length."""
+    gen = torch.Generator().manual_seed(seed)
+    free = total - n * min_len
+    if free < 0:
+        raise ValueError("total too small for n sequences of min_len")
+    cuts = sorted(torch.randint(0, free + 1, (n - 1,), generator=gen).tolist())
+    edges = [0] + cuts + [free]
+    return [edges[i + 1] - edges[i] + min_len for i in range(n)]
+
+
 def to_numpy64(inputs: dict) -> dict:
     """The exact (already rounded) values as float64 numpy arrays, for the oracle."""
     res = {}
     for key, val in inputs.items():
         if val is None:
             res[key] = None
-        elif key == "valid_len":
+        elif key in ("valid_len", "cu_seqlens"):
             res[key] = val.numpy().astype("int32")
         else:
             res[key] = val.to(torch.float64).numpy()

@@ -392,6 +392,50 @@ gdn_status gdn_conv_silu_bwd(const gdn_conv_problem* p, const void* x, const flo
                              size_t workspace_bytes, void* stream);
 
 /*
+ * Packed variable-length rows (several sequences in one row, each with its own state):
+ * the test report's variable-length training samples ("Linear Attention CP 融合算子
+ * PR #1114 测试报告", section 5.2, there as trailing padding of each batch row)
+ * generalised to any number of samples per row.  Sequence i is the tokens
+ * cu[i] .. cu[i+1]-1 of the row; it runs the gated delta rule from h0[i] (zero when h0
+ * is NULL) and ends in h_T[i]; nothing flows across a boundary.  Gradients are those of
+ * sum_t <dO_t, o_t> + sum_i <dHT[i], h_T[i]>.
+ *  - p: B = 1, T = the row's token count (T_stride 0 or T); the other fields as gdn_fwd.
+ *  - cu_seqlens: DEVICE int32 [n_seqs + 1]; cu_seqlens_host: the same offsets in HOST
+ *    memory (0 = cu[0] <= cu[1] <= ... <= cu[n_seqs] = T), read during the call to size
+ *    the launches; the two must agree.  A device copy that does not (an offset outside
+ *    [0, T] or a length above the host copy's longest) is recorded in the status word
+ *    and its sequence skipped; read it with gdn_varlen_check_device_status.
+ *  - q, k [1,T,Hqk,dk], v, o, dO, dv [1,T,H,dv], a, b, dg, dbeta [1,T,H] as in gdn_fwd /
+ *    gdn_bwd; h0, hT, dHT, dH0 [n_seqs,H,dk,dv] fp32 (nullable as in gdn_fwd / gdn_bwd).
+ *  - Work: the sequences are copied into a padded batch [n_seqs, Lmax] (Lmax = the
+ *    longest sequence) inside the workspace, run by the batched path with valid_len = the
+ *    lengths, and the outputs copied back; the padded tails cost masked-token work.
+ *  - Workspace: gdn_varlen_workspace_size (op GDN_OP_FWD or GDN_OP_BWD), 256-byte aligned.
+ * Errors: as gdn_fwd / gdn_bwd; offsets that are not non-decreasing from 0 to T, B != 1
+ * or n_seqs < 0: GDN_ERR_INVALID_ARG.  n_seqs = 0 (T = 0) does nothing.
+ */
+gdn_status gdn_varlen_workspace_size(const gdn_problem* p, const int32_t* cu_seqlens_host,
+                                     int32_t n_seqs, int32_t op, size_t* bytes);
+gdn_status gdn_fwd_varlen(const gdn_problem* p, const int32_t* cu_seqlens,
+                          const int32_t* cu_seqlens_host, int32_t n_seqs, const void* q,
+                          const void* k, const void* v, const void* a, const void* b,
+                          const float* A_log, const float* dt_bias, const float* h0, void* o,
+                          float* hT, void* workspace, size_t workspace_bytes, void* stream);
+gdn_status gdn_bwd_varlen(const gdn_problem* p, const int32_t* cu_seqlens,
+                          const int32_t* cu_seqlens_host, int32_t n_seqs, const void* q,
+                          const void* k, const void* v, const void* a, const void* b,
+                          const float* A_log, const float* dt_bias, const float* h0,
+                          const void* dO, const float* dHT, void* dq, void* dk, void* dv,
+                          float* dg, float* dbeta, float* dH0, void* workspace,
+                          size_t workspace_bytes, void* stream);
+/* Synchronises `stream`, then reads and clears the status words of a varlen call's
+   workspace (its own and the batched call's): GDN_ERR_DEVICE_TIMEOUT, GDN_ERR_INVALID_ARG
+   (device offsets disagreed with the host copy, or a clamped length) or GDN_OK. */
+gdn_status gdn_varlen_check_device_status(void* workspace, const gdn_problem* p,
+                                          const int32_t* cu_seqlens_host, int32_t n_seqs,
+                                          int32_t op, void* stream);
+
+/*
  * Gated RMSNorm on the core's output: the step after the core ("linear attention cp
  * #1035", section "What does this PR do": the output goes through RMSNorm, the gate and
  * the output projection; the test report names the module "RMSNormGated").  For every
