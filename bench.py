@@ -126,7 +126,7 @@ def kernel_alg(name, w):
         return (f_local * tok * H, in_fwd) if op == "fwd" else (0.0, 0.0)
     if kname == "apply_chain_tc":
         return f_chain * tok * H, tok * H * dv * e + state * (2 if w.h0_std else 1)
-    if kname == "states_pair_tc":
+    if kname in ("states_pair_tc", "dstates_chain_tc"):
         return f_rev * tok * H, state * ((1 if w.h0_std else 0) + (1 if w.with_dHT else 0) + 1)
     if kname == "grad_tc":
         return (2 * f_fwd - f_rev) * tok * H, in_fwd + tok * (H * dv * e + H * dv * e + 2 * H * 4)
@@ -178,9 +178,10 @@ def kernel_work(name, w, P):
         f1, b1 = kernel_work("bwd.states_chain_tc", w, P)
         f2, b2 = kernel_work("bwd.dstate_chain_tc", w, P)
         return f1 + f2, b1 + b2
-    if kname == "apply_chain_tc":
+    if kname == "apply_chain_tc":  # gdn_fwd_ctx: also every chunk-start state image
         f = (2 * mm(C, dv, dk) + mm(dk, dv, C) + mm(C, dv, C)) * ch
-        byt = ch * (5 * tile + tile_p + C * 12) + B * H * state * (1 + (1 if P > 1 or w.h0_std else 0))
+        byt = ch * (5 * tile + tile_p + C * 12 + dk * dv * 2) + \
+            B * H * state * (1 + (1 if P > 1 or w.h0_std else 0))
         return f, byt
     if kname == "states_chain_tc":
         f = (mm(C, dv, dk) + mm(dk, dv, C)) * ch
@@ -801,6 +802,47 @@ def run_ours(args):
             "algorithmic_bytes": {"fwd": bytes_f, "bwd": bytes_b},
             "peak": f"{peaks['hbm_gbs']} GB/s ({peaks['source']})"}
         del rd, ry, rdo, rdz, rdw, rws
+
+    # Packed variable-length row (the "next" row f4): the workload's T tokens as eight
+    # sequences of mixed length (seeded cut points), each with its own h0 and dH_T;
+    # gdn_fwd_varlen and gdn_fwd_varlen + gdn_bwd_varlen, each timed alone.  The padded batch
+    # the call runs holds N x Lmax token slots; tokens/s count the row's T real tokens, and
+    # the roofline fraction is that of the monolithic algorithmic work of T tokens.
+    if not args.no_kernel_profile and world == 1:
+        lens = gi.length_mix(w.T, 8, seed=w.seed + 91)
+        vi = gi.make_varlen_inputs(w, lens, seed=w.seed + 91)
+        vd = {k: (v.cuda() if torch.is_tensor(v) and k != "cu_seqlens" else v)
+              for k, v in vi.items()}
+        cu = gdn.Varlen(vi["cu_seqlens"])
+        vfin = (vd["q"], vd["k"], vd["v"], vd["a"], vd["b"], vd["A_log"], vd["dt_bias"])
+        vp = gdn.make_problem(vd["q"], vd["v"])
+        vwf = gdn.varlen_workspace(vp, cu, gdn.GDN_OP_FWD)
+        vwb = gdn.varlen_workspace(vp, cu, gdn.GDN_OP_BWD)
+        vo = torch.empty_like(vd["v"])
+        vhT = torch.empty((len(lens), H, dk, dv), dtype=torch.float32, device="cuda")
+
+        def vl_fwd():
+            gdn.gdn_fwd_varlen(*vfin, cu, vd["h0"], o=vo, hT=vhT, ws=vwf, problem=vp,
+                               stream=stream)
+
+        def vl_step():
+            vl_fwd()
+            gdn.gdn_bwd_varlen(*vfin, cu, vd["dO"], vd["dHT"], vd["h0"], ws=vwb, problem=vp,
+                               stream=stream)
+
+        for _ in range(3):
+            vl_step()
+        torch.cuda.synchronize()
+        assert gdn.gdn_varlen_check_device_status(vwb, vp, cu, gdn.GDN_OP_BWD) == gdn.GDN_OK
+        ms_vf, ms_vs = timed(vl_fwd, args.steps), timed(vl_step, args.steps)
+        line["varlen"] = {
+            "lengths": lens, "tokens": w.T, "padded_slots": len(lens) * max(lens),
+            "fwd_ms": ms_vf, "fwd_tokens_per_s": w.T / (ms_vf / 1e3),
+            "fwd_bwd_ms": ms_vs, "fwd_bwd_tokens_per_s": w.T / (ms_vs / 1e3),
+            "fwd_roofline_frac": 1e3 * t_roof_fwd / ms_vf,
+            "fwd_bwd_roofline_frac": 1e3 * t_roof_step / ms_vs,
+            "calls": "gdn_fwd_varlen; gdn_fwd_varlen + gdn_bwd_varlen (recomputing backward)"}
+        del vd, vi, vo, vhT, vwf, vwb
 
     # End to end: pinned host inputs copied in, fwd + bwd, result states read back, every
     # step.  As an input pipeline would, the inputs are double-buffered on the device: the

@@ -614,7 +614,10 @@ def gdn_conv_silu_fwd(x, w, bias=None, halo=None, *, y=None, stream=None, proble
 
 def gdn_conv_silu_bwd(x, w, bias, halo, dy, *, want_dbias=True, want_dhalo=True, dx=None,
                       dw=None, dbias=None, dhalo=None, ws=None, stream=None, problem=None):
-    """(dx [B,T,C], dw [C,K] fp32, dbias [C] fp32 or None, dhalo [B,K-1,C] or None)."""
+    """(dx [B,T,C], dw [C,K] fp32, dbias [C] fp32 or None, dhalo [B,K-1,C] or None).
+
+    With a problem whose T_stride exceeds T, only tokens [0, T) of each row of dx are
+    written; a dx allocated here (like x) leaves the rest of each row uninitialised."""
     p = problem or make_conv_problem(x, w.shape[1])
     B, _, C = x.shape
     K = w.shape[1]

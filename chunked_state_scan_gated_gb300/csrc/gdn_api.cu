@@ -170,12 +170,11 @@ size_t workspace_layout(const Prob& pr, int op, void* base, WS* ws) {
   w.status = (int*)take(64);
   if (in_ctx) {
     if (fwd && P > 1) w.Sseg = take(P * B * H * dk * dv);
-    if (bwd) {
+    if (bwd) {  // the chunk-start states come from the context too
       if (P > 1) {
         w.Dseg = take(P * B * H * dk * dv);
         w.dHout = take(P * B * H * dk * dv);
       }
-      w.hc16 = take(B * H * NC * dk * dv / 2);
       w.dhc16 = take(B * H * NC * dk * dv / 2);
       w.dqp = take(B * Tp * H * dk / 2);  // bf16
       w.dkp = take(B * Tp * H * dk / 2);
@@ -308,11 +307,12 @@ bool inputs_ok(const Prob& pr, const Inputs& in, bool need_q, bool need_v) {
 // Forward context (gdn_fwd_ctx / gdn_bwd_ctx): the transitions M of every segment and
 // the start states H_in of every segment, fp32, [P][B][H][dk][dk] then [P][B][H][dk][dv];
 // on the tensor-core path then the chunk prologue's outputs (norm factors, gates and the
-// W, U, P, T tile images), which the backward reads instead of recomputing them.
+// W, U, P, T tile images) and the bf16 image of every chunk-start state (written by the
+// forward's output chain), which the backward reads instead of recomputing them.
 struct Ctx {
   float* M;
   float* Hin;
-  WS pro;  // rqk, wim, uim, pim, tim, gl (tensor-core path), else all null
+  WS pro;  // rqk, wim, uim, pim, tim, gl, hc16 (tensor-core path), else all null
 };
 size_t ctx_layout(const Prob& pr, void* base, Ctx* c) {
   Ctx x;
@@ -334,6 +334,7 @@ size_t ctx_layout(const Prob& pr, void* base, Ctx* c) {
     x.pro.pim = take(B * H * NC * 2048);
     x.pro.tim = take(B * H * NC * 2048);
     x.pro.gl = take(B * H * NC * 64);
+    x.pro.hc16 = take(B * H * NC * pr.dk * pr.dv / 2);
   }
   if (c) *c = x;
   return off;
@@ -353,6 +354,7 @@ void use_ctx_prologue(const Prob& pr, const Ctx& cx, WS* ws) {
   ws->pim = cx.pro.pim;
   ws->tim = cx.pro.tim;
   ws->gl = cx.pro.gl;
+  ws->hc16 = cx.pro.hc16;
 }
 // H_in of the only segment: h0, or zero
 cudaError_t ctx_single(const Prob& pr, const float* h0, float* Hin, cudaStream_t st) {
@@ -394,7 +396,7 @@ gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* 
     }
     GDN_RUN(sc, "apply_chain_tc",
             launch_chain_tc(pr, in, ws, 0, 0, pr.P, init, init_stride, o, hT, nullptr, nullptr,
-                            0, nullptr, st));
+                            0, cx ? ws.hc16 : nullptr, st));  // context: keep chunk-start states
     return GDN_OK;
   }
   GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, false, st));
@@ -465,7 +467,11 @@ gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const
       dinit = ws.dHout;
       dinit_stride = sstride;
     }
-    {  // every chunk-start state with every chunk-end state gradient
+    if (cx && tc_path(pr)) {  // chunk-start states kept by the forward: the reverse chain alone
+      GDN_RUN(sc, "dstates_chain_tc",
+              launch_dchain_tc(pr, in, ws, 0, 0, pr.P, dinit, dinit_stride, ws.dhc16, dH0,
+                               nullptr, 0, st));
+    } else {  // every chunk-start state with every chunk-end state gradient
       const ChainPass f{0, pr.P, init, init_stride, nullptr, nullptr, 0, ws.hc16};
       const ReversePass r{0, pr.P, dinit, dinit_stride, ws.dhc16, dH0, nullptr, 0};
       GDN_RUN(sc, "states_pair_tc", launch_chain_pair_tc(pr, in, ws, 2, f, 0, r, st));

@@ -32,7 +32,8 @@ using namespace vec;
 constexpr int CONV_NT = 256;  // threads: 32 channel quads x 8 token runs
 constexpr int CONV_CH = 128;  // channels per CTA
 // tokens per CTA: forward 256 (bf16) / 128 (fp32), backward half that, so that a CTA's
-// staged rows take ~66 KB and three CTAs share an SM
+// staged rows take ~66 KB.  Forward: three CTAs per SM (shared memory; 62 registers at
+// K = 4).  Backward: two CTAs per SM (100 registers at K = 4)
 template <typename T>
 struct Tile {
   static constexpr int ROWB = CONV_CH * (int)sizeof(T);  // bytes of one staged token row
@@ -157,7 +158,9 @@ __global__ void __launch_bounds__(CONV_NT) k_conv_bwd(ConvArgs ar) {
     for (int i = 0; i <= K; ++i) acc[j][i] = 0.f;
   if (live) {
     const int uend = (int)(t0 + u0 + RUN < ar.T ? u0 + RUN : ar.T - t0);  // own tokens
-    const int ulast = (int)(ar.T - t0);  // tokens at or past it have no ds
+    // tokens at or past ulast have no ds (clamped before the cast: T - t0 may exceed int)
+    const int64_t rest = ar.T - t0, span = TOK + 2 * (K - 1);
+    const int ulast = (int)(rest < span ? rest : span);
     float w[4][K], bs[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {

@@ -580,7 +580,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
       // apply: the scaled q tile must be complete; otherwise the loop's last barrier
       // already ordered the state tile S(c) before MMA_a
       if (kApply) CHAIN_SYNC();
-      if (MODE == CH_STATES && tid == 0) {  // chunk-start state: the bf16 S tile image, as is
+      // chunk-start state: the bf16 S tile image, as is (states; apply when asked to keep them)
+      if ((MODE == CH_STATES || (kApply && ar.hc != nullptr)) && tid == 0) {
         bulk_store(ar.hc + (bh * ar.NC + c) * (int64_t)(2 * kImg), sm + OFF_S, 2 * kImg);
         bulk_commit();
       }

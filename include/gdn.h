@@ -166,12 +166,13 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
  * the bf16 tensor-core path (dk = dv = 128) the context also keeps the outputs of
  * the chunk prologue (per-token norm factors, cumulative gates, and bf16 tile images
  * of W = T diag(beta gamma) K, U = T diag(beta) V, P = tril(Q K^T o Gamma) and
- * T = (I + A)^-1 for every chunk and V head): ~24.8 KB per token at H = 32, d = 128
- * (812 MiB at T = 32K, P = 9), against 36 MiB without them; the workspaces of
+ * T = (I + A)^-1 for every chunk and V head) and the bf16 image of every chunk-start
+ * state S (written by the forward's output chain): ~41.2 KB per token at H = 32,
+ * d = 128 (1.32 GiB at T = 32K, P = 9), against 36 MiB without them; the workspaces of
  * GDN_OP_FWD_CTX and GDN_OP_BWD_CTX shrink by the same images.  gdn_bwd_ctx is
  * gdn_bwd with h0 replaced by that context: it reads H_in (which already holds h0 as
- * H_in,0), M and the prologue outputs instead of recomputing the forward summaries,
- * their prefix and the prologue.  The context is only valid for the same problem
+ * H_in,0), M, the prologue outputs and the chunk-start states instead of recomputing
+ * the forward summaries, their prefix, the prologue and the forward state chain.  The context is only valid for the same problem
  * (same resolved P), inputs and h0; the library cannot check that.  Invalid pointer
  * or size: GDN_ERR_INVALID_ARG.  gdn_fwd_ctx_kernel / gdn_bwd_ctx_kernel and the ops
  * GDN_OP_FWD_CTX / GDN_OP_BWD_CTX of gdn_kernel_info are the profiling aids below

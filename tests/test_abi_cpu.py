@@ -157,11 +157,12 @@ def test_compose_prefix_validation(lib):
 
 def test_ctx_size_and_validation(lib):
     """The forward context holds M and H_in of every resolved segment and, on the bf16
-    tensor-core path, the chunk prologue's outputs per chunk: rq/rk (Hqk x 128 fp32), and per
-    V head the W, U images (16 KB each), the P, T images (8 KB each) and 64 fp32 gates; a
-    missing, short or misaligned context is refused before any launch."""
+    tensor-core path, per chunk the prologue's outputs -- rq/rk (Hqk x 128 fp32), and per V head
+    the W, U images (16 KB each), the P, T images (8 KB each) and 64 fp32 gates -- and the bf16
+    image of the chunk-start state of every V head (32 KB); a missing, short or misaligned
+    context is refused before any launch."""
     NC = 8192 // 64
-    pro = NC * (16 * 128 * 4 + 32 * (16384 + 16384 + 8192 + 8192 + 64 * 4))
+    pro = NC * (16 * 128 * 4 + 32 * (16384 + 16384 + 8192 + 8192 + 64 * 4 + 32768))
     for seg in (0, 1, 5):
         p = problem(segments=seg)
         P = gdn.gdn_resolved_segments(p, gdn.GDN_OP_FWD)
@@ -191,6 +192,7 @@ def test_ctx_size_and_validation(lib):
     names = gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD_CTX)
     assert "summary_pair_tc" not in names and "grad_tc" in names      # no forward summaries
     assert "prep_tc" not in names                                      # nor the prologue
+    assert "dstates_chain_tc" in names and "states_pair_tc" not in names  # nor the states
     assert "prep_tc" in gdn.gdn_kernel_info(p, gdn.GDN_OP_BWD)
     assert gdn.gdn_kernel_info(p, gdn.GDN_OP_FWD_CTX)[-1] == "apply_chain_tc"
 
