@@ -364,6 +364,14 @@ cudaError_t ctx_single(const Prob& pr, const float* h0, float* Hin, cudaStream_t
             : cudaMemsetAsync(Hin, 0, n, st);
 }
 
+cudaError_t pad_zero_grads(const Prob& pr, const int32_t* valid_len, void* dv, float* dg,
+                           float* dbeta, cudaStream_t st) {
+  cudaError_t e = launch_pad_tail_zero(pr, valid_len, dv, pr.H * pr.dv * 2, st);
+  if (e == cudaSuccess) e = launch_pad_tail_zero(pr, valid_len, dg, pr.H * 4, st);
+  if (e == cudaSuccess) e = launch_pad_tail_zero(pr, valid_len, dbeta, pr.H * 4, st);
+  return e;
+}
+
 gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* o, float* hT,
                        const WS& ws, cudaStream_t st, Sched& sc, const Ctx* cx = nullptr) {
   const float* init = h0;
@@ -397,6 +405,8 @@ gdn_status run_forward(const Prob& pr, const Inputs& in, const float* h0, void* 
     GDN_RUN(sc, "apply_chain_tc",
             launch_chain_tc(pr, in, ws, 0, 0, pr.P, init, init_stride, o, hT, nullptr, nullptr,
                             0, cx ? ws.hc16 : nullptr, st));  // context: keep chunk-start states
+    if (in.valid_len)  // chunks of padding only were skipped: their outputs are zero
+      GDN_RUN(sc, "pad_zero", launch_pad_tail_zero(pr, in.valid_len, o, pr.H * pr.dv * 2, st));
     return GDN_OK;
   }
   GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, false, st));
@@ -477,7 +487,9 @@ gdn_status run_backward(const Prob& pr, const Inputs& in, const float* h0, const
       GDN_RUN(sc, "states_pair_tc", launch_chain_pair_tc(pr, in, ws, 2, f, 0, r, st));
     }
     GDN_RUN(sc, "grad_tc", launch_grad2_tc(pr, in, ws, ws.hc16, ws.dhc16, dv, dg, dbeta, st));
-    GDN_RUN(sc, "qk_grad_tc", launch_qk_grad_tc(pr, in, ws, dq, dk, st));
+    GDN_RUN(sc, "qk_grad_tc", launch_qk_grad_tc(pr, in, ws, dq, dk, st));  // masks padding
+    if (in.valid_len)  // chunks of padding only were skipped: their gradients are zero
+      GDN_RUN(sc, "pad_zero", pad_zero_grads(pr, in.valid_len, dv, dg, dbeta, st));
     return GDN_OK;
   }
   GDN_RUN(sc, "prep", launch_prep(pr, in, ws, true, true, st));

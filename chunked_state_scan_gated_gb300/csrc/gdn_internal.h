@@ -159,6 +159,10 @@ cudaError_t launch_chain_pair_tc(const Prob& pr, const Inputs& in, const WS& ws,
                                  const ChainPass& f, int rmode, const ReversePass& r,
                                  cudaStream_t st);
 // dq, dk (bf16) from the per-V-head bf16 gradients of q_hat, k_hat in ws.dqp / ws.dkp
+// Zeroes tokens [ceil(valid_len[b] / 64) * 64, T) of every row b of a token-major tensor
+// of row_bytes per token (row stride Ts tokens); nothing without valid_len.
+cudaError_t launch_pad_tail_zero(const Prob& pr, const int32_t* valid_len, void* dst,
+                                 int64_t row_bytes, cudaStream_t st);
 cudaError_t launch_qk_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, void* dq, void* dk,
                               cudaStream_t st);
 // chunk-parallel local gradients from chunk-start states and chunk-end state gradients

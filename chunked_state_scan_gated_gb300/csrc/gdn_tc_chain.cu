@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(PT, 2)
   const int64_t t0 = c * 64;
   const int64_t L = clamp_len(ar.valid_len, b, ar.T, ar.status, tid == 0 && c == 0 && h == 0);
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  if (t0 >= L) return;  // a chunk of padding only: every consumer skips it
 
   if (tid == 0) {
     mbar_init(bar_qk, 1);
@@ -423,8 +424,9 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
   const int seg = ar.seg_first + (int)(zi % ar.nseg);
   const int64_t hq = h / ar.r, bh = b * ar.H + h;
   const int64_t cs = (int64_t)seg * ar.CPS;
-  const int64_t ce = cs + ar.CPS < ar.NC ? cs + ar.CPS : ar.NC;
   const int64_t L = clamp_len(ar.valid_len, b, ar.T, ar.status, false);
+  // chunks of padding only (from ceil(L / 64) on) leave the state unchanged: not walked
+  const int64_t ce = min(cs + ar.CPS < ar.NC ? cs + ar.CPS : ar.NC, (L + 63) / 64);
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   uint32_t pend = 0;  // tid 0: barriers with a copy or MMA in flight (drained on an abort)
 
@@ -840,8 +842,9 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
   const int seg = ar.seg_first + (int)(zi % ar.nseg);
   const int64_t hq = h / ar.r, bh = b * ar.H + h;
   const int64_t cs = (int64_t)seg * ar.CPS;
-  const int64_t ce = cs + ar.CPS < ar.NC ? cs + ar.CPS : ar.NC;
   const int64_t L = clamp_len(ar.valid_len, b, ar.T, ar.status, false);
+  // chunks of padding only pass the state gradient through unchanged: not walked
+  const int64_t ce = min(cs + ar.CPS < ar.NC ? cs + ar.CPS : ar.NC, (L + 63) / 64);
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   uint32_t pend = 0;
 

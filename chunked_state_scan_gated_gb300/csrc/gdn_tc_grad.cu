@@ -324,13 +324,26 @@ __global__ void __launch_bounds__(GT, 1)
     dst[192 + t] = dexp_(dst[63], v);
   };
 
+  // The CTA's chunks, skipping those of padding only (from ceil(valid_len / 64) on: the
+  // chains and the prologue skip them too; their outputs are zeroed by a separate pass).
+  auto next_live = [&](int64_t w) {
+    for (; w < ar.NW; w += gridDim.x) {
+      if (!ar.valid_len) break;
+      const int64_t bb = w / (ar.NC * ar.H);
+      int64_t Lb = ar.valid_len[bb];
+      Lb = Lb < 0 ? 0 : (Lb > ar.T ? ar.T : Lb);
+      if ((w % ar.NC) * 64 < Lb) break;
+    }
+    return w;
+  };
+  const int64_t w0 = next_live(blockIdx.x);
   GateIn gnext{0.f, 0.f, false};  // warps 2, 3: inputs of the next chunk's gates
-  if (warp == 2 || warp == 3) {
-    const Item it0 = item_of(blockIdx.x);
+  if ((warp == 2 || warp == 3) && w0 < ar.NW) {
+    const Item it0 = item_of(w0);
     gates(gate_in(it0), it0.h, sGate);
   }
-  if (mover && blockIdx.x < ar.NW) {  // every tile of the first chunk
-    const Item it = item_of(blockIdx.x);
+  if (mover && w0 < ar.NW) {  // every tile of the first chunk
+    const Item it = item_of(w0);
     const Lay L = layout_of(0);
     ld_qk(it, L, 0);
     arm(0, GA, kBytesA);
@@ -345,14 +358,15 @@ __global__ void __launch_bounds__(GT, 1)
     ld_v(it, L, 0);
   }
 
-  for (int64_t w = blockIdx.x, k = 0; w < ar.NW; w += gridDim.x, ++k) {
+  for (int64_t w = w0, wn = 0, k = 0; w < ar.NW; w = wn, ++k) {
     const int lc = (int)(k & 1), ln = lc ^ 1;
     const uint32_t bpar = (uint32_t)((k >> 1) & 1);  // phase parity of this layout's barriers
     const Lay L = layout_of(lc);
     const Lay N = layout_of(ln);
     const Item it = item_of(w);
-    const bool more = w + gridDim.x < ar.NW;
-    const Item nx = item_of(more ? w + gridDim.x : w);
+    wn = next_live(w + gridDim.x);
+    const bool more = wn < ar.NW;
+    const Item nx = item_of(more ? wn : w);
     const int64_t h = it.h, b = it.b, t0 = it.t0;
     int64_t L_len = ar.T;
     if (ar.valid_len) {

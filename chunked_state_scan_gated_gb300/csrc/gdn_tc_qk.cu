@@ -28,6 +28,7 @@ struct QkArgs {
   const __nv_bfloat16* k;
   const __nv_bfloat16* dqp;
   const __nv_bfloat16* dkp;
+  const int32_t* valid_len;
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
 };
@@ -53,6 +54,15 @@ __global__ void __launch_bounds__(256) k_qk_grad_tc(QkArgs ar) {
   const int64_t hq = rowid % ar.Hqk, t = (rowid / ar.Hqk) % ar.T, b = rowid / (ar.Hqk * ar.T);
   const int64_t xo = ((b * ar.Ts + t) * ar.Hqk + hq) * 128 + sub * 8;
   const int64_t po0 = ((b * ar.Tp + t) * ar.H + hq * ar.r) * 128 + sub * 8;
+  if (ar.valid_len) {  // padded token: zero gradient (its chunk may not have been computed)
+    int64_t L = ar.valid_len[b];
+    L = L < 0 ? 0 : (L > ar.T ? ar.T : L);
+    if (t >= L) {
+      *reinterpret_cast<uint4*>(ar.dq + xo) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(ar.dk + xo) = make_uint4(0, 0, 0, 0);
+      return;
+    }
+  }
   float xq[8], xk[8], gq[8], gk[8];
   ld8bf(ar.q + xo, xq);
   ld8bf(ar.k + xo, xk);
@@ -109,7 +119,42 @@ __global__ void __launch_bounds__(256) k_qk_grad_tc(QkArgs ar) {
   *reinterpret_cast<uint4*>(ar.dk + xo) = vk;
 }
 
+// ============================================================================
+// k_pad_tail_zero: zero the tokens of every row from the end of its last chunk that
+// holds a valid token (ceil(valid_len / 64) * 64) to T, in a token-major tensor of
+// `row` bytes per token.  The tensor-core kernels skip chunks of padding only, so
+// their outputs there (o; dv, dg, dbeta) are written here instead.  grid (x, B).
+// ============================================================================
+template <typename U>
+__global__ void __launch_bounds__(256) k_pad_tail_zero(const int32_t* __restrict__ valid_len,
+                                                       int64_t T, int64_t Ts, int64_t row,
+                                                       uint8_t* __restrict__ dst) {
+  const int64_t b = blockIdx.y;
+  int64_t L = valid_len[b];
+  L = L < 0 ? 0 : (L > T ? T : L);
+  const int64_t start = (L + 63) / 64 * 64;
+  if (start >= T) return;
+  const int64_t per = row / (int64_t)sizeof(U);
+  const int64_t n = (T - start) * per;
+  U* base = reinterpret_cast<U*>(dst + (b * Ts + start) * row);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    base[i] = U{};
+}
+
 }  // namespace
+
+cudaError_t launch_pad_tail_zero(const Prob& pr, const int32_t* valid_len, void* dst,
+                                 int64_t row_bytes, cudaStream_t st) {
+  if (!valid_len || !dst || pr.B == 0 || pr.T == 0 || row_bytes <= 0) return cudaSuccess;
+  const dim3 grid(64, (unsigned)pr.B);
+  uint8_t* d = (uint8_t*)dst;
+  if (row_bytes % 16 == 0 && ((uintptr_t)dst & 15u) == 0)
+    k_pad_tail_zero<uint4><<<grid, 256, 0, st>>>(valid_len, pr.T, pr.Ts, row_bytes, d);
+  else
+    k_pad_tail_zero<uint32_t><<<grid, 256, 0, st>>>(valid_len, pr.T, pr.Ts, row_bytes, d);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_qk_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, void* dq, void* dk,
                               cudaStream_t st) {
@@ -120,6 +165,7 @@ cudaError_t launch_qk_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, vo
   ar.r = pr.r; ar.l2norm = pr.l2norm; ar.eps = pr.eps; ar.scale = pr.scale;
   ar.q = (const __nv_bfloat16*)in.q; ar.k = (const __nv_bfloat16*)in.k;
   ar.dqp = (const __nv_bfloat16*)ws.dqp; ar.dkp = (const __nv_bfloat16*)ws.dkp;
+  ar.valid_len = in.valid_len;
   ar.dq = (__nv_bfloat16*)dq; ar.dk = (__nv_bfloat16*)dk;
   k_qk_grad_tc<<<(unsigned)((rows + QK_ROWS - 1) / QK_ROWS), 256, 0, st>>>(ar);
   return cudaGetLastError();

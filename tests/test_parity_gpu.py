@@ -224,6 +224,45 @@ def test_bf16_head_groups_and_raw_qk(r, l2norm):
         assert (grads[0][bi, Lb:] == 0).all() and (grads[1][bi, Lb:] == 0).all()
 
 
+@pytest.mark.parametrize("segments", [0, 2, 3])
+def test_bf16_padding_only_chunks_are_skipped_and_zeroed(segments):
+    """Rows with chunks of padding only (valid_len 0, 70, 191 of T = 320: the tensor-core
+    kernels skip every chunk from ceil(valid_len / 64) on): every output and gradient
+    matches the oracle, and every padded token's output and gradient is exactly zero even
+    in output buffers that held NaN before the call (plain and training-step calls)."""
+    w = gi.Workload("bf16_pad_chunks", B=3, T=320, Hqk=1, H=2, dk=128, dv=128,
+                    dtype=torch.bfloat16, h0_std=0.1, with_dHT=True, valid_len=[0, 70, 191],
+                    decay_stress=True, seed=47)
+    inp = gi.make_inputs(w)
+    d = dev(inp)
+    n = np64(inp)
+    fin = (d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"])
+    nan = float("nan")
+    o = torch.full_like(d["v"], nan)
+    o, hT = gdn.gdn_fwd(*fin, d["h0"], d["valid_len"], segments=segments, o=o)
+    outs = dict(dq=torch.full_like(d["q"], nan), dk=torch.full_like(d["k"], nan),
+                dv=torch.full_like(d["v"], nan),
+                dg=torch.full((3, 320, 2), nan, device="cuda"),
+                dbeta=torch.full((3, 320, 2), nan, device="cuda"))
+    grads = gdn.gdn_bwd(*fin, d["dO"], d["dHT"], d["h0"], d["valid_len"], segments=segments,
+                        **outs)
+    o2, hT2, ctx = gdn.gdn_fwd_ctx(*fin, d["h0"], d["valid_len"], segments=segments,
+                                   o=torch.full_like(d["v"], nan))
+    grads2 = gdn.gdn_bwd_ctx(*fin, ctx, d["dO"], d["dHT"], d["valid_len"], segments=segments)
+    torch.cuda.synchronize()
+    ro, rhT = oracle_fwd(n)
+    rg = oracle_bwd(n)
+    for oo, hh, gg in ((o, hT, grads), (o2, hT2, grads2)):
+        assert_close("o", oo, ro, w.dtype)
+        assert_close("hT", hh, rhT, w.dtype)
+        for name, g, r in zip(NAMES_BWD, gg, rg):
+            assert_close(name, g, r, w.dtype)
+        for bi, Lb in enumerate(w.valid_len):
+            for x in (oo, *gg[:5]):
+                assert (x[bi, Lb:] == 0).all()
+        torch.testing.assert_close(hh[0], d["h0"][0], rtol=0, atol=0)  # an empty row
+
+
 def test_bf16_summary_matches_oracle():
     w = gi.Workload("bf16_summary", B=2, T=190, Hqk=1, H=2, dk=128, dv=128, dtype=torch.bfloat16,
                     decay_stress=True, valid_len=[190, 150], seed=18)
