@@ -212,9 +212,9 @@ E2E_COPY_STREAMS = 4  # side streams for the host-to-device copies of the end-to
 
 
 MEASURED_TRAFFIC = {
-    "bwd.grad_tc": {"T": 32768, "bytes_per_launch": 3059040512 + 837605376,
+    "bwd.grad_tc": {"T": 32768, "bytes_per_launch": 3058718720 + 836861184,
                     "src": "chunked_state_scan_gated_gb300/csrc/gdn_tc_grad.cu",
-                    "sha256": "b13ed0e10356fdc4ce63bd11e477c588c98259366530aef9b11e36386b898dbd"},
+                    "sha256": "c6bbeb858e79db59e9ca94f70f9e272918172c202416ec1eb7f1de6349430aa7"},
 }
 
 

@@ -10,8 +10,8 @@
 // leave the state unchanged and get zero output and gradients), and copies the valid
 // tokens of each output back into the packed row.  h0, h_T, dH_T and dH0 of sequence i
 // are row i of the batch, so they need no copy.  The copies are bandwidth-bound 16-byte
-// moves; the padded tail of a row costs the batched path's work on up to Lmax - L_i
-// masked tokens.
+// moves; the tensor-core path skips the chunks of a row's padded tail (only their
+// outputs are zeroed).
 #include <string.h>
 
 #include "gdn_internal.h"

@@ -410,7 +410,8 @@ gdn_status gdn_conv_silu_bwd(const gdn_conv_problem* p, const void* x, const flo
  *    gdn_bwd; h0, hT, dHT, dH0 [n_seqs,H,dk,dv] fp32 (nullable as in gdn_fwd / gdn_bwd).
  *  - Work: the sequences are copied into a padded batch [n_seqs, Lmax] (Lmax = the
  *    longest sequence) inside the workspace, run by the batched path with valid_len = the
- *    lengths, and the outputs copied back; the padded tails cost masked-token work.
+ *    lengths, and the outputs copied back; on the bf16 path the chunks of the padded
+ *    tails are skipped (their outputs zeroed), on the fp32 path they cost masked work.
  *  - Workspace: gdn_varlen_workspace_size (op GDN_OP_FWD or GDN_OP_BWD), 256-byte aligned.
  * Errors: as gdn_fwd / gdn_bwd; offsets that are not non-decreasing from 0 to T, B != 1
  * or n_seqs < 0: GDN_ERR_INVALID_ARG.  n_seqs = 0 (T = 0) does nothing.
