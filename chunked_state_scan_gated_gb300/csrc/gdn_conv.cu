@@ -14,12 +14,16 @@
 // halo rows from the halo, rows outside the row's tokens zero-filled), then computes from
 // there: a thread owns 4 adjacent channels and walks a run of the tile's tokens with the
 // last K - 1 inputs (and, backward, the last K - 1 ds) in registers, storing each output
-// straight to global memory.  The backward recomputes a and ds of the K - 1 tokens after
-// each run to form their dx.  dw and dbias: per-CTA partials (the CTA's 8 runs summed in
-// a fixed order) in the workspace, then one pass that sums the partials of every tile in
-// a fixed order (fp64).
+// straight to global memory.  The backward's walk is unrolled over its run, with the
+// bounds checks compiled out for the tiles that need none, and does its arithmetic on
+// channel pairs with packed f32x2 operations; it recomputes a and ds of the K - 1 tokens
+// after each run to form their dx.  dw and dbias: per-CTA partials (the
+// CTA's 8 runs summed in a fixed order) in the workspace, then one pass that sums the
+// partials of every tile in a fixed order (fp64).
 #include <cuda_bf16.h>
 #include <string.h>
+
+#include <type_traits>
 
 #include "gdn.h"
 #include "gdn_vec.cuh"
@@ -50,6 +54,38 @@ __device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
 }
 __device__ __forceinline__ void cp_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+
+// Two fp32 lanes at once (sm_100+ packed f32x2 arithmetic; each lane rounds as the scalar
+// operation does).
+__device__ __forceinline__ uint64_t f2bits(float2 a) { return *reinterpret_cast<uint64_t*>(&a); }
+__device__ __forceinline__ float2 bits2f(uint64_t d) { return *reinterpret_cast<float2*>(&d); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2bits(a)), "l"(f2bits(b)), "l"(f2bits(c)));
+  return bits2f(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2bits(a)), "l"(f2bits(b)));
+  return bits2f(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2bits(a)), "l"(f2bits(b)));
+  return bits2f(d);
+}
+__device__ __forceinline__ void ld4p(const __nv_bfloat16* p, float2 (&v)[2]) {
+  float x[4];
+  ld4(p, x);
+  v[0] = make_float2(x[0], x[1]);
+  v[1] = make_float2(x[2], x[3]);
+}
+__device__ __forceinline__ void ld4p(const float* p, float2 (&v)[2]) {
+  const float4 f = *reinterpret_cast<const float4*>(p);
+  v[0] = make_float2(f.x, f.y);
+  v[1] = make_float2(f.z, f.w);
 }
 
 struct ConvArgs {
@@ -151,85 +187,96 @@ __global__ void __launch_bounds__(CONV_NT) k_conv_bwd(ConvArgs ar) {
   __syncthreads();
   const int u0 = run * RUN;
   const bool live = c < ar.C && t0 + u0 < ar.T;
-  float acc[4][K + 1];  // dw taps, then dbias
+  float2 acc[2][K + 1];  // channel pairs (0, 1), (2, 3): dw taps, then dbias
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int p = 0; p < 2; ++p)
 #pragma unroll
-    for (int i = 0; i <= K; ++i) acc[j][i] = 0.f;
+    for (int i = 0; i <= K; ++i) acc[p][i] = make_float2(0.f, 0.f);
   if (live) {
     const int uend = (int)(t0 + u0 + RUN < ar.T ? u0 + RUN : ar.T - t0);  // own tokens
     // tokens at or past ulast have no ds (clamped before the cast: T - t0 may exceed int)
     const int64_t rest = ar.T - t0, span = TOK + 2 * (K - 1);
     const int ulast = (int)(rest < span ? rest : span);
-    float w[4][K], bs[4];
+    float2 w[2][K], bs[2];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int p = 0; p < 2; ++p) {
 #pragma unroll
-      for (int i = 0; i < K; ++i) w[j][i] = ar.w[(c + j) * K + i];
-      bs[j] = ar.bias ? ar.bias[c + j] : 0.f;
+      for (int i = 0; i < K; ++i)
+        w[p][i] = make_float2(ar.w[(c + 2 * p) * K + i], ar.w[(c + 2 * p + 1) * K + i]);
+      bs[p] = ar.bias ? make_float2(ar.bias[c + 2 * p], ar.bias[c + 2 * p + 1])
+                      : make_float2(0.f, 0.f);
     }
     const T* xs = reinterpret_cast<const T*>(xsb) + lane * 4;
     const T* dys = reinterpret_cast<const T*>(dysb) + lane * 4;
-    float xw[K][4];   // x~[u-K+1 .. u]
-    float dsw[K][4];  // dsw[0 .. K-2]: ds[u-K+1 .. u-1]; dsw[K-1]: ds[u]
+    // rings over the window: at step k (token u = u0 + k) slot (k + i) % K holds x~[u-K+1+i]
+    // and ds[u-K+1+i] (i = 0 .. K-1); the loop is unrolled, so the slots are fixed registers
+    float2 xw[K][2];
+    float2 dsw[K][2];
 #pragma unroll
     for (int i = 0; i < K - 1; ++i) {
-      ld4(xs + (u0 + i) * CONV_CH, xw[i]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) dsw[i][j] = 0.f;  // ds before the run feeds no dx it emits
+      ld4p(xs + (u0 + i) * CONV_CH, xw[i]);
+      dsw[i][0] = dsw[i][1] = make_float2(0.f, 0.f);  // ds before the run feeds no dx it emits
     }
     T* dx = reinterpret_cast<T*>(ar.y) + (b * ar.Ts + t0) * ar.C + c;
     T* dh = reinterpret_cast<T*>(ar.dhalo);
     const int e_first = t0 + u0 == 0 ? -(K - 1) : u0;  // the row's first run also emits dhalo
-#pragma unroll 4
-    for (int u = u0; u < uend + K - 1; ++u) {
-      if (u < ulast) {
-        ld4(xs + (u + K - 1) * CONV_CH, xw[K - 1]);
-        float g[4];
-        ld4(dys + u * CONV_CH, g);
+    // FULL: the run and the K-1 tokens after it lie inside the row, so no step needs a
+    // bounds check (every tile but a row's last)
+    auto walk = [&](auto full_tag) {
+      constexpr bool FULL = decltype(full_tag)::value;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float a = bs[j];
+      for (int k = 0; k < RUN + K - 1; ++k) {
+        const int u = u0 + k;
+        if (!FULL && u >= uend + K - 1) break;
+        if (FULL || u < ulast) {
+          ld4p(xs + (u + K - 1) * CONV_CH, xw[(k + K - 1) % K]);
+          float2 g[2];
+          ld4p(dys + u * CONV_CH, g);
 #pragma unroll
-          for (int i = 0; i < K; ++i) a = fmaf(w[j][i], xw[i][j], a);
-          const float s = sigm(a);
-          dsw[K - 1][j] = g[j] * s * (1.f + a * (1.f - s));
+          for (int p = 0; p < 2; ++p) {
+            float2 a = bs[p];
+#pragma unroll
+            for (int i = 0; i < K; ++i) a = fma2(w[p][i], xw[(k + i) % K][p], a);
+            const float2 s = make_float2(sigm(a.x), sigm(a.y));
+            const float2 one = make_float2(1.f, 1.f);
+            const float2 t = fma2(a, add2(one, make_float2(-s.x, -s.y)), one);  // 1 + a (1 - s)
+            dsw[(k + K - 1) % K][p] = mul2(mul2(g[p], s), t);
+          }
+        } else {
+          dsw[(k + K - 1) % K][0] = dsw[(k + K - 1) % K][1] = make_float2(0.f, 0.f);
         }
-      } else {
+        if (FULL ? (k < RUN) : (u < uend)) {  // own token: dw, dbias
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dsw[K - 1][j] = 0.f;
+          for (int p = 0; p < 2; ++p) {
+#pragma unroll
+            for (int i = 0; i < K; ++i)
+              acc[p][i] = fma2(dsw[(k + K - 1) % K][p], xw[(k + i) % K][p], acc[p][i]);
+            acc[p][K] = add2(acc[p][K], dsw[(k + K - 1) % K][p]);
+          }
+        }
+        const int e = u - (K - 1);  // dx~[e] = sum_i w[i] ds[u - i]
+        const bool emit = FULL ? (k >= K - 1 || e >= e_first) : (e >= e_first && e < uend);
+        if (emit) {
+          float o[4];
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            float2 v = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < K; ++i) v = fma2(w[p][i], dsw[(k + K - 1 - i) % K][p], v);
+            o[2 * p] = v.x;
+            o[2 * p + 1] = v.y;
+          }
+          if (e >= 0)
+            st4(dx + (int64_t)e * ar.C, o);
+          else if (dh)
+            st4(dh + (b * (K - 1) + (K - 1) + e) * ar.C + c, o);
+        }
       }
-      if (u < uend) {  // own token: dw, dbias
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int i = 0; i < K; ++i) acc[j][i] = fmaf(dsw[K - 1][j], xw[i][j], acc[j][i]);
-          acc[j][K] += dsw[K - 1][j];
-        }
-      }
-      const int e = u - (K - 1);  // dx~[e] = sum_i w[i] ds[u - i]
-      if (e >= e_first && e < uend) {
-        float o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float v = 0.f;
-#pragma unroll
-          for (int i = 0; i < K; ++i) v = fmaf(w[j][i], dsw[K - 1 - i][j], v);
-          o[j] = v;
-        }
-        if (e >= 0)
-          st4(dx + (int64_t)e * ar.C, o);
-        else if (dh)
-          st4(dh + (b * (K - 1) + (K - 1) + e) * ar.C + c, o);
-      }
-#pragma unroll
-      for (int i = 0; i < K - 1; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          xw[i][j] = xw[i + 1][j];
-          dsw[i][j] = dsw[i + 1][j];
-        }
-    }
+    };
+    if (t0 + u0 + RUN + 2 * (K - 1) <= ar.T && uend == u0 + RUN)
+      walk(std::true_type{});
+    else
+      walk(std::false_type{});
   }
   // this CTA's partial sums (in the staged-x space, no longer read): its 8 runs added in
   // order by the threads of run 0
@@ -238,7 +285,8 @@ __global__ void __launch_bounds__(CONV_NT) k_conv_bwd(ConvArgs ar) {
 #pragma unroll
   for (int j = 0; j < 4; ++j)
 #pragma unroll
-    for (int i = 0; i <= K; ++i) red[(run * CONV_CH + lane * 4 + j) * (K + 1) + i] = acc[j][i];
+    for (int i = 0; i <= K; ++i)
+      red[(run * CONV_CH + lane * 4 + j) * (K + 1) + i] = (j & 1) ? acc[j >> 1][i].y : acc[j >> 1][i].x;
   __syncthreads();
   if (run == 0 && c < ar.C) {
     float* dst = ar.part + ((b * ar.tiles + blockIdx.x) * ar.C + c) * (K + 1);
