@@ -154,21 +154,23 @@ __global__ void __launch_bounds__(PT, 2)
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   if (t0 >= L) return;  // a chunk of padding only: every consumer skips it
 
-  if (tid == 0) {
+  // Gate inputs (warps 2, 3: token tid - 64), read before anything else: with the q, k, v
+  // copies they are the longest wait of the CTA's start.
+  const int tg = tid - 64;
+  const bool gate_warp = warp == 2 || warp == 3;
+  float xa = 0.f, xb = 0.f;
+  const bool glive = gate_warp && t0 + tg < L;
+  if (glive) {
+    const int64_t gi = (b * ar.Ts + t0 + tg) * ar.H + h;
+    xa = __bfloat162float(ar.a[gi]) + ar.dt_bias[h];
+    xb = __bfloat162float(ar.b[gi]);
+  }
+  if (tid == 0) {  // the barriers are this thread's own: the copies go out at once
     mbar_init(bar_qk, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
     fence_barrier_init();
     *s_abort = 0;
-  }
-  if (warp == 0) tmem_alloc(s_tmem, 256);
-  for (int e = tid; e < 1024; e += PT)  // [T_u; T_w]: the solve writes only the lower triangle
-    reinterpret_cast<uint4*>(sm + P_TA)[e] = make_uint4(0, 0, 0, 0);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *s_tmem;
-  if (tid == 0) {
     mbar_arrive_expect_tx(bar_qk, 32768u);
     for (int at = 0; at < 2; ++at) {
       tma_load_4d(sm + P_QK + at * 16384, &mq, at * 64, (int)hq, (int)t0, (int)b, bar_qk);
@@ -178,41 +180,54 @@ __global__ void __launch_bounds__(PT, 2)
     for (int at = 0; at < 2; ++at)
       tma_load_4d(sm + P_V + at * 8192, &mv, at * 64, (int)h, (int)t0, (int)b, bar_v);
   }
-  if (tid < 64) {
-    const int64_t t = t0 + tid;
-    float g = 0.f, be = 0.f;
-    if (t < L) {
-      const int64_t gi = (b * ar.Ts + t) * ar.H + h;
-      const float x = __bfloat162float(ar.a[gi]) + ar.dt_bias[h];
-      const float sp = x > 20.f ? x : log1pf(expf(x));
-      g = -expf(ar.A_log[h]) * sp;
-      be = 1.f / (1.f + expf(-__bfloat162float(ar.b[gi])));
+  if (warp == 0) tmem_alloc(s_tmem, 256);
+  for (int e = tid; e < 1024; e += PT)  // [T_u; T_w]: the solve writes only the lower triangle
+    reinterpret_cast<uint4*>(sm + P_TA)[e] = make_uint4(0, 0, 0, 0);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  // ---- [Q; K] [Q; K]^T -> cols [0, 128): row norms on the diagonal, Q K^T and K K^T in cols
+  //      64..127, issued as soon as q and k land; the gates are formed meanwhile
+  if (tid == 0) {
+    if (!mbar_wait(bar_qk, 0, ar.status, kStatusTimeout)) {
+      *s_abort = 1;
+    } else {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16(128, 128, 0, 0);
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t at = ks >> 2, kk = ks & 3;
+        const uint64_t d = (d16 + ((P_QK + at * 16384 + kk * 32) >> 4));
+        mma_bf16(tmem, d, d, id, ks > 0);
+      }
+      mma_commit(bar_mma);
     }
-    sG[tid] = g * kLog2e;
-    sBeta[tid] = be;
   }
-  __syncthreads();
-  cumsum64f(sG);
-  __syncthreads();
-  if (tid < 64) {
-    sGam[tid] = exp2f(sG[tid]);
-    ar.gl[(bh * ar.NC + c) * 64 + tid] = sG[tid];
+  if (gate_warp) {  // g, beta and the cumulative gate in log2 units (scan over 64 tokens)
+    float g = 0.f, be = 0.f;
+    if (glive) {
+      const float sp = xa > 20.f ? xa : log1pf(expf(xa));
+      g = -expf(ar.A_log[h]) * sp;
+      be = 1.f / (1.f + expf(-xb));
+    }
+    float v = g * kLog2e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (tg == 31) sY[0] = v;  // the first half's total (the solve's scratch is free until then)
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    if (tg >= 32) v += sY[0];
+    sG[tg] = v;
+    sBeta[tg] = be;
+    sGam[tg] = exp2f(v);
+    ar.gl[(bh * ar.NC + c) * 64 + tg] = v;
   }
-  if (!mbar_wait(bar_qk, 0, ar.status, kStatusTimeout)) *s_abort = 1;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (*s_abort) goto done;
-  // ---- [Q; K] [Q; K]^T -> cols [0, 128): row norms on the diagonal, Q K^T and K K^T in cols 64..127
-  if (tid == 0) {
-    const uint32_t id = idesc_bf16(128, 128, 0, 0);
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t at = ks >> 2, kk = ks & 3;
-      const uint64_t d = (d16 + ((P_QK + at * 16384 + kk * 32) >> 4));
-      mma_bf16(tmem, d, d, id, ks > 0);
-    }
-    mma_commit(bar_mma);
-  }
   if (!mbar_wait(bar_mma, 0, ar.status, kStatusTimeout)) *s_abort = 1;
   tc_fence_after();
   if (half == 0) {  // diagonal element (row, row) sits in column group `quad`, element `lane`

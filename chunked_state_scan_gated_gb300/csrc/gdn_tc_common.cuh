@@ -427,32 +427,41 @@ struct NoEmit {
 };
 
 // T = (I + A)^-1 for strictly lower A (64 x 64, fp32, leading dim lda).  The
-// 16 x 16 diagonal blocks come from forward substitution on CUDA cores; the
-// blocks below them, block diagonal by block diagonal, from
-// T_ij = -T_ii (sum_{j <= m < i} A_im T_mj) with warp-level tf32 MMAs (one warp
-// per 16 x 8 half block).  Y needs 8 warps x 128 floats.  Needs blockDim.x >= 256.
+// 16 x 16 diagonal blocks come from forward substitution on CUDA cores (four lanes per
+// column of T, every thread of the CTA); the blocks below them, block diagonal by block
+// diagonal, from T_ij = -T_ii (sum_{j <= m < i} A_im T_mj) with warp-level tf32 MMAs (one
+// warp per 16 x 8 half block).  Y needs 8 warps x 128 floats.  Needs blockDim.x == 256.
 // Every entry on or below the diagonal is also handed to emit.one(i, j, t) or, for
 // the column pair j, j + 1 (j even), emit.two(i, j, t_j, t_j+1) once it is final.
 template <typename Emit = NoEmit>
 __device__ __forceinline__ void solve_unit_lower64_mma(const float* A, float* T, float* Y,
                                                        const int lda, const Emit& emit = Emit()) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (warp < 4 && lane < 16) {
-    // column j of the block, by columns of A: once x[l] is final it is removed from every
-    // later row, so the dependent chain is 15 FMAs long and the loads of A do not wait
-    const int b0 = warp * 16, j = lane;
-    float x[16];
+  {
+    // column j of diagonal block b0 / 16, by columns of A: once x_l is final it is removed
+    // from every later row.  Lane q of the column's four owns rows q, q + 4, q + 8, q + 12
+    // and hands x_l to the other three when it owns row l, so each lane does a quarter of
+    // the updates and the dependent chain is 15 shuffle + FMA steps.
+    const int col = tid >> 2, q = tid & 3;
+    const int b0 = (col >> 4) * 16, j = col & 15;
+    float x[4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
+    for (int sl = 0; sl < 4; ++sl) x[sl] = (q + 4 * sl == j) ? 1.f : 0.f;
 #pragma unroll
     for (int l = 0; l < 15; ++l) {
+      const float xl = __shfl_sync(0xffffffffu, x[l >> 2], l & 3, 4);
 #pragma unroll
-      for (int i = l + 1; i < 16; ++i) x[i] = fmaf(-A[(b0 + i) * lda + b0 + l], x[l], x[i]);
+      for (int sl = 0; sl < 4; ++sl) {
+        const int r = q + 4 * sl;
+        const float y = fmaf(-A[(b0 + r) * lda + b0 + l], xl, x[sl]);
+        x[sl] = r > l ? y : x[sl];
+      }
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      T[(b0 + i) * lda + b0 + j] = x[i];  // zero above the diagonal (x[i] = 0 for i < j)
-      if (i >= j) emit.one(b0 + i, b0 + j, x[i]);
+    for (int sl = 0; sl < 4; ++sl) {
+      const int r = q + 4 * sl;
+      T[(b0 + r) * lda + b0 + j] = x[sl];  // zero above the diagonal (x = 0 for r < j)
+      if (r >= j) emit.one(b0 + r, b0 + j, x[sl]);
     }
   }
   __syncthreads();
