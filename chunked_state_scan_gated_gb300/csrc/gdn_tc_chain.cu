@@ -155,15 +155,16 @@ __global__ void __launch_bounds__(PT, 2)
   if (t0 >= L) return;  // a chunk of padding only: every consumer skips it
 
   // Gate inputs (warps 2, 3: token tid - 64), read before anything else: with the q, k, v
-  // copies they are the longest wait of the CTA's start.
+  // copies they are the longest wait of the CTA's start.  Only loaded here: their first
+  // use, after the set-up barrier, is where the threads wait for them.
   const int tg = tid - 64;
   const bool gate_warp = warp == 2 || warp == 3;
-  float xa = 0.f, xb = 0.f;
+  __nv_bfloat16 ra = __float2bfloat16_rn(0.f), rb = ra;
   const bool glive = gate_warp && t0 + tg < L;
   if (glive) {
     const int64_t gi = (b * ar.Ts + t0 + tg) * ar.H + h;
-    xa = __bfloat162float(ar.a[gi]) + ar.dt_bias[h];
-    xb = __bfloat162float(ar.b[gi]);
+    ra = ar.a[gi];
+    rb = ar.b[gi];
   }
   if (tid == 0) {  // the barriers are this thread's own: the copies go out at once
     mbar_init(bar_qk, 1);
@@ -206,9 +207,10 @@ __global__ void __launch_bounds__(PT, 2)
   if (gate_warp) {  // g, beta and the cumulative gate in log2 units (scan over 64 tokens)
     float g = 0.f, be = 0.f;
     if (glive) {
+      const float xa = __bfloat162float(ra) + ar.dt_bias[h];
       const float sp = xa > 20.f ? xa : log1pf(expf(xa));
       g = -expf(ar.A_log[h]) * sp;
-      be = 1.f / (1.f + expf(-xb));
+      be = 1.f / (1.f + expf(-__bfloat162float(rb)));
     }
     float v = g * kLog2e;
 #pragma unroll
@@ -318,10 +320,10 @@ __global__ void __launch_bounds__(PT, 2)
   }
   if (!mbar_wait(bar_mma, 1, ar.status, kStatusTimeout)) *s_abort = 1;
   tc_fence_after();
-  {
+  {  // W and U images staged where q and k were (both products are done), then bulk-stored
     const bool isw = row >= 64;
     const int i = row & 63;
-    uint8_t* dst = (isw ? ar.wim : ar.uim) + (bh * ar.NC + c) * (int64_t)kImg;
+    uint8_t* dst = sm + P_QK + (isw ? 0 : kImg);
     const uint32_t src = tmem + lane_off + (isw ? 128 : 0) + 64 * half;
 #pragma unroll
     for (int q2 = 0; q2 < 2; ++q2) {
@@ -331,6 +333,14 @@ __global__ void __launch_bounds__(PT, 2)
       for (int cc = 0; cc < 4; ++cc)
         *reinterpret_cast<uint4*>(dst + img_chunk(i, half * 8 + q2 * 4 + cc)) = pack8(&v[cc * 8]);
     }
+  }
+  fence_proxy_async();
+  __syncthreads();
+  if (tid == 0) {
+    bulk_store(ar.wim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_QK, kImg);
+    bulk_store(ar.uim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_QK + kImg, kImg);
+    bulk_commit();
+    bulk_wait_read();  // shared memory is released when the CTA exits
   }
 done:
   if (*s_abort && tid == 0) {  // let the loads still in flight land before the CTA exits
