@@ -77,6 +77,7 @@ __device__ __forceinline__ int64_t clamp_len(const int32_t* valid_len, int64_t b
 // ============================================================================
 constexpr int PT = 256;
 constexpr uint32_t P_QK = 0;                   // atoms a at a*16384: [Q_a | K_a], raw, 8 KB each
+constexpr uint32_t P_PST = P_QK + 16384;       // P image staging (Q_1: free after [Q;K][Q;K]^T)
 constexpr uint32_t P_V = 32768;                // V atoms at a*8192
 constexpr uint32_t P_TA = 49152;               // [T_u; T_w], 128 x 64 K-major
 constexpr uint32_t P_A = 65536;                // fp32 A [64][LDA]
@@ -266,8 +267,8 @@ __global__ void __launch_bounds__(PT, 2)
         }
       }
     }
-    if (row < 64) {  // P = tril(Q K^T o Gamma) with the norm factors: bf16 image
-      uint8_t* dst = ar.pim + (bh * ar.NC + c) * (int64_t)kImgP;
+    if (row < 64) {  // P = tril(Q K^T o Gamma) with the norm factors: bf16 image, staged
+      uint8_t* dst = sm + P_PST;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         float p[8];
@@ -284,13 +285,19 @@ __global__ void __launch_bounds__(PT, 2)
       }
     }
   }
+  fence_proxy_async();
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) {  // the P image (group 1 of this thread's bulk stores)
+    bulk_store(ar.pim + (bh * ar.NC + c) * (int64_t)kImgP, sm + P_PST, kImgP);
+    bulk_commit();
+  }
   // T = (I + A)^-1, with [T_u; T_w] = [T diag(beta); T diag(beta gamma rk)] (bf16, W is
   // formed from raw k) written as each entry of T is final
   solve_unit_lower64_mma(sA, sT, sY, LDA, TaEmit{sm + P_TA, sBeta, sCw});
-  if (ar.tim) {  // T for the backward, bf16 image
-    uint8_t* dst = ar.tim + (bh * ar.NC + c) * (int64_t)kImgP;
+  if (ar.tim) {  // T for the backward, bf16 image, staged where A was (the solve is done)
+    __syncthreads();
+    uint8_t* dst = sm + P_A;
     for (int e = tid; e < 512; e += PT) {
       const int i = e >> 3, cc = e & 7;
       float x[8];
@@ -308,8 +315,15 @@ __global__ void __launch_bounds__(PT, 2)
   __syncthreads();
   tc_fence_after();
   if (*s_abort) goto done;
+  if (tid == 0 && ar.tim) {  // the T image (group 2)
+    bulk_store(ar.tim + (bh * ar.NC + c) * (int64_t)kImgP, sm + P_A, kImgP);
+    bulk_commit();
+  }
   // ---- [T_u; T_w] V -> cols [0,128) (U in rows 0..63); [T_u; T_w] K -> cols [128,256) (W in 64..127)
   if (tid == 0) {
+    // the P image's staging (under the U image's) has been read before the product
+    // completes, and so before any thread stages W and U
+    if (ar.tim) bulk_wait_read_but1(); else bulk_wait_read();
     const uint32_t id = idesc_bf16(128, 128, 0, 1);
     for (int ks = 0; ks < 4; ++ks) {
       const uint64_t a = (d16 + ((P_TA + ks * 32) >> 4));
@@ -346,6 +360,7 @@ done:
   if (*s_abort && tid == 0) {  // let the loads still in flight land before the CTA exits
     mbar_wait(bar_qk, 0, nullptr, 0);
     mbar_wait(bar_v, 0, nullptr, 0);
+    bulk_wait_read();  // and the stores issued so far read their staging
   }
   tc_fence_before();
   __syncthreads();
