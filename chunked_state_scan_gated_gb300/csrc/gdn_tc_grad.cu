@@ -227,12 +227,15 @@ __global__ void __launch_bounds__(GT, 1)
   struct Item {
     int64_t c, h, b, hq, im, t0;
   };
+  // chunk w: 32-bit index arithmetic (the host keeps NW below 2^31; 64-bit division costs
+  // ~80 instructions, and every thread runs this twice per chunk)
   auto item_of = [&](int64_t w) {
     Item it;
-    it.c = w % ar.NC;
-    it.h = (w / ar.NC) % ar.H;
-    it.b = w / (ar.NC * ar.H);
-    it.hq = it.h / ar.r;
+    const uint32_t uw = (uint32_t)w, q1 = uw / (uint32_t)ar.NC, hh = q1 % (uint32_t)ar.H;
+    it.c = uw - q1 * (uint32_t)ar.NC;
+    it.h = hh;
+    it.b = q1 / (uint32_t)ar.H;
+    it.hq = hh / (uint32_t)ar.r;
     it.im = (it.b * ar.H + it.h) * ar.NC + it.c;
     it.t0 = it.c * 64;
     return it;
@@ -329,10 +332,10 @@ __global__ void __launch_bounds__(GT, 1)
   auto next_live = [&](int64_t w) {
     for (; w < ar.NW; w += gridDim.x) {
       if (!ar.valid_len) break;
-      const int64_t bb = w / (ar.NC * ar.H);
-      int64_t Lb = ar.valid_len[bb];
+      const uint32_t uw = (uint32_t)w, q1 = uw / (uint32_t)ar.NC;
+      int64_t Lb = ar.valid_len[q1 / (uint32_t)ar.H];
       Lb = Lb < 0 ? 0 : (Lb > ar.T ? ar.T : Lb);
-      if ((w % ar.NC) * 64 < Lb) break;
+      if ((int64_t)(uw - q1 * (uint32_t)ar.NC) * 64 < Lb) break;
     }
     return w;
   };
@@ -817,6 +820,7 @@ cudaError_t launch_grad2_tc(const Prob& pr, const Inputs& in, const WS& ws, cons
   Grad2Args ar;
   ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.r = pr.r; ar.NC = pr.NC; ar.Tp = pr.Tp;
   ar.NW = pr.B * pr.H * pr.NC;
+  if (ar.NW + 1024 >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // 32-bit chunk indices
   ar.l2norm = pr.l2norm; ar.eps = pr.eps; ar.scale = pr.scale;
   ar.a = (const __nv_bfloat16*)in.a; ar.b = (const __nv_bfloat16*)in.b;
   ar.A_log = in.A_log; ar.dt_bias = in.dt_bias; ar.valid_len = in.valid_len;
