@@ -48,10 +48,12 @@ constexpr int QK_ROWS = 16;  // rows per 256-thread block
 
 __global__ void __launch_bounds__(256) k_qk_grad_tc(QkArgs ar) {
   const int sub = threadIdx.x & 15;
-  const int64_t rowid = (int64_t)blockIdx.x * QK_ROWS + (threadIdx.x >> 4);
-  if (rowid >= ar.B * ar.T * ar.Hqk) return;  // whole 16-lane groups leave together
+  const uint32_t rowid = blockIdx.x * QK_ROWS + (threadIdx.x >> 4);  // below 2^31 (host)
+  if (rowid >= (uint32_t)(ar.B * ar.T * ar.Hqk)) return;  // whole 16-lane groups leave together
   const unsigned gmask = 0xffffu << (threadIdx.x & 16);
-  const int64_t hq = rowid % ar.Hqk, t = (rowid / ar.Hqk) % ar.T, b = rowid / (ar.Hqk * ar.T);
+  const uint32_t q1 = rowid / (uint32_t)ar.Hqk;
+  const int64_t hq = rowid - q1 * (uint32_t)ar.Hqk, t = q1 % (uint32_t)ar.T,
+                b = q1 / (uint32_t)ar.T;
   const int64_t xo = ((b * ar.Ts + t) * ar.Hqk + hq) * 128 + sub * 8;
   const int64_t po0 = ((b * ar.Tp + t) * ar.H + hq * ar.r) * 128 + sub * 8;
   if (ar.valid_len) {  // padded token: zero gradient (its chunk may not have been computed)
@@ -160,6 +162,7 @@ cudaError_t launch_qk_grad_tc(const Prob& pr, const Inputs& in, const WS& ws, vo
                               cudaStream_t st) {
   const int64_t rows = pr.B * pr.T * pr.Hqk;
   if (rows == 0) return cudaSuccess;
+  if (rows >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // 32-bit row indices
   QkArgs ar;
   ar.B = pr.B; ar.T = pr.T; ar.Ts = pr.Ts; ar.Tp = pr.Tp; ar.Hqk = pr.Hqk; ar.H = pr.H;
   ar.r = pr.r; ar.l2norm = pr.l2norm; ar.eps = pr.eps; ar.scale = pr.scale;

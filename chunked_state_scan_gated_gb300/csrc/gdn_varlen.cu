@@ -57,6 +57,10 @@ gdn_status shape_of(const gdn_problem* p, const int32_t* cu_host, int32_t n_seqs
     if (L < 0) return GDN_ERR_INVALID_ARG;
     if (L > Lmax) Lmax = L;
   }
+  // the copies index a sequence's bytes in 32 bits and take one grid row per sequence
+  const int64_t esz = p->dtype == GDN_BF16 ? 2 : 4;
+  const int64_t widest = (p->H * p->dv > p->Hqk * p->dk ? p->H * p->dv : p->Hqk * p->dk) * esz;
+  if (n_seqs > 65535 || Lmax * widest >= ((int64_t)1 << 31)) return GDN_ERR_UNSUPPORTED;
   s->inner = *p;
   s->inner.B = n_seqs;
   s->inner.T = Lmax;
@@ -131,25 +135,28 @@ __global__ void k_varlen_lengths(const int32_t* __restrict__ cu, int64_t N, int6
 // Moves `unit`-byte pieces of token rows of `row` bytes between the packed row and the
 // padded batch.  Pack = false: padded[n][t] = packed[cu[n] + t] for t < len[n], zero after
 // (gather).  Pack = true: packed[cu[n] + t] = padded[n][t] for t < len[n] (scatter).
+// grid (x, N): blockIdx.y is the sequence; the x blocks stride over its Lmax * per pieces
+// (below 2^31: checked on the host) with 32-bit index arithmetic.
 template <typename U, bool Pack>
 __global__ void __launch_bounds__(256) k_varlen_move(const int32_t* __restrict__ cu,
                                                      const int32_t* __restrict__ vlen, int64_t N,
                                                      int64_t Lmax, int64_t row,
                                                      const uint8_t* __restrict__ src,
                                                      uint8_t* __restrict__ dst) {
-  const int64_t per = row / (int64_t)sizeof(U);  // pieces per token row
-  const int64_t total = N * Lmax * per;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t pc = i % per, tok = i / per, t = tok % Lmax, n = tok / Lmax;
-    const bool valid = t < vlen[n];
-    const int64_t packed = ((int64_t)cu[n] + t) * per + pc;  // read only when valid
+  const uint32_t per = (uint32_t)(row / (int64_t)sizeof(U));  // pieces per token row
+  const int64_t n = blockIdx.y;
+  const uint32_t span = (uint32_t)Lmax * per;
+  const uint32_t lim = (uint32_t)vlen[n] * per;  // pieces of the valid tokens (vlen <= Lmax)
+  const int64_t row0 = n * (int64_t)span;  // first piece of the sequence in the padded batch
+  const int64_t pk0 = (int64_t)cu[n] * per;  // ... and in the packed row (read when valid)
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < span; i += gridDim.x * blockDim.x) {
+    const bool valid = i < lim;
     if (Pack) {
-      if (valid) reinterpret_cast<U*>(dst)[packed] = reinterpret_cast<const U*>(src)[i];
+      if (valid) reinterpret_cast<U*>(dst)[pk0 + i] = reinterpret_cast<const U*>(src)[row0 + i];
     } else {
       U v{};
-      if (valid) v = reinterpret_cast<const U*>(src)[packed];
-      reinterpret_cast<U*>(dst)[i] = v;
+      if (valid) v = reinterpret_cast<const U*>(src)[pk0 + i];
+      reinterpret_cast<U*>(dst)[row0 + i] = v;
     }
   }
 }
@@ -159,10 +166,12 @@ cudaError_t move(const int32_t* cu, const int32_t* vlen, const Shape& s, int64_t
                  const void* src, void* dst, cudaStream_t st) {
   const int64_t bytes = s.N * s.Lmax * row;
   if (bytes == 0) return cudaSuccess;
-  const int64_t maxg = 152 * 8;
-  auto grid = [&](int64_t pieces) {
-    const int64_t g = (pieces + 255) / 256;
-    return (unsigned)(g < maxg ? g : maxg);
+  if (s.Lmax * row >= ((int64_t)1 << 31) || s.N > 65535) return cudaErrorInvalidValue;
+  const int64_t per_seq_blocks = (1216 + s.N - 1) / s.N;  // ~1216 CTAs in all
+  auto grid = [&](int64_t pieces) {  // pieces of the whole batch
+    const int64_t per_seq = (pieces / s.N + 255) / 256;
+    return dim3((unsigned)(per_seq < per_seq_blocks ? (per_seq > 0 ? per_seq : 1) : per_seq_blocks),
+                (unsigned)s.N);
   };
   const uint8_t* a = (const uint8_t*)src;
   uint8_t* b = (uint8_t*)dst;

@@ -414,7 +414,9 @@ gdn_status gdn_conv_silu_bwd(const gdn_conv_problem* p, const void* x, const flo
  *    tails are skipped (their outputs zeroed), on the fp32 path they cost masked work.
  *  - Workspace: gdn_varlen_workspace_size (op GDN_OP_FWD or GDN_OP_BWD), 256-byte aligned.
  * Errors: as gdn_fwd / gdn_bwd; offsets that are not non-decreasing from 0 to T, B != 1
- * or n_seqs < 0: GDN_ERR_INVALID_ARG.  n_seqs = 0 (T = 0) does nothing.
+ * or n_seqs < 0: GDN_ERR_INVALID_ARG; more than 65535 sequences, or a longest sequence
+ * whose widest token row (H dv or Hqk dk elements) spans 2^31 bytes or more:
+ * GDN_ERR_UNSUPPORTED.  n_seqs = 0 (T = 0) does nothing.
  */
 gdn_status gdn_varlen_workspace_size(const gdn_problem* p, const int32_t* cu_seqlens_host,
                                      int32_t n_seqs, int32_t op, size_t* bytes);
