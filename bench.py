@@ -212,9 +212,9 @@ E2E_COPY_STREAMS = 4  # side streams for the host-to-device copies of the end-to
 
 
 MEASURED_TRAFFIC = {
-    "bwd.grad_tc": {"T": 32768, "bytes_per_launch": 3058718720 + 836861184,
+    "bwd.grad_tc": {"T": 32768, "bytes_per_launch": 3068695552 + 837829632,
                     "src": "chunked_state_scan_gated_gb300/csrc/gdn_tc_grad.cu",
-                    "sha256": "c6bbeb858e79db59e9ca94f70f9e272918172c202416ec1eb7f1de6349430aa7"},
+                    "sha256": "fd7cac4bf946ce21e8a5d94bf83623dff22cfa26777f2c1d113fa8746c11464a"},
 }
 
 
