@@ -584,7 +584,25 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
         if (!mbar_wait(bar_x, xpar, ar.status, kStatusTimeout)) *s_abort = 1;
         if (tid == 0) pend &= kApply ? ~(1u << bi) : ~1u;
       }
-      if (tid == 0) {  // pull the tiles of the next loads into L2
+      if (kApply) {  // q rows scaled by gamma_i rq_i (every chunk of a row shares the factor)
+        for (int e = tid; e < 1024; e += CT) {
+          const int r = e >> 4, at = (e >> 3) & 1, p = e & 7;
+          const uint32_t off = xa + at * XSTR + 8192 + r * 128 + p * 16;
+          float x[8];
+          ld_chunk(sm, off, x);
+          const float f = exp2f(sGc[r]) * sGc[64 + r];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x[q] *= f;
+          st_chunk(sm, off, x);
+        }
+      }
+      // apply: the scaled q tile must be complete; otherwise the loop's last barrier
+      // already ordered the state tile S(c) before MMA_a
+      if (kApply) CHAIN_SYNC();
+      // pull the tiles of the next loads into L2, from warp 2 while thread 0 issues this
+      // chunk's products (each prefetch takes ~100 cycles to issue; warp 2 is idle until
+      // the first product's epilogue)
+      if (tid == 64) {
         if (!kApply && c + 1 < ce) {
           l2_prefetch(wsrc + (c + 1) * kImg, kImg);
           if (needU) l2_prefetch(usrc + (c + 1) * kImg, kImg);
@@ -607,23 +625,10 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
           l2_prefetch(rsrc + (c + 2) * 128, 512);
         }
       }
-      if (kApply) {  // q rows scaled by gamma_i rq_i (every chunk of a row shares the factor)
-        for (int e = tid; e < 1024; e += CT) {
-          const int r = e >> 4, at = (e >> 3) & 1, p = e & 7;
-          const uint32_t off = xa + at * XSTR + 8192 + r * 128 + p * 16;
-          float x[8];
-          ld_chunk(sm, off, x);
-          const float f = exp2f(sGc[r]) * sGc[64 + r];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) x[q] *= f;
-          st_chunk(sm, off, x);
-        }
-      }
-      // apply: the scaled q tile must be complete; otherwise the loop's last barrier
-      // already ordered the state tile S(c) before MMA_a
-      if (kApply) CHAIN_SYNC();
-      // chunk-start state: the bf16 S tile image, as is (states; apply when asked to keep them)
-      if ((MODE == CH_STATES || (kApply && ar.hc != nullptr)) && tid == 0) {
+      // chunk-start state: the bf16 S tile image, as is (states; apply when asked to keep
+      // them), stored by warp 2 so that thread 0 goes straight to the products
+      const bool keep_s = MODE == CH_STATES || (kApply && ar.hc != nullptr);
+      if (keep_s && tid == 64) {
         bulk_store(ar.hc + (bh * ar.NC + c) * (int64_t)(2 * kImg), sm + OFF_S, 2 * kImg);
         bulk_commit();
       }
@@ -713,7 +718,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
         }
       }
       // the S tile (states) and the previous O tile (apply) are rewritten below
-      if ((MODE == CH_STATES || kApply) && tid == 0) bulk_wait_read();
+      if ((kApply && tid == 0) || (keep_s && tid == 64)) bulk_wait_read();
       CHAIN_SYNC();
       // ---- MMA_b: K^T V2 -> tB; apply: MMA_c: [0; P] V' accumulated into tA rows 64..127
       if (tid == 0) {
@@ -803,7 +808,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
     }
   }
 done:
-  if (tid == 0) bulk_wait_all();  // stores read shared memory until they complete
+  if (tid == 0 || tid == 64) bulk_wait_all();  // stores read shared memory until they complete
   if (tid == 0 && pend) {  // abort: let every copy and MMA still in flight finish first
     for (int i = 0; i < 5; ++i)
       if (pend & (1u << i)) {
@@ -939,7 +944,7 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
       const int64_t k = ce - 1 - c;
       const int64_t t0 = c * 64;
       const uint32_t par = (uint32_t)(k & 1);
-      if (tid == 0 && c - 1 >= cs) {  // pull the tiles of chunk c-1 into L2
+      if (tid == 64 && c - 1 >= cs) {  // pull the tiles of chunk c-1 into L2 (off thread 0)
         const int tp = (int)((c - 1) * 64);
         for (int a = 0; a < 2; ++a) {
           l2_prefetch_tile(&mk, a * 64, (int)hq, tp, (int)b);
@@ -974,7 +979,8 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
       }
       const float gC = exp2f(sG[63]);
       CHAIN_SYNC();
-      if (store && tid == 0) {  // gradient of chunk c's end state: the bf16 dS tile image, as is
+      if (store && tid == 64) {  // gradient of chunk c's end state: the bf16 dS tile image, as is
+        // (warp 2: thread 0 goes straight to the products)
         bulk_store(ar.dhc + (bh * ar.NC + c) * (int64_t)(2 * kImg), sm + D_DS, 2 * kImg);
         bulk_commit();
       }
@@ -1011,7 +1017,7 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) st_chunk(sm + D_DO, kmaj_chunk(row, half * 4 + cc), &v[cc * 8]);
       }
-      if (store && tid == 0) bulk_wait_read();  // the dS tile is rewritten below
+      if (store && tid == 64) bulk_wait_read();  // the dS tile is rewritten below
       CHAIN_SYNC();
       // ---- tS += W^T (-dV')  (B from the K-major -dV'^T tile)
       if (tid == 0) {
@@ -1058,7 +1064,7 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
     }
   }
 done:
-  if (tid == 0) bulk_wait_all();
+  if (tid == 64) bulk_wait_all();
   if (tid == 0 && pend) {
     for (int i = 0; i < 3; ++i)
       if (pend & (1u << i)) {
