@@ -588,12 +588,7 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
         for (int e = tid; e < 1024; e += CT) {
           const int r = e >> 4, at = (e >> 3) & 1, p = e & 7;
           const uint32_t off = xa + at * XSTR + 8192 + r * 128 + p * 16;
-          float x[8];
-          ld_chunk(sm, off, x);
-          const float f = exp2f(sGc[r]) * sGc[64 + r];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) x[q] *= f;
-          st_chunk(sm, off, x);
+          scale_chunk(sm, off, exp2f(sGc[r]) * sGc[64 + r]);
         }
       }
       // apply: the scaled q tile must be complete; otherwise the loop's last barrier
@@ -963,12 +958,7 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
       for (int e = tid; e < 2048; e += CT) {
         const int isq = e >> 10, r = (e >> 4) & 63, at = (e >> 3) & 1, p = e & 7;
         const uint32_t off = D_XA + at * 16384 + isq * 8192 + r * 128 + p * 16;
-        const float f = isq ? exp2f(sG[r]) * sRq[r] : exp2f(sG[63] - sG[r]) * sRk[r];
-        float x[8];
-        ld_chunk(sm, off, x);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] *= f;
-        st_chunk(sm, off, x);
+        scale_chunk(sm, off, isq ? exp2f(sG[r]) * sRq[r] : exp2f(sG[63] - sG[r]) * sRk[r]);
       }
       if (t0 + 64 > L) {
         for (int e = tid; e < 1024; e += CT) {

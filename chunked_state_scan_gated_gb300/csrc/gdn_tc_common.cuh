@@ -336,6 +336,20 @@ __device__ __forceinline__ void ld_chunk(const uint8_t* base, uint32_t off, floa
   }
 }
 
+// Multiply a 16-byte chunk of 8 bf16 in place by f (rounded to bf16), two at a time.
+__device__ __forceinline__ void scale_chunk(uint8_t* base, uint32_t off, float f) {
+  uint4 v = *reinterpret_cast<const uint4*>(base + off);
+  const __nv_bfloat162 f2 = __float2bfloat162_rn(f);
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    b = __hmul2(b, f2);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  *reinterpret_cast<uint4*>(base + off) = v;
+}
+
 constexpr int LDA = 65;  // default leading dim of the fp32 64 x 64 tiles of the solve
 
 // Cumulative gates are kept in fp32 and in log2 units (G * log2 e), so every
