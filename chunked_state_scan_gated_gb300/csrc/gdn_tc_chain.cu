@@ -716,11 +716,9 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
       if ((kApply && tid == 0) || (keep_s && tid == 64)) bulk_wait_read();
       CHAIN_SYNC();
       // ---- MMA_b: K^T V2 -> tB; apply: MMA_c: [0; P] V' accumulated into tA rows 64..127
+      if (tid == 64 && needU && c + 1 < ce) issue_u(c + 1);  // U(c) consumed; off thread 0
       if (tid == 0) {
-        if (needU && c + 1 < ce) {  // U(c) consumed
-          issue_u(c + 1);
-          pend |= 4u;
-        }
+        if (needU && c + 1 < ce) pend |= 4u;  // (issued by warp 2)
         const uint32_t id = idesc_bf16(128, 128, 1, kApply ? 1 : 0);  // B: V2 (apply) or V2^T
         for (int ks = 0; ks < 4; ++ks)
           mma_bf16(tB, (dxs + ((xa + KOFF + ks * 2048) >> 4)),
