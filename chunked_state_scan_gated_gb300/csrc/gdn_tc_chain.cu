@@ -233,22 +233,23 @@ __global__ void __launch_bounds__(PT, 2)
   if (*s_abort) goto done;
   if (!mbar_wait(bar_mma, 0, ar.status, kStatusTimeout)) *s_abort = 1;
   tc_fence_after();
+  float v[32];  // row . k_j for j = 32*half + e (read with the diagonal block: one wait)
   if (half == 0) {  // diagonal element (row, row) sits in column group `quad`, element `lane`
     float d[32];
-    tmem_ld32(tmem + lane_off + 32 * quad, d);
+    tmem_ld32x2(tmem + lane_off + 32 * quad, d, tmem + lane_off + 64 + 32 * half, v);
     float nrm = 0.f;
 #pragma unroll
     for (int e = 0; e < 32; ++e) nrm = (e == lane) ? d[e] : nrm;
     float inv = ar.l2norm ? rsqrtf(nrm + ar.eps) : 1.f;
     if (row < 64) inv *= ar.scale;
     sInv[row] = inv;
+  } else {
+    tmem_ld32(tmem + lane_off + 64 + 32 * half, v);
   }
   __syncthreads();
   if (h % ar.r == 0 && tid < 128) ar.rqk[((b * ar.Hqk + hq) * ar.NC + c) * 128 + tid] = sInv[tid];
   if (tid >= 128 && tid < 192) sCw[tid - 128] = sBeta[tid - 128] * sGam[tid - 128] * sInv[tid - 64];
   {
-    float v[32];  // row . k_j for j = 32*half + e
-    tmem_ld32(tmem + lane_off + 64 + 32 * half, v);
     const int i = row & 63;
     const float gi = sG[i], si = sInv[row];
     // v[e] <- row . k_j rk_j e^{G_i - G_j} (j = 32 half + e), zero above the diagonal; a
