@@ -373,7 +373,7 @@ done:
 // k_chain_tc: grid (parts, H, B * nseg), 256 threads.  Warp w reads TMEM lane
 // quadrant w & 3 (state row `row`) and owns state columns (w >> 2) * 64 .. +63.
 // q and k tiles are the raw inputs (TMA); their norm factors rq, rk come from
-// the prologue and are applied to the rows of V2 and of the scaled q tile.
+// the prologue and are applied to the rows of V2 and of the product Q S.
 // ============================================================================
 constexpr int CT = 256;
 enum { CH_APPLY = 0, CH_SUM = 1, CH_STATES = 2 };
@@ -585,16 +585,8 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
         if (!mbar_wait(bar_x, xpar, ar.status, kStatusTimeout)) *s_abort = 1;
         if (tid == 0) pend &= kApply ? ~(1u << bi) : ~1u;
       }
-      if (kApply) {  // q rows scaled by gamma_i rq_i (every chunk of a row shares the factor)
-        for (int e = tid; e < 1024; e += CT) {
-          const int r = e >> 4, at = (e >> 3) & 1, p = e & 7;
-          const uint32_t off = xa + at * XSTR + 8192 + r * 128 + p * 16;
-          scale_chunk(sm, off, exp2f(sGc[r]) * sGc[64 + r]);
-        }
-      }
-      // apply: the scaled q tile must be complete; otherwise the loop's last barrier
-      // already ordered the state tile S(c) before MMA_a
-      if (kApply) CHAIN_SYNC();
+      // the loop's last barrier already ordered the state tile S(c) before MMA_a; the q
+      // tile is used raw (its rows' factors gamma_i rq_i are applied to Q S in TMEM)
       // pull the tiles of the next loads into L2, from warp 2 while thread 0 issues this
       // chunk's products (each prefetch takes ~100 cycles to issue; warp 2 is idle until
       // the first product's epilogue)
@@ -713,6 +705,19 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
           }
         }
       }
+      if (kApply && quad >= 2) {  // Q S (rows 64..127 of tA) times gamma_i rq_i, in place,
+        // while quadrants 0, 1 form V'; MMA_c then adds P V' to the scaled rows
+        const int i = row - 64;
+        const float f = exp2f(sGc[i]) * sGc[64 + i];
+        float v0[32], v1[32];
+        tmem_ld32x2(tA + lane_off + half * 64, v0, tA + lane_off + half * 64 + 32, v1);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          v0[e] *= f;
+          v1[e] *= f;
+        }
+        tmem_st32x2(tA + lane_off + half * 64, v0, tA + lane_off + half * 64 + 32, v1);
+      }
       // the S tile (states) and the previous O tile (apply) are rewritten below
       if ((kApply && tid == 0) || (keep_s && tid == 64)) bulk_wait_read();
       CHAIN_SYNC();
@@ -829,7 +834,7 @@ done:
 // mode 1 starts from dS = 0 and returns the segment's gradient summary D (the
 // reverse-direction state-gradient pass of "linear attention cp #1035").
 // ============================================================================
-constexpr uint32_t D_XA = 0;        // atoms a at a*16384: [Kt_a | Qg_a] (scaled k, scaled q)
+constexpr uint32_t D_XA = 0;        // atoms a at a*16384: [K_a | Q_a] (q rows scaled in place)
 constexpr uint32_t D_W = 32768;     // W image
 constexpr uint32_t D_P = 49152;     // P image (8 KB)
 constexpr uint32_t D_DO = 57344;    // dO tile [tok][dv]; later -dV'^T [dv][tok] (K-major)
@@ -865,8 +870,8 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
   // operand descriptors: base descriptor + byte offset / 16 (the start address field)
   const uint64_t d16 = sdesc(base, 16, 1024), d8192 = sdesc(base, 8192, 1024),
                  d16384 = sdesc(base, 16384, 1024);
-  uint64_t* bars = (uint64_t*)(sm + D_SC);  // a: K, Q, P, G/rq/rk; b: W, dO; mma
-  uint64_t* bar_a = bars, *bar_b = bars + 1, *bar_mma = bars + 2;
+  uint64_t* bars = (uint64_t*)(sm + D_SC);  // a: K, Q, P, G/rq/rk; b: W, dO; mma; Qg^T dO
+  uint64_t* bar_a = bars, *bar_b = bars + 1, *bar_mma = bars + 2, *bar_q = bars + 3;
   uint32_t* s_tmem = (uint32_t*)(bars + 4);
   int* s_abort = (int*)(s_tmem + 1);
   const float* sG = (const float*)(sm + D_G);
@@ -888,7 +893,7 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
   uint32_t pend = 0;
 
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bars + i, 1);
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -897,7 +902,7 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t tV = tmem, tS = tmem + 128;
+  const uint32_t tV = tmem, tV2 = tmem + 64, tS = tmem + 128;
 
   float dS[64];
 #pragma unroll
@@ -907,6 +912,8 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
   }
 #pragma unroll
   for (int cc = 0; cc < 8; ++cc) st_chunk(sm + D_DS, mnmaj_chunk(row, half * 8 + cc, 16384), &dS[cc * 8]);
+  fence_proxy_async();  // the first round 1a reads the initial dS tile
+  __syncthreads();
 
   {
     const uint8_t* wsrc = ar.wim + bh * ar.NC * (int64_t)kImg;
@@ -953,28 +960,26 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
       if (!mbar_wait(bar_a, par, ar.status, kStatusTimeout)) *s_abort = 1;
       if (!mbar_wait(bar_b, par, ar.status, kStatusTimeout)) *s_abort = 1;
       if (tid == 0) pend &= ~3u;
-      // ---- scale k rows by rk e^{G_C - G}, q rows by gamma rq; zero dO rows past valid_len
-      for (int e = tid; e < 2048; e += CT) {
-        const int isq = e >> 10, r = (e >> 4) & 63, at = (e >> 3) & 1, p = e & 7;
-        const uint32_t off = D_XA + at * 16384 + isq * 8192 + r * 128 + p * 16;
-        scale_chunk(sm, off, isq ? exp2f(sG[r]) * sRq[r] : exp2f(sG[63] - sG[r]) * sRk[r]);
-      }
-      if (t0 + 64 > L) {
+      // k is used raw (its rows' factors rk e^{G_C - G} scale the token columns of dS^T K^T
+      // in the epilogue); q rows are scaled by gamma rq while round 1a runs
+      const float gC = exp2f(sG[63]);
+      const int tl = half * 32 + lane;  // this lane's token column of the epilogue
+      const float ktr = exp2f(sG[63] - sG[tl]) * sRk[tl];
+      if (t0 + 64 > L) {  // zero dO rows past valid_len (a CTA-uniform branch)
         for (int e = tid; e < 1024; e += CT) {
           const int i = e >> 4, cc = e & 15;
           if (t0 + i >= L)
             *reinterpret_cast<uint4*>(sm + D_DO + mnmaj_chunk(i, cc, 8192)) = make_uint4(0, 0, 0, 0);
         }
+        CHAIN_SYNC();
       }
-      const float gC = exp2f(sG[63]);
-      CHAIN_SYNC();
       if (store && tid == 64) {  // gradient of chunk c's end state: the bf16 dS tile image, as is
         // (warp 2: thread 0 goes straight to the products)
         bulk_store(ar.dhc + (bh * ar.NC + c) * (int64_t)(2 * kImg), sm + D_DS, 2 * kImg);
         bulk_commit();
       }
-      // ---- dV'^T = dO^T P + dS^T Kt^T -> tV (feature-major: M = 128 rows of dv, 64 token
-      //      columns); Qg^T dO -> tS
+      // ---- round 1a: dO^T P -> tV, dS^T K^T -> tV2 (feature-major: M = 128 rows of dv,
+      //      64 token columns; the previous step's last barrier ordered dS)
       if (tid == 0) {
         const uint32_t idv = idesc_bf16(128, 64, 1, 1);
         for (int ks = 0; ks < 4; ++ks)  // K = tokens i
@@ -982,29 +987,46 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
                    idv, ks > 0);
         const uint32_t idk = idesc_bf16(128, 64, 1, 0);
         for (int ks = 0; ks < 8; ++ks)  // K = dk
-          mma_bf16(tV, (d16384 + ((D_DS + ks * 2048) >> 4)),
-                   (d16 + ((D_XA + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4)), idk, 1);
+          mma_bf16(tV2, (d16384 + ((D_DS + ks * 2048) >> 4)),
+                   (d16 + ((D_XA + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4)), idk, ks > 0);
+        mma_commit(bar_mma);
+        pend |= 4u;
+      }
+      for (int e = tid; e < 1024; e += CT) {  // Qg = diag(gamma rq) Q, in place
+        const int r = e >> 4, at = (e >> 3) & 1, p = e & 7;
+        scale_chunk(sm, D_XA + at * 16384 + 8192 + r * 128 + p * 16, exp2f(sG[r]) * sRq[r]);
+      }
+      CHAIN_SYNC();
+      // ---- round 1b: Qg^T dO -> tS
+      if (tid == 0) {
         const uint32_t idmm = idesc_bf16(128, 128, 1, 1);
         for (int ks = 0; ks < 4; ++ks)
           mma_bf16(tS, (d16384 + ((D_XA + 8192 + ks * 2048) >> 4)),
                    (d8192 + ((D_DO + ks * 2048) >> 4)), idmm, ks > 0);
-        mma_commit(bar_mma);
-        pend |= 4u;
+        mma_commit(bar_q);
+        pend |= 8u;
       }
       if (!mbar_wait(bar_mma, 0, ar.status, kStatusTimeout)) *s_abort = 1;
       if (tid == 0) pend &= ~4u;
       tc_fence_after();
-      if (tid == 0 && c - 1 >= cs) {  // K, Q, P, gates of chunk c consumed
-        issue_a(c - 1);
-        pend |= 1u;
-      }
-      {  // -dV'^T over the dO tile: thread row `row` (dv), tokens 32 half + e, K-major
-        float v[32];
-        tmem_ld32(tV + lane_off + half * 32, v);
+      {  // -dV'^T = -(tV + tV2 diag(rk e^{G_C - G})): thread row `row` (dv), tokens 32 half + e,
+        // stored K-major over the dO tile once round 1b has read it
+        // (16 columns at a time: the 64 dS registers stay live)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = -v[e];
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[16], w[16];
+          tmem_ld16x2(tV + lane_off + half * 32 + hh * 16, tV2 + lane_off + half * 32 + hh * 16, v, w);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) st_chunk(sm + D_DO, kmaj_chunk(row, half * 4 + cc), &v[cc * 8]);
+          for (int e = 0; e < 16; ++e)
+            v[e] = -fmaf(__shfl_sync(0xffffffffu, ktr, hh * 16 + e), w[e], v[e]);
+          if (hh == 0) {
+            if (!mbar_wait(bar_q, par, ar.status, kStatusTimeout)) *s_abort = 1;
+            if (tid == 0) pend &= ~8u;
+          }
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+            st_chunk(sm + D_DO, kmaj_chunk(row, half * 4 + hh * 2 + cc), &v[cc * 8]);
+        }
       }
       if (store && tid == 64) bulk_wait_read();  // the dS tile is rewritten below
       CHAIN_SYNC();
@@ -1016,6 +1038,10 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
                    1);
         mma_commit(bar_mma);
         pend |= 4u;
+        if (c - 1 >= cs) {  // K, Q, P of chunk c consumed by rounds 1a, 1b; gates read above
+          issue_a(c - 1);
+          pend |= 1u;
+        }
       }
       if (!mbar_wait(bar_mma, 1, ar.status, kStatusTimeout)) *s_abort = 1;
       if (tid == 0) pend &= ~4u;
@@ -1055,7 +1081,7 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
 done:
   if (tid == 64) bulk_wait_all();
   if (tid == 0 && pend) {
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < 4; ++i)
       if (pend & (1u << i)) {
         mbar_wait(bars + i, 0, nullptr, 0);
         mbar_wait(bars + i, 1, nullptr, 0);

@@ -231,6 +231,20 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, float (&va)[32], uint32
   }
 }
 
+// Two 32-column stores to this thread's TMEM lane (warp-wide), then one wait: the stores
+// are complete in TMEM when it returns (an MMA issued after a tcgen05 fence and a thread
+// barrier sees them).
+__device__ __forceinline__ void tmem_st32x2(uint32_t ta, const float (&va)[32], uint32_t tb,
+                                            const float (&vb)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};\n"
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%1], {%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65};\n"
+      "tcgen05.wait::st.sync.aligned;"
+      :: "r"(ta), "r"(tb),
+      "r"(__float_as_uint(va[0])), "r"(__float_as_uint(va[1])), "r"(__float_as_uint(va[2])), "r"(__float_as_uint(va[3])), "r"(__float_as_uint(va[4])), "r"(__float_as_uint(va[5])), "r"(__float_as_uint(va[6])), "r"(__float_as_uint(va[7])), "r"(__float_as_uint(va[8])), "r"(__float_as_uint(va[9])), "r"(__float_as_uint(va[10])), "r"(__float_as_uint(va[11])), "r"(__float_as_uint(va[12])), "r"(__float_as_uint(va[13])), "r"(__float_as_uint(va[14])), "r"(__float_as_uint(va[15])), "r"(__float_as_uint(va[16])), "r"(__float_as_uint(va[17])), "r"(__float_as_uint(va[18])), "r"(__float_as_uint(va[19])), "r"(__float_as_uint(va[20])), "r"(__float_as_uint(va[21])), "r"(__float_as_uint(va[22])), "r"(__float_as_uint(va[23])), "r"(__float_as_uint(va[24])), "r"(__float_as_uint(va[25])), "r"(__float_as_uint(va[26])), "r"(__float_as_uint(va[27])), "r"(__float_as_uint(va[28])), "r"(__float_as_uint(va[29])), "r"(__float_as_uint(va[30])), "r"(__float_as_uint(va[31])),
+      "r"(__float_as_uint(vb[0])), "r"(__float_as_uint(vb[1])), "r"(__float_as_uint(vb[2])), "r"(__float_as_uint(vb[3])), "r"(__float_as_uint(vb[4])), "r"(__float_as_uint(vb[5])), "r"(__float_as_uint(vb[6])), "r"(__float_as_uint(vb[7])), "r"(__float_as_uint(vb[8])), "r"(__float_as_uint(vb[9])), "r"(__float_as_uint(vb[10])), "r"(__float_as_uint(vb[11])), "r"(__float_as_uint(vb[12])), "r"(__float_as_uint(vb[13])), "r"(__float_as_uint(vb[14])), "r"(__float_as_uint(vb[15])), "r"(__float_as_uint(vb[16])), "r"(__float_as_uint(vb[17])), "r"(__float_as_uint(vb[18])), "r"(__float_as_uint(vb[19])), "r"(__float_as_uint(vb[20])), "r"(__float_as_uint(vb[21])), "r"(__float_as_uint(vb[22])), "r"(__float_as_uint(vb[23])), "r"(__float_as_uint(vb[24])), "r"(__float_as_uint(vb[25])), "r"(__float_as_uint(vb[26])), "r"(__float_as_uint(vb[27])), "r"(__float_as_uint(vb[28])), "r"(__float_as_uint(vb[29])), "r"(__float_as_uint(vb[30])), "r"(__float_as_uint(vb[31]))
+      : "memory");
+}
 
 // Several loads of this thread's TMEM lane issued back to back, then one wait: the
 // loads overlap instead of each paying the full round trip.  (One asm statement, so that
