@@ -155,17 +155,20 @@ __global__ void __launch_bounds__(PT, 2)
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   if (t0 >= L) return;  // a chunk of padding only: every consumer skips it
 
-  // Gate inputs (warps 2, 3: token tid - 64), read before anything else: with the q, k, v
-  // copies they are the longest wait of the CTA's start.  Only loaded here: their first
-  // use, after the set-up barrier, is where the threads wait for them.
+  // Gate inputs (warps 2, 3: token tid - 64; a, b, dt_bias, A_log), read before anything
+  // else: with the q, k, v copies they are the longest wait of the CTA's start.  Only loaded
+  // here: their first use, after the set-up barrier, is where the threads wait for them.
   const int tg = tid - 64;
   const bool gate_warp = warp == 2 || warp == 3;
   __nv_bfloat16 ra = __float2bfloat16_rn(0.f), rb = ra;
+  float dtb = 0.f, alog = 0.f;
   const bool glive = gate_warp && t0 + tg < L;
   if (glive) {
     const int64_t gi = (b * ar.Ts + t0 + tg) * ar.H + h;
     ra = ar.a[gi];
     rb = ar.b[gi];
+    dtb = ar.dt_bias[h];
+    alog = ar.A_log[h];
   }
   if (tid == 0) {  // the barriers are this thread's own: the copies go out at once
     mbar_init(bar_qk, 1);
@@ -208,9 +211,9 @@ __global__ void __launch_bounds__(PT, 2)
   if (gate_warp) {  // g, beta and the cumulative gate in log2 units (scan over 64 tokens)
     float g = 0.f, be = 0.f;
     if (glive) {
-      const float xa = __bfloat162float(ra) + ar.dt_bias[h];
+      const float xa = __bfloat162float(ra) + dtb;
       const float sp = xa > 20.f ? xa : log1pf(expf(xa));
-      g = -expf(ar.A_log[h]) * sp;
+      g = -expf(alog) * sp;
       be = 1.f / (1.f + expf(-__bfloat162float(rb)));
     }
     float v = g * kLog2e;
@@ -279,10 +282,16 @@ __global__ void __launch_bounds__(PT, 2)
       }
     } else if (!upper) {  // A = strictly lower part, times beta_i (the solve never reads above it)
       const float bs = sBeta[i] * si;
+      float4* dst = reinterpret_cast<float4*>(sA + i * LDA + half * 32);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = half * 32 + e;
-        sA[i * LDA + j] = (j < i) ? bs * v[e] : 0.f;
+      for (int q4 = 0; q4 < 8; ++q4) {
+        float w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = half * 32 + 4 * q4 + u;
+          w[u] = (j < i) ? bs * v[4 * q4 + u] : 0.f;
+        }
+        dst[q4] = make_float4(w[0], w[1], w[2], w[3]);
       }
     }
   }

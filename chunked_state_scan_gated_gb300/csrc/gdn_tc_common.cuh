@@ -382,7 +382,10 @@ __device__ __forceinline__ void scale_chunk(uint8_t* base, uint32_t off, float f
   *reinterpret_cast<uint4*>(base + off) = v;
 }
 
-constexpr int LDA = 65;  // default leading dim of the fp32 64 x 64 tiles of the solve
+// Leading dim of the fp32 64 x 64 tiles of the solve: 68 = 4 (mod 32) makes the tf32 A-fragment
+// loads (rows g, columns t) conflict-free and the B-fragment loads (rows t, columns g) 2-way;
+// rows stay 16-byte aligned for vector stores.
+constexpr int LDA = 68;
 
 // Cumulative gates are kept in fp32 and in log2 units (G * log2 e), so every
 // decay factor is one exp2f of a difference; fp32 is ample at bf16 tolerance
@@ -407,47 +410,6 @@ __device__ __forceinline__ void cumsum64f(float* x) {
     v1 += __shfl_sync(0xffffffffu, v0, 31);
     x[lane] = v0;
     x[lane + 32] = v1;
-  }
-}
-
-// T = (I + A)^-1 for strictly lower A (64 x 64, fp32, leading dim LDA): 16 x 16
-// diagonal blocks by substitution, off-diagonal blocks by
-// T_ij = -T_ii sum_{j <= m < i} A_im T_mj, block diagonal by block diagonal.
-// Needs blockDim.x >= 128 and a multiple of 32 (all threads of the block call it).
-__device__ __forceinline__ void solve_unit_lower64(const float* A, float* T, float* Y,
-                                                   const int LDA = 65) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (warp < 4 && lane < 16) {
-    const int b0 = warp * 16, j = lane;
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float v = (i == j) ? 1.f : 0.f;
-#pragma unroll
-      for (int l = 0; l < i; ++l) v = fmaf(-A[(b0 + i) * LDA + b0 + l], x[l], v);
-      x[i] = (i >= j) ? v : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) T[(b0 + i) * LDA + b0 + j] = x[i];
-  }
-  __syncthreads();
-  for (int d = 1; d <= 3; ++d) {
-    const int nb = 4 - d;
-    for (int e = tid; e < nb * 256; e += blockDim.x) {
-      const int bj = e >> 8, bi = bj + d, r = (e >> 4) & 15, c = e & 15;
-      float y = 0.f;
-      for (int m = bj * 16; m < bi * 16; ++m) y = fmaf(A[(bi * 16 + r) * LDA + m], T[m * LDA + bj * 16 + c], y);
-      Y[e] = y;
-    }
-    __syncthreads();
-    for (int e = tid; e < nb * 256; e += blockDim.x) {
-      const int bj = e >> 8, bi = bj + d, r = (e >> 4) & 15, c = e & 15;
-      float t = 0.f;
-#pragma unroll
-      for (int l = 0; l < 16; ++l) t = fmaf(T[(bi * 16 + r) * LDA + bi * 16 + l], Y[(bj << 8) + l * 16 + c], t);
-      T[(bi * 16 + r) * LDA + bj * 16 + c] = -t;
-    }
-    __syncthreads();
   }
 }
 
