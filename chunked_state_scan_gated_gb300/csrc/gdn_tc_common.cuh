@@ -482,27 +482,37 @@ __device__ __forceinline__ void solve_unit_lower64_mma(const float* A, float* T,
   for (int d = 1; d <= 3; ++d) {
     if (warp < 2 * (4 - d)) {
       const int bj = warp >> 1, bi = bj + d, r0 = bi * 16, n0 = bj * 16 + (warp & 1) * 8;
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int m = bj * 16; m < bi * 16; m += 8) {  // Y = A[bi, bj..bi) T[bj..bi, bj]
-        const float a[4] = {A[(r0 + g) * lda + m + t], A[(r0 + g + 8) * lda + m + t],
-                            A[(r0 + g) * lda + m + t + 4], A[(r0 + g + 8) * lda + m + t + 4]};
-        const float b[2] = {T[(m + t) * lda + n0 + g], T[(m + t + 4) * lda + n0 + g]};
-        mma_tf32_16x8x8(c, a, b);
-      }
-      Yw[g * 8 + 2 * t] = c[0];
-      Yw[g * 8 + 2 * t + 1] = c[1];
-      Yw[(g + 8) * 8 + 2 * t] = c[2];
-      Yw[(g + 8) * 8 + 2 * t + 1] = c[3];
-      __syncwarp();
-      float e[4] = {0.f, 0.f, 0.f, 0.f};
+      // Y = A[bi, bj..bi) T[bj..bi, bj], the 8-wide K steps alternating between two
+      // accumulators so that two MMA chains are in flight
+      float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int m = bj * 16; m < bi * 16; m += 16) {
 #pragma unroll
-      for (int k = 0; k < 16; k += 8) {  // T_ij = -T_ii Y
+        for (int h8 = 0; h8 < 16; h8 += 8) {
+          const int mm = m + h8;
+          const float a[4] = {A[(r0 + g) * lda + mm + t], A[(r0 + g + 8) * lda + mm + t],
+                              A[(r0 + g) * lda + mm + t + 4], A[(r0 + g + 8) * lda + mm + t + 4]};
+          const float b[2] = {T[(mm + t) * lda + n0 + g], T[(mm + t + 4) * lda + n0 + g]};
+          if (h8 == 0) mma_tf32_16x8x8(c, a, b);
+          else mma_tf32_16x8x8(c2, a, b);
+        }
+      }
+      Yw[g * 8 + 2 * t] = c[0] + c2[0];
+      Yw[g * 8 + 2 * t + 1] = c[1] + c2[1];
+      Yw[(g + 8) * 8 + 2 * t] = c[2] + c2[2];
+      Yw[(g + 8) * 8 + 2 * t + 1] = c[3] + c2[3];
+      __syncwarp();
+      float e[4] = {0.f, 0.f, 0.f, 0.f}, e2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 16; k += 8) {  // T_ij = -T_ii Y (two independent products, summed)
         const float a[4] = {T[(r0 + g) * lda + r0 + k + t], T[(r0 + g + 8) * lda + r0 + k + t],
                             T[(r0 + g) * lda + r0 + k + t + 4],
                             T[(r0 + g + 8) * lda + r0 + k + t + 4]};
         const float b[2] = {Yw[(k + t) * 8 + g], Yw[(k + t + 4) * 8 + g]};
-        mma_tf32_16x8x8(e, a, b);
+        if (k == 0) mma_tf32_16x8x8(e, a, b);
+        else mma_tf32_16x8x8(e2, a, b);
       }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) e[q] += e2[q];
       T[(r0 + g) * lda + n0 + 2 * t] = -e[0];
       T[(r0 + g) * lda + n0 + 2 * t + 1] = -e[1];
       T[(r0 + g + 8) * lda + n0 + 2 * t] = -e[2];
