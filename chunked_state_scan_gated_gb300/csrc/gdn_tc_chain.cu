@@ -752,15 +752,14 @@ __device__ __forceinline__ void chain_cta(const CUtensorMap& mq, const CUtensorM
       if (!mbar_wait(bar_mma, 1, ar.status, kStatusTimeout)) *s_abort = 1;
       if (tid == 0) pend &= kApply ? ~(16u | 8u) : ~16u;  // (P consumed by tid 32's products)
       tc_fence_after();
-      if (tid == 0 && c + 1 < ce) {
-        if (kApply) {
-          issue_p(c + 1);  // P(c) consumed by MMA_c
-          pend |= 8u;
-          if (c + 2 < ce) {  // buffer bi free: MMA_a, MMA_b of chunk c are done
-            issue_x(c + 2, bars + bi, xa, A_G + bi * 768);
-            pend |= 1u << bi;
+      if (c + 1 < ce) {
+        if (kApply) {  // copies from warp 4; thread 0 keeps the drain record
+          if (tid == 128) {
+            issue_p(c + 1);  // P(c) consumed by MMA_c
+            if (c + 2 < ce) issue_x(c + 2, bars + bi, xa, A_G + bi * 768);  // buffer bi free
           }
-        } else {
+          if (tid == 0) pend |= 8u | (c + 2 < ce ? 1u << bi : 0u);
+        } else if (tid == 0) {
           issue_k(c + 1);  // K(c) consumed by MMA_b; G(c), rk(c) already read
           pend |= 2u;
         }
@@ -954,7 +953,7 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
       const int64_t k = ce - 1 - c;
       const int64_t t0 = c * 64;
       const uint32_t par = (uint32_t)(k & 1);
-      if (tid == 64 && c - 1 >= cs) {  // pull the tiles of chunk c-1 into L2 (off thread 0)
+      if (tid == 160 && c - 1 >= cs) {  // pull the tiles of chunk c-1 into L2 (warp 5)
         const int tp = (int)((c - 1) * 64);
         for (int a = 0; a < 2; ++a) {
           l2_prefetch_tile(&mk, a * 64, (int)hq, tp, (int)b);
@@ -1047,17 +1046,16 @@ __device__ __forceinline__ void dchain_cta(const CUtensorMap& mq, const CUtensor
                    1);
         mma_commit(bar_mma);
         pend |= 4u;
-        if (c - 1 >= cs) {  // K, Q, P of chunk c consumed by rounds 1a, 1b; gates read above
-          issue_a(c - 1);
-          pend |= 1u;
-        }
+        if (c - 1 >= cs) pend |= 1u;  // (issued by warp 3)
+      } else if (tid == 96 && c - 1 >= cs) {  // K, Q, P of chunk c consumed by rounds 1a, 1b;
+        issue_a(c - 1);                        // gates read above
       }
       if (!mbar_wait(bar_mma, 1, ar.status, kStatusTimeout)) *s_abort = 1;
       if (tid == 0) pend &= ~4u;
       tc_fence_after();
-      if (tid == 0 && c - 1 >= cs) {  // W and the dO / -dV' tile consumed
-        issue_b(c - 1);
-        pend |= 2u;
+      if (c - 1 >= cs) {  // W and the dO / -dV' tile consumed: warp 4 copies, thread 0 records
+        if (tid == 128) issue_b(c - 1);
+        if (tid == 0) pend |= 2u;
       }
       {  // dS <- gamma_C dS + tS
 #pragma unroll
