@@ -43,7 +43,8 @@ constexpr int GT = 512;
 // already finished with (see k_grad2_tc), then the scalars.
 constexpr uint32_t SLOT = 16384;
 constexpr uint32_t R_SC = 13 * SLOT;  // scalars
-constexpr uint32_t SC_BYTES = 2 * 4 * 64 * 4 + 3 * 64 * 4 + 4 * 4 * 64 * 4 + 3 * 4 * 64 * 4 + 128;
+constexpr uint32_t SC_BYTES = 2 * 4 * 64 * 4 + 3 * 64 * 4 + 4 * 4 * 64 * 4 + 3 * 4 * 64 * 4 +
+                               2 * 128 * 4 + 128;
 constexpr uint32_t GR_SMEM = R_SC + SC_BYTES + 1024;
 static_assert(GR_SMEM <= 232448, "shared memory of k_grad2_tc");
 
@@ -94,6 +95,7 @@ struct Grad2Args {
   const uint8_t* uim;
   const uint8_t* pim;
   const uint8_t* tim;
+  const float* rqk;    // [B][Hqk][NC][128] q, k row factors of the prologue (rq with the scale)
   int* status;
 };
 
@@ -181,7 +183,8 @@ __global__ void __launch_bounds__(GT, 1)
   float* sDBh = sRed + 4 * 4 * 64;     // [4 column parts][64] dbeta terms of A
   float* sZr = sDBh + 4 * 64;          // [4 column parts][64 rows] row sums of dP o P + dA o A
   float* sZc = sZr + 4 * 64;           // [4 row quadrants][64 columns] their column sums
-  uint64_t* bars = (uint64_t*)(sZc + 4 * 64);  // per layout: q/k, round-A tiles, U/V/T; MMA
+  float* sRqk = sZc + 4 * 64;          // per layout: rq (64), rk (64) of the chunk's q, k rows
+  uint64_t* bars = (uint64_t*)(sRqk + 2 * 128);  // per layout: q/k, round-A tiles, U/V/T; MMA
   uint64_t* bar_mma = bars + 6;
   uint32_t* s_tmem = (uint32_t*)(bars + 7);
   int* s_abort = (int*)(s_tmem + 1);
@@ -248,10 +251,12 @@ __global__ void __launch_bounds__(GT, 1)
     for (int at = 0; at < 2; ++at)
       tma_load_4d(sm + dst + at * 8192, m, at * 64, (int)head, (int)it.t0, (int)it.b, bar);
   };
-  auto ld_qk = [&](const Item& it, const Lay& L, int l) {
-    arm(l, GQK, 2 * 16384u);
+  auto ld_qk = [&](const Item& it, const Lay& L, int l) {  // q, k tiles and their row factors
+    arm(l, GQK, 2 * 16384u + 512u);
     tile2(L.q, &mq, it.hq, it, bars + 3 * l + GQK);
     tile2(L.k, &mk, it.hq, it, bars + 3 * l + GQK);
+    bulk_load(sRqk + l * 128, ar.rqk + ((it.b * (ar.H / ar.r) + it.hq) * ar.NC + it.c) * 128, 512,
+              bars + 3 * l + GQK);
   };
   auto ld_s = [&](const Item& it, const Lay& L, int l) {
     bulk_load(sm + L.s, ar.hc + it.im * 32768, 32768, bars + 3 * l + GA);
@@ -393,26 +398,23 @@ __global__ void __launch_bounds__(GT, 1)
         ld_u(it, L, lc);  // where the dq staging was
     }
     if (!mbar_wait(bars + 3 * lc + GQK, bpar, ar.status, kStatusTimeout)) *s_abort = 1;
-    // q, k rows normalised in place (16 threads per row); padded dO rows zeroed
-    for (int i4 = 0; i4 < 4; ++i4) {
-      const int rr = (tid >> 4) + 32 * i4;
-      const bool isk = rr >= 64;
-      const int sub = tid & 15, at = sub >> 3, ch = sub & 7, r6 = rr & 63;
-      const uint32_t off = (isk ? L.k : L.q) + at * 8192 + kmaj_chunk(r6, ch);
-      float x[8];
-      ld_chunk(sm, off, x);
-      float ss = 0.f;
+    // q, k rows scaled in place by the prologue's row factors (rq = scale / |q| or the scale
+    // alone, rk = 1 / |k| or 1; rows 0..63 of the factors are q's, 64..127 k's), 16 threads
+    // per row; padded dO rows zeroed
+    {
+      const float* sR = sRqk + lc * 128;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      float sc = ar.l2norm ? rsqrtf(ss + ar.eps) : 1.f;
-      if (!isk) sc *= ar.scale;
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const int rr = (tid >> 4) + 32 * i4;  // q rows, then k rows
+        const int sub = tid & 15, at = sub >> 3, ch = sub & 7, r6 = rr & 63;
+        const uint32_t off = (rr >= 64 ? L.k : L.q) + at * 8192 + kmaj_chunk(r6, ch);
+        const float f = sR[rr];
+        float x[8];
+        ld_chunk(sm, off, x);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] *= sc;
-      st_chunk(sm, off, x);
+        for (int e = 0; e < 8; ++e) x[e] *= f;  // (fp32 product, one rounding)
+        st_chunk(sm, off, x);
+      }
     }
     if (!mbar_wait(bars + 3 * lc + GA, bpar, ar.status, kStatusTimeout)) *s_abort = 1;
     armed &= ~((1u << (3 * lc + GQK)) | (1u << (3 * lc + GA)));
@@ -828,6 +830,7 @@ cudaError_t launch_grad2_tc(const Prob& pr, const Inputs& in, const WS& ws, cons
   ar.hc = (const uint8_t*)hc; ar.dhc = (const uint8_t*)dhc;
   ar.wim = (const uint8_t*)ws.wim; ar.uim = (const uint8_t*)ws.uim;
   ar.pim = (const uint8_t*)ws.pim; ar.tim = (const uint8_t*)ws.tim;
+  ar.rqk = ws.rqk;
   cudaError_t e = cudaFuncSetAttribute(k_grad2_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)GR_SMEM);
   if (e != cudaSuccess) return e;
