@@ -96,6 +96,7 @@ struct Grad2Args {
   const uint8_t* pim;
   const uint8_t* tim;
   const float* rqk;    // [B][Hqk][NC][128] q, k row factors of the prologue (rq with the scale)
+  const float* gl;     // [B][H][NC][64] cumulative gates of the prologue (log2 units)
   int* status;
 };
 
@@ -186,7 +187,8 @@ __global__ void __launch_bounds__(GT, 1)
   float* sRqk = sZc + 4 * 64;          // per layout: rq (64), rk (64) of the chunk's q, k rows
   uint64_t* bars = (uint64_t*)(sRqk + 2 * 128);  // per layout: q/k, round-A tiles, U/V/T; MMA
   uint64_t* bar_mma = bars + 6;
-  uint32_t* s_tmem = (uint32_t*)(bars + 7);
+  uint64_t* bar_g = bars + 7;          // per layout: the chunk's cumulative gates G
+  uint32_t* s_tmem = (uint32_t*)(bars + 9);
   int* s_abort = (int*)(s_tmem + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -200,10 +202,13 @@ __global__ void __launch_bounds__(GT, 1)
   const bool mover = tid == 160;  // issues every tile copy and store (warp 5: no MMA issue)
   enum { RQ = 0, RV = 1, RKW = 2, RKD = 3 };  // column-sum types
   enum { GQK = 0, GA = 1, GB = 2 };            // load groups
-  uint32_t armed = 0;  // mover: bit 3 l + g: group g of layout l armed and not yet consumed
+  uint32_t armed = 0;  // mover: bit 3 l + g: group g of layout l armed and not yet consumed;
+                       // bit 6 + l: the gates G of layout l
 
   if (tid == 0) {
     for (int i = 0; i < 6; ++i) mbar_init(bars + i, 1);
+    mbar_init(bar_g, 1);
+    mbar_init(bar_g + 1, 1);
     mbar_init(bar_mma, 5);  // each round's products are issued from five warps (lane 0 of 0..4)
     fence_barrier_init();
     *s_abort = 0;
@@ -282,12 +287,13 @@ __global__ void __launch_bounds__(GT, 1)
   constexpr uint32_t kBytesA = 32768u + 32768u + 16384u + 16384u + 8192u;  // S, dS, W, dO, P
   constexpr uint32_t kBytesB = 16384u + 8192u + 16384u;                    // U, T, V
 
-  // Gates of chunk `it` into buffer dst (G, gamma, beta, Kt at 0, 64, 128, 192), by warps 2
-  // and 3 (token = tid - 64) while the rest of the CTA works.
-  // Gate inputs of chunk `it` for token tid - 64 (warps 2, 3): a + dt_bias and b, read early
-  // into registers so that their latency stays off the chunk's critical path.
+  // Gates of a chunk in buffer dst (G, gamma, beta, Kt at 0, 64, 128, 192): G, the cumulative
+  // gate in log2 units, is the prologue's (copied in by the mover, on bar_g); warps 2 and 3
+  // (token = tid - 64) form gamma = 2^G, beta = sigmoid(b) and Kt = 2^(G_C - G) from it.
+  // Their b input is read early into a register so that its latency stays off the chunk's
+  // critical path.
   struct GateIn {
-    float xa, xb;
+    float xb;
     bool live;
   };
   auto gate_in = [&](const Item& it) {
@@ -297,39 +303,21 @@ __global__ void __launch_bounds__(GT, 1)
       Lg = ar.valid_len[it.b];
       if (Lg < 0 || Lg > ar.T) Lg = Lg < 0 ? 0 : ar.T;
     }
-    GateIn gi{0.f, 0.f, it.t0 + t < Lg};
-    if (gi.live) {
-      const int64_t ix = (it.b * ar.Ts + it.t0 + t) * ar.H + it.h;
-      gi.xa = __bfloat162float(ar.a[ix]) + ar.dt_bias[it.h];
-      gi.xb = __bfloat162float(ar.b[ix]);
-    }
+    GateIn gi{0.f, it.t0 + t < Lg};
+    if (gi.live) gi.xb = __bfloat162float(ar.b[(it.b * ar.Ts + it.t0 + t) * ar.H + it.h]);
     return gi;
   };
-  // Gates of a chunk of head h from its inputs into buffer dst (G, gamma, beta, Kt at 0, 64,
-  // 128, 192), by warps 2 and 3 (token = tid - 64) while the rest of the CTA works.
-  auto gates = [&](const GateIn& gi, int64_t h, float* dst) {
+  auto ld_g = [&](const Item& it, int l) {  // mover: the chunk's G into buffer l
+    armed |= 1u << (6 + l);
+    mbar_arrive_expect_tx(bar_g + l, 256);
+    bulk_load(sGate + l * 256, ar.gl + it.im * 64, 256, bar_g + l);
+  };
+  auto gates = [&](const GateIn& gi, float* dst) {
     const int t = tid - 64;
-    float g = 0.f, be = 0.f;
-    if (gi.live) {
-      const float sp = gi.xa > 20.f ? gi.xa : log1pf(expf(gi.xa));
-      g = -expf(ar.A_log[h]) * sp;
-      be = 1.f / (1.f + expf(-gi.xb));
-    }
-    float v = g * kLog2e;  // inclusive scan over the 64 tokens
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += y;
-    }
-    if (t == 31) dst[255] = v;  // Kt slot of token 63: scratch for the first half's total
-    asm volatile("bar.sync 1, 64;" ::: "memory");
-    if (t >= 32) v += dst[255];
-    asm volatile("bar.sync 1, 64;" ::: "memory");
-    dst[t] = v;
-    dst[64 + t] = exp2f(v);
-    dst[128 + t] = be;
-    asm volatile("bar.sync 1, 64;" ::: "memory");
-    dst[192 + t] = dexp_(dst[63], v);
+    const float G = dst[t];
+    dst[64 + t] = exp2f(G);
+    dst[128 + t] = gi.live ? 1.f / (1.f + expf(-gi.xb)) : 0.f;
+    dst[192 + t] = dexp_(dst[63], G);
   };
 
   // The CTA's chunks, skipping those of padding only (from ceil(valid_len / 64) on: the
@@ -345,14 +333,17 @@ __global__ void __launch_bounds__(GT, 1)
     return w;
   };
   const int64_t w0 = next_live(blockIdx.x);
-  GateIn gnext{0.f, 0.f, false};  // warps 2, 3: inputs of the next chunk's gates
+  GateIn gnext{0.f, false};  // warps 2, 3: b of the next chunk's gates
   if ((warp == 2 || warp == 3) && w0 < ar.NW) {
     const Item it0 = item_of(w0);
-    gates(gate_in(it0), it0.h, sGate);
+    const GateIn g0 = gate_in(it0);
+    if (!mbar_wait(bar_g, 0, ar.status, kStatusTimeout)) *s_abort = 1;
+    gates(g0, sGate);
   }
   if (mover && w0 < ar.NW) {  // every tile of the first chunk
     const Item it = item_of(w0);
     const Lay L = layout_of(0);
+    ld_g(it, 0);
     ld_qk(it, L, 0);
     arm(0, GA, kBytesA);
     ld_s(it, L, 0);
@@ -390,6 +381,10 @@ __global__ void __launch_bounds__(GT, 1)
     float* sBeta = sG + 128;
     float* sKt = sG + 192;
     __syncthreads();  // the previous chunk's scalars have been consumed, these gates written
+    if (mover) {  // this chunk's G has landed (warps 2, 3 waited for it); the next chunk's G
+      if (mbar_wait(bar_g + lc, bpar, ar.status, kStatusTimeout)) armed &= ~(1u << (6 + lc));
+      if (more) ld_g(nx, ln);  // into the other buffer, free since the previous chunk ended
+    }
     if (mover && k > 0) {  // tiles of this chunk that waited for the previous stores
       bulk_wait_read();  // the previous chunk's dv, dq, dk stores have read their slots
       if (lc == 1)
@@ -746,7 +741,9 @@ __global__ void __launch_bounds__(GT, 1)
       sDB[t] = rv + gm * rkw + sDBh[t] + sDBh[64 + t] + sDBh[128 + t] + sDBh[192 + t];
       sRed[t] = (t < 63) ? s_t : 0.f;                       // reuse: Kt terms to sum into dG_C
     } else if (more && (warp == 2 || warp == 3)) {
-      gates(gnext, nx.h, sGate + ln * 256);
+      if (!mbar_wait(bar_g + ln, (uint32_t)(((k + 1) >> 1) & 1), ar.status, kStatusTimeout))
+        *s_abort = 1;
+      gates(gnext, sGate + ln * 256);
     }
     __syncthreads();
     if (tid < 32) {  // dG_C gets the Kt terms and the state term; then dg_j = sum_{i >= j} dG_i
@@ -785,11 +782,12 @@ __global__ void __launch_bounds__(GT, 1)
 done:
   if (mover) bulk_wait_all();
   if (armed) {  // abort: let every copy still in flight land before the CTA exits
-    for (int i = 0; i < 6; ++i)
+    for (int i = 0; i < 8; ++i)
       if (armed & (1u << i)) {
         // one of the two parities is the phase in flight; the other returns at once
-        mbar_wait(bars + i, 0, nullptr, 0);
-        mbar_wait(bars + i, 1, nullptr, 0);
+        uint64_t* bar = i < 6 ? bars + i : bar_g + (i - 6);
+        mbar_wait(bar, 0, nullptr, 0);
+        mbar_wait(bar, 1, nullptr, 0);
       }
   }
   tc_fence_before();
@@ -830,7 +828,7 @@ cudaError_t launch_grad2_tc(const Prob& pr, const Inputs& in, const WS& ws, cons
   ar.hc = (const uint8_t*)hc; ar.dhc = (const uint8_t*)dhc;
   ar.wim = (const uint8_t*)ws.wim; ar.uim = (const uint8_t*)ws.uim;
   ar.pim = (const uint8_t*)ws.pim; ar.tim = (const uint8_t*)ws.tim;
-  ar.rqk = ws.rqk;
+  ar.rqk = ws.rqk; ar.gl = ws.gl;
   cudaError_t e = cudaFuncSetAttribute(k_grad2_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)GR_SMEM);
   if (e != cudaSuccess) return e;
