@@ -202,8 +202,9 @@ __global__ void __launch_bounds__(GT, 1)
   const bool mover = tid == 160;  // issues every tile copy and store (warp 5: no MMA issue)
   enum { RQ = 0, RV = 1, RKW = 2, RKD = 3 };  // column-sum types
   enum { GQK = 0, GA = 1, GB = 2 };            // load groups
-  uint32_t armed = 0;  // mover: bit 3 l + g: group g of layout l armed and not yet consumed;
-                       // bit 6 + l: the gates G of layout l
+  uint32_t armed = 0;  // the arming thread (the mover; warp 6 for q, k and G): bit 3 l + g,
+                       // group g of layout l armed and not yet consumed; bit 6 + l, the G copy
+                       // of layout l
 
   if (tid == 0) {
     for (int i = 0; i < 6; ++i) mbar_init(bars + i, 1);
@@ -340,10 +341,10 @@ __global__ void __launch_bounds__(GT, 1)
     if (!mbar_wait(bar_g, 0, ar.status, kStatusTimeout)) *s_abort = 1;
     gates(g0, sGate);
   }
+  if (tid == 192 && w0 < ar.NW) ld_g(item_of(w0), 0);  // (warp 6 arms every G copy)
   if (mover && w0 < ar.NW) {  // every tile of the first chunk
     const Item it = item_of(w0);
     const Lay L = layout_of(0);
-    ld_g(it, 0);
     ld_qk(it, L, 0);
     arm(0, GA, kBytesA);
     ld_s(it, L, 0);
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(GT, 1)
     float* sBeta = sG + 128;
     float* sKt = sG + 192;
     __syncthreads();  // the previous chunk's scalars have been consumed, these gates written
-    if (mover) {  // this chunk's G has landed (warps 2, 3 waited for it); the next chunk's G
+    if (tid == 192) {  // this chunk's G has landed (warps 2, 3 waited for it); the next G
       if (mbar_wait(bar_g + lc, bpar, ar.status, kStatusTimeout)) armed &= ~(1u << (6 + lc));
       if (more) ld_g(nx, ln);  // into the other buffer, free since the previous chunk ended
     }
@@ -718,7 +719,8 @@ __global__ void __launch_bounds__(GT, 1)
       tma_store_4d(&mdkp, sm + L.ds1, 0, (int)h, (int)t0, (int)b);
       tma_store_4d(&mdkp, sm + L.ds1 + 8192, 64, (int)h, (int)t0, (int)b);
       bulk_commit();
-      if (more) ld_qk(nx, N, ln);  // q and k are consumed (round D and the dots above)
+    } else if (tid == 192 && more) {  // q and k are consumed (round D and the dots above): the
+      ld_qk(nx, N, ln);                // next ones from warp 6, which arms and drains them
     }
     // ---- gate gradients: column sums of the four row dots, Kt terms, state term; the
     //      next chunk's gates meanwhile (warps 2, 3)
