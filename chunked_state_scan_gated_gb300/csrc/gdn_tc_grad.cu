@@ -452,9 +452,11 @@ __global__ void __launch_bounds__(GT, 1)
       }
       mma_commit(bar_mma);
     }
-    {  // <S, dS> (same tile layout): warp partials into sMisc
+    {  // <S, dS> (same tile layout): warp partials into sMisc, from warps 6.. only (the
+       // round's issuers wait on the tensor core's queue and warp 5 issues the copies; their
+       // partials are zero)
       float acc = 0.f;
-      for (int q = tid; q < 2048; q += GT) {
+      for (int q = tid - 192; q >= 0 && q < 2048; q += GT - 192) {
         float x[8], y[8];
         ld_chunk(sm + L.s, q * 16, x);
         ld_chunk(sm + ((q < 1024) ? L.ds0 : L.ds1) + (q & 1023) * 16, 0, y);
