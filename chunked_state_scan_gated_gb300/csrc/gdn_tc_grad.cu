@@ -289,8 +289,9 @@ __global__ void __launch_bounds__(GT, 1)
   constexpr uint32_t kBytesB = 16384u + 8192u + 16384u;                    // U, T, V
 
   // Gates of a chunk in buffer dst (G, gamma, beta, Kt at 0, 64, 128, 192): G, the cumulative
-  // gate in log2 units, is the prologue's (copied in by the mover, on bar_g); warps 2 and 3
-  // (token = tid - 64) form gamma = 2^G, beta = sigmoid(b) and Kt = 2^(G_C - G) from it.
+  // gate in log2 units, is the prologue's (copied in by warp 6, on bar_g); warps 14 and 15
+  // (token = tid - 448: no MMA issue, no copies) form gamma = 2^G, beta = sigmoid(b) and
+  // Kt = 2^(G_C - G) from it.
   // Their b input is read early into a register so that its latency stays off the chunk's
   // critical path.
   struct GateIn {
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(GT, 1)
     bool live;
   };
   auto gate_in = [&](const Item& it) {
-    const int t = tid - 64;
+    const int t = tid - 448;
     int64_t Lg = ar.T;
     if (ar.valid_len) {
       Lg = ar.valid_len[it.b];
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(GT, 1)
     bulk_load(sGate + l * 256, ar.gl + it.im * 64, 256, bar_g + l);
   };
   auto gates = [&](const GateIn& gi, float* dst) {
-    const int t = tid - 64;
+    const int t = tid - 448;
     const float G = dst[t];
     dst[64 + t] = exp2f(G);
     dst[128 + t] = gi.live ? 1.f / (1.f + expf(-gi.xb)) : 0.f;
@@ -334,8 +335,8 @@ __global__ void __launch_bounds__(GT, 1)
     return w;
   };
   const int64_t w0 = next_live(blockIdx.x);
-  GateIn gnext{0.f, false};  // warps 2, 3: b of the next chunk's gates
-  if ((warp == 2 || warp == 3) && w0 < ar.NW) {
+  GateIn gnext{0.f, false};  // warps 14, 15: b of the next chunk's gates
+  if (warp >= 14 && w0 < ar.NW) {
     const Item it0 = item_of(w0);
     const GateIn g0 = gate_in(it0);
     if (!mbar_wait(bar_g, 0, ar.status, kStatusTimeout)) *s_abort = 1;
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(GT, 1)
     float* sBeta = sG + 128;
     float* sKt = sG + 192;
     __syncthreads();  // the previous chunk's scalars have been consumed, these gates written
-    if (tid == 192) {  // this chunk's G has landed (warps 2, 3 waited for it); the next G
+    if (tid == 192) {  // this chunk's G has landed (warps 14, 15 waited for it); the next G
       if (mbar_wait(bar_g + lc, bpar, ar.status, kStatusTimeout)) armed &= ~(1u << (6 + lc));
       if (more) ld_g(nx, ln);  // into the other buffer, free since the previous chunk ended
     }
@@ -513,7 +514,7 @@ __global__ void __launch_bounds__(GT, 1)
       }
       mma_commit(bar_mma);
     }
-    if (more && (warp == 2 || warp == 3)) gnext = gate_in(nx);  // lands before the tail
+    if (more && warp >= 14) gnext = gate_in(nx);  // lands before the tail
     {  // while round B runs: (diag(gamma) dO S^T)^T and q_t . (gamma_t S dO_t)
       const int f = fr;
       float pq[16];
@@ -725,7 +726,7 @@ __global__ void __launch_bounds__(GT, 1)
       ld_qk(nx, N, ln);                // next ones from warp 6, which arms and drains them
     }
     // ---- gate gradients: column sums of the four row dots, Kt terms, state term; the
-    //      next chunk's gates meanwhile (warps 2, 3)
+    //      next chunk's gates meanwhile (warps 14, 15)
     if (tid < 64) {
       const int t = tid;
       float rq = 0.f, rv = 0.f, rkw = 0.f, rkd = 0.f, zp = 0.f;
@@ -744,7 +745,7 @@ __global__ void __launch_bounds__(GT, 1)
       sFin[t] = d;
       sDB[t] = rv + gm * rkw + sDBh[t] + sDBh[64 + t] + sDBh[128 + t] + sDBh[192 + t];
       sRed[t] = (t < 63) ? s_t : 0.f;                       // reuse: Kt terms to sum into dG_C
-    } else if (more && (warp == 2 || warp == 3)) {
+    } else if (more && warp >= 14) {
       if (!mbar_wait(bar_g + ln, (uint32_t)(((k + 1) >> 1) & 1), ar.status, kStatusTimeout))
         *s_abort = 1;
       gates(gnext, sGate + ln * 256);
