@@ -212,9 +212,9 @@ E2E_COPY_STREAMS = 4  # side streams for the host-to-device copies of the end-to
 
 
 MEASURED_TRAFFIC = {
-    "bwd.grad_tc": {"T": 32768, "bytes_per_launch": 3068695552 + 837829632,
+    "bwd.grad_tc": {"T": 32768, "bytes_per_launch": 3022233856 + 837304320,
                     "src": "chunked_state_scan_gated_gb300/csrc/gdn_tc_grad.cu",
-                    "sha256": "fd7cac4bf946ce21e8a5d94bf83623dff22cfa26777f2c1d113fa8746c11464a"},
+                    "sha256": "b91b783c856d86caebb1645ef9b1beef4e804b3fbdd19921f705ec142da90e2d"},
 }
 
 
