@@ -139,7 +139,8 @@ __global__ void __launch_bounds__(PT, 2)
   uint64_t* bar_qk = (uint64_t*)(sm + P_SC + 1536);
   uint64_t* bar_v = bar_qk + 1;
   uint64_t* bar_mma = bar_qk + 2;
-  uint32_t* s_tmem = (uint32_t*)(bar_qk + 3);
+  uint64_t* bar_w = bar_qk + 3;  // the W product (the U product completes on bar_mma)
+  uint32_t* s_tmem = (uint32_t*)(bar_qk + 4);
   int* s_abort = (int*)(s_tmem + 1);
   float* sA = (float*)(sm + P_A);
   float* sT = (float*)(sm + P_T);
@@ -174,6 +175,7 @@ __global__ void __launch_bounds__(PT, 2)
     mbar_init(bar_qk, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_w, 1);
     fence_barrier_init();
     *s_abort = 0;
     mbar_arrive_expect_tx(bar_qk, 32768u);
@@ -330,24 +332,25 @@ __global__ void __launch_bounds__(PT, 2)
     bulk_commit();
   }
   // ---- [T_u; T_w] V -> cols [0,128) (U in rows 0..63); [T_u; T_w] K -> cols [128,256) (W in 64..127)
-  if (tid == 0) {
-    // the P image's staging (under the U image's) has been read before the product
-    // completes, and so before any thread stages W and U
-    if (ar.tim) bulk_wait_read_but1(); else bulk_wait_read();
+  if (tid == 0) {  // U first, on its own commit, so that its image is on its way sooner
     const uint32_t id = idesc_bf16(128, 128, 0, 1);
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint64_t a = (d16 + ((P_TA + ks * 32) >> 4));
-      mma_bf16(tmem, a, (d8192 + ((P_V + ks * 2048) >> 4)), id, ks > 0);
-      mma_bf16(tmem + 128, a, (d16384 + ((P_QK + 8192 + ks * 2048) >> 4)), id, ks > 0);
-    }
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem, (d16 + ((P_TA + ks * 32) >> 4)), (d8192 + ((P_V + ks * 2048) >> 4)), id,
+               ks > 0);
     mma_commit(bar_mma);
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem + 128, (d16 + ((P_TA + ks * 32) >> 4)),
+               (d16384 + ((P_QK + 8192 + ks * 2048) >> 4)), id, ks > 0);
+    mma_commit(bar_w);
   }
-  if (!mbar_wait(bar_mma, 1, ar.status, kStatusTimeout)) *s_abort = 1;
-  tc_fence_after();
-  {  // W and U images staged where q and k were (both products are done), then bulk-stored
+  {  // U (rows 0..63: quadrants 0, 1) staged where V was once its product is done, W (rows
+     // 64..127: quadrants 2, 3) where q and k were once its product is done; each half stores
+     // its image as soon as its 128 threads have staged it
     const bool isw = row >= 64;
     const int i = row & 63;
-    uint8_t* dst = sm + P_QK + (isw ? 0 : kImg);
+    if (!mbar_wait(isw ? bar_w : bar_mma, isw ? 0 : 1, ar.status, kStatusTimeout)) *s_abort = 1;
+    tc_fence_after();
+    uint8_t* dst = sm + (isw ? P_QK : P_V);
     const uint32_t src = tmem + lane_off + (isw ? 128 : 0) + 64 * half;
 #pragma unroll
     for (int q2 = 0; q2 < 2; ++q2) {
@@ -357,14 +360,17 @@ __global__ void __launch_bounds__(PT, 2)
       for (int cc = 0; cc < 4; ++cc)
         *reinterpret_cast<uint4*>(dst + img_chunk(i, half * 8 + q2 * 4 + cc)) = pack8(&v[cc * 8]);
     }
-  }
-  fence_proxy_async();
-  __syncthreads();
-  if (tid == 0) {
-    bulk_store(ar.wim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_QK, kImg);
-    bulk_store(ar.uim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_QK + kImg, kImg);
-    bulk_commit();
-    bulk_wait_read();  // shared memory is released when the CTA exits
+    fence_proxy_async();
+    if (isw) asm volatile("bar.sync 3, 128;" ::: "memory");  // warps 2, 3, 6, 7
+    else asm volatile("bar.sync 2, 128;" ::: "memory");      // warps 0, 1, 4, 5
+    if (tid == 0) {
+      bulk_store(ar.uim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_V, kImg);
+      bulk_commit();
+    } else if (tid == 64) {
+      bulk_store(ar.wim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_QK, kImg);
+      bulk_commit();
+    }
+    if (tid == 0 || tid == 64) bulk_wait_read();  // shared memory is released when the CTA exits
   }
 done:
   if (*s_abort && tid == 0) {  // let the loads still in flight land before the CTA exits
@@ -372,6 +378,7 @@ done:
     mbar_wait(bar_v, 0, nullptr, 0);
     bulk_wait_read();  // and the stores issued so far read their staging
   }
+  if (*s_abort && tid == 64) bulk_wait_read();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
