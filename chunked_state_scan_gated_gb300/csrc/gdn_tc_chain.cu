@@ -120,6 +120,7 @@ struct PrepArgs {
   uint8_t* tim;  // [B][H][NC] images of T = (I + A)^-1 (64 x 64), or null
   float* gl;     // [B][H][NC][64] cumulative gate in log2 units
   int* status;
+  int64_t NW;    // B * H * NC chunks of work
 };
 
 __global__ void __launch_bounds__(PT, 2)
@@ -149,43 +150,78 @@ __global__ void __launch_bounds__(PT, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
   const int row = quad * 32 + lane;  // TMEM lane of this thread
-  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int64_t hq = h / ar.r, bh = b * ar.H + h;
-  const int64_t t0 = c * 64;
-  const int64_t L = clamp_len(ar.valid_len, b, ar.T, ar.status, tid == 0 && c == 0 && h == 0);
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  if (t0 >= L) return;  // a chunk of padding only: every consumer skips it
-
-  // Gate inputs (warps 2, 3: token tid - 64; a, b, dt_bias, A_log), read before anything
-  // else: with the q, k, v copies they are the longest wait of the CTA's start.  Only loaded
-  // here: their first use, after the set-up barrier, is where the threads wait for them.
-  const int tg = tid - 64;
+  const int tg = tid - 64;  // gate warps 2, 3: token tg
   const bool gate_warp = warp == 2 || warp == 3;
+
+  // Persistent: CTA i takes chunks w = i, i + gridDim.x, ... (w: c = w % NC, h = (w / NC) % H,
+  // b = w / (NC H); 32-bit index arithmetic, the host keeps NW below 2^31), skipping chunks of
+  // padding only (every consumer skips them).  The next chunk's q, k copies go out as soon as
+  // the current chunk's last product has read k, its gate inputs are read a chunk ahead, and
+  // its v copy goes out before the current chunk's solve.
+  struct Item {
+    int64_t c, h, b;
+  };
+  auto item_of = [&](int64_t w) {
+    const uint32_t uw = (uint32_t)w, q1 = uw / (uint32_t)ar.NC;
+    return Item{(int64_t)(uw - q1 * (uint32_t)ar.NC), (int64_t)(q1 % (uint32_t)ar.H),
+                (int64_t)(q1 / (uint32_t)ar.H)};
+  };
+  auto len_of = [&](int64_t bb, bool report) { return clamp_len(ar.valid_len, bb, ar.T, ar.status, report); };
+  auto next_live = [&](int64_t w) {
+    for (; w < ar.NW; w += gridDim.x) {
+      if (!ar.valid_len) break;
+      const Item it = item_of(w);
+      if (it.c * 64 < len_of(it.b, false)) break;
+    }
+    return w;
+  };
+  auto issue_qk = [&](const Item& it) {
+    mbar_arrive_expect_tx(bar_qk, 32768u);
+    for (int at = 0; at < 2; ++at) {
+      tma_load_4d(sm + P_QK + at * 16384, &mq, at * 64, (int)(it.h / ar.r), (int)(it.c * 64),
+                  (int)it.b, bar_qk);
+      tma_load_4d(sm + P_QK + at * 16384 + 8192, &mk, at * 64, (int)(it.h / ar.r),
+                  (int)(it.c * 64), (int)it.b, bar_qk);
+    }
+  };
+  auto issue_v = [&](const Item& it) {
+    mbar_arrive_expect_tx(bar_v, 16384u);
+    for (int at = 0; at < 2; ++at)
+      tma_load_4d(sm + P_V + at * 8192, &mv, at * 64, (int)it.h, (int)(it.c * 64), (int)it.b,
+                  bar_v);
+  };
+  // Gate inputs (warps 2, 3: a, b, dt_bias, A_log of token tg), kept as loaded: their first
+  // use, in the chunk's gate step, is where the threads wait for them.
   __nv_bfloat16 ra = __float2bfloat16_rn(0.f), rb = ra;
   float dtb = 0.f, alog = 0.f;
-  const bool glive = gate_warp && t0 + tg < L;
-  if (glive) {
-    const int64_t gi = (b * ar.Ts + t0 + tg) * ar.H + h;
-    ra = ar.a[gi];
-    rb = ar.b[gi];
-    dtb = ar.dt_bias[h];
-    alog = ar.A_log[h];
-  }
-  if (tid == 0) {  // the barriers are this thread's own: the copies go out at once
+  bool glive = false;
+  auto gate_load = [&](const Item& it) {
+    glive = gate_warp && it.c * 64 + tg < len_of(it.b, false);
+    if (glive) {
+      const int64_t gi = (it.b * ar.Ts + it.c * 64 + tg) * ar.H + it.h;
+      ra = ar.a[gi];
+      rb = ar.b[gi];
+      dtb = ar.dt_bias[it.h];
+      alog = ar.A_log[it.h];
+    }
+  };
+  uint32_t pend = 0;  // tid 0: 1 = a q/k copy, 2 = a v copy in flight (drained on an abort)
+
+  const int64_t w0 = next_live(blockIdx.x);
+  if (w0 < ar.NW) gate_load(item_of(w0));
+  if (tid == 0) {  // the barriers are this thread's own: the first copies go out at once
     mbar_init(bar_qk, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
     mbar_init(bar_w, 1);
     fence_barrier_init();
     *s_abort = 0;
-    mbar_arrive_expect_tx(bar_qk, 32768u);
-    for (int at = 0; at < 2; ++at) {
-      tma_load_4d(sm + P_QK + at * 16384, &mq, at * 64, (int)hq, (int)t0, (int)b, bar_qk);
-      tma_load_4d(sm + P_QK + at * 16384 + 8192, &mk, at * 64, (int)hq, (int)t0, (int)b, bar_qk);
+    if (w0 < ar.NW) {
+      issue_qk(item_of(w0));
+      issue_v(item_of(w0));
+      pend = 3;
     }
-    mbar_arrive_expect_tx(bar_v, 16384u);
-    for (int at = 0; at < 2; ++at)
-      tma_load_4d(sm + P_V + at * 8192, &mv, at * 64, (int)h, (int)t0, (int)b, bar_v);
   }
   if (warp == 0) tmem_alloc(s_tmem, 256);
   for (int e = tid; e < 1024; e += PT)  // [T_u; T_w]: the solve writes only the lower triangle
@@ -194,17 +230,26 @@ __global__ void __launch_bounds__(PT, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  for (int64_t w = w0, kk = 0; w < ar.NW; ++kk) {
+  const Item cur = item_of(w);
+  const int64_t wn = next_live(w + gridDim.x);
+  const int64_t c = cur.c, h = cur.h, b = cur.b;
+  const int64_t hq = h / ar.r, bh = b * ar.H + h;
+  (void)len_of(b, tid == 0 && c == 0 && h == 0);  // (reports a clamped valid_len once)
+  const uint32_t par = (uint32_t)(kk & 1);
   // ---- [Q; K] [Q; K]^T -> cols [0, 128): row norms on the diagonal, Q K^T and K K^T in cols
   //      64..127, issued as soon as q and k land; the gates are formed meanwhile
   if (tid == 0) {
-    if (!mbar_wait(bar_qk, 0, ar.status, kStatusTimeout)) {
+    if (*s_abort) {  // (the previous chunk gave up before issuing this chunk's copies)
+    } else if (!mbar_wait(bar_qk, par, ar.status, kStatusTimeout)) {
       *s_abort = 1;
     } else {
+      pend &= ~1u;
       tc_fence_after();
       const uint32_t id = idesc_bf16(128, 128, 0, 0);
       for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t at = ks >> 2, kk = ks & 3;
-        const uint64_t d = (d16 + ((P_QK + at * 16384 + kk * 32) >> 4));
+        const uint32_t at = ks >> 2, k4 = ks & 3;
+        const uint64_t d = (d16 + ((P_QK + at * 16384 + k4 * 32) >> 4));
         mma_bf16(tmem, d, d, id, ks > 0);
       }
       mma_commit(bar_mma);
@@ -231,6 +276,7 @@ __global__ void __launch_bounds__(PT, 2)
     sBeta[tg] = be;
     sGam[tg] = exp2f(v);
     ar.gl[(bh * ar.NC + c) * 64 + tg] = v;
+    if (wn < ar.NW) gate_load(item_of(wn));  // the next chunk's, read a chunk ahead
   }
   tc_fence_before();
   __syncthreads();
@@ -297,12 +343,18 @@ __global__ void __launch_bounds__(PT, 2)
       }
     }
   }
+  if (tid == 64) bulk_wait_read();  // the previous chunk's W image (over sT) has been read
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
-  if (tid == 0) {  // the P image (group 1 of this thread's bulk stores)
+  if (tid == 0) {  // the P image, then this chunk's v (the previous U image has been read)
     bulk_store(ar.pim + (bh * ar.NC + c) * (int64_t)kImgP, sm + P_PST, kImgP);
     bulk_commit();
+    if (kk > 0) {
+      bulk_wait_read_but1();
+      issue_v(cur);
+      pend |= 2u;
+    }
   }
   // T = (I + A)^-1, with [T_u; T_w] = [T diag(beta); T diag(beta gamma rk)] (bf16, W is
   // formed from raw k) written as each entry of T is final
@@ -321,7 +373,8 @@ __global__ void __launch_bounds__(PT, 2)
       *reinterpret_cast<uint4*>(dst + kmaj_chunk(i, cc)) = pack8(x);
     }
   }
-  if (!mbar_wait(bar_v, 0, ar.status, kStatusTimeout)) *s_abort = 1;
+  if (!mbar_wait(bar_v, par, ar.status, kStatusTimeout)) *s_abort = 1;
+  if (tid == 0) pend &= ~2u;
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
@@ -344,13 +397,13 @@ __global__ void __launch_bounds__(PT, 2)
     mma_commit(bar_w);
   }
   {  // U (rows 0..63: quadrants 0, 1) staged where V was once its product is done, W (rows
-     // 64..127: quadrants 2, 3) where q and k were once its product is done; each half stores
-     // its image as soon as its 128 threads have staged it
+     // 64..127: quadrants 2, 3) over the solve's T tile (free since the T image was staged);
+     // each half stores its image as soon as its 128 threads have staged it
     const bool isw = row >= 64;
     const int i = row & 63;
-    if (!mbar_wait(isw ? bar_w : bar_mma, isw ? 0 : 1, ar.status, kStatusTimeout)) *s_abort = 1;
+    if (!mbar_wait(isw ? bar_w : bar_mma, isw ? par : 1, ar.status, kStatusTimeout)) *s_abort = 1;
     tc_fence_after();
-    uint8_t* dst = sm + (isw ? P_QK : P_V);
+    uint8_t* dst = sm + (isw ? P_T : P_V);
     const uint32_t src = tmem + lane_off + (isw ? 128 : 0) + 64 * half;
 #pragma unroll
     for (int q2 = 0; q2 < 2; ++q2) {
@@ -361,21 +414,39 @@ __global__ void __launch_bounds__(PT, 2)
         *reinterpret_cast<uint4*>(dst + img_chunk(i, half * 8 + q2 * 4 + cc)) = pack8(&v[cc * 8]);
     }
     fence_proxy_async();
+    tc_fence_before();
     if (isw) asm volatile("bar.sync 3, 128;" ::: "memory");  // warps 2, 3, 6, 7
     else asm volatile("bar.sync 2, 128;" ::: "memory");      // warps 0, 1, 4, 5
     if (tid == 0) {
       bulk_store(ar.uim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_V, kImg);
       bulk_commit();
+      // the next chunk's q and k go where this chunk's were, once the W product has read k
+      // and the P and T images have read their staging (all but the U store just issued)
+      if (!mbar_wait(bar_w, par, ar.status, kStatusTimeout)) *s_abort = 1;
+      bulk_wait_read_but1();
+      if (wn < ar.NW && !*s_abort) {
+        issue_qk(item_of(wn));
+        pend |= 1u;
+      }
     } else if (tid == 64) {
-      bulk_store(ar.wim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_QK, kImg);
+      bulk_store(ar.wim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_T, kImg);
       bulk_commit();
     }
-    if (tid == 0 || tid == 64) bulk_wait_read();  // shared memory is released when the CTA exits
   }
+  w = wn;
+  }  // chunk loop
+  if (tid == 0 || tid == 64) bulk_wait_read();  // shared memory is released when the CTA exits
+
 done:
-  if (*s_abort && tid == 0) {  // let the loads still in flight land before the CTA exits
-    mbar_wait(bar_qk, 0, nullptr, 0);
-    mbar_wait(bar_v, 0, nullptr, 0);
+  if (*s_abort && tid == 0) {  // let the copies still in flight land before the CTA exits
+    if (pend & 1u) {
+      mbar_wait(bar_qk, 0, nullptr, 0);
+      mbar_wait(bar_qk, 1, nullptr, 0);
+    }
+    if (pend & 2u) {
+      mbar_wait(bar_v, 0, nullptr, 0);
+      mbar_wait(bar_v, 1, nullptr, 0);
+    }
     bulk_wait_read();  // and the stores issued so far read their staging
   }
   if (*s_abort && tid == 64) bulk_wait_read();
@@ -1160,10 +1231,12 @@ cudaError_t launch_prep_tc(const Prob& pr, const Inputs& in, const WS& ws, cudaS
   ar.rqk = ws.rqk; ar.wim = (uint8_t*)ws.wim; ar.uim = (uint8_t*)ws.uim;
   ar.pim = (uint8_t*)ws.pim; ar.tim = (uint8_t*)ws.tim; ar.gl = ws.gl;
   ar.status = ws.status;
+  ar.NW = pr.B * pr.H * pr.NC;
+  if (ar.NW + 1024 >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // 32-bit chunk indices
   cudaError_t e = smem_attr(k_prep_tc, P_SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)pr.NC, (unsigned)pr.H, (unsigned)pr.B);
-  k_prep_tc<<<grid, PT, P_SMEM, st>>>(mq, mk, mv, ar);
+  const int64_t nblk = ar.NW < 2 * (int64_t)device_sms() ? ar.NW : 2 * (int64_t)device_sms();
+  k_prep_tc<<<(unsigned)nblk, PT, P_SMEM, st>>>(mq, mk, mv, ar);  // two CTAs per SM, persistent
   return cudaGetLastError();
 }
 
