@@ -67,8 +67,9 @@ __device__ __forceinline__ int64_t clamp_len(const int32_t* valid_len, int64_t b
 }
 
 // ============================================================================
-// k_prep_tc: grid (NC, H, B), 256 threads.  Warp w reads TMEM lane quadrant
-// w & 3 (tile row `row`) and handles column half w >> 2 of that row.
+// k_prep_tc: persistent, min(B H NC, 2 SMs) CTAs of 256 threads (two per SM), each
+// walking chunks.  Warp w reads TMEM lane quadrant w & 3 (tile row `row`) and handles
+// column half w >> 2 of that row.
 //
 // The q and k row norms come from the diagonal of one product [Q;K][Q;K]^T of
 // the raw tiles, so neither tile is rewritten: every later use of q_hat = rq q
