@@ -360,8 +360,20 @@ __global__ void __launch_bounds__(PT, 2)
   // T = (I + A)^-1, with [T_u; T_w] = [T diag(beta); T diag(beta gamma rk)] (bf16, W is
   // formed from raw k) written as each entry of T is final
   solve_unit_lower64_mma(sA, sT, sY, LDA, TaEmit{sm + P_TA, sBeta, sCw});
+  // [T_u; T_w] is final: the W product (it needs only that tile and k) goes out at once, so
+  // that k's slot, and with it the next chunk's q/k copies, free up as early as possible
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    const uint32_t id = idesc_bf16(128, 128, 0, 1);
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem + 128, (d16 + ((P_TA + ks * 32) >> 4)),
+               (d16384 + ((P_QK + 8192 + ks * 2048) >> 4)), id, ks > 0);
+    mma_commit(bar_w);
+  }
   if (ar.tim) {  // T for the backward, bf16 image, staged where A was (the solve is done)
-    __syncthreads();
     uint8_t* dst = sm + P_A;
     for (int e = tid; e < 512; e += PT) {
       const int i = e >> 3, cc = e & 7;
@@ -381,21 +393,26 @@ __global__ void __launch_bounds__(PT, 2)
   __syncthreads();
   tc_fence_after();
   if (*s_abort) goto done;
-  if (tid == 0 && ar.tim) {  // the T image (group 2)
-    bulk_store(ar.tim + (bh * ar.NC + c) * (int64_t)kImgP, sm + P_A, kImgP);
-    bulk_commit();
-  }
-  // ---- [T_u; T_w] V -> cols [0,128) (U in rows 0..63); [T_u; T_w] K -> cols [128,256) (W in 64..127)
-  if (tid == 0) {  // U first, on its own commit, so that its image is on its way sooner
+  // ---- [T_u; T_w] V -> cols [0,128) (U in rows 0..63); [T_u; T_w] K -> cols [128,256) (W in
+  //      64..127, issued above)
+  if (tid == 0) {
+    if (ar.tim) {  // the T image (group 2)
+      bulk_store(ar.tim + (bh * ar.NC + c) * (int64_t)kImgP, sm + P_A, kImgP);
+      bulk_commit();
+    }
+    // the next chunk's q and k go where this chunk's are once the W product has read k and
+    // the P image has read its staging (every group but the T image's)
+    if (!mbar_wait(bar_w, par, ar.status, kStatusTimeout)) *s_abort = 1;
+    if (ar.tim) bulk_wait_read_but1(); else bulk_wait_read();
+    if (wn < ar.NW && !*s_abort) {
+      issue_qk(item_of(wn));
+      pend |= 1u;
+    }
     const uint32_t id = idesc_bf16(128, 128, 0, 1);
     for (int ks = 0; ks < 4; ++ks)
       mma_bf16(tmem, (d16 + ((P_TA + ks * 32) >> 4)), (d8192 + ((P_V + ks * 2048) >> 4)), id,
                ks > 0);
     mma_commit(bar_mma);
-    for (int ks = 0; ks < 4; ++ks)
-      mma_bf16(tmem + 128, (d16 + ((P_TA + ks * 32) >> 4)),
-               (d16384 + ((P_QK + 8192 + ks * 2048) >> 4)), id, ks > 0);
-    mma_commit(bar_w);
   }
   {  // U (rows 0..63: quadrants 0, 1) staged where V was once its product is done, W (rows
      // 64..127: quadrants 2, 3) over the solve's T tile (free since the T image was staged);
@@ -421,14 +438,6 @@ __global__ void __launch_bounds__(PT, 2)
     if (tid == 0) {
       bulk_store(ar.uim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_V, kImg);
       bulk_commit();
-      // the next chunk's q and k go where this chunk's were, once the W product has read k
-      // and the P and T images have read their staging (all but the U store just issued)
-      if (!mbar_wait(bar_w, par, ar.status, kStatusTimeout)) *s_abort = 1;
-      bulk_wait_read_but1();
-      if (wn < ar.NW && !*s_abort) {
-        issue_qk(item_of(wn));
-        pend |= 1u;
-      }
     } else if (tid == 64) {
       bulk_store(ar.wim + (bh * ar.NC + c) * (int64_t)kImg, sm + P_T, kImg);
       bulk_commit();
