@@ -39,7 +39,7 @@ EXPORTS = (
     "gdn_apply_state_bwd", "gdn_check_device_status", "gdn_kernel_info", "gdn_fwd_kernel",
     "gdn_bwd_kernel", "gdn_fwd_noalloc", "gdn_noalloc_check_device_status", "gdn_ctx_size",
     "gdn_fwd_ctx", "gdn_bwd_ctx",
-    "gdn_fwd_ctx_kernel", "gdn_bwd_ctx_kernel", "gdn_conv_silu_fwd",
+    "gdn_fwd_ctx_kernel", "gdn_bwd_ctx_kernel", "gdn_conv_silu_fwd", "gdn_fwd_conv",
     "gdn_conv_silu_bwd_workspace_size", "gdn_conv_silu_bwd", "gdn_rmsnorm_gated_fwd",
     "gdn_rmsnorm_gated_bwd_workspace_size", "gdn_rmsnorm_gated_bwd",
     "gdn_varlen_workspace_size", "gdn_fwd_varlen", "gdn_bwd_varlen",
@@ -68,6 +68,14 @@ class ConvProblem(ctypes.Structure):
 
     _fields_ = [("dtype", ctypes.c_int32), ("K", ctypes.c_int32), ("B", ctypes.c_int64),
                 ("T", ctypes.c_int64), ("C", ctypes.c_int64), ("T_stride", ctypes.c_int64)]
+
+
+class ConvQkv(ctypes.Structure):
+    """Mirror of ``gdn_conv_qkv`` (include/gdn.h)."""
+
+    _fields_ = [("K", ctypes.c_int32), ("x", ctypes.c_void_p * 3), ("w", ctypes.c_void_p * 3),
+                ("bias", ctypes.c_void_p * 3), ("halo", ctypes.c_void_p * 3),
+                ("y", ctypes.c_void_p * 3)]
 
 
 class RmsNormProblem(ctypes.Structure):
@@ -137,6 +145,8 @@ def load_library(path: str | None = None):
             "gdn_bwd_ctx_kernel": ([_PP, ctypes.c_int32] + [_VP] * 8 + [ctypes.c_size_t]
                                    + [_VP] * 10 + [ctypes.c_size_t, _VP], ctypes.c_int),
             "gdn_conv_silu_fwd": ([_CPP] + [_VP] * 6, ctypes.c_int),
+            "gdn_fwd_conv": ([_PP, ctypes.POINTER(ConvQkv)] + [_VP] * 8
+                             + [_VP, ctypes.c_size_t, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
             "gdn_conv_silu_bwd_workspace_size": ([_CPP, ctypes.POINTER(ctypes.c_size_t)],
                                                  ctypes.c_int),
             "gdn_conv_silu_bwd": ([_CPP] + [_VP] * 10 + [ctypes.c_size_t, _VP], ctypes.c_int),
@@ -610,6 +620,42 @@ def gdn_conv_silu_fwd(x, w, bias=None, halo=None, *, y=None, stream=None, proble
     _check("gdn_conv_silu_fwd", load_library().gdn_conv_silu_fwd(
         ctypes.byref(p), _ptr(x), _ptr(w), _ptr(bias), _ptr(halo), _ptr(y), _stream(stream)))
     return y
+
+
+def gdn_fwd_conv(x, w, a, b, A_log, dt_bias, h0=None, valid_len=None, *,
+                 bias=(None, None, None), halo=(None, None, None), y=None, with_ctx=True,
+                 ctx=None, segments=0, l2norm=True, eps=1e-6, scale=0.0, o=None, hT=None,
+                 want_hT=True, ws=None, stream=None, problem=None):
+    """The Conv1D + SiLU of x = (x_q, x_k, x_v) (layouts of q, k, v) with taps
+    w = (w_q, w_k, w_v) [channels, K] fused into the forward (gdn_fwd_ctx when with_ctx,
+    else gdn_fwd).  Returns (o, hT, ctx or None, (q, k, v)) with q, k, v the activated
+    inputs the backward takes."""
+    xq, xk, xv = x
+    p = problem or make_problem(xq, xv, segments=segments, l2norm=l2norm, eps=eps, scale=scale)
+    B, T, H, dv = xv.shape
+    y = tuple(y) if y is not None else tuple(torch.empty_like(t) for t in x)
+    cv = ConvQkv()
+    cv.K = int(w[0].shape[1])
+    for i in range(3):
+        cv.x[i] = _ptr(x[i])
+        cv.w[i] = _ptr(w[i])
+        cv.bias[i] = _ptr(bias[i])
+        cv.halo[i] = _ptr(halo[i])
+        cv.y[i] = _ptr(y[i])
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=xq.dtype, device=xq.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, xq.shape[3], dv), dtype=torch.float32, device=xq.device)
+    if with_ctx:
+        ctx = ctx if ctx is not None else ctx_buffer(p, xq.device)
+    else:
+        ctx = None
+    ws = _ws(p, GDN_OP_FWD_CTX if with_ctx else GDN_OP_FWD, ws, xq.device)
+    _check("gdn_fwd_conv", load_library().gdn_fwd_conv(
+        ctypes.byref(p), ctypes.byref(cv), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+        _ptr(h0), _ptr(valid_len), _ptr(o), _ptr(hT), _ptr(ctx),
+        ctx.numel() if ctx is not None else 0, _ptr(ws), ws.numel(), _stream(stream)))
+    return o, hT, ctx, y
 
 
 def gdn_conv_silu_bwd(x, w, bias, halo, dy, *, want_dbias=True, want_dhalo=True, dx=None,

@@ -592,7 +592,8 @@ static gdn_status fwd_impl(const gdn_problem* p, const void* q, const void* k, c
                            const float* dt_bias, const float* h0, const int32_t* valid_len,
                            void* o, float* hT, void* workspace, size_t workspace_bytes,
                            void* stream, Sched& sc, void* ctx = nullptr,
-                           size_t ctx_size = 0, bool with_ctx = false) {
+                           size_t ctx_size = 0, bool with_ctx = false,
+                           const gdn_conv_qkv* conv = nullptr) {
   Prob pr;
   gdn_status s = resolve_op(p, GDN_OP_FWD, &pr);
   if (s != GDN_OK) return s;
@@ -600,6 +601,27 @@ static gdn_status fwd_impl(const gdn_problem* p, const void* q, const void* k, c
   if (!inputs_ok(pr, in, true, true)) return GDN_ERR_INVALID_ARG;
   if (!ok_ptr(o, pr.B * pr.T * pr.H * pr.dv) || !ok_opt(h0) || !ok_opt(hT))
     return GDN_ERR_INVALID_ARG;
+  ConvIn cv;  // the Conv1D in front (q, k, v are its outputs y)
+  if (conv) {
+    const int64_t C[3] = {pr.Hqk * pr.dk, pr.Hqk * pr.dk, pr.H * pr.dv};
+    const int64_t es = pr.dtype == GDN_BF16 ? 2 : 4;
+    for (int i = 0; i < 3; ++i) {
+      const int64_t n = pr.B * pr.T * C[i], span = pr.B * pr.Ts * C[i] * es;
+      if (!ok_ptr(conv->x[i], n) || !ok_ptr(conv->w[i], C[i]) || !ok_opt(conv->bias[i]) ||
+          !ok_opt(conv->halo[i]))
+        return GDN_ERR_INVALID_ARG;
+      const uintptr_t x0 = (uintptr_t)conv->x[i], y0 = (uintptr_t)conv->y[i];
+      if (n > 0 && x0 < y0 + (uintptr_t)span && y0 < x0 + (uintptr_t)span)
+        return GDN_ERR_INVALID_ARG;  // y overlaps its x
+      cv.x[i] = conv->x[i];
+      cv.w[i] = conv->w[i];
+      cv.bias[i] = conv->bias[i];
+      cv.halo[i] = conv->K > 1 ? conv->halo[i] : nullptr;
+      cv.y[i] = conv->y[i];
+    }
+    if (conv->K < 1 || conv->K > 4) return GDN_ERR_UNSUPPORTED;
+    cv.K = conv->K;
+  }
   Ctx cx;
   if (with_ctx) {
     if (ctx == nullptr || !aligned16(ctx) || ctx_size < ctx_bytes(pr)) return GDN_ERR_INVALID_ARG;
@@ -611,7 +633,30 @@ static gdn_status fwd_impl(const gdn_problem* p, const void* q, const void* k, c
                    &pr, &ws)) != GDN_OK)
     return s;
   if (with_ctx) use_ctx_prologue(pr, cx, &ws);
-  return run_forward(pr, in, h0, o, hT, ws, st, sc, with_ctx ? &cx : nullptr);
+  if (conv && tc_path(pr)) {
+    in.conv = &cv;  // the chunk prologue convolves x itself and writes y
+  } else if (conv) {  // other paths: the stand-alone Conv1D, then the forward
+    for (int i = 0; i < 3; ++i) {
+      gdn_conv_problem cp;
+      cp.dtype = pr.dtype;
+      cp.K = cv.K;
+      cp.B = pr.B;
+      cp.T = pr.T;
+      cp.C = i < 2 ? pr.Hqk * pr.dk : pr.H * pr.dv;
+      cp.T_stride = pr.Ts;
+      if ((s = gdn_conv_silu_fwd(&cp, cv.x[i], cv.w[i], cv.bias[i], cv.halo[i], cv.y[i],
+                                 stream)) != GDN_OK)
+        return s;
+    }
+  }
+  s = run_forward(pr, in, h0, o, hT, ws, st, sc, with_ctx ? &cx : nullptr);
+  if (s == GDN_OK && conv && valid_len) {  // y of the chunks of padding only: zero
+    const int64_t es = pr.dtype == GDN_BF16 ? 2 : 4;
+    for (int i = 0; i < 3 && s == GDN_OK; ++i)
+      s = cuda_status(launch_pad_tail_zero(pr, valid_len, cv.y[i],
+                                           (i < 2 ? pr.Hqk * pr.dk : pr.H * pr.dv) * es, st));
+  }
+  return s;
 }
 
 static gdn_status bwd_impl(const gdn_problem* p, const void* q, const void* k, const void* v,
@@ -710,6 +755,17 @@ gdn_status gdn_bwd_ctx(const gdn_problem* p, const void* q, const void* k, const
   Sched sc;
   return bwd_impl(p, q, k, v, a, b, A_log, dt_bias, nullptr, valid_len, dO, dHT, dq, dk, dv, dg,
                   dbeta, dH0, workspace, workspace_bytes, stream, sc, ctx, ctx_bytes_, true);
+}
+
+gdn_status gdn_fwd_conv(const gdn_problem* p, const gdn_conv_qkv* conv, const void* a,
+                        const void* b, const float* A_log, const float* dt_bias, const float* h0,
+                        const int32_t* valid_len, void* o, float* hT, void* ctx, size_t ctx_bytes_,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (!conv) return GDN_ERR_INVALID_ARG;
+  Sched sc;
+  return fwd_impl(p, conv->y[0], conv->y[1], conv->y[2], a, b, A_log, dt_bias, h0, valid_len, o,
+                  hT, workspace, workspace_bytes, stream, sc, ctx, ctx_bytes_, ctx != nullptr,
+                  conv);
 }
 
 gdn_status gdn_fwd_ctx_kernel(const gdn_problem* p, int32_t index, const void* q, const void* k,

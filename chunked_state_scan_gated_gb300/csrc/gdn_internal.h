@@ -58,11 +58,24 @@ struct WS {
 };
 
 // Raw inputs of a call (device pointers; type of q..dO is Prob::dtype).
+// Causal depthwise Conv1D + SiLU in front of the core (index 0: q, 1: k, 2: v): the
+// tensor-core prologue loads x[i] (layout of q, k, v), convolves it in shared memory and
+// writes y[i] = SiLU(conv(x[i])), which every later kernel reads as q, k, v.
+struct ConvIn {
+  int K;                 // taps, 1..4
+  const void* x[3];      // pre-conv activations
+  const float* w[3];     // [channels][K]
+  const float* bias[3];  // [channels] or null
+  const void* halo[3];   // [B][K-1][channels] or null (zeros)
+  void* y[3];            // activated q, k, v (the Inputs' q, k, v point here)
+};
+
 struct Inputs {
   const void *q, *k, *v, *a, *b;
   const float *A_log, *dt_bias;
   const int32_t* valid_len;
   const void* dO;
+  const ConvIn* conv = nullptr;  // set: the prologue runs the Conv1D + SiLU (forward only)
 };
 
 gdn_status resolve(const gdn_problem* p, Prob* out);

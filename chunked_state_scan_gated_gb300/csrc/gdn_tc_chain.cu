@@ -30,10 +30,13 @@
 
 #include "gdn_internal.h"
 #include "gdn_tc_common.cuh"
+#include "gdn_vec.cuh"
 
 namespace gdn {
 
 bool tc_make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t Ts, int64_t heads);
+bool tc_make_map_rows(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t Ts,
+                      int64_t heads, int rows);
 
 namespace {
 
@@ -86,6 +89,10 @@ constexpr uint32_t P_T = P_A + 64 * LDA * 4;   // fp32 T [64][LDA]
 constexpr uint32_t P_Y = P_T + 64 * LDA * 4;   // solve scratch, 8 warps x 128 floats
 constexpr uint32_t P_SC = P_Y + 1024 * 4;      // gates, row factors, barriers
 constexpr uint32_t P_SMEM = P_SC + 1536 + 64 + 1024;
+// With the Conv1D in front: the 3 tokens before the chunk of x_q, x_k, x_v (3 x 256 bytes
+// each, unswizzled), read by the convolution of the chunk's first rows.
+constexpr uint32_t P_LB = (P_SC + 1536 + 64 + 127) / 128 * 128;
+constexpr uint32_t P_SMEM_CONV = P_LB + 3 * 768 + 1024;
 
 // Writes T diag(beta) (rows 0..63) and T diag(beta gamma rk) (rows 64..127) of the
 // 128 x 64 K-major bf16 tile [T_u; T_w] as the solve finalises each entry of T.
@@ -122,11 +129,97 @@ struct PrepArgs {
   float* gl;     // [B][H][NC][64] cumulative gate in log2 units
   int* status;
   int64_t NW;    // B * H * NC chunks of work
+  // Conv1D + SiLU in front (index 0: q, 1: k, 2: v); the tiles are loaded from x
+  int convK;                       // taps, 1..4
+  const float* cw[3];              // [channels][convK]
+  const float* cb[3];              // [channels] or null
+  const __nv_bfloat16* chalo[3];   // [B][convK - 1][channels] or null (zeros)
+  __nv_bfloat16* cy[3];            // the activated q, k, v, written for the later kernels
 };
 
+// Causal depthwise Conv1D + SiLU of one 8-channel column (16-byte chunk `ccs` of a
+// 128-byte-swizzled 64-row atom) over rows u0 .. u0 + n - 1 of the tile, in place: row u
+// (token t0 + u) becomes SiLU(bias + sum of the taps over x~[t - K + 1 .. t]), rounded to
+// bf16, with the same operation order as the stand-alone Conv1D pass, so both give the
+// same bits.  back[i] holds the inputs of token u0 - 3 + i (bf16, 8 channels).  Rows past
+// the end of the row (t0 + u >= T) become zero, as a copy of the activated tensor would
+// read there; the others also go to y + u * ystride when y is set.  Channels ch .. ch + 7
+// of w [C][K] and bias.  Four channels at a time.
+__device__ __forceinline__ void conv_column(uint8_t* atom, int ccs, int u0, int n,
+                                            const uint4 (&back)[3], const float* __restrict__ w,
+                                            const float* __restrict__ bias, int K, int64_t ch,
+                                            int64_t t0, int64_t T, __nv_bfloat16* y,
+                                            int64_t ystride) {
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    float wv[4][4], bv[4], xw[3][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t cj = ch + 4 * hh + j;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) wv[j][i] = (i >= 4 - K) ? w[cj * K + i - (4 - K)] : 0.f;
+      bv[j] = bias ? bias[cj] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const uint32_t lo = hh ? back[i].z : back[i].x, hi = hh ? back[i].w : back[i].y;
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo));
+      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
+      xw[i][0] = a.x; xw[i][1] = a.y; xw[i][2] = c.x; xw[i][3] = c.y;
+    }
+    for (int u = u0; u < u0 + n; ++u) {
+      const uint32_t off = kmaj_chunk(u, ccs) + 8 * hh;
+      const uint2 raw = *reinterpret_cast<const uint2*>(atom + off);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+      const float xc[4] = {a.x, a.y, c.x, c.y};
+      float o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float acc = bv[j];
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+          if (i >= 4 - K) acc = fmaf(wv[j][i], xw[i][j], acc);
+        acc = fmaf(wv[j][3], xc[j], acc);
+        o[j] = (t0 + u < T) ? acc * vec::sigm(acc) : 0.f;
+      }
+      const uint2 packed = make_uint2(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]));
+      *reinterpret_cast<uint2*>(atom + off) = packed;
+      if (y && t0 + u < T) *reinterpret_cast<uint2*>(y + u * ystride + 4 * hh) = packed;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xw[0][j] = xw[1][j];
+        xw[1][j] = xw[2][j];
+        xw[2][j] = xc[j];
+      }
+    }
+  }
+}
+
+// The inputs of token u (relative to the chunk start t0) of an 8-channel column: a row of the
+// tile (u >= 0), of the halo (first chunk of a row), zero before the halo, or the copy of the
+// 3 tokens before the chunk (side: rows of 256 bytes, 16-byte chunk cc).
+__device__ __forceinline__ uint4 conv_back_row(const uint8_t* atom, int ccs, const uint8_t* side,
+                                               int cc, int u, int64_t c,
+                                               const __nv_bfloat16* halo, int K, int64_t b,
+                                               int64_t C, int64_t ch) {
+  if (u >= 0) return *reinterpret_cast<const uint4*>(atom + kmaj_chunk(u, ccs));
+  if (c == 0) {
+    const int hr = K - 1 + u;  // halo row of token u
+    if (!halo || hr < 0) return make_uint4(0, 0, 0, 0);
+    return *reinterpret_cast<const uint4*>(halo + (b * (K - 1) + hr) * C + ch);
+  }
+  return *reinterpret_cast<const uint4*>(side + (u + 3) * 256 + cc * 16);
+}
+
+// CONV: the q, k, v tiles are loaded from the Conv1D inputs x (maps mq, mk, mv), with the 3
+// tokens before the chunk (maps mlq, mlk, mlv), and convolved in place before their first use.
+template <bool CONV>
 __global__ void __launch_bounds__(PT, 2)
     k_prep_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-              const __grid_constant__ CUtensorMap mv, PrepArgs ar) {
+              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mlq,
+              const __grid_constant__ CUtensorMap mlk, const __grid_constant__ CUtensorMap mlv,
+              PrepArgs ar) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   const uint32_t base = smem_u32(sm);
@@ -178,19 +271,27 @@ __global__ void __launch_bounds__(PT, 2)
     return w;
   };
   auto issue_qk = [&](const Item& it) {
-    mbar_arrive_expect_tx(bar_qk, 32768u);
+    mbar_arrive_expect_tx(bar_qk, CONV ? 32768u + 1536u : 32768u);
     for (int at = 0; at < 2; ++at) {
       tma_load_4d(sm + P_QK + at * 16384, &mq, at * 64, (int)(it.h / ar.r), (int)(it.c * 64),
                   (int)it.b, bar_qk);
       tma_load_4d(sm + P_QK + at * 16384 + 8192, &mk, at * 64, (int)(it.h / ar.r),
                   (int)(it.c * 64), (int)it.b, bar_qk);
     }
+    if (CONV) {  // tokens t0 - 3 .. t0 - 1 (zero-filled before the row's first token)
+      tma_load_4d(sm + P_LB, &mlq, 0, (int)(it.h / ar.r), (int)(it.c * 64) - 3, (int)it.b,
+                  bar_qk);
+      tma_load_4d(sm + P_LB + 768, &mlk, 0, (int)(it.h / ar.r), (int)(it.c * 64) - 3,
+                  (int)it.b, bar_qk);
+    }
   };
   auto issue_v = [&](const Item& it) {
-    mbar_arrive_expect_tx(bar_v, 16384u);
+    mbar_arrive_expect_tx(bar_v, CONV ? 16384u + 768u : 16384u);
     for (int at = 0; at < 2; ++at)
       tma_load_4d(sm + P_V + at * 8192, &mv, at * 64, (int)it.h, (int)(it.c * 64), (int)it.b,
                   bar_v);
+    if (CONV)
+      tma_load_4d(sm + P_LB + 1536, &mlv, 0, (int)it.h, (int)(it.c * 64) - 3, (int)it.b, bar_v);
   };
   // Gate inputs (warps 2, 3: a, b, dt_bias, A_log of token tg), kept as loaded: their first
   // use, in the chunk's gate step, is where the threads wait for them.
@@ -240,12 +341,39 @@ __global__ void __launch_bounds__(PT, 2)
   const uint32_t par = (uint32_t)(kk & 1);
   // ---- [Q; K] [Q; K]^T -> cols [0, 128): row norms on the diagonal, Q K^T and K K^T in cols
   //      64..127, issued as soon as q and k land; the gates are formed meanwhile
+  if (CONV) {  // every thread waits for the x tiles: the Conv1D + SiLU runs in place first
+    const bool landed = !*s_abort && mbar_wait(bar_qk, par, ar.status, kStatusTimeout);
+    if (!landed) *s_abort = 1;
+    if (tid == 0 && landed) pend &= ~1u;
+    __syncthreads();
+    if (*s_abort) goto done;
+    {  // lane: q or k (tq), 8-channel column cc; warp: tokens 8 warp .. + 7
+      const int jc = tid & 31, tq = jc >> 4, cc = jc & 15, u0 = warp * 8;
+      uint8_t* atom = sm + P_QK + (cc >> 3) * 16384 + tq * 8192;
+      const int64_t C = ar.Hqk * 128, ch = hq * 128 + cc * 8;
+      const __nv_bfloat16* halo = tq ? ar.chalo[1] : ar.chalo[0];
+      uint4 back[3];
+#pragma unroll
+      for (int i = 0; i < 3; ++i)
+        back[i] = conv_back_row(atom, cc & 7, sm + P_LB + tq * 768, cc, u0 - 3 + i, c, halo,
+                                ar.convK, b, C, ch);
+      __syncthreads();  // the rows before each thread's own are read: convolve in place
+      __nv_bfloat16* y = h % ar.r ? nullptr  // one V head of the group writes q and k
+                                  : (tq ? ar.cy[1] : ar.cy[0]) + (b * ar.Ts + c * 64) * C + ch;
+      conv_column(atom, cc & 7, u0, 8, back, tq ? ar.cw[1] : ar.cw[0],
+                  tq ? ar.cb[1] : ar.cb[0], ar.convK, ch, c * 64, ar.T, y, C);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   if (tid == 0) {
     if (*s_abort) {  // (the previous chunk gave up before issuing this chunk's copies)
-    } else if (!mbar_wait(bar_qk, par, ar.status, kStatusTimeout)) {
+    } else if (!CONV && !mbar_wait(bar_qk, par, ar.status, kStatusTimeout)) {
       *s_abort = 1;
     } else {
-      pend &= ~1u;
+      if (!CONV) pend &= ~1u;
       tc_fence_after();
       const uint32_t id = idesc_bf16(128, 128, 0, 0);
       for (int ks = 0; ks < 8; ++ks) {
@@ -393,6 +521,23 @@ __global__ void __launch_bounds__(PT, 2)
   __syncthreads();
   tc_fence_after();
   if (*s_abort) goto done;
+  if (CONV) {  // the Conv1D + SiLU of the v tile, in place; 16-lane groups: tokens 4 (tid / 16) ..
+    const int cc = tid & 15, u0 = (tid >> 4) * 4;
+    uint8_t* atom = sm + P_V + (cc >> 3) * 8192;
+    const int64_t C = ar.H * 128, ch = h * 128 + cc * 8;
+    uint4 back[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+      back[i] = conv_back_row(atom, cc & 7, sm + P_LB + 1536, cc, u0 - 3 + i, c, ar.chalo[2],
+                              ar.convK, b, C, ch);
+    __syncthreads();
+    conv_column(atom, cc & 7, u0, 4, back, ar.cw[2], ar.cb[2], ar.convK, ch, c * 64, ar.T,
+                ar.cy[2] + (b * ar.Ts + c * 64) * C + ch, C);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   // ---- [T_u; T_w] V -> cols [0,128) (U in rows 0..63); [T_u; T_w] K -> cols [128,256) (W in
   //      64..127, issued above)
   if (tid == 0) {
@@ -1225,14 +1370,28 @@ cudaError_t smem_attr(K kern, uint32_t bytes) {
 
 cudaError_t launch_prep_tc(const Prob& pr, const Inputs& in, const WS& ws, cudaStream_t st) {
   if (pr.B == 0 || pr.NC == 0) return cudaSuccess;
-  CUtensorMap mq, mk, mv;
+  const ConvIn* cv = in.conv;  // set: the tiles come from the Conv1D inputs
+  CUtensorMap mq, mk, mv, mlq, mlk, mlv;
   memset(&mq, 0, sizeof(mq));
   memset(&mk, 0, sizeof(mk));
   memset(&mv, 0, sizeof(mv));
-  if (!tc_make_map(&mq, in.q, pr.B, pr.T, pr.Ts, pr.Hqk) ||
-      !tc_make_map(&mk, in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
-      !tc_make_map(&mv, in.v, pr.B, pr.T, pr.Ts, pr.H))
+  if (!tc_make_map(&mq, cv ? cv->x[0] : in.q, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mk, cv ? cv->x[1] : in.k, pr.B, pr.T, pr.Ts, pr.Hqk) ||
+      !tc_make_map(&mv, cv ? cv->x[2] : in.v, pr.B, pr.T, pr.Ts, pr.H))
     return cudaErrorInvalidValue;
+  if (cv) {
+    memset(&mlq, 0, sizeof(mlq));
+    memset(&mlk, 0, sizeof(mlk));
+    memset(&mlv, 0, sizeof(mlv));
+    if (!tc_make_map_rows(&mlq, cv->x[0], pr.B, pr.T, pr.Ts, pr.Hqk, 3) ||
+        !tc_make_map_rows(&mlk, cv->x[1], pr.B, pr.T, pr.Ts, pr.Hqk, 3) ||
+        !tc_make_map_rows(&mlv, cv->x[2], pr.B, pr.T, pr.Ts, pr.H, 3))
+      return cudaErrorInvalidValue;
+  } else {
+    mlq = mq;  // (not read)
+    mlk = mk;
+    mlv = mv;
+  }
   PrepArgs ar;
   ar.T = pr.T; ar.Ts = pr.Ts; ar.H = pr.H; ar.Hqk = pr.Hqk; ar.r = pr.r; ar.NC = pr.NC;
   ar.l2norm = pr.l2norm; ar.eps = pr.eps; ar.scale = pr.scale;
@@ -1242,11 +1401,23 @@ cudaError_t launch_prep_tc(const Prob& pr, const Inputs& in, const WS& ws, cudaS
   ar.pim = (uint8_t*)ws.pim; ar.tim = (uint8_t*)ws.tim; ar.gl = ws.gl;
   ar.status = ws.status;
   ar.NW = pr.B * pr.H * pr.NC;
+  ar.convK = cv ? cv->K : 0;
+  for (int i = 0; i < 3; ++i) {
+    ar.cw[i] = cv ? cv->w[i] : nullptr;
+    ar.cb[i] = cv ? cv->bias[i] : nullptr;
+    ar.chalo[i] = cv ? (const __nv_bfloat16*)cv->halo[i] : nullptr;
+    ar.cy[i] = cv ? (__nv_bfloat16*)cv->y[i] : nullptr;
+  }
   if (ar.NW + 1024 >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // 32-bit chunk indices
-  cudaError_t e = smem_attr(k_prep_tc, P_SMEM);
-  if (e != cudaSuccess) return e;
   const int64_t nblk = ar.NW < 2 * (int64_t)device_sms() ? ar.NW : 2 * (int64_t)device_sms();
-  k_prep_tc<<<(unsigned)nblk, PT, P_SMEM, st>>>(mq, mk, mv, ar);  // two CTAs per SM, persistent
+  cudaError_t e;
+  if (cv) {
+    if ((e = smem_attr(k_prep_tc<true>, P_SMEM_CONV)) != cudaSuccess) return e;
+    k_prep_tc<true><<<(unsigned)nblk, PT, P_SMEM_CONV, st>>>(mq, mk, mv, mlq, mlk, mlv, ar);
+  } else {
+    if ((e = smem_attr(k_prep_tc<false>, P_SMEM)) != cudaSuccess) return e;
+    k_prep_tc<false><<<(unsigned)nblk, PT, P_SMEM, st>>>(mq, mk, mv, mlq, mlk, mlv, ar);
+  }  // two CTAs per SM, persistent
   return cudaGetLastError();
 }
 

@@ -53,6 +53,21 @@ bool tc_make_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t 
   return make_map(m, ptr, B, T, Ts, heads);
 }
 
+// The same tensor, boxes of `rows` tokens x the whole 128-column head, unswizzled (rows of
+// 256 bytes): the K - 1 tokens before a chunk that the Conv1D reads.
+bool tc_make_map_rows(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t Ts,
+                      int64_t heads, int rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || rows < 1 || rows > 256) return false;
+  cuuint64_t dims[4] = {128, (cuuint64_t)heads, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {256, (cuuint64_t)(heads * 256), (cuuint64_t)(Ts * heads * 256)};
+  cuuint32_t box[4] = {128, 1, (cuuint32_t)rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc_path(const Prob& pr) {
   return pr.dtype == GDN_BF16 && pr.dk == 128 && pr.dv == 128 && pr.B > 0 && pr.NC > 0;
 }

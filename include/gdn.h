@@ -393,6 +393,40 @@ gdn_status gdn_conv_silu_bwd(const gdn_conv_problem* p, const void* x, const flo
                              size_t workspace_bytes, void* stream);
 
 /*
+ * The Conv1D + SiLU fused into the core's forward ("linear attention cp #1035", section
+ * "What does this PR do": the depthwise Conv1D feeds q, k and v of the Gated DeltaNet; the
+ * test report "Linear Attention CP 融合算子 PR #1114 测试报告" lists the fused Conv1D as not
+ * yet done there).  Result: for i = q, k, v, y[i] = gdn_conv_silu_fwd of x[i] (channels
+ * Hqk*dk, Hqk*dk, H*dv; taps K; same B, T, T_stride as p; the same bits), followed by
+ * gdn_fwd (ctx NULL) or gdn_fwd_ctx (ctx set) with q, k, v = y[0], y[1], y[2].  On the bf16
+ * tensor-core path (dk = dv = 128) the chunk prologue reads x itself: each chunk's x tiles
+ * and the K - 1 tokens before them are convolved in shared memory and y is written once
+ * from there, so q, k and v are never read back for the prologue; the other paths run the
+ * stand-alone Conv1D, then the forward.  y holds every token of every chunk that has a valid
+ * token; with valid_len, the tokens of chunks of padding only are zero.  The backward of a
+ * training step is gdn_bwd_ctx on q, k, v = y, then gdn_conv_silu_bwd on each of x_q, x_k,
+ * x_v with dy = dq, dk, dv.
+ * Layouts: x[i], y[i] as q, k, v (p->dtype); w[i] [channels][K] fp32; bias[i] [channels]
+ * fp32 or NULL; halo[i] [B][K-1][channels] in p->dtype or NULL (zeros before token 0).
+ * Workspace: gdn_workspace_size of GDN_OP_FWD (ctx NULL) or GDN_OP_FWD_CTX.  Errors: those
+ * of gdn_fwd / gdn_fwd_ctx; a null or misaligned x, w or y, a misaligned bias or halo, or a
+ * y that overlaps its x: GDN_ERR_INVALID_ARG; K outside 1..4: GDN_ERR_UNSUPPORTED.
+ */
+typedef struct gdn_conv_qkv {
+  int32_t K;             /* taps, 1..4 */
+  const void* x[3];      /* x_q, x_k, x_v: pre-activation inputs, layouts of q, k, v */
+  const float* w[3];     /* taps [channels][K] */
+  const float* bias[3];  /* [channels] or NULL */
+  const void* halo[3];   /* [B][K-1][channels] or NULL */
+  void* y[3];            /* written: q, k, v = SiLU(conv(x)) */
+} gdn_conv_qkv;
+
+gdn_status gdn_fwd_conv(const gdn_problem* p, const gdn_conv_qkv* conv, const void* a,
+                        const void* b, const float* A_log, const float* dt_bias, const float* h0,
+                        const int32_t* valid_len, void* o, float* hT, void* ctx, size_t ctx_bytes,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Packed variable-length rows (several sequences in one row, each with its own state):
  * the test report's variable-length training samples ("Linear Attention CP 融合算子
  * PR #1114 测试报告", section 5.2, there as trailing padding of each batch row)
