@@ -771,6 +771,57 @@ def run_ours(args):
             "peak": f"{peaks['hbm_gbs']} GB/s ({peaks['source']})"}
         del cd, cy, cdx, cdw, cdh, cws
 
+        # The same Conv1D fused into the training-step forward (gdn_fwd_conv: the chunk
+        # prologue loads x_q, x_k, x_v, convolves each chunk in shared memory and writes the
+        # activated q, k, v once), against the stand-alone Conv1D of the three tensors followed
+        # by gdn_fwd_ctx; both calls timed alone with CUDA events, and their outputs compared.
+        xs, wts, hls = [], [], []
+        for i, heads in enumerate((w.Hqk, w.Hqk, w.H)):
+            c = gi.make_conv_inputs(B, T, heads * dk, Kc, torch.bfloat16, seed=w.seed + 80 + i,
+                                    bias=False)
+            xs.append(c["x"].view(B, T, heads, dk).cuda())
+            wts.append(c["w"].cuda())
+            hls.append(c["halo"].cuda())
+        ys = [torch.empty_like(x) for x in xs]
+        cps = [gdn.make_conv_problem(x.view(B, T, -1), Kc) for x in xs]
+
+        def conv_fused():
+            gdn.gdn_fwd_conv(tuple(xs), tuple(wts), d["a"], d["b"], d["A_log"], d["dt_bias"],
+                             d["h0"], None, halo=tuple(hls), y=tuple(ys), ctx=ctx, o=o, hT=hT,
+                             ws=wsfc, problem=p, stream=stream)
+
+        def conv_only():
+            for x, wt, hl, y_, cp_ in zip(xs, wts, hls, ys, cps):
+                gdn.gdn_conv_silu_fwd(x.view(B, T, -1), wt, None, hl, y=y_.view(B, T, -1),
+                                      problem=cp_, stream=stream)
+
+        def conv_separate():
+            conv_only()
+            gdn.gdn_fwd_ctx(ys[0], ys[1], ys[2], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                            d["h0"], None, ctx=ctx, o=o, hT=hT, ws=wsfc, problem=p,
+                            stream=stream)
+
+        conv_separate()
+        torch.cuda.synchronize()
+        o_sep, y_sep = o.clone(), [y_.clone() for y_ in ys]
+        conv_fused()
+        torch.cuda.synchronize()
+        same = torch.equal(o, o_sep) and all(torch.equal(a_, b_) for a_, b_ in zip(ys, y_sep))
+        del o_sep, y_sep
+        for _ in range(3):
+            conv_fused()
+            conv_separate()
+        ms_fused = timed(conv_fused, args.steps)
+        ms_sep = timed(conv_separate, args.steps)
+        ms_conv3 = timed(conv_only, args.steps)
+        line["conv_fused_fwd"] = {
+            "shape": f"B={B} T={T} x_q, x_k [{w.Hqk}x{dk}], x_v [{w.H}x{dv}] bf16, K={Kc}, halo",
+            "fused_ms": ms_fused, "fused_tokens_per_s": B * T / (ms_fused / 1e3),
+            "separate_ms": ms_sep, "separate_conv_ms": ms_conv3,
+            "bit_identical": bool(same),
+            "calls": "gdn_fwd_conv (ctx) vs gdn_conv_silu_fwd x3 + gdn_fwd_ctx"}
+        del xs, wts, hls, ys
+
         # The gated RMSNorm epilogue on o (rows = B T H, D = dv), forward and backward.
         ri = gi.make_rmsnorm_inputs((B, T, H, dv), torch.bfloat16, seed=w.seed + 78)
         rd = {k: v.cuda() for k, v in ri.items()}

@@ -137,62 +137,121 @@ struct PrepArgs {
   __nv_bfloat16* cy[3];            // the activated q, k, v, written for the later kernels
 };
 
+// Taps and bias of channels ch .. ch + 7 of w [C][KK] (8 KK contiguous floats) and bias
+// [C], as float4 loads; wv[j][i] holds the tap of x~[t - 3 + i] (zero for i < 4 - KK).
+template <int KK>
+__device__ __forceinline__ void conv_taps_k(const float* __restrict__ w,
+                                            const float* __restrict__ bias, int64_t ch,
+                                            float (&wv)[8][4], float (&bv)[8]) {
+  float t[8 * KK];
+  const float4* w4 = reinterpret_cast<const float4*>(w + ch * KK);  // 16-byte aligned: ch % 8 == 0
+#pragma unroll
+  for (int q = 0; q < 2 * KK; ++q) {
+    const float4 f = __ldg(w4 + q);
+    t[4 * q] = f.x; t[4 * q + 1] = f.y; t[4 * q + 2] = f.z; t[4 * q + 3] = f.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) wv[j][i] = (i >= 4 - KK) ? t[j * KK + i - (4 - KK)] : 0.f;
+  if (bias) {
+    const float4 b0 = __ldg(reinterpret_cast<const float4*>(bias + ch));
+    const float4 b1 = __ldg(reinterpret_cast<const float4*>(bias + ch) + 1);
+    bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+    bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) bv[j] = 0.f;
+  }
+}
+__device__ __forceinline__ void conv_taps(const float* w, const float* bias, int K, int64_t ch,
+                                          float (&wv)[8][4], float (&bv)[8]) {
+  switch (K) {
+    case 1: conv_taps_k<1>(w, bias, ch, wv, bv); break;
+    case 2: conv_taps_k<2>(w, bias, ch, wv, bv); break;
+    case 3: conv_taps_k<3>(w, bias, ch, wv, bv); break;
+    default: conv_taps_k<4>(w, bias, ch, wv, bv); break;
+  }
+}
+
+// Two fp32 lanes at once: fma.rn.f32x2 rounds each lane as fmaf does.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
 // Causal depthwise Conv1D + SiLU of one 8-channel column (16-byte chunk `ccs` of a
-// 128-byte-swizzled 64-row atom) over rows u0 .. u0 + n - 1 of the tile, in place: row u
-// (token t0 + u) becomes SiLU(bias + sum of the taps over x~[t - K + 1 .. t]), rounded to
-// bf16, with the same operation order as the stand-alone Conv1D pass, so both give the
-// same bits.  back[i] holds the inputs of token u0 - 3 + i (bf16, 8 channels).  Rows past
-// the end of the row (t0 + u >= T) become zero, as a copy of the activated tensor would
-// read there; the others also go to y + u * ystride when y is set.  Channels ch .. ch + 7
-// of w [C][K] and bias.  Four channels at a time.
-__device__ __forceinline__ void conv_column(uint8_t* atom, int ccs, int u0, int n,
-                                            const uint4 (&back)[3], const float* __restrict__ w,
-                                            const float* __restrict__ bias, int K, int64_t ch,
-                                            int64_t t0, int64_t T, __nv_bfloat16* y,
-                                            int64_t ystride) {
-#pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {
-    float wv[4][4], bv[4], xw[3][4];
+// 128-byte-swizzled 64-row atom) over rows u0 .. u0 + N - 1 of the tile, in place: row u
+// (token t0 + u) becomes SiLU(bias + sum of the KK taps over x~[t - KK + 1 .. t]), rounded
+// to bf16, with the same operation order and rounding as the stand-alone Conv1D pass
+// (channel pairs on packed fp32 operations), so both give the same bits.  back[i] holds the
+// inputs of token u0 - 3 + i (bf16, 8 channels); wv, bv the column's taps and bias
+// (conv_taps).  Rows past the end of the row (t0 + u >= T) become zero, as a copy of the
+// activated tensor would read there; the others also go to y + u * ystride when y is set.
+template <int N, int KK>
+__device__ __forceinline__ void conv_column(uint8_t* atom, int ccs, int u0,
+                                            const uint4 (&back)[3], const float (&wv)[8][4],
+                                            const float (&bv)[8], int64_t t0, int64_t T,
+                                            __nv_bfloat16* y, int64_t ystride) {
+  float xw[3][8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t cj = ch + 4 * hh + j;
+  for (int i = 0; i < 3; ++i) {
+    const uint32_t wd[4] = {back[i].x, back[i].y, back[i].z, back[i].w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) wv[j][i] = (i >= 4 - K) ? w[cj * K + i - (4 - K)] : 0.f;
-      bv[j] = bias ? bias[cj] : 0.f;
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[e]));
+      xw[i][2 * e] = f.x;
+      xw[i][2 * e + 1] = f.y;
     }
+  }
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const uint32_t lo = hh ? back[i].z : back[i].x, hi = hh ? back[i].w : back[i].y;
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo));
-      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
-      xw[i][0] = a.x; xw[i][1] = a.y; xw[i][2] = c.x; xw[i][3] = c.y;
+  for (int r = 0; r < N; ++r) {
+    const int u = u0 + r;
+    const uint32_t off = kmaj_chunk(u, ccs);
+    float xc[8];
+    ld_chunk(atom, off, xc);
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      float2 acc = make_float2(bv[j], bv[j + 1]);
+#pragma unroll
+      for (int i = 4 - KK; i < 3; ++i)
+        acc = fma2(make_float2(wv[j][i], wv[j + 1][i]), make_float2(xw[i][j], xw[i][j + 1]), acc);
+      acc = fma2(make_float2(wv[j][3], wv[j + 1][3]), make_float2(xc[j], xc[j + 1]), acc);
+      o[j] = acc.x * vec::sigm(acc.x);
+      o[j + 1] = acc.y * vec::sigm(acc.y);
     }
-    for (int u = u0; u < u0 + n; ++u) {
-      const uint32_t off = kmaj_chunk(u, ccs) + 8 * hh;
-      const uint2 raw = *reinterpret_cast<const uint2*>(atom + off);
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-      const float xc[4] = {a.x, a.y, c.x, c.y};
-      float o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float acc = bv[j];
-#pragma unroll
-        for (int i = 0; i < 3; ++i)
-          if (i >= 4 - K) acc = fmaf(wv[j][i], xw[i][j], acc);
-        acc = fmaf(wv[j][3], xc[j], acc);
-        o[j] = (t0 + u < T) ? acc * vec::sigm(acc) : 0.f;
-      }
-      const uint2 packed = make_uint2(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]));
-      *reinterpret_cast<uint2*>(atom + off) = packed;
-      if (y && t0 + u < T) *reinterpret_cast<uint2*>(y + u * ystride + 4 * hh) = packed;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        xw[0][j] = xw[1][j];
-        xw[1][j] = xw[2][j];
-        xw[2][j] = xc[j];
-      }
+    uint4 packed = make_uint4(0, 0, 0, 0);
+    if (t0 + u < T) {
+      packed.x = pack_bf16(o[0], o[1]);
+      packed.y = pack_bf16(o[2], o[3]);
+      packed.z = pack_bf16(o[4], o[5]);
+      packed.w = pack_bf16(o[6], o[7]);
+      if (y) *reinterpret_cast<uint4*>(y + u * ystride) = packed;
     }
+    *reinterpret_cast<uint4*>(atom + off) = packed;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      xw[0][j] = xw[1][j];
+      xw[1][j] = xw[2][j];
+      xw[2][j] = xc[j];
+    }
+  }
+}
+template <int N>
+__device__ __forceinline__ void conv_column_k(int K, uint8_t* atom, int ccs, int u0,
+                                              const uint4 (&back)[3], const float (&wv)[8][4],
+                                              const float (&bv)[8], int64_t t0, int64_t T,
+                                              __nv_bfloat16* y, int64_t ystride) {
+  switch (K) {
+    case 1: conv_column<N, 1>(atom, ccs, u0, back, wv, bv, t0, T, y, ystride); break;
+    case 2: conv_column<N, 2>(atom, ccs, u0, back, wv, bv, t0, T, y, ystride); break;
+    case 3: conv_column<N, 3>(atom, ccs, u0, back, wv, bv, t0, T, y, ystride); break;
+    default: conv_column<N, 4>(atom, ccs, u0, back, wv, bv, t0, T, y, ystride); break;
   }
 }
 
@@ -342,15 +401,19 @@ __global__ void __launch_bounds__(PT, 2)
   // ---- [Q; K] [Q; K]^T -> cols [0, 128): row norms on the diagonal, Q K^T and K K^T in cols
   //      64..127, issued as soon as q and k land; the gates are formed meanwhile
   if (CONV) {  // every thread waits for the x tiles: the Conv1D + SiLU runs in place first
+    // lane: q or k (tq), 8-channel column cc; warp: tokens 8 warp .. + 7.  The taps are
+    // read while the copies land.
+    const int jc = tid & 31, tq = jc >> 4, cc = jc & 15, u0 = warp * 8;
+    const int64_t C = ar.Hqk * 128, ch = hq * 128 + cc * 8;
+    float wv[8][4], bv[8];
+    conv_taps(tq ? ar.cw[1] : ar.cw[0], tq ? ar.cb[1] : ar.cb[0], ar.convK, ch, wv, bv);
     const bool landed = !*s_abort && mbar_wait(bar_qk, par, ar.status, kStatusTimeout);
     if (!landed) *s_abort = 1;
     if (tid == 0 && landed) pend &= ~1u;
     __syncthreads();
     if (*s_abort) goto done;
-    {  // lane: q or k (tq), 8-channel column cc; warp: tokens 8 warp .. + 7
-      const int jc = tid & 31, tq = jc >> 4, cc = jc & 15, u0 = warp * 8;
+    {
       uint8_t* atom = sm + P_QK + (cc >> 3) * 16384 + tq * 8192;
-      const int64_t C = ar.Hqk * 128, ch = hq * 128 + cc * 8;
       const __nv_bfloat16* halo = tq ? ar.chalo[1] : ar.chalo[0];
       uint4 back[3];
 #pragma unroll
@@ -360,8 +423,7 @@ __global__ void __launch_bounds__(PT, 2)
       __syncthreads();  // the rows before each thread's own are read: convolve in place
       __nv_bfloat16* y = h % ar.r ? nullptr  // one V head of the group writes q and k
                                   : (tq ? ar.cy[1] : ar.cy[0]) + (b * ar.Ts + c * 64) * C + ch;
-      conv_column(atom, cc & 7, u0, 8, back, tq ? ar.cw[1] : ar.cw[0],
-                  tq ? ar.cb[1] : ar.cb[0], ar.convK, ch, c * 64, ar.T, y, C);
+      conv_column_k<8>(ar.convK, atom, cc & 7, u0, back, wv, bv, c * 64, ar.T, y, C);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -514,6 +576,12 @@ __global__ void __launch_bounds__(PT, 2)
       *reinterpret_cast<uint4*>(dst + kmaj_chunk(i, cc)) = pack8(x);
     }
   }
+  // the Conv1D + SiLU of the v tile comes after the copy lands; its taps are read first.
+  // 16-lane groups: 8-channel column cc, tokens 4 (tid / 16) .. + 3
+  const int vcc = tid & 15, vu0 = (tid >> 4) * 4;
+  const int64_t vC = ar.H * 128, vch = h * 128 + vcc * 8;
+  float vwv[8][4], vbv[8];
+  if (CONV) conv_taps(ar.cw[2], ar.cb[2], ar.convK, vch, vwv, vbv);
   if (!mbar_wait(bar_v, par, ar.status, kStatusTimeout)) *s_abort = 1;
   if (tid == 0) pend &= ~2u;
   fence_proxy_async();
@@ -521,18 +589,16 @@ __global__ void __launch_bounds__(PT, 2)
   __syncthreads();
   tc_fence_after();
   if (*s_abort) goto done;
-  if (CONV) {  // the Conv1D + SiLU of the v tile, in place; 16-lane groups: tokens 4 (tid / 16) ..
-    const int cc = tid & 15, u0 = (tid >> 4) * 4;
-    uint8_t* atom = sm + P_V + (cc >> 3) * 8192;
-    const int64_t C = ar.H * 128, ch = h * 128 + cc * 8;
+  if (CONV) {
+    uint8_t* atom = sm + P_V + (vcc >> 3) * 8192;
     uint4 back[3];
 #pragma unroll
     for (int i = 0; i < 3; ++i)
-      back[i] = conv_back_row(atom, cc & 7, sm + P_LB + 1536, cc, u0 - 3 + i, c, ar.chalo[2],
-                              ar.convK, b, C, ch);
+      back[i] = conv_back_row(atom, vcc & 7, sm + P_LB + 1536, vcc, vu0 - 3 + i, c, ar.chalo[2],
+                              ar.convK, b, vC, vch);
     __syncthreads();
-    conv_column(atom, cc & 7, u0, 4, back, ar.cw[2], ar.cb[2], ar.convK, ch, c * 64, ar.T,
-                ar.cy[2] + (b * ar.Ts + c * 64) * C + ch, C);
+    conv_column_k<4>(ar.convK, atom, vcc & 7, vu0, back, vwv, vbv, c * 64, ar.T,
+                     ar.cy[2] + (b * ar.Ts + c * 64) * vC + vch, vC);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
