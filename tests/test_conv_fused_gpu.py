@@ -30,17 +30,18 @@ def _lib():
     gdn.load_library()
 
 
-def make_case(B, T, Hqk, H, K, *, halo, bias, seed, valid_len=None):
+def make_case(B, T, Hqk, H, K, *, halo, bias, seed, valid_len=None, d=128,
+              dtype=torch.bfloat16):
     """Core inputs of the shape plus, per q, k, v, the Conv1D inputs x (layout of q, k, v),
     taps w [channels, K], bias and halo (all seeded, on the CPU)."""
-    w = gi.Workload("conv_fused", B=B, T=T, Hqk=Hqk, H=H, dk=128, dv=128, h0_std=0.1,
+    w = gi.Workload("conv_fused", B=B, T=T, Hqk=Hqk, H=H, dk=d, dv=d, dtype=dtype, h0_std=0.1,
                     valid_len=valid_len, seed=seed)
     core = gi.make_inputs(w)
     conv = []
     for i, heads in enumerate((Hqk, Hqk, H)):
-        c = gi.make_conv_inputs(B, T, heads * 128, K, torch.bfloat16, seed=seed * 10 + i,
-                                halo=halo, bias=bias)
-        conv.append({"x": c["x"].view(B, T, heads, 128), "w": c["w"], "bias": c["bias"],
+        c = gi.make_conv_inputs(B, T, heads * d, K, dtype, seed=seed * 10 + i, halo=halo,
+                                bias=bias)
+        conv.append({"x": c["x"].view(B, T, heads, d), "w": c["w"], "bias": c["bias"],
                      "halo": c["halo"]})
     return core, conv
 
@@ -82,9 +83,9 @@ def run_separate(core, conv, with_ctx=True):
     for c in conv:
         x = cuda(c["x"])
         B, T, heads, _ = x.shape
-        yi = gdn.gdn_conv_silu_fwd(x.view(B, T, heads * 128), cuda(c["w"]), cuda(c["bias"]),
+        yi = gdn.gdn_conv_silu_fwd(x.reshape(B, T, -1), cuda(c["w"]), cuda(c["bias"]),
                                    cuda(c["halo"]))
-        y.append(yi.view(B, T, heads, 128))
+        y.append(yi.view(x.shape))
     args = (y[0], y[1], y[2], d["a"], d["b"], d["A_log"], d["dt_bias"], d["h0"], d["valid_len"])
     if with_ctx:
         o, hT, ctx = gdn.gdn_fwd_ctx(*args, ctx=zero_ctx(core))
@@ -108,6 +109,8 @@ CASES = [  # B, T, Hqk, H, K, halo, bias, valid_len
     (1, 100, 1, 4, 1, False, False, None),
     (2, 200, 2, 4, 3, True, True, [130, 200]),
     (1, 64, 2, 4, 4, True, False, None),
+    (1, 1, 2, 4, 4, True, True, None),            # one token: every tap but one is halo
+    (2, 130, 2, 4, 4, True, True, [0, 70]),       # a row of padding only
 ]
 IDS = [f"B{c[0]}_T{c[1]}_h{c[2]}x{c[3]}_K{c[4]}{'_halo' if c[5] else ''}"
        f"{'_bias' if c[6] else ''}{'_padded' if c[7] else ''}" for c in CASES]
@@ -123,9 +126,9 @@ def test_fused_conv_matches_oracle(case):
     for c in conv:
         x = to64(c["x"])
         Bx, Tx, heads, _ = x.shape
-        r = oracle.conv_silu_fwd(x.reshape(Bx, Tx, heads * 128), to64(c["w"]), to64(c["bias"]),
+        r = oracle.conv_silu_fwd(x.reshape(Bx, Tx, -1), to64(c["w"]), to64(c["bias"]),
                                  to64(c["halo"]))
-        ry.append(r.reshape(Bx, Tx, heads, 128))
+        ry.append(r.reshape(x.shape))
     ends = live_tokens(vl, T, B)
     for name, yi, ri in zip("qkv", y, ry):
         for bb, end in enumerate(ends):
@@ -196,3 +199,56 @@ def test_fused_conv_rejects_bad_arguments():
     with pytest.raises(gdn.GDNError) as e:
         gdn.gdn_fwd_conv(x, w5, d["a"], d["b"], d["A_log"], d["dt_bias"])
     assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_fused_conv_row_stride():
+    """Rows T_stride = 200 tokens apart, T = 150 of them used: the fused call reads x and
+    writes y (and o) in those rows only, as the separate passes do."""
+    B, T, Ts, Hqk, H, K = 2, 150, 200, 2, 4, 4
+    core, conv = make_case(B, Ts, Hqk, H, K, halo=True, bias=True, seed=21)
+    d = {k: cuda(v) for k, v in core.items()}
+    x = tuple(cuda(c["x"]) for c in conv)
+    w = tuple(cuda(c["w"]) for c in conv)
+    bias = tuple(cuda(c["bias"]) for c in conv)
+    halo = tuple(cuda(c["halo"]) for c in conv)
+    p = gdn.make_problem(d["q"], d["v"], T=T, T_stride=Ts)
+    o = torch.zeros_like(d["v"])
+    y = tuple(torch.zeros_like(t) for t in x)
+    o, hT, _, y = gdn.gdn_fwd_conv(x, w, d["a"], d["b"], d["A_log"], d["dt_bias"], d["h0"],
+                                   bias=bias, halo=halo, y=y, o=o, with_ctx=False, problem=p)
+    sy = []
+    for xi, wi, bi, hi in zip(x, w, bias, halo):
+        cp = gdn.make_conv_problem(xi.reshape(B, Ts, -1), K, T=T, T_stride=Ts)
+        yi = torch.zeros_like(xi)
+        gdn.gdn_conv_silu_fwd(xi.reshape(B, Ts, -1), wi, bi, hi, y=yi.view(B, Ts, -1),
+                              problem=cp)
+        sy.append(yi)
+    so = torch.zeros_like(d["v"])
+    so, shT = gdn.gdn_fwd(sy[0], sy[1], sy[2], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                          d["h0"], o=so, problem=p)[:2]
+    torch.cuda.synchronize()
+    for name, a_, b_ in zip("qkv", y, sy):
+        assert torch.equal(a_, b_), f"y_{name} differs"
+        assert not torch.any(a_[:, T:] != 0), f"y_{name} written past T"
+    assert torch.equal(o, so) and torch.equal(hT, shT)
+
+
+def test_fused_conv_fp32_cuda_core_route():
+    """fp32 (CUDA-core path, d = 32): the call runs the stand-alone Conv1D, then the forward;
+    checked against the composed fp64 oracles at the fp32 bar (rel-L2 <= 1e-5)."""
+    B, T, Hqk, H, K = 1, 150, 2, 4, 3
+    core, conv = make_case(B, T, Hqk, H, K, halo=True, bias=True, seed=31, d=32,
+                           dtype=torch.float32)
+    o, hT, ctx, y = run_fused(core, conv)
+    ry = []
+    for c in conv:
+        x = to64(c["x"])
+        r = oracle.conv_silu_fwd(x.reshape(B, T, -1), to64(c["w"]), to64(c["bias"]),
+                                 to64(c["halo"]))
+        ry.append(r.reshape(x.shape))
+    for name, yi, ri in zip("qkv", y, ry):
+        assert_close(f"y_{name}", yi, ri, torch.float32)
+    ro, rhT = oracle.fwd(ry[0], ry[1], ry[2], to64(core["a"]), to64(core["b"]),
+                         to64(core["A_log"]), to64(core["dt_bias"]), to64(core["h0"]))
+    assert_close("o", o, ro, torch.float32)
+    assert_close("hT", hT, rhT, torch.float32)
