@@ -14,7 +14,10 @@
 // parallel and leaves its results in the workspace as bf16 "tile images": the
 // exact bytes of a 128-byte-swizzled K-major shared-memory tile, so that a
 // consumer fetches each with one plain bulk copy and hands it to tcgen05.mma
-// as is.  k_chain_tc then walks the chunks of one segment of one (batch row,
+// as is.  With the depthwise Conv1D + SiLU of "linear attention cp #1035" in front
+// (gdn_fwd_conv), k_prep_tc<true> loads the Conv1D inputs instead, convolves each
+// chunk's tiles in shared memory and writes the activated q, k, v once for the
+// later kernels.  k_chain_tc then walks the chunks of one segment of one (batch row,
 // V head) with the state in fp32 registers and only the two state products
 // per chunk (W S, then K^T V2) on its critical path.  It produces segment
 // summaries (the "p2p" map H_out = M H_in + S of "linear attention cp #1035":
@@ -75,9 +78,12 @@ __device__ __forceinline__ int64_t clamp_len(const int32_t* valid_len, int64_t b
 // column half w >> 2 of that row.
 //
 // The q and k row norms come from the diagonal of one product [Q;K][Q;K]^T of
-// the raw tiles, so neither tile is rewritten: every later use of q_hat = rq q
-// and k_hat = rk k applies the per-token factors rq = scale / |q|, rk = 1 / |k|
-// (kept in the workspace) to an fp32 result or to a row of bf16 operands.
+// the raw tiles, so neither tile is rewritten for the norm: every later use of
+// q_hat = rq q and k_hat = rk k applies the per-token factors rq = scale / |q|,
+// rk = 1 / |k| (kept in the workspace) to an fp32 result or to a row of bf16 operands.
+// With the Conv1D in front (k_prep_tc<true>), the tiles arrive as the Conv1D inputs
+// x and are replaced in place by SiLU(conv(x)) before their first product (q, k at the
+// chunk start, v before the U product), each activated row also written out as q, k, v.
 // ============================================================================
 constexpr int PT = 256;
 constexpr uint32_t P_QK = 0;                   // atoms a at a*16384: [Q_a | K_a], raw, 8 KB each
