@@ -4,6 +4,7 @@ before any launch (no GPU needed: these calls never reach CUDA)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -315,3 +316,74 @@ def test_varlen_validation_and_workspace(lib):
     st = lib.gdn_fwd_varlen(ctypes.byref(problem(T=200, Hqk=1, H=2)), vp(A), arr, 2,
                             *[vp(A)] * 5, vp(A), vp(A), None, vp(A), None, vp(A), 16, None)
     assert st == gdn.GDN_ERR_WORKSPACE
+
+
+STRUCTS = {  # C struct name -> (ctypes mirror, its fields as named in the header)
+    "gdn_problem": (gdn.Problem, [f for f, _ in gdn.Problem._fields_]),
+    "gdn_conv_problem": (gdn.ConvProblem, [f for f, _ in gdn.ConvProblem._fields_]),
+    "gdn_conv_qkv": (gdn.ConvQkv, [f for f, _ in gdn.ConvQkv._fields_]),
+    "gdn_rmsnorm_problem": (gdn.RmsNormProblem, [f for f, _ in gdn.RmsNormProblem._fields_]),
+}
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """sizeof and every field offset of the public structs, as gcc lays them out from
+    include/gdn.h, equal those of the binding's ctypes mirrors."""
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "gdn.h"', "int main(void) {"]
+    for name, (_, fields) in STRUCTS.items():
+        lines.append(f'  printf("{name} size %zu\\n", sizeof({name}));')
+        for f in fields:
+            lines.append(f'  printf("{name} {f} %zu\\n", offsetof({name}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = {}
+    for line in out.splitlines():
+        name, key, val = line.split()
+        got[(name, key)] = int(val)
+    for name, (cls, fields) in STRUCTS.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for f in fields:
+            assert got[(name, f)] == getattr(cls, f).offset, (name, f)
+
+
+def call_fwd_conv(lib, p, cv, ws=None, ws_bytes=0):
+    vp = ctypes.c_void_p
+    return lib.gdn_fwd_conv(ctypes.byref(p), None if cv is None else ctypes.byref(cv),
+                            *[vp(A)] * 4, None, None, vp(A), None, None, 0,
+                            None if ws is None else vp(ws), ws_bytes, None)
+
+
+def conv_qkv(**over):
+    cv = gdn.ConvQkv()
+    cv.K = over.pop("K", 4)
+    for i in range(3):
+        cv.x[i] = A
+        cv.w[i] = A
+        cv.y[i] = A + (1 << 30) + i * (1 << 28)   # clear of every x
+    for key, (i, val) in over.items():
+        getattr(cv, key)[i] = val
+    return cv
+
+
+@pytest.mark.parametrize("over,status", [
+    ({"x": (0, None)}, gdn.GDN_ERR_INVALID_ARG),
+    ({"w": (2, None)}, gdn.GDN_ERR_INVALID_ARG),
+    ({"y": (1, None)}, gdn.GDN_ERR_INVALID_ARG),
+    ({"bias": (0, A + 4)}, gdn.GDN_ERR_INVALID_ARG),     # misaligned
+    ({"halo": (2, A + 8)}, gdn.GDN_ERR_INVALID_ARG),
+    ({"y": (1, A + 64)}, gdn.GDN_ERR_INVALID_ARG),       # y overlaps its x
+    ({"K": 5}, gdn.GDN_ERR_UNSUPPORTED),
+    ({"K": 0}, gdn.GDN_ERR_UNSUPPORTED),
+    ({}, gdn.GDN_ERR_WORKSPACE),                          # valid up to the missing workspace
+])
+def test_fwd_conv_validation_fails_before_launch(lib, over, status):
+    assert call_fwd_conv(lib, problem(), conv_qkv(**over)) == status
+
+
+def test_fwd_conv_needs_its_description(lib):
+    assert call_fwd_conv(lib, problem(), None) == gdn.GDN_ERR_INVALID_ARG
